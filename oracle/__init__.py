@@ -1,0 +1,233 @@
+"""CPU oracle for the inverse-RoPE + block-FP8 quant epilogue (test infrastructure).
+
+This package is the correctness reference the CUDA library is checked
+against. Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline / reference leg may import it; the library itself never does.
+It shares no code with the CUDA path: the arithmetic lives in ``rq_oracle.c``
+(plain scalar C, fp32 as the pages fix it, compiled with FMA contraction off)
+and this module only builds it and marshals numpy / torch-CPU arrays.
+
+What it computes, and the page sections each step follows, is stated in the
+header of ``rq_oracle.c``. Every function here has a pin in
+``tests/test_oracle_*.py`` that checks it against something other than
+itself (the OFP8 spec's value table, torch's float8 cast, exact ceil-log2
+from float64 frexp, complex multiplication, hand-built worked cases).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rq_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-pthread"]
+
+HEAD_DIM = 512
+BLOCKS_PER_HEAD = 4
+RECORD_BYTES = 528
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile rq_oracle.c into oracle/_build/liboracle.so (gcc, no CUDA)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *_CFLAGS, _SRC, "-lm", "-o", tmp], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        sig = {
+            "rqo_e4m3_encode": (ctypes.c_uint8, [ctypes.c_double]),
+            "rqo_e4m3_decode": (ctypes.c_double, [ctypes.c_uint8]),
+            "rqo_ceil_log2": (ctypes.c_int, [ctypes.c_float]),
+            "rqo_block_scale": (ctypes.c_float, [ctypes.c_float]),
+            "rqo_e4m3_encode_f32_array": (None, [P, i64, P]),
+            "rqo_e4m3_decode_array": (None, [P, i64, P]),
+            "rqo_ceil_log2_array": (None, [P, i64, P]),
+            "rqo_block_scale_array": (None, [P, i64, P]),
+            "rqo_rope_rows": (ctypes.c_int, [P, i64, P, P, i64, ctypes.c_int]),
+            "rqo_quant_rows": (None, [P, i64, ctypes.c_float, P, P]),
+            "rqo_inv_rope_fp8_quant": (ctypes.c_int, [P, i64, i64, i64, i64, P, P, i64, i64,
+                                                      ctypes.c_float, P, P, ctypes.c_int]),
+            "rqo_rope_fp8_quant_insert": (ctypes.c_int, [P, i64, i64, P, P, i64, P, P, i64,
+                                                         i64, i64, ctypes.c_float, ctypes.c_int]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _np(a, dtype):
+    """Contiguous numpy view/copy of a numpy array or CPU torch tensor."""
+    if hasattr(a, "detach"):  # torch tensor
+        import torch
+        t = a.detach().cpu()
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        a = t.numpy()
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        if a.dtype.itemsize == np.dtype(dtype).itemsize and dtype in (np.uint16, np.int16):
+            a = a.view(dtype)
+        else:
+            a = a.astype(dtype)
+    return a
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+# ------------------------------------------------------------------ scalars
+
+def e4m3_encode(v) -> np.ndarray:
+    """OFP8 E4M3 codes of fp32 values (RNE, saturate at 448, NaN -> 0x7F)."""
+    v = _np(v, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _load().rqo_e4m3_encode_f32_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def e4m3_encode_scalar(v: float) -> int:
+    """E4M3 code of one real value given as a Python float (double)."""
+    return int(_load().rqo_e4m3_encode(float(v)))
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Real value (float64) of each E4M3 code; NaN for 0x7F / 0xFF."""
+    c = _np(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().rqo_e4m3_decode_array(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def ceil_log2(r) -> np.ndarray:
+    """Exact ceil(log2(r)) of positive finite fp32 values."""
+    r = _np(r, np.float32)
+    out = np.empty(r.shape, np.int32)
+    _load().rqo_ceil_log2_array(_ptr(r), r.size, _ptr(out))
+    return out
+
+
+def block_scale(amax) -> np.ndarray:
+    """2^ceil(log2(fl32(amax / 448))) for clamped block amax values."""
+    a = _np(amax, np.float32)
+    out = np.empty(a.shape, np.float32)
+    _load().rqo_block_scale_array(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+# ------------------------------------------------------------------ row steps
+
+def rope_rows(rows, positions, cos_sin_cache, inverse: bool) -> np.ndarray:
+    """Rotate the RoPE tail of fp32 rows [R, 512] (a rotated copy is returned)."""
+    y = _np(rows, np.float32).reshape(-1, HEAD_DIM).copy()
+    pos = _np(positions, np.int64).reshape(-1)
+    cs = _np(cos_sin_cache, np.float32)
+    if pos.size != y.shape[0]:
+        raise OracleError("one position per row")
+    rc = _load().rqo_rope_rows(_ptr(y), y.shape[0], _ptr(pos), _ptr(cs), cs.shape[0],
+                               1 if inverse else 0)
+    if rc:
+        raise OracleError(f"rope_rows status {rc}")
+    return y
+
+
+def quant_rows(rows, eps: float = 1e-10):
+    """Block-128 E4M3 quant of fp32 rows [R, 512] -> (codes [R,512] u8, scales [R,4] f32)."""
+    y = _np(rows, np.float32).reshape(-1, HEAD_DIM)
+    codes = np.empty(y.shape, np.uint8)
+    scales = np.empty((y.shape[0], BLOCKS_PER_HEAD), np.float32)
+    _load().rqo_quant_rows(_ptr(y), y.shape[0], float(eps), _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+# ------------------------------------------------------------------ full ops
+
+def inv_rope_fp8_quant(x, positions, cos_sin_cache, heads_per_group: int,
+                       eps: float = 1e-10, threads: int = 1):
+    """Inverse RoPE + block-FP8 quant of x [N, H, 512] bf16.
+
+    Returns (codes [N, G, hpg*512] uint8, scales [N, G, hpg*4] float32),
+    G = H / heads_per_group. ``x`` may be a torch bf16 tensor (any token and
+    head strides are honoured) or a uint16 numpy array of bf16 bit patterns.
+    """
+    if hasattr(x, "detach"):
+        # torch tensor: honour its token / head strides, pass its data pointer
+        t = x.detach().cpu()
+        if t.stride(-1) != 1 or t.shape[-1] != HEAD_DIM:
+            raise OracleError("x must be [N, H, 512] with a contiguous last dim")
+        n, h = t.shape[0], t.shape[1]
+        sx_t, sx_h = t.stride(0), t.stride(1)
+        ptr, keep = t.data_ptr(), t
+    else:
+        arr = _np(x, np.uint16)
+        n, h = arr.shape[0], arr.shape[1]
+        sx_t, sx_h = arr.shape[1] * arr.shape[2], arr.shape[2]
+        ptr, keep = arr.ctypes.data, arr
+    pos = _np(positions, np.int64)
+    cs = _np(cos_sin_cache, np.float32)
+    hpg = int(heads_per_group)
+    if hpg < 1 or h % hpg:
+        raise OracleError("heads_per_group must divide the head count")
+    g = h // hpg
+    codes = np.empty((n, g, hpg * HEAD_DIM), np.uint8)
+    scales = np.empty((n, g, hpg * BLOCKS_PER_HEAD), np.float32)
+    rc = _load().rqo_inv_rope_fp8_quant(ptr, n, h, sx_t, sx_h, _ptr(pos), _ptr(cs), cs.shape[0],
+                                        hpg, float(eps), _ptr(codes), _ptr(scales), int(threads))
+    del keep
+    if rc:
+        raise OracleError(f"rqo_inv_rope_fp8_quant status {rc}")
+    return codes, scales
+
+
+def rope_fp8_quant_insert(kv, positions, cos_sin_cache, slot_mapping, k_cache,
+                          block_size: int, block_stride_bytes: int | None = None,
+                          eps: float = 1e-10, threads: int = 1) -> np.ndarray:
+    """Forward RoPE + block-FP8 quant of kv [N, 512] bf16 into a paged cache.
+
+    ``k_cache`` is a uint8 array [num_blocks, block_bytes]; a copy with the
+    mapped records written is returned (the input is not modified).
+    """
+    a = _np(kv, np.uint16)
+    n = a.shape[0]
+    pos = _np(positions, np.int64)
+    cs = _np(cos_sin_cache, np.float32)
+    slots = _np(slot_mapping, np.int64)
+    cache = _np(k_cache, np.uint8).copy()
+    stride = int(block_stride_bytes if block_stride_bytes is not None else cache.shape[1])
+    rc = _load().rqo_rope_fp8_quant_insert(_ptr(a), n, a.shape[1], _ptr(pos), _ptr(cs),
+                                           cs.shape[0], _ptr(slots), _ptr(cache),
+                                           cache.shape[0], int(block_size), stride,
+                                           float(eps), int(threads))
+    if rc:
+        raise OracleError(f"rqo_rope_fp8_quant_insert status {rc}")
+    return cache

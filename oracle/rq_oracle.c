@@ -1,0 +1,459 @@
+/*
+ * rq_oracle.c -- plain CPU oracle for the inverse-RoPE + block-FP8 quant
+ * epilogue and its forward-RoPE + paged-insert sibling.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is the slow, scalar statement of what the
+ * CUDA library must compute.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline / reference leg load it.  It shares no code,
+ * header, table or helper with the CUDA library, and the library never
+ * calls it.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fPIC -shared
+ *        -pthread rq_oracle.c -lm
+ * (-ffp-contract=off keeps every product and sum separately rounded to
+ * fp32, as the op order below states.)
+ *
+ * Sources, cited by page title and section:
+ *  [INV] "[vllm] 한 프로그램이 4개 head를 처리하게 하라: DeepSeek-V4 inverse
+ *        RoPE + FP8 quant 커널 3.5배 가속기" (analysis of vLLM PR #63540).
+ *        Intro: bf16 [token, head, 512] input, inverse RoPE then block FP8.
+ *        S1 (BLOCK_H): output group g = head // heads_per_group, position
+ *        of the head inside its group, per-head scale slot = 4 * that.
+ *        S2 (register swap): the GPT-J (even, odd) pair rotation of the
+ *        last 64 dims, cos in cache columns 0..31, sin in 32..63.
+ *        S3 (3-D quant): amax over 128-element blocks, clamped below by eps.
+ *  [KV]  "[vllm] vLLM DeepSeek-V4 성능 최적화: Eager Break 시 Workspace 재사용
+ *        개선" (analysis of vLLM PR #49236), S1: kv [N, 512] is rotated,
+ *        quantised and inserted into a paged uint8 k_cache by slot_mapping.
+ *  [IDX] "[vllm] vLLM의 GLM5.2 성능 최적화: Triton 커널 융합을 통한 E2E
+ *        Throughput 향상" (analysis of vLLM PR #46862), S1: the power-of-two
+ *        scale exp2(ceil(log2(raw scale))).
+ *  [OFP8] OCP 8-bit Floating Point Specification (OFP8) rev 1.0: E4M3
+ *        (bias 7, no infinities, S.1111.111 is NaN, max normal 448).
+ *
+ * Readings where the pages are silent (each one is listed in the design
+ * notes of the repository):
+ *  - raw scale = fl32(amax / 448) (the FP8 maximum of E4M3); the exponent is
+ *    the exact ceiling of log2 of that fp32 value;
+ *  - e4m3 encode rounds to nearest, ties to even, and saturates finite and
+ *    infinite magnitudes at 448; NaN encodes as 0x7F; zero keeps its sign;
+ *  - rotation: two separately rounded fp32 products, then one rounded fp32
+ *    add or subtract, in the order the page writes them;
+ *  - the forward rotation (insert sibling) is the rotation by +theta, the
+ *    inverse one by -theta;
+ *  - paged record of one token: 512 code bytes then the 4 fp32 block scales
+ *    (528 bytes) at k_cache + (slot / block_size) * block_stride
+ *    + (slot % block_size) * 528; a negative slot means "skip this token".
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define HEAD_DIM 512        /* [INV] intro: 512-wide heads            */
+#define NOPE_DIM 448        /* [INV] S2: pairs >= NOPE_DIM/2 are RoPE  */
+#define HALF_ROPE 32        /* [INV] S2: sin starts at column 32       */
+#define QUANT_BLOCK 128     /* [INV] S3: QUANT_GROUP_SIZE              */
+#define BLOCKS_PER_HEAD 4   /* [INV] S3: CHUNKS_PER_HEAD = 512 / 128   */
+#define CACHE_WIDTH 64      /* [KV] S1: cos_sin_cache.size(1) == 64    */
+#define RECORD_BYTES 528    /* paged record: 512 codes + 4 fp32 scales */
+#define E4M3_MAX 448.0      /* [OFP8] largest finite E4M3 magnitude    */
+
+/* status codes of the oracle's own argument checks */
+#define RQO_OK 0
+#define RQO_ERR_ARG 1
+#define RQO_ERR_GROUPING 4
+#define RQO_ERR_POSITION 6
+#define RQO_ERR_SLOT 7
+
+/* ---------------------------------------------------------------- scalars */
+
+/* bf16 is the upper half of an IEEE-754 binary32 pattern, so widening is a
+ * 16-bit shift and exact ([INV] S1: the tile is loaded and converted to fp32). */
+float rqo_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* [OFP8] E4M3 decode: s eeee mmm; e == 0 is subnormal m/8 * 2^-6,
+ * otherwise (1 + m/8) * 2^(e-7); s 1111 111 is NaN. */
+double rqo_e4m3_decode(uint8_t c)
+{
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    mag = (e == 0) ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return s ? -mag : mag;
+}
+
+/* [OFP8] E4M3 encode of a real value v (given exactly as a double): round
+ * to the nearest representable value, ties to an even mantissa; magnitudes
+ * at or beyond 448 (and infinities) saturate to 448; NaN -> 0x7F. */
+uint8_t rqo_e4m3_encode(double v)
+{
+    uint8_t sign;
+    double a, quantum, r;
+    int ex, e2;
+
+    if (isnan(v))
+        return 0x7F;
+    sign = signbit(v) ? 0x80 : 0x00;
+    a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    if (a >= E4M3_MAX)
+        return sign | 0x7E;
+    /* a = f * 2^ex2 with f in [0.5, 1): the binade of a is 2^(ex2-1). */
+    frexp(a, &ex);
+    ex -= 1;
+    if (ex < -6)
+        ex = -6;                      /* subnormal binade shares 2^-6's step */
+    quantum = ldexp(1.0, ex - 3);     /* 3 mantissa bits -> 8 steps a binade */
+    r = nearbyint(a / quantum) * quantum; /* a / quantum is exact (power of 2);
+                                             nearbyint rounds ties to even */
+    if (r == 0.0)
+        return sign;
+    if (r >= E4M3_MAX)
+        return sign | 0x7E;
+    frexp(r, &e2);
+    e2 -= 1;
+    if (e2 < -6)                      /* subnormal: m * 2^-9, m = 1..7 */
+        return sign | (uint8_t)(r / ldexp(1.0, -9));
+    return sign | (uint8_t)((e2 + 7) << 3) |
+           (uint8_t)((int)(r / ldexp(1.0, e2 - 3)) - 8);
+}
+
+/* Exact ceil(log2(r)) for finite r > 0.  frexp writes r = f * 2^E with f in
+ * [0.5, 1) (subnormals included, after widening to double); r is a power of
+ * two exactly when f == 0.5, and then log2 r = E - 1; otherwise
+ * E - 1 < log2 r < E. */
+int rqo_ceil_log2(float r)
+{
+    int E;
+    double f = frexp((double)r, &E);
+    return (f == 0.5) ? E - 1 : E;
+}
+
+/* Power-of-two block scale, [IDX] S1 and the [INV] quant step:
+ * scale = 2^ceil(log2(amax / 448)), the division rounded once to fp32.
+ * amax is the already-clamped block absmax (>= eps). */
+float rqo_block_scale(float amax)
+{
+    float raw = amax / 448.0f;
+    return ldexpf(1.0f, rqo_ceil_log2(raw));
+}
+
+/* ------------------------------------------------------------- row steps */
+
+/* [INV] S2 rotation of one 512-wide fp32 row in place.  Pair j (0..31) is
+ * (row[448+2j], row[449+2j]) with cos = cs_row[j], sin = cs_row[32+j].
+ * inverse != 0:  even' = even*cos + odd*sin,  odd' = odd*cos - even*sin
+ * inverse == 0:  even' = even*cos - odd*sin,  odd' = odd*cos + even*sin
+ * Dims 0..447 pass through. */
+void rqo_rope_row(float *row, const float *cs_row, int inverse)
+{
+    int j;
+    for (j = 0; j < HALF_ROPE; ++j) {
+        float even = row[NOPE_DIM + 2 * j];
+        float odd = row[NOPE_DIM + 2 * j + 1];
+        float c = cs_row[j];
+        float s = cs_row[HALF_ROPE + j];
+        float ec = even * c, os = odd * s, oc = odd * c, es = even * s;
+        if (inverse) {
+            row[NOPE_DIM + 2 * j] = ec + os;
+            row[NOPE_DIM + 2 * j + 1] = oc - es;
+        } else {
+            row[NOPE_DIM + 2 * j] = ec - os;
+            row[NOPE_DIM + 2 * j + 1] = oc + es;
+        }
+    }
+}
+
+/* [INV] S3 block quant of one 512-wide fp32 row: for each 128-element block,
+ * amax = max(max |y|, eps), scale = 2^ceil(log2(fl32(amax/448))),
+ * code = E4M3(y / scale).  y / scale is exact in double (scale is a power
+ * of two), so the only rounding is the E4M3 one. */
+void rqo_quant_row(const float *row, float eps, uint8_t *codes, float *scales)
+{
+    int b, k;
+    for (b = 0; b < BLOCKS_PER_HEAD; ++b) {
+        const float *y = row + b * QUANT_BLOCK;
+        float amax = 0.0f, scale;
+        for (k = 0; k < QUANT_BLOCK; ++k) {
+            float m = fabsf(y[k]);
+            if (m > amax)
+                amax = m;
+        }
+        if (amax < eps)
+            amax = eps;
+        scale = rqo_block_scale(amax);
+        scales[b] = scale;
+        for (k = 0; k < QUANT_BLOCK; ++k)
+            codes[b * QUANT_BLOCK + k] =
+                rqo_e4m3_encode((double)y[k] / (double)scale);
+    }
+}
+
+/* ------------------------------------------------------------ array forms */
+
+void rqo_e4m3_encode_f32_array(const float *v, int64_t n, uint8_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = rqo_e4m3_encode((double)v[i]);
+}
+
+void rqo_e4m3_decode_array(const uint8_t *c, int64_t n, double *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = rqo_e4m3_decode(c[i]);
+}
+
+void rqo_ceil_log2_array(const float *r, int64_t n, int32_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = rqo_ceil_log2(r[i]);
+}
+
+void rqo_block_scale_array(const float *amax, int64_t n, float *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = rqo_block_scale(amax[i]);
+}
+
+/* rows: [R, 512] fp32, rotated in place with cache row pos[r] */
+int rqo_rope_rows(float *rows, int64_t R, const int64_t *pos,
+                  const float *cache, int64_t cache_rows, int inverse)
+{
+    int64_t r;
+    for (r = 0; r < R; ++r) {
+        if (pos[r] < 0 || pos[r] >= cache_rows)
+            return RQO_ERR_POSITION;
+        rqo_rope_row(rows + r * HEAD_DIM, cache + pos[r] * CACHE_WIDTH,
+                     inverse);
+    }
+    return RQO_OK;
+}
+
+/* rows: [R, 512] fp32 -> codes [R, 512], scales [R, 4] */
+void rqo_quant_rows(const float *rows, int64_t R, float eps, uint8_t *codes,
+                    float *scales)
+{
+    int64_t r;
+    for (r = 0; r < R; ++r)
+        rqo_quant_row(rows + r * HEAD_DIM, eps, codes + r * HEAD_DIM,
+                      scales + r * BLOCKS_PER_HEAD);
+}
+
+/* --------------------------------------------------------- inverse op */
+
+struct inv_args {
+    const uint16_t *x;
+    int64_t n_heads, sx_t, sx_h;
+    const int64_t *pos;
+    const float *cache;
+    int64_t hpg;
+    float eps;
+    uint8_t *out;
+    float *scales;
+    int64_t t0, t1;
+};
+
+static void *inv_worker(void *p)
+{
+    const struct inv_args *a = (const struct inv_args *)p;
+    const int64_t H = a->n_heads, hpg = a->hpg, G = H / hpg;
+    float row[HEAD_DIM];
+    int64_t t, h;
+    int k;
+    for (t = a->t0; t < a->t1; ++t) {
+        const float *cs_row = a->cache + a->pos[t] * CACHE_WIDTH;
+        for (h = 0; h < H; ++h) {
+            /* [INV] S1: group and place of the head in its group */
+            int64_t g = h / hpg, hig = h % hpg;
+            const uint16_t *src = a->x + t * a->sx_t + h * a->sx_h;
+            /* out [N, G, hpg*512]: head hig of group g owns bytes
+             * [hig*512, hig*512 + 512) of row (t, g) */
+            uint8_t *dst = a->out + ((t * G + g) * hpg + hig) * HEAD_DIM;
+            /* scales [N, G, hpg*4]: block b of that head is qb = hig*4 + b */
+            float *sdst = a->scales + (t * G + g) * (hpg * BLOCKS_PER_HEAD) +
+                          hig * BLOCKS_PER_HEAD;
+            for (k = 0; k < HEAD_DIM; ++k)
+                row[k] = rqo_bf16_to_f32(src[k]);
+            rqo_rope_row(row, cs_row, 1);
+            rqo_quant_row(row, a->eps, dst, sdst);
+        }
+    }
+    return NULL;
+}
+
+static int split_run(void *(*fn)(void *), void *args, size_t arg_size,
+                     int64_t n_tokens, int nthreads,
+                     void (*set_range)(void *, int64_t, int64_t))
+{
+    pthread_t tid[256];
+    int started[256];
+    unsigned char *buf;
+    int i;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    if (nthreads > n_tokens)
+        nthreads = (int)(n_tokens > 0 ? n_tokens : 1);
+    buf = (unsigned char *)malloc(arg_size * (size_t)nthreads);
+    if (!buf)
+        return RQO_ERR_ARG;
+    /* contiguous token ranges; each token's arithmetic does not depend on
+     * which thread runs it */
+    for (i = 0; i < nthreads; ++i) {
+        int64_t t0 = n_tokens * i / nthreads, t1 = n_tokens * (i + 1) / nthreads;
+        void *slot = buf + arg_size * (size_t)i;
+        memcpy(slot, args, arg_size);
+        set_range(slot, t0, t1);
+        started[i] = nthreads > 1 && pthread_create(&tid[i], NULL, fn, slot) == 0;
+        if (!started[i])
+            fn(slot);
+    }
+    for (i = 0; i < nthreads; ++i)
+        if (started[i])
+            pthread_join(tid[i], NULL);
+    free(buf);
+    return RQO_OK;
+}
+
+static void inv_set_range(void *p, int64_t t0, int64_t t1)
+{
+    ((struct inv_args *)p)->t0 = t0;
+    ((struct inv_args *)p)->t1 = t1;
+}
+
+/* Inverse RoPE + block-FP8 quant over a [N, H, 512] bf16 tensor with token
+ * and head strides in elements.  out: [N, H/hpg, hpg*512] E4M3 codes,
+ * scales: [N, H/hpg, hpg*4] fp32, both contiguous.  Tokens are split across
+ * nthreads threads (each token is computed exactly as with one thread). */
+int rqo_inv_rope_fp8_quant(const uint16_t *x, int64_t n_tokens,
+                           int64_t n_heads, int64_t sx_t, int64_t sx_h,
+                           const int64_t *pos, const float *cache,
+                           int64_t cache_rows, int64_t hpg, float eps,
+                           uint8_t *out, float *scales, int nthreads)
+{
+    struct inv_args a;
+    int64_t t;
+    if (n_tokens < 0 || n_heads < 1 || cache_rows < 1 || !(eps > 0.0f))
+        return RQO_ERR_ARG;
+    if (hpg < 1 || n_heads % hpg != 0)
+        return RQO_ERR_GROUPING;
+    if (n_tokens == 0)
+        return RQO_OK;
+    if (!x || !pos || !cache || !out || !scales)
+        return RQO_ERR_ARG;
+    for (t = 0; t < n_tokens; ++t)
+        if (pos[t] < 0 || pos[t] >= cache_rows)
+            return RQO_ERR_POSITION;
+    a.x = x;
+    a.n_heads = n_heads;
+    a.sx_t = sx_t;
+    a.sx_h = sx_h;
+    a.pos = pos;
+    a.cache = cache;
+    a.hpg = hpg;
+    a.eps = eps;
+    a.out = out;
+    a.scales = scales;
+    a.t0 = 0;
+    a.t1 = n_tokens;
+    return split_run(inv_worker, &a, sizeof a, n_tokens, nthreads,
+                     inv_set_range);
+}
+
+/* ---------------------------------------------------------- insert op */
+
+struct ins_args {
+    const uint16_t *kv;
+    int64_t skv;
+    const int64_t *pos;
+    const float *cache;
+    const int64_t *slots;
+    uint8_t *k_cache;
+    int64_t block_size, block_stride;
+    float eps;
+    int64_t t0, t1;
+};
+
+static void *ins_worker(void *p)
+{
+    const struct ins_args *a = (const struct ins_args *)p;
+    float row[HEAD_DIM];
+    float sc[BLOCKS_PER_HEAD];
+    int64_t t;
+    int k;
+    for (t = a->t0; t < a->t1; ++t) {
+        int64_t slot = a->slots[t];
+        uint8_t *rec;
+        if (slot < 0)
+            continue; /* negative slot: token not cached */
+        rec = a->k_cache + (slot / a->block_size) * a->block_stride +
+              (slot % a->block_size) * RECORD_BYTES;
+        for (k = 0; k < HEAD_DIM; ++k)
+            row[k] = rqo_bf16_to_f32(a->kv[t * a->skv + k]);
+        rqo_rope_row(row, a->cache + a->pos[t] * CACHE_WIDTH, 0);
+        rqo_quant_row(row, a->eps, rec, sc);
+        memcpy(rec + HEAD_DIM, sc, sizeof sc);
+    }
+    return NULL;
+}
+
+static void ins_set_range(void *p, int64_t t0, int64_t t1)
+{
+    ((struct ins_args *)p)->t0 = t0;
+    ((struct ins_args *)p)->t1 = t1;
+}
+
+/* Forward RoPE + block-FP8 quant of kv [N, 512] bf16 (token stride skv
+ * elements), each token's 528-byte record written to its slot of the paged
+ * k_cache [num_blocks, block_stride] bytes.  Slots must be distinct. */
+int rqo_rope_fp8_quant_insert(const uint16_t *kv, int64_t n_tokens,
+                              int64_t skv, const int64_t *pos,
+                              const float *cache, int64_t cache_rows,
+                              const int64_t *slots, uint8_t *k_cache,
+                              int64_t num_blocks, int64_t block_size,
+                              int64_t block_stride, float eps, int nthreads)
+{
+    struct ins_args a;
+    int64_t t;
+    if (n_tokens < 0 || cache_rows < 1 || num_blocks < 1 || block_size < 1 ||
+        block_stride < block_size * RECORD_BYTES || !(eps > 0.0f))
+        return RQO_ERR_ARG;
+    if (n_tokens == 0)
+        return RQO_OK;
+    if (!kv || !pos || !cache || !slots || !k_cache)
+        return RQO_ERR_ARG;
+    for (t = 0; t < n_tokens; ++t) {
+        if (pos[t] < 0 || pos[t] >= cache_rows)
+            return RQO_ERR_POSITION;
+        if (slots[t] >= num_blocks * block_size)
+            return RQO_ERR_SLOT;
+    }
+    a.kv = kv;
+    a.skv = skv;
+    a.pos = pos;
+    a.cache = cache;
+    a.slots = slots;
+    a.k_cache = k_cache;
+    a.block_size = block_size;
+    a.block_stride = block_stride;
+    a.eps = eps;
+    a.t0 = 0;
+    a.t1 = n_tokens;
+    return split_run(ins_worker, &a, sizeof a, n_tokens, nthreads,
+                     ins_set_range);
+}

@@ -1,0 +1,467 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Each check is chosen so that a plausible slip in the oracle (a wrong rounding
+rule, an off-by-one exponent, a swapped sign or cos/sin column, a transposed
+head / group index) fails at least one of them:
+
+* E4M3 decode / encode: the OFP8 spec's code points (tests/golden), torch's
+  float8_e4m3fn cast (a library routine) over every fp32 pattern in
+  [2^-12, 448), brute-force nearest search over the 127 finite magnitudes.
+* ceil(log2): exact rational arithmetic (fractions.Fraction) and the defining
+  inequality 2^(e-1) < r <= 2^e over a dense sweep of fp32 patterns.
+* Rotation: complex multiplication by exp(-i*theta) / exp(+i*theta) in
+  complex128 (a library routine), textbook RoPE angles evaluated from the
+  positions, cos=0/sin=1 swap, position-0 identity, forward/inverse round trip.
+* Whole op: hand-built worked cases whose codes and scales follow from the
+  spec by hand, layout fingerprints per (token, group, head), the block-amax
+  invariant 224 <= amax/scale <= 448, the dequantisation error bound.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- E4M3 table
+
+def _spec_points():
+    pts = []
+    with open(os.path.join(GOLDEN, "ofp8_e4m3_points.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            code, val = line.split()
+            pts.append((int(code, 16), val))
+    return pts
+
+
+def test_e4m3_decode_matches_spec_points(oracle_lib):
+    for code, val in _spec_points():
+        got = oracle_lib.e4m3_decode(np.array([code], np.uint8))[0]
+        if val == "nan":
+            assert np.isnan(got), hex(code)
+        elif val == "-0":
+            assert got == 0.0 and np.signbit(got), hex(code)
+        else:
+            assert Fraction(got) == Fraction(val), (hex(code), got, val)
+
+
+def test_e4m3_decode_matches_torch_for_all_codes(oracle_lib):
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle_lib.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_e4m3_roundtrip_every_code(oracle_lib):
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle_lib.e4m3_decode(codes)
+    for c, v in zip(codes, vals):
+        if np.isnan(v):
+            continue
+        assert oracle_lib.e4m3_encode_scalar(v) == c, (hex(c), v)
+
+
+def test_e4m3_encode_matches_torch_dense_sweep(oracle_lib):
+    """Every fp32 pattern with magnitude in [2^-12, 448): 174M values, both signs
+    on a stride. torch's float8_e4m3fn cast rounds to nearest even there."""
+    lo = np.float32(2.0 ** -12).view(np.uint32)
+    hi = np.float32(448.0).view(np.uint32)
+    step = 1 << 24
+    for start in range(int(lo), int(hi), step):
+        bits = np.arange(start, min(start + step, int(hi)), dtype=np.uint32)
+        v = bits.view(np.float32)
+        ours = oracle_lib.e4m3_encode(v)
+        ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        bad = np.nonzero(ours != ref)[0]
+        assert bad.size == 0, (v[bad[:5]], ours[bad[:5]], ref[bad[:5]])
+        neg = -v[::97]
+        ours_n = oracle_lib.e4m3_encode(neg)
+        ref_n = torch.from_numpy(neg).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(ours_n, ref_n)
+
+
+def _nearest_even_bruteforce(a: Fraction, mags):
+    """Nearest finite E4M3 magnitude to a >= 0 by direct search; ties -> even code."""
+    best = None
+    for code, m in mags:
+        d = abs(a - m)
+        if best is None or d < best[0] or (d == best[0] and code % 2 == 0):
+            best = (d, code, m)
+    return best[1]
+
+
+def test_e4m3_encode_bruteforce_nearest(oracle_lib):
+    codes = np.arange(0x7F, dtype=np.uint8)  # 0x00..0x7E: the 127 finite magnitudes
+    mags = [(int(c), Fraction(float(v))) for c, v in zip(codes, oracle_lib.e4m3_decode(codes))]
+    rng = np.random.default_rng(1)
+    samples = [Fraction(0)]
+    # every midpoint between neighbours (the ties), and one fp32 ulp either side
+    for (c0, m0), (c1, m1) in zip(mags[:-1], mags[1:]):
+        mid = (m0 + m1) / 2
+        f = np.float32(float(mid))
+        samples += [mid, Fraction(float(np.nextafter(f, np.float32(0)))),
+                    Fraction(float(np.nextafter(f, np.float32(1e9))))]
+    samples += [Fraction(float(v)) for v in rng.uniform(0, 448, 3000).astype(np.float32)]
+    samples += [Fraction(float(v)) for v in
+                np.exp2(rng.uniform(-14, 8.8, 3000)).astype(np.float32)]
+    for a in samples:
+        f = float(a)
+        assert Fraction(f) == a  # every sample is an exact double
+        want = _nearest_even_bruteforce(a, mags)
+        got = oracle_lib.e4m3_encode_scalar(f)
+        assert got == want, (f, hex(got), hex(want))
+        assert oracle_lib.e4m3_encode_scalar(-f) == (want | 0x80), f
+
+
+@pytest.mark.parametrize("value,code", [
+    (310.0, 0x7A),          # 310 lies between 288 and 320, nearer 320 (S.1111.010)
+    (2.0 ** -10, 0x00),     # tie between 0 and 2^-9 -> even (zero)
+    (3 * 2.0 ** -10, 0x02), # tie between 2^-9 (odd) and 2*2^-9 (even)
+    (460.0, 0x7E),          # above max normal: saturates
+    (1e30, 0x7E),
+    (float("inf"), 0x7E),
+    (float("-inf"), 0xFE),
+    (-1e-9, 0x80),          # negative underflow keeps the sign
+    (-0.0, 0x80),
+    (float("nan"), 0x7F),
+    (17.0, 0x58),           # tie 16 | 18 -> 16 (even mantissa), S.1011.000
+    (19.0, 0x5A),           # tie 18 | 20 -> 20 (even mantissa), S.1011.010
+])
+def test_e4m3_encode_worked_cases(oracle_lib, value, code):
+    assert oracle_lib.e4m3_encode_scalar(value) == code
+
+
+def test_e4m3_encode_saturation_and_tiny(oracle_lib):
+    v = np.array([448.0, 449.0, 463.99, 464.0, 500.0, 3.4e38, 2.0 ** -11, 2.0 ** -30,
+                  1e-45], np.float32)
+    got = oracle_lib.e4m3_encode(v)
+    assert list(got) == [0x7E] * 6 + [0x00] * 3
+    assert list(oracle_lib.e4m3_encode(-v)) == [0xFE] * 6 + [0x80] * 3
+
+
+# ----------------------------------------------------------------- ceil(log2)
+
+def _ceil_log2_exact(r: float) -> int:
+    """Smallest integer e with r <= 2^e, by exact rational comparison."""
+    q = Fraction(r)
+    e = q.numerator.bit_length() - q.denominator.bit_length() - 1
+    while Fraction(2) ** e < q:
+        e += 1
+    while Fraction(2) ** (e - 1) >= q:
+        e -= 1
+    return e
+
+
+def test_ceil_log2_exact_rational(oracle_lib):
+    vals = []
+    for k in range(-149, 128):
+        p = np.float32(2.0 ** k)
+        vals += [p, np.nextafter(p, np.float32(0)), np.nextafter(p, np.float32(np.inf))]
+    rng = np.random.default_rng(2)
+    vals += list(rng.integers(1, 0x7F800000, 20000, dtype=np.uint32).view(np.float32))
+    vals = np.array([v for v in vals if np.isfinite(v) and v > 0], np.float32)
+    got = oracle_lib.ceil_log2(vals)
+    for v, e in zip(vals, got):
+        assert e == _ceil_log2_exact(float(v)), (float(v), e)
+
+
+def test_ceil_log2_defining_inequality_sweep(oracle_lib):
+    """2^(e-1) < r <= 2^e for every 61st positive finite fp32 (all binades)."""
+    bits = np.arange(1, 0x7F800000, 61, dtype=np.uint32)
+    r = bits.view(np.float32)
+    e = oracle_lib.ceil_log2(r).astype(np.int64)
+    r64 = r.astype(np.float64)
+    assert np.all(np.ldexp(1.0, e) >= r64)
+    assert np.all(np.ldexp(1.0, e - 1) < r64)
+
+
+def test_block_scale_closed_forms(oracle_lib):
+    for k in range(-60, 100):
+        amax = np.float32(448.0 * 2.0 ** k)
+        assert oracle_lib.block_scale(np.array([amax]))[0] == np.float32(2.0 ** k)
+        up = np.nextafter(amax, np.float32(np.inf))
+        assert oracle_lib.block_scale(np.array([up]))[0] == np.float32(2.0 ** (k + 1))
+        dn = np.nextafter(amax, np.float32(0))
+        assert oracle_lib.block_scale(np.array([dn]))[0] == np.float32(2.0 ** k)
+
+
+def test_block_scale_is_ceil_pow2_of_rounded_quotient(oracle_lib):
+    rng = np.random.default_rng(3)
+    amax = np.exp2(rng.uniform(-33, 60, 20000)).astype(np.float32)
+    s = oracle_lib.block_scale(amax)
+    for a, sc in zip(amax[:4000], s[:4000]):
+        raw = np.float32(a) / np.float32(448.0)       # fp32 division, RN-even
+        assert Fraction(float(sc)) == Fraction(2) ** _ceil_log2_exact(float(raw))
+    # every scale is a power of two: zero mantissa bits
+    assert np.all((s.view(np.uint32) & 0x7FFFFF) == 0)
+
+
+@pytest.mark.parametrize("eps", [1e-10, 1e-4])
+def test_zero_block_scale_follows_eps(oracle_lib, eps):
+    raw = np.float32(eps) / np.float32(448.0)
+    want = Fraction(2) ** _ceil_log2_exact(float(raw))
+    codes, scales = oracle_lib.quant_rows(np.zeros((1, 512), np.float32), eps=eps)
+    assert np.all(codes == 0)
+    assert all(Fraction(float(s)) == want for s in scales[0])
+    assert {1e-10: -42, 1e-4: -22}[eps] == _ceil_log2_exact(float(raw))
+
+
+# ----------------------------------------------------------------- rotation
+
+def _complex_rotate(rows, positions, cache, inverse):
+    """(even + i odd) * conj(cos + i sin) for inverse, * (cos + i sin) forward."""
+    rows = np.asarray(rows, np.float64)
+    cs = np.asarray(cache, np.float64)[np.asarray(positions)]
+    z = rows[:, 448::2] + 1j * rows[:, 449::2]
+    w = cs[:, :32] + 1j * cs[:, 32:]
+    z = z * (np.conj(w) if inverse else w)
+    out = rows.copy()
+    out[:, 448::2] = z.real
+    out[:, 449::2] = z.imag
+    return out
+
+
+@pytest.mark.parametrize("inverse", [True, False])
+def test_rotation_matches_complex_multiply(oracle_lib, inverse):
+    rng = np.random.default_rng(4)
+    R = 400
+    rows = (rng.standard_normal((R, 512)) * np.exp2(rng.integers(-6, 7, (R, 1)))).astype(np.float32)
+    cache = W.rope_cache(65536).numpy()
+    pos = rng.integers(0, 65536, R)
+    got = oracle_lib.rope_rows(rows, pos, cache, inverse=inverse).astype(np.float64)
+    ref = _complex_rotate(rows, pos, cache, inverse)
+    assert np.array_equal(got[:, :448], rows[:, :448].astype(np.float64))
+    e = rows[:, 448::2].astype(np.float64)
+    o = rows[:, 449::2].astype(np.float64)
+    bound = 2.0 ** -22 * (np.abs(e) + np.abs(o))
+    assert np.all(np.abs(got[:, 448::2] - ref[:, 448::2]) <= bound)
+    assert np.all(np.abs(got[:, 449::2] - ref[:, 449::2]) <= bound)
+
+
+def test_rotation_matches_textbook_angles(oracle_lib):
+    """Forward RoPE rotates pair j by +p*10000^(-j/32), inverse by the negative angle,
+    with the angle computed here from the position (not from the cache)."""
+    rng = np.random.default_rng(5)
+    R = 64
+    rows = rng.standard_normal((R, 512)).astype(np.float32)
+    pos = rng.integers(0, 4096, R)
+    cache = W.rope_cache(4096).numpy()
+    theta = 10000.0 ** (-np.arange(32) / 32.0)
+    ang = pos[:, None] * theta[None, :]
+    z = rows[:, 448::2].astype(np.float64) + 1j * rows[:, 449::2].astype(np.float64)
+    for inverse, sign in ((False, 1.0), (True, -1.0)):
+        got = oracle_lib.rope_rows(rows, pos, cache, inverse=inverse)
+        zr = z * np.exp(1j * sign * ang)
+        assert np.allclose(got[:, 448::2], zr.real, atol=2e-6, rtol=0)
+        assert np.allclose(got[:, 449::2], zr.imag, atol=2e-6, rtol=0)
+
+
+def test_rotation_swap_and_identity(oracle_lib):
+    rng = np.random.default_rng(6)
+    rows = rng.standard_normal((8, 512)).astype(np.float32)
+    rows[0, 448:452] = [-0.0, 0.0, 1.5, -2.25]
+    swap = np.zeros((1, 64), np.float32)
+    swap[0, 32:] = 1.0                         # cos 0, sin 1: rotation by +-90 degrees
+    z = np.zeros(8, np.int64)
+    inv = oracle_lib.rope_rows(rows, z, swap, inverse=True)
+    fwd = oracle_lib.rope_rows(rows, z, swap, inverse=False)
+    assert np.array_equal(inv[:, 448::2], rows[:, 449::2])     # e' = o
+    assert np.array_equal(inv[:, 449::2], -rows[:, 448::2])    # o' = -e
+    assert np.array_equal(fwd[:, 448::2], -rows[:, 449::2])
+    assert np.array_equal(fwd[:, 449::2], rows[:, 448::2])
+    ident = W.rope_cache(1).numpy()            # position 0: cos 1, sin 0
+    for inverse in (True, False):
+        out = oracle_lib.rope_rows(rows, z, ident, inverse=inverse)
+        assert np.array_equal(out, rows)       # equal as values (+0 == -0)
+
+
+def test_rotation_round_trip(oracle_lib):
+    rng = np.random.default_rng(7)
+    rows = rng.standard_normal((256, 512)).astype(np.float32)
+    cache = W.rope_cache(65536).numpy()
+    pos = rng.integers(0, 65536, 256)
+    back = oracle_lib.rope_rows(oracle_lib.rope_rows(rows, pos, cache, False), pos, cache, True)
+    norm = np.hypot(rows[:, 448::2], rows[:, 449::2]).repeat(2, axis=1)
+    assert np.all(np.abs(back[:, 448:] - rows[:, 448:]) <= 2.0 ** -21 * norm + 1e-30)
+    assert np.array_equal(back[:, :448], rows[:, :448])
+
+
+# ----------------------------------------------------------------- whole op
+
+def _bf16(a):
+    return torch.tensor(np.asarray(a, np.float32)).to(torch.bfloat16)
+
+
+def test_worked_case_single_448(oracle_lib):
+    x = np.zeros((1, 1, 512), np.float32)
+    x[0, 0, 5] = 448.0
+    x[0, 0, 130] = -3.0
+    codes, scales = oracle_lib.inv_rope_fp8_quant(_bf16(x), torch.zeros(1, dtype=torch.int64),
+                                                  W.rope_cache(1), 1)
+    assert scales[0, 0, 0] == 1.0                      # 448/448 = 1 = 2^0
+    assert codes[0, 0, 5] == 0x7E
+    assert scales[0, 0, 1] == 2.0 ** -7                # ceil(log2(3/448)) = -7
+    assert codes[0, 0, 130] == 0xFC                    # -3 * 2^7 = -384 = -1.5*2^8
+    expect_zero = Fraction(2) ** _ceil_log2_exact(float(np.float32(1e-10) / np.float32(448)))
+    assert Fraction(float(scales[0, 0, 2])) == expect_zero
+    assert Fraction(float(scales[0, 0, 3])) == expect_zero
+    mask = np.ones(512, bool)
+    mask[[5, 130]] = False
+    assert np.all(codes[0, 0, mask] == 0)
+
+
+def test_worked_case_exact_grid_block(oracle_lib):
+    """A block whose values are E4M3 values times 2^s (max 448*2^s) quantises to
+    exactly those codes with scale 2^s, for every s the bf16 range allows."""
+    rng = np.random.default_rng(8)
+    grid_codes = rng.integers(0, 0x7F, 512).astype(np.uint8)
+    grid_codes[[0, 128, 256, 384]] = 0x7E              # each block holds the max
+    signs = rng.integers(0, 2, 512).astype(np.uint8) << 7
+    grid = oracle_lib.e4m3_decode(grid_codes | signs)
+    for s in (-20, -3, 0, 5, 40):
+        x = (grid * 2.0 ** s).astype(np.float32).reshape(1, 1, 512)
+        assert np.array_equal(_bf16(x).float().numpy(), x)   # bf16-exact
+        codes, scales = oracle_lib.inv_rope_fp8_quant(_bf16(x), torch.zeros(1, dtype=torch.int64),
+                                                      W.rope_cache(1), 1)
+        assert np.all(scales == np.float32(2.0 ** s))
+        want = grid_codes | signs
+        zero = grid_codes == 0     # a rotated -0 may come back as +0: compare magnitudes
+        assert np.array_equal(codes[0, 0][~zero], want[~zero])
+        assert np.all(codes[0, 0][zero] & 0x7F == 0)
+        assert np.array_equal(codes[0, 0, :448][zero[:448]], signs[:448][zero[:448]])
+
+
+def test_layout_fingerprint_groups(oracle_lib):
+    """Token t, head h filled with 2^(h + 2t - 12): scale 2^(h + 2t - 20); codes all
+    equal. The scale of every (t, g, hig*4+b) slot identifies which head landed there."""
+    N, H, hpg = 3, 12, 4
+    G = H // hpg
+    x = np.zeros((N, H, 512), np.float32)
+    for t in range(N):
+        for h in range(H):
+            x[t, h] = 2.0 ** (h + 2 * t - 12)
+    codes, scales = oracle_lib.inv_rope_fp8_quant(_bf16(x), torch.zeros(N, dtype=torch.int64),
+                                                  W.rope_cache(1), hpg)
+    assert codes.shape == (N, G, hpg * 512) and scales.shape == (N, G, hpg * 4)
+    for t in range(N):
+        for g in range(G):
+            for hig in range(hpg):
+                h = g * hpg + hig
+                for b in range(4):
+                    # 2^k / 448 -> ceil(log2) = k - 8 (448 = 1.75 * 2^8)
+                    assert scales[t, g, hig * 4 + b] == np.float32(2.0 ** (h + 2 * t - 12 - 8))
+    assert np.all(codes == 0x78)   # value / scale = 2^8 = 256 -> S.1111.000
+
+
+def test_strided_input_and_batch_invariance(oracle_lib):
+    spec = W.InverseSpec("t", 24, 6, 3, 4096, "uniform", True, seed=11)
+    inp = W.inverse_inputs(spec)
+    x = inp["x"]
+    c_ref, s_ref = oracle_lib.inv_rope_fp8_quant(x, inp["positions"], inp["cos_sin_cache"], 3)
+    # head-major storage viewed token-major: token stride 512, head stride N*512
+    xt = x.transpose(0, 1).contiguous().transpose(0, 1)
+    c2, s2 = oracle_lib.inv_rope_fp8_quant(xt, inp["positions"], inp["cos_sin_cache"], 3)
+    assert np.array_equal(c_ref, c2) and np.array_equal(s_ref, s2)
+    # padded heads: a slice of a wider buffer
+    wide = torch.zeros(24, 9, 512, dtype=torch.bfloat16)
+    wide[:, 2:8] = x
+    c3, s3 = oracle_lib.inv_rope_fp8_quant(wide[:, 2:8], inp["positions"], inp["cos_sin_cache"], 3)
+    assert np.array_equal(c_ref, c3) and np.array_equal(s_ref, s3)
+    # batch invariance: tokens 5..12 alone give the same rows
+    c4, s4 = oracle_lib.inv_rope_fp8_quant(x[5:13], inp["positions"][5:13], inp["cos_sin_cache"], 3)
+    assert np.array_equal(c_ref[5:13], c4) and np.array_equal(s_ref[5:13], s4)
+    # threads do not change anything
+    c5, s5 = oracle_lib.inv_rope_fp8_quant(x, inp["positions"], inp["cos_sin_cache"], 3, threads=5)
+    assert np.array_equal(c_ref, c5) and np.array_equal(s_ref, s5)
+
+
+def test_grouping_is_a_view(oracle_lib):
+    """With contiguous outputs every heads_per_group gives the same bytes."""
+    inp = W.inverse_inputs(W.InverseSpec("t", 4, 24, 1, 4096, "uniform", True, seed=12))
+    ref = None
+    for hpg in (1, 2, 3, 4, 6, 8, 12, 24):
+        c, s = oracle_lib.inv_rope_fp8_quant(inp["x"], inp["positions"], inp["cos_sin_cache"], hpg)
+        cur = (c.reshape(4, -1).copy(), s.reshape(4, -1).copy())
+        if ref is None:
+            ref = cur
+        assert np.array_equal(cur[0], ref[0]) and np.array_equal(cur[1], ref[1])
+
+
+def test_op_invariants(oracle_lib):
+    """Whole-op properties on the tiny workload: the rotated rows (pinned above
+    against complex multiplication) quantise with 224 <= amax/scale <= 448,
+    power-of-two scales, and |decode(code) - y/scale| <= half an E4M3 step."""
+    inp = W.inverse_inputs(W.TINY)
+    x, pos, cache = inp["x"], inp["positions"], inp["cos_sin_cache"]
+    codes, scales = oracle_lib.inv_rope_fp8_quant(x, pos, cache, 8)
+    N, H = x.shape[:2]
+    rows = x.float().numpy().reshape(N * H, 512)
+    y = oracle_lib.rope_rows(rows, np.repeat(pos.numpy(), H), cache.numpy(), True)
+    y = y.astype(np.float64)
+    sc = scales.reshape(N * H, 4).astype(np.float64)
+    assert np.all((scales.view(np.uint32) & 0x7FFFFF) == 0)
+    amax = np.abs(y).reshape(N * H, 4, 128).max(axis=2)
+    ratio = amax / sc
+    assert np.all(ratio <= 448.0 * (1 + 2.0 ** -22)) and np.all(ratio >= 224.0 * (1 - 2.0 ** -22))
+    deq = oracle_lib.e4m3_decode(codes.reshape(N * H, 512)).reshape(N * H, 4, 128)
+    yb = y.reshape(N * H, 4, 128) / sc[:, :, None]
+    # half-step of the E4M3 grid at |v|: 2^(max(floor(log2|v|), -6) - 4)
+    ex = np.floor(np.log2(np.maximum(np.abs(yb), 2.0 ** -30)))
+    half = np.exp2(np.maximum(ex, -6) - 4)
+    assert np.all(np.abs(deq - yb) <= half)
+    # the worst case is reached: the bound is not loose by a factor of two
+    assert np.max(np.abs(deq - yb) / half) > 0.9
+
+
+def test_tiny_workload_digest_is_stable(oracle_lib):
+    """Regression pin: the committed digest of the oracle's output on the tiny
+    workload (written by tests/golden/make_golden.py, which calls only the oracle)."""
+    import hashlib
+    inp = W.inverse_inputs(W.TINY)
+    codes, scales = oracle_lib.inv_rope_fp8_quant(inp["x"], inp["positions"],
+                                                  inp["cos_sin_cache"], 8)
+    h = hashlib.sha256(codes.tobytes() + scales.tobytes()).hexdigest()
+    with open(os.path.join(GOLDEN, "tiny_oracle_digest.txt")) as f:
+        want = [l.split()[1] for l in f if l.startswith("inverse")][0]
+    assert h == want
+
+
+# ----------------------------------------------------------------- insert op
+
+def test_insert_placement_and_sentinel(oracle_lib):
+    spec = W.InsertSpec("t", 40, 4096, 6, 8, seed=13)
+    inp = W.insert_inputs(spec)
+    slots = inp["slot_mapping"].clone()
+    slots[3] = -1                                    # skipped token
+    pad = 64                                         # block stride with padding
+    bs = spec.block_size
+    k_cache = torch.full((spec.num_blocks, bs * 528 + pad), 0xA5, dtype=torch.uint8)
+    out = oracle_lib.rope_fp8_quant_insert(inp["kv"], inp["positions"], inp["cos_sin_cache"],
+                                           slots, k_cache, bs)
+    rows = inp["kv"].float().numpy()
+    y = oracle_lib.rope_rows(rows, inp["positions"].numpy(), inp["cos_sin_cache"].numpy(), False)
+    codes, scales = oracle_lib.quant_rows(y)
+    touched = np.zeros(out.shape, bool)
+    for t, s in enumerate(slots.tolist()):
+        if s < 0:
+            continue
+        b, o = divmod(s, bs)
+        rec = out[b, o * 528:(o + 1) * 528]
+        touched[b, o * 528:(o + 1) * 528] = True
+        assert np.array_equal(rec[:512], codes[t])
+        assert np.array_equal(rec[512:].view(np.float32), scales[t])
+    assert np.all(out[~touched] == 0xA5)
+    # the forward rotation is the +theta one (complex pin)
+    ref = _complex_rotate(rows, inp["positions"].numpy(), inp["cos_sin_cache"].numpy(), False)
+    assert np.allclose(y, ref, atol=1e-5, rtol=0)

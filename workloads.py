@@ -1,0 +1,144 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests / bench and the oracle.
+
+This module only draws inputs; it holds none of the method's arithmetic (no
+rotation, no scale, no FP8 encoding). Every tensor is created on the CPU with
+a ``torch.Generator`` seeded explicitly, in a fixed draw order:
+
+1. ``x = randn(shape)`` (fp32),
+2. where outliers apply: ``m = rand(shape) < 0.01`` and ``x = where(m, 50 x, x)``,
+3. ``x`` cast to bf16 (round to nearest even),
+4. positions (when drawn), then slots (when drawn).
+
+The cos/sin cache is an input of the op, not part of it: row p holds
+``cos(p * theta_j)`` in columns 0..31 and ``sin(p * theta_j)`` in 32..63 with
+``theta_j = 10000 ** (-j / 32)``, evaluated in float64 and rounded to fp32
+(the RoPE cache layout of the DeepSeek-V4 inverse-RoPE page, S2: cos at
+column j, sin at column 32 + j).
+
+Workloads (named by what they are):
+
+* ``tiny``       N=64, H=8, heads_per_group=8, positions U[0,4096), cache 4096 rows.
+* ``prefill16k`` N=16384, H=32, heads_per_group=8, positions 0..16383, cache 65536.
+* ``decode``     N in {1,...,64}, H=32, heads_per_group=8, no outliers,
+                 positions U[0,65536), cache 65536.
+* ``irregular``  N=8192, H=24, heads_per_group=6, positions U[0,32768), cache 32768.
+* ``insert16k``  kv [16384, 512], positions 0..16383, cache 65536,
+                 slots = randperm(512*64)[:N], paged cache 512 blocks x 64 slots x 528 B.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+HEAD_DIM = 512
+CACHE_WIDTH = 64
+RECORD_BYTES = 528
+ROPE_BASE = 10000.0
+OUTLIER_RATE = 0.01
+OUTLIER_GAIN = 50.0
+
+
+@dataclass(frozen=True)
+class InverseSpec:
+    name: str
+    n_tokens: int
+    n_heads: int
+    heads_per_group: int
+    cache_rows: int
+    positions: str          # "arange" or "uniform"
+    outliers: bool
+    seed: int = 0
+
+
+@dataclass(frozen=True)
+class InsertSpec:
+    name: str
+    n_tokens: int
+    cache_rows: int
+    num_blocks: int
+    block_size: int
+    seed: int = 0
+
+
+TINY = InverseSpec("tiny", 64, 8, 8, 4096, "uniform", True)
+PREFILL16K = InverseSpec("prefill16k", 16384, 32, 8, 65536, "arange", True)
+IRREGULAR = InverseSpec("irregular", 8192, 24, 6, 32768, "uniform", True)
+DECODE_TOKENS = (1, 2, 4, 8, 16, 32, 64)
+INSERT16K = InsertSpec("insert16k", 16384, 65536, 512, 64)
+
+
+def decode_spec(n_tokens: int) -> InverseSpec:
+    return InverseSpec(f"decode{n_tokens}", n_tokens, 32, 8, 65536, "uniform", False)
+
+
+# (H, groups) pairs the inverse-RoPE page's test parametrisation lists (S5);
+# heads_per_group = H / groups.
+PAGE_TEST_SHAPES = ((64, 8), (32, 4), (128, 8), (24, 4))
+
+
+def rope_cache(rows: int, base: float = ROPE_BASE) -> torch.Tensor:
+    """[rows, 64] fp32 cos/sin cache: cos(p*theta_j) | sin(p*theta_j), float64 then fp32."""
+    half = CACHE_WIDTH // 2
+    j = torch.arange(half, dtype=torch.float64)
+    theta = base ** (-j / half)
+    ang = torch.arange(rows, dtype=torch.float64)[:, None] * theta[None, :]
+    return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32).contiguous()
+
+
+def _activations(gen: torch.Generator, shape, outliers: bool) -> torch.Tensor:
+    x = torch.randn(shape, generator=gen, dtype=torch.float32)
+    if outliers:
+        m = torch.rand(shape, generator=gen) < OUTLIER_RATE
+        x = torch.where(m, x * OUTLIER_GAIN, x)
+    return x.to(torch.bfloat16)
+
+
+def inverse_inputs(spec: InverseSpec, cache: torch.Tensor | None = None) -> dict:
+    """x [N,H,512] bf16, positions [N] int64, cos_sin_cache [P,64] fp32 (all CPU)."""
+    gen = torch.Generator().manual_seed(spec.seed)
+    x = _activations(gen, (spec.n_tokens, spec.n_heads, HEAD_DIM), spec.outliers)
+    if spec.positions == "arange":
+        pos = torch.arange(spec.n_tokens, dtype=torch.int64)
+    else:
+        pos = torch.randint(0, spec.cache_rows, (spec.n_tokens,), generator=gen,
+                            dtype=torch.int64)
+    if cache is None:
+        cache = rope_cache(spec.cache_rows)
+    return {"x": x, "positions": pos, "cos_sin_cache": cache,
+            "heads_per_group": spec.heads_per_group}
+
+
+def insert_inputs(spec: InsertSpec, cache: torch.Tensor | None = None,
+                  fill: int = 0xA5) -> dict:
+    """kv [N,512] bf16, positions, slot_mapping (distinct), k_cache filled with ``fill``."""
+    gen = torch.Generator().manual_seed(spec.seed)
+    kv = _activations(gen, (spec.n_tokens, HEAD_DIM), False)
+    pos = torch.arange(spec.n_tokens, dtype=torch.int64)
+    n_slots = spec.num_blocks * spec.block_size
+    slots = torch.randperm(n_slots, generator=gen)[: spec.n_tokens].to(torch.int64)
+    if cache is None:
+        cache = rope_cache(spec.cache_rows)
+    block_bytes = spec.block_size * RECORD_BYTES
+    k_cache = torch.full((spec.num_blocks, block_bytes), fill, dtype=torch.uint8)
+    return {"kv": kv, "positions": pos, "cos_sin_cache": cache, "slot_mapping": slots,
+            "k_cache": k_cache, "block_size": spec.block_size}
+
+
+def inverse_bytes(n_tokens: int, n_heads: int) -> int:
+    """Algorithmic HBM bytes of one inverse op: x read, codes + scales written,
+    positions and one 256-byte cos/sin row read per token."""
+    per_head = HEAD_DIM * 2 + HEAD_DIM + 4 * 4
+    per_token = 8 + CACHE_WIDTH * 4
+    return n_tokens * (n_heads * per_head + per_token)
+
+
+def insert_bytes(n_tokens: int) -> int:
+    """Algorithmic bytes of one insert op: kv read, position + slot + cos/sin row
+    read, one 528-byte record written per token."""
+    return n_tokens * (HEAD_DIM * 2 + 8 + 8 + CACHE_WIDTH * 4 + RECORD_BYTES)
+
+
+def ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
