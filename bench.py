@@ -1,0 +1,443 @@
+"""Benchmark of the inverse-RoPE + block-FP8 quant hot path on one or more GPUs.
+
+One step = one pass of the whole hot path over one batch of seeded synthetic
+input resident in HBM:
+  1. inverse RoPE + block-FP8 quant of the DeepSeek-V4-Flash TP2 prefill shape
+     (x [16384, 32, 512] bf16, heads_per_group 8, positions 0..16383,
+     cos/sin cache [65536, 64]),
+  2. forward RoPE + FP8 quant + paged insert of kv [16384, 512] into a
+     512-block x 64-slot cache (slots: a seeded permutation of the 32768 slots).
+``value`` = algorithmic bytes of the step (every tensor read or written once)
+/ step time, in GB/s, summed over ranks (each rank runs its own full copy:
+weak scaling, no collective on the data path).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (the plain C statement of the op)
+on the host cores over a bounded sample of the same workload.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "µs and achieved HBM GB/s (% of B300 peak) at N=16384,H=32,D=512"
+INV_SPEC = W.PREFILL16K
+INS_SPEC = W.INSERT16K
+INV_BYTES = W.inverse_bytes(INV_SPEC.n_tokens, INV_SPEC.n_heads)
+INS_BYTES = W.insert_bytes(INS_SPEC.n_tokens)
+STEP_BYTES = INV_BYTES + INS_BYTES
+L2_BYTES = 126 * 2 ** 20
+FALLBACK_HBM_GBS = 6400.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps of the host-buffer end-to-end leg (default min(steps, 20))")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--inv-tokens", type=int, default=None,
+                    help="tokens of the inverse op (default 16384; smaller cases are for "
+                         "profiling captures and are not bench lines)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons of one GPU through NVML (reads only)."""
+
+    REASONS = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+        0x100: "display_clock_setting",
+    }
+
+    def __init__(self, device_index: int, period_s: float = 0.01):
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.error = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            bus = torch.cuda.get_device_properties(device_index).pci_bus_id \
+                if hasattr(torch.cuda.get_device_properties(device_index), "pci_bus_id") else None
+            if bus:
+                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+            else:
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.nv = pynvml
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # no NVML: report that instead of clocks
+            self.nv = None
+            self.error = f"{type(e).__name__}: {e}"
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                self.reasons |= nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+            except Exception as e:
+                self.error = f"{type(e).__name__}: {e}"
+                return
+            self._stop.wait(self.period)
+
+    def __enter__(self):
+        if self.nv is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread:
+            self._thread.join()
+
+    def summary(self):
+        if self.nv is None or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "error": self.error or "no samples"}
+        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def make_inputs(inv_tokens=None):
+    cache = W.rope_cache(INV_SPEC.cache_rows)
+    spec = INV_SPEC
+    if inv_tokens:
+        spec = W.InverseSpec(f"prefill{inv_tokens}", inv_tokens, INV_SPEC.n_heads,
+                             INV_SPEC.heads_per_group, INV_SPEC.cache_rows, "arange", True)
+    inv = W.inverse_inputs(spec, cache=cache)
+    ins = W.insert_inputs(INS_SPEC, cache=cache)
+    return inv, ins
+
+
+def cpu_baseline(inv, ins):
+    """The oracle, as it stands, on the host cores over one full step of the workload."""
+    import oracle
+    threads = os.cpu_count() or 1
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.inv_rope_fp8_quant(inv["x"], inv["positions"], inv["cos_sin_cache"],
+                              inv["heads_per_group"], threads=threads)
+    oracle.rope_fp8_quant_insert(ins["kv"], ins["positions"], ins["cos_sin_cache"],
+                                 ins["slot_mapping"], ins["k_cache"], ins["block_size"],
+                                 threads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": round(STEP_BYTES / dt / 1e9, 3), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": "one full step: inverse 16384 tok x 32 heads + insert 16384 tok"}
+
+
+def run_ours(args, world, rank, local):
+    import rope_block_fp8_inverse_b300 as rq
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inv_h, ins_h = make_inputs(args.inv_tokens)
+    inv_bytes = W.inverse_bytes(inv_h["x"].shape[0], inv_h["x"].shape[1])
+    step_bytes = inv_bytes + INS_BYTES
+
+    # device-resident inputs and caller-owned outputs
+    x = inv_h["x"].to(dev)
+    pos = inv_h["positions"].to(dev)
+    cache = inv_h["cos_sin_cache"].to(dev)
+    hpg = inv_h["heads_per_group"]
+    n, h = x.shape[0], x.shape[1]
+    out = torch.empty((n, h // hpg, hpg * 512), dtype=torch.uint8, device=dev)
+    scales = torch.empty((n, h // hpg, hpg * 4), dtype=torch.float32, device=dev)
+    kv = ins_h["kv"].to(dev)
+    kpos = ins_h["positions"].to(dev)
+    slots = ins_h["slot_mapping"].to(dev)
+    k_cache = ins_h["k_cache"].to(dev)
+    bs = ins_h["block_size"]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        rq.inv_rope_fp8_quant(x, pos, cache, hpg, out=out, scales=scales)
+        rq.rope_fp8_quant_insert(kv, kpos, cache, slots, k_cache, bs)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # per-launch timing of the dominant kernel (events on the launching stream)
+    inv_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with sampler:
+        start.record(stream)
+        for i in range(args.steps):
+            inv_ev[i][0].record(stream)
+            rq.inv_rope_fp8_quant(x, pos, cache, hpg, out=out, scales=scales)
+            inv_ev[i][1].record(stream)
+            rq.rope_fp8_quant_insert(kv, kpos, cache, slots, k_cache, bs)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    total_ms = max_over_ranks(start.elapsed_time(end), world)
+    inv_ms = statistics.fmean(a.elapsed_time(b) for a, b in inv_ev)
+    inv_ms_med = statistics.median(a.elapsed_time(b) for a, b in inv_ev)
+    ms_step = total_ms / args.steps
+
+    # end to end through the public API from pinned host buffers
+    e2e_steps = args.e2e_steps or min(args.steps, 20)
+    x_host = inv_h["x"].pin_memory()
+    pos_host = inv_h["positions"].pin_memory()
+    kv_host = ins_h["kv"].pin_memory()
+    kpos_host = ins_h["positions"].pin_memory()
+    slots_host = ins_h["slot_mapping"].pin_memory()
+    out_host = torch.empty(out.shape, dtype=torch.uint8).pin_memory()
+    scales_host = torch.empty(scales.shape, dtype=torch.float32).pin_memory()
+    kc_host = torch.empty(k_cache.shape, dtype=torch.uint8).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (x_host, pos_host, kv_host, kpos_host, slots_host))
+    d2h = sum(t.numel() * t.element_size() for t in (out_host, scales_host, kc_host))
+
+    def e2e_step():
+        x.copy_(x_host, non_blocking=True)
+        pos.copy_(pos_host, non_blocking=True)
+        kv.copy_(kv_host, non_blocking=True)
+        kpos.copy_(kpos_host, non_blocking=True)
+        slots.copy_(slots_host, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+        scales_host.copy_(scales, non_blocking=True)
+        kc_host.copy_(k_cache, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+
+    peak, peak_src = measured_peaks()
+    achieved = inv_bytes / (inv_ms * 1e-3) / 1e9
+    traffic = _committed_traffic()
+    result = {
+        "metric": METRIC,
+        "value": round(world * step_bytes / (ms_step * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms_step, 5),
+        "us_per_step": round(ms_step * 1e3, 2),
+        "inverse_us": round(inv_ms * 1e3, 2),
+        "inverse_us_median": round(inv_ms_med * 1e3, 2),
+        "insert_us": round((ms_step - inv_ms) * 1e3, 2),
+        "frac_of_nominal_8tbs": round(step_bytes / (ms_step * 1e-3) / 8e12, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in, fp32 math, e4m3 out",
+        "data": "synthetic (seeded: randn + 1% x50 outliers, bf16)",
+        "config": {
+            "workload": "prefill16k inverse RoPE+FP8 quant (N=16384,H=32,hpg=8,D=512) "
+                        "+ insert16k forward RoPE+FP8 paged insert (N=16384, 512x64 slots)",
+            "bytes_per_step": step_bytes,
+            "inverse_bytes": inv_bytes,
+            "insert_bytes": INS_BYTES,
+            "l2": f"inputs larger than L2: {step_bytes / 2**20:.0f} MiB streamed per step "
+                  f"vs {L2_BYTES / 2**20:.0f} MiB L2",
+            "parallelism": f"replicas x{world} (each rank its own full step)",
+        },
+        "roofline": {
+            "kernel": "inv_rope_fp8_quant_kernel",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                           else "fallback 6.4 TB/s",
+            "algorithmic_bytes_per_launch": inv_bytes,
+        },
+        "e2e": {
+            "value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 3),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_ms, 3),
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "steps": e2e_steps,
+            "path": "pinned host -> device copies, both C-ABI calls, device -> pinned host",
+        },
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(),
+    }
+    if args.inv_tokens and args.inv_tokens != INV_SPEC.n_tokens:
+        result["config"]["workload"] = (f"profiling case: inverse N={args.inv_tokens},H=32,hpg=8 "
+                                        "+ insert16k (not the benchmarked configuration)")
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(inv_h, ins_h)
+    return result
+
+
+def _committed_traffic():
+    """dram bytes per launch of the inverse kernel from the committed ncu summary
+    (profiles/inv_rope_fp8_quant_prefill16k.md), or None when absent."""
+    path = os.path.join(ROOT, "profiles", "inv_rope_fp8_quant_prefill16k.md")
+    try:
+        with open(path) as f:
+            for line in f:
+                if line.startswith("traffic_bytes_per_launch:"):
+                    v = line.split(":", 1)[1].strip()
+                    return None if v in ("", "null") else int(float(v))
+    except OSError:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, world, rank):
+    """The CPU oracle timed on the host cores, on a bounded sample per step."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    inv_h, ins_h = make_inputs()
+    total_steps = args.steps + max(3, args.warmup)
+    # ~13 us of CPU per (token, head) row: size the sample so the run takes ~60 s
+    budget_rows = 60.0 * threads / 13e-6 / max(1, total_steps)
+    tokens = int(max(1, min(INV_SPEC.n_tokens, budget_rows // (INV_SPEC.n_heads + 1))))
+    xi, pi = inv_h["x"][:tokens].contiguous(), inv_h["positions"][:tokens].contiguous()
+    kv, kp, sl = (ins_h["kv"][:tokens].contiguous(), ins_h["positions"][:tokens].contiguous(),
+                  ins_h["slot_mapping"][:tokens].contiguous())
+    cache = inv_h["cos_sin_cache"]
+    sample_bytes = W.inverse_bytes(tokens, INV_SPEC.n_heads) + W.insert_bytes(tokens)
+
+    def step():
+        oracle.inv_rope_fp8_quant(xi, pi, cache, inv_h["heads_per_group"], threads=threads)
+        oracle.rope_fp8_quant_insert(kv, kp, cache, sl, ins_h["k_cache"], ins_h["block_size"],
+                                     threads=threads)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = round(sample_bytes / dt / 1e9, 4)
+    sample = (f"first {tokens} tokens of each op per step (inverse {tokens}x32 heads, "
+              f"insert {tokens}); oracle with {threads} threads")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(dt * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in, fp32 math, e4m3 out",
+        "data": "synthetic (seeded: randn + 1% x50 outliers, bf16)",
+        "config": {"workload": "prefill16k + insert16k (bounded sample, see cpu_baseline)",
+                   "sample_tokens": tokens, "bytes_per_step": sample_bytes},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        # CPU arm: rank 0 alone times the oracle; other ranks exit without work
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return 0
+    world, rank, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    res = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

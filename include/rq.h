@@ -1,0 +1,139 @@
+/*
+ * rq.h -- C ABI of the B300 (sm_103a) inverse-RoPE + block-FP8 quant library.
+ *
+ * Two operations, both from the DeepSeek-V4 attention path described on these
+ * pages (cited by title and section):
+ *
+ *  [INV] "[vllm] 한 프로그램이 4개 head를 처리하게 하라: DeepSeek-V4 inverse
+ *        RoPE + FP8 quant 커널 3.5배 가속기" (analysis of vLLM PR #63540):
+ *        intro (the op and its [token, head, 512] bf16 input), S1 (output
+ *        groups of heads_per_group heads, per-head scale slots), S2 (GPT-J
+ *        pair rotation of dims 448..511 from a [P, 64] cos|sin cache), S3
+ *        (128-element block amax clamped by eps).
+ *  [KV]  "[vllm] vLLM DeepSeek-V4 성능 최적화: Eager Break 시 Workspace 재사용
+ *        개선" (analysis of vLLM PR #49236), S1-S2: kv [N, 512] is rotated,
+ *        quantised and inserted into a paged uint8 k_cache by slot_mapping;
+ *        outputs are preallocated by the caller (the `_out` form, void return).
+ *  [IDX] "[vllm] vLLM의 GLM5.2 성능 최적화: Triton 커널 융합을 통한 E2E
+ *        Throughput 향상" (analysis of vLLM PR #46862), S1: power-of-two
+ *        scale exp2(ceil(log2(raw scale))).
+ *
+ * Numerics shared by both operations (all fp32):
+ *   y = float(x)                                   (bf16 -> fp32, exact)
+ *   pair j = (y[448+2j], y[449+2j]), c = cache[p][j], s = cache[p][32+j]:
+ *     inverse: even' = even*c + odd*s,  odd' = odd*c - even*s
+ *     forward: even' = even*c - odd*s,  odd' = odd*c + even*s
+ *     (each product and each sum rounded to fp32 separately, no FMA)
+ *   per 128-element block b: amax = max(max|y'|, eps),
+ *     scale = 2^ceil(log2(fl32(amax / 448))), exactly (a power of two),
+ *     code  = e4m3fn(y' / scale): round to nearest even, saturate at +-448.
+ *
+ * Conventions:
+ *  - The caller allocates every buffer; the library allocates nothing and
+ *    keeps no state beyond a per-device cache of launch limits.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls
+ *    are asynchronous and stream-ordered; nothing synchronises.
+ *  - The return value reports host-side argument checks, or a launch error
+ *    from cudaGetLastError (RQ_ERR_CUDA; the CUDA error is then cleared).
+ *    On any error nothing is launched and no buffer is touched.
+ *  - Device-side index checks: a token whose position is outside
+ *    [0, cache_rows), or whose slot is >= num_blocks * block_size, is
+ *    skipped (its outputs are left untouched) and the matching bit is OR-ed
+ *    into *error_flags (RQ_FLAG_*) when error_flags is not NULL. No kernel
+ *    traps or waits.
+ *  - NaN / Inf inputs are outside the contract: results are unspecified
+ *    but no memory access depends on them.
+ *  - Every pointer is a device pointer (or managed / mapped memory the
+ *    device can reach) on the current device.
+ */
+#ifndef RQ_H_
+#define RQ_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rq_status {
+    RQ_OK = 0,
+    RQ_ERR_NULL = 1,     /* a required pointer is NULL                      */
+    RQ_ERR_SHAPE = 2,    /* a size or stride is out of range                */
+    RQ_ERR_ALIGN = 3,    /* a pointer or stride breaks the 16-byte rule     */
+    RQ_ERR_GROUPING = 4, /* heads_per_group < 1 or does not divide n_heads  */
+    RQ_ERR_CUDA = 5,     /* the CUDA runtime reported an error              */
+    RQ_ERR_ARG = 6       /* eps outside [2^-100, 2^100] or not finite       */
+} rq_status;
+
+/* device-side error bits (OR-ed into *error_flags) */
+#define RQ_FLAG_POSITION_RANGE 1u /* a position was outside [0, cache_rows)   */
+#define RQ_FLAG_SLOT_RANGE 2u     /* a slot was >= num_blocks * block_size    */
+
+/* Static, NUL-terminated description of a status code. */
+const char *rq_status_string(int status);
+
+/* Library ABI version, (major << 16) | minor. */
+int rq_version(void);
+
+/*
+ * Inverse RoPE + block-FP8 quant ([INV] intro, S1-S3).
+ *
+ *  x_bf16          [n_tokens, n_heads, 512] bf16; element (t, h, k) at
+ *                  x_bf16 + t*x_stride_token + h*x_stride_head + k
+ *                  (strides in elements; the last dim is contiguous).
+ *                  Base 16-byte aligned, both strides multiples of 8.
+ *  positions       [n_tokens] int64, 8-byte aligned; row of the cache.
+ *  cos_sin_cache   [cache_rows, 64] fp32 contiguous, 16-byte aligned:
+ *                  columns 0..31 cos, 32..63 sin.
+ *  heads_per_group >= 1, divides n_heads; G = n_heads / heads_per_group.
+ *  eps             lower clamp of every block amax, in [2^-100, 2^100].
+ *  out_fp8         [n_tokens, G, heads_per_group*512] e4m3fn codes,
+ *                  contiguous, 16-byte aligned: head h = g*hpg + i of token
+ *                  t owns bytes [i*512, i*512+512) of row (t, g).
+ *  out_scales      [n_tokens, G, heads_per_group*4] fp32, contiguous,
+ *                  16-byte aligned: block b of that head at i*4 + b.
+ *  error_flags     optional device uint32 (may be NULL), see RQ_FLAG_*.
+ *  stream          cudaStream_t.
+ *
+ * n_tokens == 0 returns RQ_OK with no launch. n_tokens * n_heads must be
+ * below 2^31.
+ */
+rq_status rq_inv_rope_fp8_quant(const void *x_bf16, int64_t n_tokens, int64_t n_heads,
+                                int64_t x_stride_token, int64_t x_stride_head,
+                                const int64_t *positions, const float *cos_sin_cache,
+                                int64_t cache_rows, int64_t heads_per_group, float eps,
+                                uint8_t *out_fp8, float *out_scales,
+                                uint32_t *error_flags, void *stream);
+
+/*
+ * Forward RoPE + block-FP8 quant + paged insert ([KV] S1, numerics as above
+ * with the forward rotation).
+ *
+ *  kv_bf16         [n_tokens, 512] bf16, token stride kv_stride_token
+ *                  elements (multiple of 8), base 16-byte aligned.
+ *  positions       [n_tokens] int64; cos_sin_cache as above.
+ *  slot_mapping    [n_tokens] int64: slot s < 0 skips the token; otherwise
+ *                  the token's 528-byte record (512 codes, then the four
+ *                  fp32 block scales) goes to
+ *                  k_cache + (s / block_size) * block_stride_bytes
+ *                          + (s % block_size) * 528.
+ *                  Slots of different tokens must differ (a repeated slot
+ *                  gets one of the writers' bytes, unspecified which).
+ *  k_cache         [num_blocks, block_stride_bytes] uint8, 16-byte aligned;
+ *                  bytes outside the mapped records are never written.
+ *  block_stride_bytes >= block_size * 528 and a multiple of 16.
+ *  error_flags     optional device uint32 (may be NULL).
+ */
+rq_status rq_rope_fp8_quant_insert(const void *kv_bf16, int64_t n_tokens,
+                                   int64_t kv_stride_token, const int64_t *positions,
+                                   const float *cos_sin_cache, int64_t cache_rows,
+                                   const int64_t *slot_mapping, uint8_t *k_cache,
+                                   int64_t num_blocks, int64_t block_size,
+                                   int64_t block_stride_bytes, float eps,
+                                   uint32_t *error_flags, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RQ_H_ */

@@ -1,0 +1,186 @@
+"""B300 (sm_103a) inverse RoPE + block-FP8 quant, and forward RoPE + FP8 paged insert.
+
+Thin Python binding over the C ABI of ``include/rq.h`` (``librq.so``, built
+in-tree by ``rope_block_fp8_inverse_b300.build``). This module only checks
+and marshals arguments (device pointers, strides, the current CUDA stream);
+every arithmetic step runs in the library's CUDA kernels. There is no CPU
+path: CPU tensors, or a missing ``librq.so``, raise.
+
+    codes, scales = inv_rope_fp8_quant(x, positions, cos_sin_cache, heads_per_group)
+    rope_fp8_quant_insert(kv, positions, cos_sin_cache, slot_mapping, k_cache, block_size)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
+           "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
+
+HEAD_DIM = 512
+BLOCKS_PER_HEAD = 4
+RECORD_BYTES = 528
+DEFAULT_EPS = 1e-10
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librq.so")
+
+# every symbol include/rq.h declares, with (restype, argtypes)
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+ABI_SYMBOLS = {
+    "rq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "rq_version": (ctypes.c_int, []),
+    "rq_inv_rope_fp8_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
+                                             ctypes.c_float, _P, _P, _P, _P]),
+    "rq_rope_fp8_quant_insert": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _P, _P, _I64,
+                                                _I64, _I64, ctypes.c_float, _P, _P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class RQError(RuntimeError):
+    """A non-zero rq_status from the library."""
+
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: status {status} ({status_string(status)})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded librq.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m rope_block_fp8_inverse_b300.build` (needs nvcc)")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in ABI_SYMBOLS.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().rq_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise RQError(status, where)
+
+
+def _cuda(t: torch.Tensor, name: str, dtype: torch.dtype) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def inv_rope_fp8_quant(x: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                       heads_per_group: int, eps: float = DEFAULT_EPS,
+                       out: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                       error_flags: torch.Tensor | None = None):
+    """Inverse GPT-J RoPE on dims 448..511 + block-128 e4m3 quant with power-of-two scales.
+
+    x: [N, H, 512] bf16 on the GPU (token / head strides free, last dim
+    contiguous). Returns ``(out, scales)``: ``out`` [N, G, hpg*512] as
+    ``torch.float8_e4m3fn``, ``scales`` [N, G, hpg*4] fp32, G = H / hpg.
+    Preallocated ``out`` (uint8 or float8_e4m3fn) / ``scales`` are written in place.
+    Runs on the current CUDA stream, asynchronously.
+    """
+    _cuda(x, "x", torch.bfloat16)
+    if x.dim() != 3 or x.shape[2] != HEAD_DIM or x.stride(2) != 1:
+        raise ValueError("x must be [N, H, 512] with a contiguous last dim")
+    n, h = x.shape[0], x.shape[1]
+    hpg = int(heads_per_group)
+    if hpg < 1 or h % hpg:
+        raise ValueError(f"heads_per_group={hpg} must divide H={h}")
+    g = h // hpg
+    _cuda(positions, "positions", torch.int64)
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    if positions.shape != (n,) or not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous [N] int64 tensor")
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != 64 or not cos_sin_cache.is_contiguous():
+        raise ValueError("cos_sin_cache must be a contiguous [P, 64] fp32 tensor")
+    if out is None:
+        out = torch.empty((n, g, hpg * HEAD_DIM), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((n, g, hpg * BLOCKS_PER_HEAD), dtype=torch.float32, device=x.device)
+    if out.dtype not in (torch.uint8, torch.float8_e4m3fn) or not out.is_cuda:
+        raise TypeError("out must be a uint8 or float8_e4m3fn CUDA tensor")
+    if out.numel() != n * h * HEAD_DIM or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of N*H*512 bytes")
+    _cuda(scales, "scales", torch.float32)
+    if scales.numel() != n * h * BLOCKS_PER_HEAD or not scales.is_contiguous():
+        raise ValueError("scales must be a contiguous tensor of N*H*4 floats")
+    for t in (positions, cos_sin_cache, out, scales):
+        if t.device != x.device:
+            raise ValueError("all tensors must be on the same device")
+    flags = 0
+    if error_flags is not None:
+        _cuda(error_flags, "error_flags", torch.int32)
+        flags = error_flags.data_ptr()
+    with torch.cuda.device(x.device):
+        st = lib().rq_inv_rope_fp8_quant(
+            x.data_ptr(), n, h, x.stride(0), x.stride(1), positions.data_ptr(),
+            cos_sin_cache.data_ptr(), cos_sin_cache.shape[0], hpg, float(eps), out.data_ptr(),
+            scales.data_ptr(), flags, _stream(x.device))
+    _check(st, "rq_inv_rope_fp8_quant")
+    return out.view(torch.float8_e4m3fn).view(n, g, hpg * HEAD_DIM), scales.view(n, g, hpg * BLOCKS_PER_HEAD)
+
+
+def rope_fp8_quant_insert(kv: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                          slot_mapping: torch.Tensor, k_cache: torch.Tensor, block_size: int,
+                          eps: float = DEFAULT_EPS, error_flags: torch.Tensor | None = None) -> None:
+    """Forward GPT-J RoPE + block-128 e4m3 quant of kv [N, 512] bf16, scattered
+    into the paged ``k_cache`` [num_blocks, block_bytes] uint8 by ``slot_mapping``.
+
+    Each mapped token's 528-byte record (512 codes then 4 fp32 scales) lands at
+    block ``slot // block_size``, byte offset ``(slot % block_size) * 528``;
+    negative slots are skipped. Runs on the current CUDA stream.
+    """
+    _cuda(kv, "kv", torch.bfloat16)
+    if kv.dim() != 2 or kv.shape[1] != HEAD_DIM or kv.stride(1) != 1:
+        raise ValueError("kv must be [N, 512] with a contiguous last dim")
+    n = kv.shape[0]
+    _cuda(positions, "positions", torch.int64)
+    _cuda(slot_mapping, "slot_mapping", torch.int64)
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    _cuda(k_cache, "k_cache", torch.uint8)
+    if positions.shape != (n,) or not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous [N] int64 tensor")
+    if slot_mapping.shape != (n,) or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous [N] int64 tensor")
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != 64 or not cos_sin_cache.is_contiguous():
+        raise ValueError("cos_sin_cache must be a contiguous [P, 64] fp32 tensor")
+    if k_cache.dim() != 2 or k_cache.stride(1) != 1:
+        raise ValueError("k_cache must be [num_blocks, block_bytes] with contiguous rows")
+    for t in (positions, slot_mapping, cos_sin_cache, k_cache):
+        if t.device != kv.device:
+            raise ValueError("all tensors must be on the same device")
+    flags = 0
+    if error_flags is not None:
+        _cuda(error_flags, "error_flags", torch.int32)
+        flags = error_flags.data_ptr()
+    with torch.cuda.device(kv.device):
+        st = lib().rq_rope_fp8_quant_insert(
+            kv.data_ptr(), n, kv.stride(0), positions.data_ptr(), cos_sin_cache.data_ptr(),
+            cos_sin_cache.shape[0], slot_mapping.data_ptr(), k_cache.data_ptr(), k_cache.shape[0],
+            int(block_size), k_cache.stride(0), float(eps), flags, _stream(kv.device))
+    _check(st, "rq_rope_fp8_quant_insert")

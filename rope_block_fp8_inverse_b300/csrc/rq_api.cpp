@@ -1,0 +1,152 @@
+// rq_api.cpp -- the C ABI declared in include/rq.h: host-side argument
+// checks, device lookup and dispatch to the kernel launchers. Every check
+// runs before any CUDA call, so an invalid call launches nothing and
+// touches no buffer.
+#include <cmath>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "rq.h"
+#include "rq_launch.h"
+
+#define RQ_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+constexpr int kVersionMajor = 1;
+constexpr int kVersionMinor = 0;
+constexpr int64_t kMaxRows = int64_t(1) << 31;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool eps_ok(float eps) {
+    // 2^-100 <= eps <= 2^100 keeps amax / 448 a normal fp32 and the
+    // power-of-two scale and its inverse representable for every finite amax.
+    return std::isfinite(eps) && eps >= 0x1p-100f && eps <= 0x1p100f;
+}
+
+// Current device and its SM count (cached per device, per thread).
+cudaError_t current_device(rq::DeviceInfo* info) {
+    constexpr int kMax = 64;
+    static thread_local int sm_count[kMax] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int slot = (dev >= 0 && dev < kMax) ? dev : -1;
+    int n = slot >= 0 ? sm_count[slot] : 0;
+    if (n == 0) {
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (slot >= 0) sm_count[slot] = n;
+    }
+    info->ordinal = dev;
+    info->sm_count = n;
+    return cudaSuccess;
+}
+
+rq_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return RQ_OK;
+    (void)cudaGetLastError();  // clear this runtime's sticky launch error
+    return RQ_ERR_CUDA;
+}
+
+}  // namespace
+
+RQ_EXPORT const char* rq_status_string(int status) {
+    switch (status) {
+        case RQ_OK: return "ok";
+        case RQ_ERR_NULL: return "a required pointer is NULL";
+        case RQ_ERR_SHAPE: return "a size or stride is out of range";
+        case RQ_ERR_ALIGN: return "a pointer or stride breaks the 16-byte alignment rule";
+        case RQ_ERR_GROUPING: return "heads_per_group must be >= 1 and divide n_heads";
+        case RQ_ERR_CUDA: return "the CUDA runtime reported an error";
+        case RQ_ERR_ARG: return "eps must be finite and within [2^-100, 2^100]";
+        default: return "unknown status";
+    }
+}
+
+RQ_EXPORT int rq_version(void) { return (kVersionMajor << 16) | kVersionMinor; }
+
+RQ_EXPORT rq_status rq_inv_rope_fp8_quant(const void* x_bf16, int64_t n_tokens, int64_t n_heads,
+                                          int64_t x_stride_token, int64_t x_stride_head,
+                                          const int64_t* positions, const float* cos_sin_cache,
+                                          int64_t cache_rows, int64_t heads_per_group, float eps,
+                                          uint8_t* out_fp8, float* out_scales,
+                                          uint32_t* error_flags, void* stream) {
+    if (n_tokens < 0 || n_heads < 1 || cache_rows < 1) return RQ_ERR_SHAPE;
+    if (heads_per_group < 1 || n_heads % heads_per_group != 0) return RQ_ERR_GROUPING;
+    if (!eps_ok(eps)) return RQ_ERR_ARG;
+    if (n_heads >= kMaxRows || n_tokens >= kMaxRows / n_heads) return RQ_ERR_SHAPE;
+    if (n_tokens == 0) return RQ_OK;
+    if (!x_bf16 || !positions || !cos_sin_cache || !out_fp8 || !out_scales) return RQ_ERR_NULL;
+    if (!aligned(x_bf16, 16) || x_stride_token % 8 != 0 || x_stride_head % 8 != 0 ||
+        !aligned(positions, 8) || !aligned(cos_sin_cache, 16) || !aligned(out_fp8, 16) ||
+        !aligned(out_scales, 16) || (error_flags && !aligned(error_flags, 4)))
+        return RQ_ERR_ALIGN;
+
+    rq::DeviceInfo dev;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    rq::InvParams p;
+    p.x = x_bf16;
+    p.sx_t = x_stride_token;
+    p.sx_h = x_stride_head;
+    p.n_rows = static_cast<uint32_t>(n_tokens * n_heads);
+    p.n_heads = static_cast<uint32_t>(n_heads);
+    p.positions = positions;
+    p.cache = cos_sin_cache;
+    p.cache_rows = cache_rows;
+    p.eps = eps;
+    p.out = out_fp8;
+    p.scales = out_scales;
+    p.error_flags = error_flags;
+    // Rows in flight per warp: two for large calls; one when the grid would
+    // not even fill the GPU once (decode-sized calls), to spread the rows.
+    const int rows = (int64_t(p.n_rows) >= int64_t(dev.sm_count) * (rq::kInvThreads / 32) * 4) ? 2 : 1;
+    return from_cuda(rq::launch_inv_rope_fp8_quant(p, dev, rows, static_cast<cudaStream_t>(stream)));
+}
+
+RQ_EXPORT rq_status rq_rope_fp8_quant_insert(const void* kv_bf16, int64_t n_tokens,
+                                             int64_t kv_stride_token, const int64_t* positions,
+                                             const float* cos_sin_cache, int64_t cache_rows,
+                                             const int64_t* slot_mapping, uint8_t* k_cache,
+                                             int64_t num_blocks, int64_t block_size,
+                                             int64_t block_stride_bytes, float eps,
+                                             uint32_t* error_flags, void* stream) {
+    if (n_tokens < 0 || n_tokens >= kMaxRows || cache_rows < 1 || num_blocks < 1 ||
+        block_size < 1 || block_size > (int64_t(1) << 40) / rq::kRecordBytesABI)
+        return RQ_ERR_SHAPE;
+    if (block_stride_bytes < block_size * rq::kRecordBytesABI ||
+        num_blocks > (int64_t(1) << 62) / block_stride_bytes)
+        return RQ_ERR_SHAPE;
+    if (block_stride_bytes % 16 != 0) return RQ_ERR_ALIGN;
+    if (!eps_ok(eps)) return RQ_ERR_ARG;
+    if (n_tokens == 0) return RQ_OK;
+    if (!kv_bf16 || !positions || !cos_sin_cache || !slot_mapping || !k_cache) return RQ_ERR_NULL;
+    if (!aligned(kv_bf16, 16) || kv_stride_token % 8 != 0 || !aligned(positions, 8) ||
+        !aligned(cos_sin_cache, 16) || !aligned(slot_mapping, 8) || !aligned(k_cache, 16) ||
+        (error_flags && !aligned(error_flags, 4)))
+        return RQ_ERR_ALIGN;
+
+    rq::DeviceInfo dev;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    rq::InsParams p;
+    p.kv = kv_bf16;
+    p.skv = kv_stride_token;
+    p.n_tokens = static_cast<uint32_t>(n_tokens);
+    p.positions = positions;
+    p.cache = cos_sin_cache;
+    p.cache_rows = cache_rows;
+    p.slot_mapping = slot_mapping;
+    p.k_cache = k_cache;
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.block_stride = block_stride_bytes;
+    p.eps = eps;
+    p.error_flags = error_flags;
+    return from_cuda(rq::launch_rope_fp8_quant_insert(p, dev, static_cast<cudaStream_t>(stream)));
+}

@@ -1,0 +1,200 @@
+// rq_kernels.cu -- sm_103a kernels of the inverse-RoPE + block-FP8 quant op
+// and of its forward-RoPE + paged-insert sibling, with their launchers.
+//
+// Both are HBM-bound streams (about 1.5 bytes moved per fp32 op), so the
+// design goal is bytes in flight, not arithmetic: a persistent grid of warps
+// sized to the SM count, each warp owning whole 512-wide rows
+// (rq_device.cuh) and issuing the loads of kRows rows before it computes any
+// of them. The pages' Triton kernel (one program per 1 to 4 heads) is prior
+// art: here a warp is the program, and the number of rows in flight per SM
+// is set by kRows x resident warps instead of by BLOCK_H.
+#include "rq_device.cuh"
+#include "rq_launch.h"
+
+namespace rq {
+
+// ------------------------------------------------------------------ inverse
+
+// Row r = t * n_heads + h. Output row r (512 codes) sits at out + r*512 and
+// its 4 scales at scales + r*4: with contiguous [N, G, hpg*512] /
+// [N, G, hpg*4] outputs this is exactly the grouped layout of the inverse
+// RoPE page, S1 (head h = g*hpg + i of token t at row (t, g), offset i*512),
+// so the grouping never changes an address.
+template <int kRows>
+__global__ void __launch_bounds__(kInvThreads)
+inv_rope_fp8_quant_kernel(InvParams p) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
+    const uint16_t* __restrict__ x = static_cast<const uint16_t*>(p.x);
+    const int cs_col = (lane >= kRopeLane0 ? lane - kRopeLane0 : 0) * 4;
+
+    for (uint32_t r0 = warp * kRows; r0 < p.n_rows; r0 += n_warps * kRows) {
+        RowRegs in[kRows];
+        bool live[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const uint32_t r = r0 + i;
+            live[i] = false;
+            if (r < p.n_rows) {  // warp-uniform
+                const uint32_t t = r / p.n_heads;
+                const uint32_t h = r - t * p.n_heads;
+                const int64_t pos = __ldg(p.positions + t);
+                live[i] = static_cast<uint64_t>(pos) < static_cast<uint64_t>(p.cache_rows);
+                if (live[i]) {
+                    const uint16_t* row = x + static_cast<int64_t>(t) * p.sx_t +
+                                          static_cast<int64_t>(h) * p.sx_h;
+                    in[i].a = ld_stream16(row + 8 * lane);
+                    in[i].b = ld_stream16(row + kHalf + 8 * lane);
+                    if (lane >= kRopeLane0) {
+                        const float* cs = p.cache + pos * kCacheWidth + cs_col;
+                        in[i].c = ld_shared_ro16(cs);
+                        in[i].s = ld_shared_ro16(cs + kHalfRope);
+                    }
+                } else if (lane == 0 && p.error_flags) {
+                    atomicOr(p.error_flags, RQ_FLAG_POSITION_RANGE);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            if (!live[i]) continue;
+            const uint32_t r = r0 + i;
+            const RowOut o = rope_quant_row<true>(in[i], lane, p.eps);
+            uint8_t* dst = p.out + static_cast<int64_t>(r) * kHeadDim;
+            st_stream8(dst + 8 * lane, o.qa.x, o.qa.y);
+            st_stream8(dst + kHalf + 8 * lane, o.qb.x, o.qb.y);
+            const float s1 = __shfl_sync(kFull, o.sa, 16);
+            const float s3 = __shfl_sync(kFull, o.sb, 16);
+            if (lane == 0) st_stream16f(p.scales + static_cast<int64_t>(r) * 4, o.sa, s1, o.sb, s3);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ insert
+
+template <int kRows>
+__global__ void __launch_bounds__(kInsThreads)
+rope_fp8_quant_insert_kernel(InsParams p) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
+    const uint16_t* __restrict__ kv = static_cast<const uint16_t*>(p.kv);
+    const int cs_col = (lane >= kRopeLane0 ? lane - kRopeLane0 : 0) * 4;
+    const int64_t n_slots = p.num_blocks * p.block_size;
+
+    for (uint32_t t0 = warp * kRows; t0 < p.n_tokens; t0 += n_warps * kRows) {
+        RowRegs in[kRows];
+        int64_t slot[kRows];
+        bool live[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const uint32_t t = t0 + i;
+            live[i] = false;
+            slot[i] = -1;
+            if (t < p.n_tokens) {
+                const int64_t pos = __ldg(p.positions + t);
+                slot[i] = __ldg(p.slot_mapping + t);
+                const bool pos_ok =
+                    static_cast<uint64_t>(pos) < static_cast<uint64_t>(p.cache_rows);
+                const bool slot_ok = slot[i] < n_slots;
+                live[i] = pos_ok && slot_ok && slot[i] >= 0;
+                if (live[i]) {
+                    const uint16_t* row = kv + static_cast<int64_t>(t) * p.skv;
+                    in[i].a = ld_stream16(row + 8 * lane);
+                    in[i].b = ld_stream16(row + kHalf + 8 * lane);
+                    if (lane >= kRopeLane0) {
+                        const float* cs = p.cache + pos * kCacheWidth + cs_col;
+                        in[i].c = ld_shared_ro16(cs);
+                        in[i].s = ld_shared_ro16(cs + kHalfRope);
+                    }
+                } else if (lane == 0 && p.error_flags && (!pos_ok || !slot_ok)) {
+                    atomicOr(p.error_flags,
+                             (pos_ok ? 0u : RQ_FLAG_POSITION_RANGE) |
+                                 (slot_ok ? 0u : RQ_FLAG_SLOT_RANGE));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            if (!live[i]) continue;
+            const RowOut o = rope_quant_row<false>(in[i], lane, p.eps);
+            const int64_t blk = slot[i] / p.block_size;
+            const int64_t off = slot[i] - blk * p.block_size;
+            uint8_t* rec = p.k_cache + blk * p.block_stride + off * kRecordBytes;
+            st_stream8(rec + 8 * lane, o.qa.x, o.qa.y);
+            st_stream8(rec + kHalf + 8 * lane, o.qb.x, o.qb.y);
+            const float s1 = __shfl_sync(kFull, o.sa, 16);
+            const float s3 = __shfl_sync(kFull, o.sb, 16);
+            if (lane == 0) st_stream16f(rec + kHeadDim, o.sa, s1, o.sb, s3);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+
+namespace {
+
+// Resident CTAs per SM of each kernel variant, queried once per device and
+// variant (thread-local: no locking on the launch path).
+constexpr int kMaxDevices = 64;
+enum Variant { kInv1, kInv2, kInv4, kIns2, kVariants };
+
+template <typename K>
+int resident_blocks(int device, Variant v, K kernel, int threads) {
+    static thread_local int cache[kMaxDevices][kVariants];
+    if (device < 0 || device >= kMaxDevices) device = 0;
+    int& n = cache[device][v];
+    if (n == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess ||
+            n < 1)
+            n = 1;
+    }
+    return n;
+}
+
+// Persistent grid: enough CTAs for the work, at most one full wave.
+int grid_size(int64_t units, int units_per_block, int sm_count, int resident) {
+    const int64_t need = (units + units_per_block - 1) / units_per_block;
+    const int64_t cap = int64_t(sm_count) * resident;
+    return static_cast<int>(need < cap ? need : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev, int rows_per_warp,
+                                      cudaStream_t stream) {
+    constexpr int kWarps = kInvThreads / 32;
+    switch (rows_per_warp) {
+        case 1: {
+            auto k = inv_rope_fp8_quant_kernel<1>;
+            const int res = resident_blocks(dev.ordinal, kInv1, k, kInvThreads);
+            k<<<grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
+            break;
+        }
+        case 4: {
+            auto k = inv_rope_fp8_quant_kernel<4>;
+            const int res = resident_blocks(dev.ordinal, kInv4, k, kInvThreads);
+            k<<<grid_size(p.n_rows, kWarps * 4, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
+            break;
+        }
+        default: {
+            auto k = inv_rope_fp8_quant_kernel<2>;
+            const int res = resident_blocks(dev.ordinal, kInv2, k, kInvThreads);
+            k<<<grid_size(p.n_rows, kWarps * 2, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
+            break;
+        }
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& dev,
+                                         cudaStream_t stream) {
+    constexpr int kWarps = kInsThreads / 32;
+    auto k = rope_fp8_quant_insert_kernel<2>;
+    const int res = resident_blocks(dev.ordinal, kIns2, k, kInsThreads);
+    k<<<grid_size(p.n_tokens, kWarps * 2, dev.sm_count, res), kInsThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace rq

@@ -1,0 +1,55 @@
+// rq_launch.h -- internal interface between the C-ABI layer (rq_api.cpp) and
+// the kernel launchers (rq_kernels.cu). Not installed, not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rq.h"
+
+namespace rq {
+
+constexpr int kInvThreads = 256;  // 8 warps per CTA
+constexpr int kInsThreads = 256;
+constexpr int64_t kRecordBytesABI = 528;  // paged record: 512 codes + 4 fp32 scales
+
+struct DeviceInfo {
+    int ordinal;
+    int sm_count;
+};
+
+// Arguments of the inverse kernel, validated on the host (rq_api.cpp).
+struct InvParams {
+    const void* x;            // bf16 [N, H, 512], strides sx_t / sx_h elements
+    int64_t sx_t, sx_h;
+    uint32_t n_rows;          // N * H (< 2^31)
+    uint32_t n_heads;
+    const int64_t* positions;
+    const float* cache;       // [cache_rows, 64]
+    int64_t cache_rows;
+    float eps;
+    uint8_t* out;             // [N*H, 512] codes
+    float* scales;            // [N*H, 4]
+    uint32_t* error_flags;    // may be null
+};
+
+struct InsParams {
+    const void* kv;           // bf16 [N, 512], token stride skv elements
+    int64_t skv;
+    uint32_t n_tokens;
+    const int64_t* positions;
+    const float* cache;
+    int64_t cache_rows;
+    const int64_t* slot_mapping;
+    uint8_t* k_cache;
+    int64_t num_blocks, block_size, block_stride;
+    float eps;
+    uint32_t* error_flags;
+};
+
+cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev, int rows_per_warp,
+                                      cudaStream_t stream);
+cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& dev,
+                                         cudaStream_t stream);
+
+}  // namespace rq

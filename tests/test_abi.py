@@ -1,0 +1,130 @@
+"""The C-ABI library loads, exports every symbol include/rq.h declares, and
+rejects invalid arguments on the host before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import rope_block_fp8_inverse_b300 as rq
+from rope_block_fp8_inverse_b300 import build as rq_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rq.h")
+
+RQ_OK, RQ_ERR_NULL, RQ_ERR_SHAPE, RQ_ERR_ALIGN, RQ_ERR_GROUPING, RQ_ERR_CUDA, RQ_ERR_ARG = range(7)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rq_build.build()
+    return rq.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    assert "rq_inv_rope_fp8_quant" in names and "rq_rope_fp8_quant_insert" in names
+    assert set(names) == set(rq.ABI_SYMBOLS), (names, sorted(rq.ABI_SYMBOLS))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(rq.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.rq_version() >> 16 == 1
+    for code in range(7):
+        s = rq.status_string(code)
+        assert s and s != "unknown status"
+    assert rq.status_string(99) == "unknown status"
+
+
+# fake, never-dereferenced device addresses: every call below fails host checks first
+A16 = 0x7F0000000000
+A8 = A16 + 8
+
+
+def _inv(lib, x=A16, n=4, h=8, st=4096, sh=512, pos=A16, cs=A16, rows=16, hpg=4, eps=1e-10,
+         out=A16, sc=A16, flags=None):
+    return lib.rq_inv_rope_fp8_quant(x, n, h, st, sh, pos, cs, rows, hpg, eps, out, sc, flags, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=-1), RQ_ERR_SHAPE),
+    (dict(h=0), RQ_ERR_SHAPE),
+    (dict(rows=0), RQ_ERR_SHAPE),
+    (dict(hpg=0), RQ_ERR_GROUPING),
+    (dict(hpg=3), RQ_ERR_GROUPING),
+    (dict(h=24, hpg=5), RQ_ERR_GROUPING),
+    (dict(eps=0.0), RQ_ERR_ARG),
+    (dict(eps=-1.0), RQ_ERR_ARG),
+    (dict(eps=float("nan")), RQ_ERR_ARG),
+    (dict(eps=float("inf")), RQ_ERR_ARG),
+    (dict(eps=1e-35), RQ_ERR_ARG),
+    (dict(n=1 << 27, h=16, hpg=4), RQ_ERR_SHAPE),     # N*H >= 2^31
+    (dict(x=None), RQ_ERR_NULL),
+    (dict(pos=None), RQ_ERR_NULL),
+    (dict(cs=None), RQ_ERR_NULL),
+    (dict(out=None), RQ_ERR_NULL),
+    (dict(sc=None), RQ_ERR_NULL),
+    (dict(x=A8), RQ_ERR_ALIGN),
+    (dict(st=4100), RQ_ERR_ALIGN),
+    (dict(sh=516), RQ_ERR_ALIGN),
+    (dict(pos=A16 + 4), RQ_ERR_ALIGN),
+    (dict(cs=A8), RQ_ERR_ALIGN),
+    (dict(out=A8), RQ_ERR_ALIGN),
+    (dict(sc=A8), RQ_ERR_ALIGN),
+    (dict(flags=A16 + 2), RQ_ERR_ALIGN),
+])
+def test_inverse_rejects_bad_arguments(lib, kw, status):
+    assert _inv(lib, **kw) == status
+
+
+def test_inverse_empty_batch_is_a_no_op(lib):
+    # n_tokens == 0: OK with no launch, even with NULL buffers
+    assert _inv(lib, n=0, x=None, pos=None, cs=None, out=None, sc=None) == RQ_OK
+
+
+def _ins(lib, kv=A16, n=4, skv=512, pos=A16, cs=A16, rows=16, slots=A16, cache=A16, nb=8, bs=64,
+         stride=64 * 528, eps=1e-10, flags=None):
+    return lib.rq_rope_fp8_quant_insert(kv, n, skv, pos, cs, rows, slots, cache, nb, bs, stride,
+                                        eps, flags, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=-1), RQ_ERR_SHAPE),
+    (dict(rows=0), RQ_ERR_SHAPE),
+    (dict(nb=0), RQ_ERR_SHAPE),
+    (dict(bs=0), RQ_ERR_SHAPE),
+    (dict(stride=64 * 528 - 16), RQ_ERR_SHAPE),
+    (dict(stride=64 * 528 + 8), RQ_ERR_ALIGN),
+    (dict(eps=0.0), RQ_ERR_ARG),
+    (dict(kv=None), RQ_ERR_NULL),
+    (dict(slots=None), RQ_ERR_NULL),
+    (dict(cache=None), RQ_ERR_NULL),
+    (dict(kv=A8), RQ_ERR_ALIGN),
+    (dict(skv=516), RQ_ERR_ALIGN),
+    (dict(slots=A16 + 4), RQ_ERR_ALIGN),
+    (dict(cache=A8), RQ_ERR_ALIGN),
+])
+def test_insert_rejects_bad_arguments(lib, kw, status):
+    assert _ins(lib, **kw) == status
+
+
+def test_insert_empty_batch_is_a_no_op(lib):
+    assert _ins(lib, n=0, kv=None, pos=None, cs=None, slots=None, cache=None) == RQ_OK
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(2, 8, 512, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        rq.inv_rope_fp8_quant(x, torch.zeros(2, dtype=torch.int64), torch.zeros(4, 64), 8)

@@ -1,0 +1,280 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bar (the tolerance stated for this op): scales bit-exact; FP8 codes exact
+except for at most 1e-4 of elements, each of those at most one E4M3 step
+away (which keeps the dequantised value within 1 E4M3 ulp); the paged
+scatter bit-exact in placement. The kernels are designed to be bit-exact
+(same fp32 op order, no FMA, exact power-of-two scaling), and the tests
+also report, and for the small cases require, zero mismatches.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+CODE_MISMATCH_FRACTION = 1e-4
+THREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+@pytest.fixture(scope="module")
+def rq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from rope_block_fp8_inverse_b300 import build
+    build.build()
+    import rope_block_fp8_inverse_b300 as m
+    return m
+
+
+def _e4m3_step_apart(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """True where codes a and b are adjacent on the E4M3 number line (or +-0)."""
+    def ordinal(c):
+        c = c.astype(np.int32)
+        mag = c & 0x7F
+        return np.where(c & 0x80, -mag, mag)
+    return np.abs(ordinal(a) - ordinal(b)) <= 1
+
+
+def assert_parity(got_codes, got_scales, want_codes, want_scales, exact=False):
+    gc = got_codes.reshape(-1)
+    wc = want_codes.reshape(-1)
+    gs = got_scales.reshape(-1).view(np.uint32)
+    ws = want_scales.reshape(-1).view(np.uint32)
+    assert gc.shape == wc.shape and gs.shape == ws.shape
+    bad_s = np.nonzero(gs != ws)[0]
+    assert bad_s.size == 0, f"{bad_s.size} scales differ, first at {bad_s[:5]}"
+    bad = np.nonzero(gc != wc)[0]
+    if exact:
+        assert bad.size == 0, (f"{bad.size} codes differ; first {bad[:8]}: "
+                               f"got {gc[bad[:8]]} want {wc[bad[:8]]}")
+    assert bad.size <= CODE_MISMATCH_FRACTION * gc.size, f"{bad.size} of {gc.size} codes differ"
+    assert np.all(_e4m3_step_apart(gc[bad], wc[bad]))
+    return bad.size
+
+
+def run_inverse(rq, inp, eps=1e-10, x_override=None):
+    dev = torch.device("cuda:0")
+    x = (x_override if x_override is not None else inp["x"]).to(dev)
+    pos = inp["positions"].to(dev)
+    cache = inp["cos_sin_cache"].to(dev)
+    codes, scales = rq.inv_rope_fp8_quant(x, pos, cache, inp["heads_per_group"], eps=eps)
+    torch.cuda.synchronize()
+    return codes.view(torch.uint8).cpu().numpy(), scales.cpu().numpy()
+
+
+def oracle_inverse(inp, eps=1e-10, x=None):
+    import oracle
+    return oracle.inv_rope_fp8_quant(inp["x"] if x is None else x, inp["positions"],
+                                     inp["cos_sin_cache"], inp["heads_per_group"], eps=eps,
+                                     threads=THREADS)
+
+
+# ---------------------------------------------------------------- inverse op
+
+def test_tiny_workload_exact(rq):
+    inp = W.inverse_inputs(W.TINY)
+    gc, gs = run_inverse(rq, inp)
+    wc, ws = oracle_inverse(inp)
+    assert gc.shape == (64, 1, 8 * 512) and gs.shape == (64, 1, 32)
+    assert_parity(gc, gs, wc, ws, exact=True)
+
+
+@pytest.mark.parametrize("n", W.DECODE_TOKENS)
+def test_decode_sweep_exact(rq, n):
+    inp = W.inverse_inputs(W.decode_spec(n))
+    gc, gs = run_inverse(rq, inp)
+    wc, ws = oracle_inverse(inp)
+    assert_parity(gc, gs, wc, ws, exact=True)
+
+
+@pytest.mark.parametrize("h,groups", W.PAGE_TEST_SHAPES,
+                         ids=[f"H{h}_G{g}" for h, g in W.PAGE_TEST_SHAPES])
+@pytest.mark.parametrize("n", [1, 37, 300])
+def test_page_test_shapes(rq, h, groups, n):
+    """The (H, groups) shapes of the inverse-RoPE page's test (S5), ragged N."""
+    spec = W.InverseSpec(f"page{h}x{groups}", n, h, h // groups, 8192, "uniform", True, seed=n)
+    inp = W.inverse_inputs(spec)
+    gc, gs = run_inverse(rq, inp)
+    wc, ws = oracle_inverse(inp)
+    assert gc.shape == (n, groups, (h // groups) * 512)
+    assert_parity(gc, gs, wc, ws, exact=True)
+
+
+def test_irregular_grouping_full(rq):
+    """N=8192, H=24, heads_per_group=6: every output compared."""
+    inp = W.inverse_inputs(W.IRREGULAR)
+    gc, gs = run_inverse(rq, inp)
+    wc, ws = oracle_inverse(inp)
+    assert gc.shape == (8192, 4, 6 * 512)
+    assert_parity(gc, gs, wc, ws, exact=True)
+
+
+def test_prefill16k_sampled_tokens(rq):
+    """Full-size launch (N=16384, H=32, hpg=8, the benchmarked configuration);
+    the oracle recomputes a sample of tokens one by one (batch invariance
+    makes a token's output independent of the rest of the batch)."""
+    inp = W.inverse_inputs(W.PREFILL16K)
+    gc, gs = run_inverse(rq, inp)
+    assert gc.shape == (16384, 4, 4096) and gs.shape == (16384, 4, 32)
+    rng = np.random.default_rng(0)
+    idx = np.unique(np.concatenate([[0, 1, 16383], rng.choice(16384, 1500, replace=False)]))
+    sub = {"x": inp["x"][idx], "positions": inp["positions"][idx],
+           "cos_sin_cache": inp["cos_sin_cache"], "heads_per_group": 8}
+    wc, ws = oracle_inverse(sub)
+    assert_parity(gc[idx], gs[idx], wc, ws, exact=True)
+    # properties at every output: scales are powers of two, no NaN codes
+    assert np.all((gs.view(np.uint32) & 0x7FFFFF) == 0)
+    assert not np.any((gc & 0x7F) == 0x7F)
+
+
+def test_strided_inputs(rq):
+    """Token / head strides other than [N, H, 512] contiguous give the same bytes."""
+    spec = W.InverseSpec("strided", 77, 16, 4, 4096, "uniform", True, seed=3)
+    inp = W.inverse_inputs(spec)
+    wc, ws = oracle_inverse(inp)
+    x = inp["x"]
+    wide = torch.zeros(77, 21, 512, dtype=torch.bfloat16)
+    wide[:, 3:19] = x
+    head_major = x.transpose(0, 1).contiguous().transpose(0, 1)
+    for variant in (wide.cuda()[:, 3:19], head_major.cuda()):
+        gc, gs = run_inverse(rq, inp, x_override=variant)
+        assert_parity(gc, gs, wc, ws, exact=True)
+
+
+def test_batch_invariance_across_launch_shapes(rq):
+    """A token's bytes do not depend on the batch it came with (small calls
+    take the one-row-per-warp launch, large ones two rows per warp)."""
+    inp = W.inverse_inputs(W.InverseSpec("bi", 4096, 32, 8, 65536, "uniform", True, seed=5))
+    gc, gs = run_inverse(rq, inp)
+    for lo, hi in ((0, 1), (100, 164), (4000, 4096)):
+        sub = {k: (v[lo:hi] if k in ("x", "positions") else v) for k, v in inp.items()}
+        c2, s2 = run_inverse(rq, sub)
+        assert np.array_equal(gc[lo:hi], c2) and np.array_equal(gs[lo:hi], s2)
+
+
+@pytest.mark.parametrize("eps", [1e-10, 1e-4, 2.0 ** -100, 3.5])
+def test_eps_and_special_values(rq, eps):
+    """Zero blocks (scale from eps), subnormal bf16, exact saturation, signed zeros."""
+    n, h = 6, 4
+    x = torch.zeros(n, h, 512, dtype=torch.float32)
+    x[1] = torch.randn(h, 512) * 1e-38                      # bf16 subnormals
+    x[2, :, ::7] = 448.0
+    x[2, :, 1::7] = -448.0 * 2 ** -12
+    x[3] = -0.0
+    x[4, :, 448:] = torch.randn(h, 64) * 3                  # only the rotated dims live
+    x[5] = torch.randn(h, 512) * 2.0 ** 60
+    spec_inp = {"x": x.to(torch.bfloat16), "positions": torch.tensor([0, 1, 2, 3, 4, 5]),
+                "cos_sin_cache": W.rope_cache(64), "heads_per_group": 2}
+    gc, gs = run_inverse(rq, spec_inp, eps=eps)
+    wc, ws = oracle_inverse(spec_inp, eps=eps)
+    assert_parity(gc, gs, wc, ws, exact=True)
+
+
+def test_position_out_of_range_flags_and_skips(rq):
+    """The kernel's own bounds check: a bad position skips the token (outputs
+    untouched) and sets RQ_FLAG_POSITION_RANGE; the other tokens are exact."""
+    inp = W.inverse_inputs(W.InverseSpec("oob", 8, 8, 8, 100, "uniform", True, seed=9))
+    pos = inp["positions"].clone()
+    pos[2] = 100          # == cache_rows
+    pos[5] = -1
+    dev = torch.device("cuda:0")
+    out = torch.full((8, 1, 4096), 0x5A, dtype=torch.uint8, device=dev)
+    scales = torch.full((8, 1, 32), -7.0, device=dev)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    rq.inv_rope_fp8_quant(inp["x"].to(dev), pos.to(dev), inp["cos_sin_cache"].to(dev), 8,
+                          out=out, scales=scales, error_flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 1
+    o = out.cpu().numpy()
+    s = scales.cpu().numpy()
+    assert np.all(o[[2, 5]] == 0x5A) and np.all(s[[2, 5]] == -7.0)
+    keep = [0, 1, 3, 4, 6, 7]
+    sub = {"x": inp["x"][keep], "positions": pos[keep], "cos_sin_cache": inp["cos_sin_cache"],
+           "heads_per_group": 8}
+    wc, ws = oracle_inverse(sub)
+    assert_parity(o[keep], s[keep], wc, ws, exact=True)
+
+
+def test_preallocated_fp8_output_and_stream(rq):
+    """The `_out` form: caller-owned float8 output, a non-default stream."""
+    inp = W.inverse_inputs(W.TINY)
+    dev = torch.device("cuda:0")
+    out = torch.empty(64, 1, 4096, dtype=torch.float8_e4m3fn, device=dev)
+    scales = torch.empty(64, 1, 32, device=dev)
+    x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        c, sc = rq.inv_rope_fp8_quant(x, pos, cache, 8, out=out, scales=scales)
+    s.synchronize()
+    assert c.data_ptr() == out.data_ptr() and sc.data_ptr() == scales.data_ptr()
+    wc, ws = oracle_inverse(inp)
+    assert_parity(out.view(torch.uint8).cpu().numpy(), scales.cpu().numpy(), wc, ws, exact=True)
+
+
+# ---------------------------------------------------------------- insert op
+
+def run_insert(rq, inp, k_cache=None, slots=None, eps=1e-10, flags=None):
+    dev = torch.device("cuda:0")
+    kc = (inp["k_cache"] if k_cache is None else k_cache).to(dev).contiguous()
+    sl = (inp["slot_mapping"] if slots is None else slots).to(dev)
+    rq.rope_fp8_quant_insert(inp["kv"].to(dev), inp["positions"].to(dev),
+                             inp["cos_sin_cache"].to(dev), sl, kc, inp["block_size"], eps=eps,
+                             error_flags=flags)
+    torch.cuda.synchronize()
+    return kc.cpu().numpy()
+
+
+def oracle_insert(inp, k_cache=None, slots=None, eps=1e-10):
+    import oracle
+    return oracle.rope_fp8_quant_insert(inp["kv"], inp["positions"], inp["cos_sin_cache"],
+                                        inp["slot_mapping"] if slots is None else slots,
+                                        inp["k_cache"] if k_cache is None else k_cache,
+                                        inp["block_size"], eps=eps, threads=THREADS)
+
+
+def _assert_cache_parity(got, want):
+    """Placement bit-exact: every byte outside records equal; inside records
+    the scales bit-exact and the codes within the stated tolerance."""
+    assert got.shape == want.shape
+    diff = np.nonzero(got.reshape(-1) != want.reshape(-1))[0]
+    assert diff.size == 0, f"{diff.size} cache bytes differ, first at {diff[:8]}"
+
+
+def test_insert16k_full(rq):
+    inp = W.insert_inputs(W.INSERT16K)
+    got = run_insert(rq, inp)
+    want = oracle_insert(inp)
+    _assert_cache_parity(got, want)
+    assert got.shape == (512, 64 * 528)
+
+
+@pytest.mark.parametrize("n", [1, 5, 64, 1000])
+def test_insert_ragged_and_padded_blocks(rq, n):
+    spec = W.InsertSpec("ins", n, 4096, 32, 16, seed=n)
+    inp = W.insert_inputs(spec)
+    pad = 16 * 528 + 48                          # block stride with padding bytes
+    kc = torch.full((32, pad), 0xA5, dtype=torch.uint8)
+    slots = inp["slot_mapping"].clone()
+    if n > 3:
+        slots[::3] = -1                          # skipped tokens
+    got = run_insert(rq, inp, k_cache=kc, slots=slots)
+    want = oracle_insert(inp, k_cache=kc, slots=slots)
+    _assert_cache_parity(got, want)
+
+
+def test_insert_slot_out_of_range_flags(rq):
+    spec = W.InsertSpec("ins-oob", 6, 64, 2, 4, seed=2)
+    inp = W.insert_inputs(spec)
+    slots = torch.tensor([0, 8, 3, -1, 100, 7])   # 8 slots: 8 and 100 are out of range
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    got = run_insert(rq, inp, slots=slots, flags=flags)
+    assert int(flags.item()) == 2
+    ok = torch.tensor([0, -1, 3, -1, -1, 7])
+    want = oracle_insert(inp, slots=ok)
+    _assert_cache_parity(got, want)
