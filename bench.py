@@ -47,7 +47,7 @@ FALLBACK_HBM_GBS = 6400.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=None,
@@ -101,44 +101,52 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """Samples SM clock and throttle reasons of one GPU through NVML (reads only)."""
+    """Samples the SM clock and clock-event (throttle) reasons of one GPU during
+    the timed region: through NVML when pynvml imports, else by running
+    ``nvidia-smi --query-gpu=... -lms 50`` (both only read the settings)."""
 
-    REASONS = {
-        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
-        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+    REASON_BITS = {
+        0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
         0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
-        0x100: "display_clock_setting",
     }
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int, period_s: float = 0.01):
+    def __init__(self, device_index: int, period_s: float = 0.02):
         self.period = period_s
         self.samples = []
-        self.reasons = 0
+        self.reasons = set()
         self.max_mhz = None
+        self.error = None
         self._stop = threading.Event()
         self._thread = None
-        self.error = None
+        self._proc = None
+        self.bus_id = None
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            self.bus_id = "{:08X}:{:02X}:{:02X}.0".format(
+                getattr(props, "pci_domain_id", 0), props.pci_bus_id, props.pci_device_id)
+        except Exception:
+            self.bus_id = None
+        self.nv = None
         try:
             import pynvml
             pynvml.nvmlInit()
-            bus = torch.cuda.get_device_properties(device_index).pci_bus_id \
-                if hasattr(torch.cuda.get_device_properties(device_index), "pci_bus_id") else None
-            if bus:
-                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
-            else:
-                self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.nv = pynvml
+            self.h = (pynvml.nvmlDeviceGetHandleByPciBusId(self.bus_id) if self.bus_id
+                      else pynvml.nvmlDeviceGetHandleByIndex(device_index))
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # no NVML: report that instead of clocks
-            self.nv = None
-            self.error = f"{type(e).__name__}: {e}"
+            self.nv = pynvml
+        except Exception as e:
+            self.error = f"nvml: {type(e).__name__}"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
-                self.reasons |= nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                bits = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.reasons |= {n for b, n in self.REASON_BITS.items() if bits & b}
             except Exception as e:
                 self.error = f"{type(e).__name__}: {e}"
                 return
@@ -146,22 +154,56 @@ class ClockSampler:
 
     def __enter__(self):
         if self.nv is not None:
-            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread = threading.Thread(target=self._run_nvml, daemon=True)
             self._thread.start()
+        else:
+            import subprocess
+            cmd = ["nvidia-smi", f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", str(int(self.period * 1000))]
+            if self.bus_id:
+                cmd += ["-i", self.bus_id]
+            try:
+                self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                              text=True)
+                self._thread = threading.Thread(target=self._read_smi, daemon=True)
+                self._thread.start()
+            except Exception as e:
+                self.error = f"nvidia-smi: {type(e).__name__}"
         return self
+
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self._proc.stdout:
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                self.samples.append(float(f[0]))
+                self.max_mhz = float(f[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    self.reasons.add(name)
 
     def __exit__(self, *exc):
         self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
         if self._thread:
-            self._thread.join()
+            self._thread.join(timeout=5)
 
     def summary(self):
-        if self.nv is None or not self.samples:
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
                     "error": self.error or "no samples"}
-        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": names, "samples": len(self.samples)}
+                "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "source": "nvml" if self.nv is not None else "nvidia-smi"}
 
 
 # ------------------------------------------------------------------ our arm

@@ -36,11 +36,13 @@
  *  - The return value reports host-side argument checks, or a launch error
  *    from cudaGetLastError (RQ_ERR_CUDA; the CUDA error is then cleared).
  *    On any error nothing is launched and no buffer is touched.
+ *  - Every device-side wait (the shared-memory pipeline's barriers) is
+ *    bounded; one that gives up sets RQ_FLAG_TIMEOUT and its CTA returns.
  *  - Device-side index checks: a token whose position is outside
  *    [0, cache_rows), or whose slot is >= num_blocks * block_size, is
  *    skipped (its outputs are left untouched) and the matching bit is OR-ed
  *    into *error_flags (RQ_FLAG_*) when error_flags is not NULL. No kernel
- *    traps or waits.
+ *    traps.
  *  - NaN / Inf inputs are outside the contract: results are unspecified
  *    but no memory access depends on them.
  *  - Every pointer is a device pointer (or managed / mapped memory the
@@ -62,12 +64,14 @@ typedef enum rq_status {
     RQ_ERR_ALIGN = 3,    /* a pointer or stride breaks the 16-byte rule     */
     RQ_ERR_GROUPING = 4, /* heads_per_group < 1 or does not divide n_heads  */
     RQ_ERR_CUDA = 5,     /* the CUDA runtime reported an error              */
-    RQ_ERR_ARG = 6       /* eps outside [2^-100, 2^100] or not finite       */
+    RQ_ERR_ARG = 6       /* eps outside [2^-100, 2^100], or a bad variant   */
 } rq_status;
 
 /* device-side error bits (OR-ed into *error_flags) */
 #define RQ_FLAG_POSITION_RANGE 1u /* a position was outside [0, cache_rows)   */
 #define RQ_FLAG_SLOT_RANGE 2u     /* a slot was >= num_blocks * block_size    */
+#define RQ_FLAG_TIMEOUT 4u        /* a pipeline wait gave up (never expected):
+                                     the outputs of that launch are incomplete */
 
 /* Static, NUL-terminated description of a status code. */
 const char *rq_status_string(int status);
@@ -104,6 +108,24 @@ rq_status rq_inv_rope_fp8_quant(const void *x_bf16, int64_t n_tokens, int64_t n_
                                 int64_t cache_rows, int64_t heads_per_group, float eps,
                                 uint8_t *out_fp8, float *out_scales,
                                 uint32_t *error_flags, void *stream);
+
+/* Kernel variants of rq_inv_rope_fp8_quant; all produce identical bytes. */
+typedef enum rq_inv_variant {
+    RQ_INV_AUTO = 0,          /* chosen from n_tokens * n_heads (the default)        */
+    RQ_INV_WARP_ROWS = 1,     /* persistent warps, two rows in flight per warp       */
+    RQ_INV_TMA_PIPELINE = 2   /* one producer warp streams 8-row tiles into a ring of
+                                 shared-memory stages with 1-D bulk copies (TMA);
+                                 eight consumer warps compute and store              */
+} rq_inv_variant;
+
+/* rq_inv_rope_fp8_quant with an explicit kernel variant (rq_inv_variant);
+ * any other value returns RQ_ERR_ARG. Same arguments and behaviour. */
+rq_status rq_inv_rope_fp8_quant_ex(const void *x_bf16, int64_t n_tokens, int64_t n_heads,
+                                   int64_t x_stride_token, int64_t x_stride_head,
+                                   const int64_t *positions, const float *cos_sin_cache,
+                                   int64_t cache_rows, int64_t heads_per_group, float eps,
+                                   uint8_t *out_fp8, float *out_scales,
+                                   uint32_t *error_flags, void *stream, int variant);
 
 /*
  * Forward RoPE + block-FP8 quant + paged insert ([KV] S1, numerics as above

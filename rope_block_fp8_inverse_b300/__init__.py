@@ -17,11 +17,13 @@ import threading
 
 import torch
 
-__all__ = ["inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
+__all__ = ["VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_TMA_PIPELINE", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
 
 HEAD_DIM = 512
 BLOCKS_PER_HEAD = 4
+# kernel variants of the inverse op (rq_inv_variant); all give identical bytes
+VARIANT_AUTO, VARIANT_WARP_ROWS, VARIANT_TMA_PIPELINE = 0, 1, 2
 RECORD_BYTES = 528
 DEFAULT_EPS = 1e-10
 
@@ -35,6 +37,8 @@ ABI_SYMBOLS = {
     "rq_version": (ctypes.c_int, []),
     "rq_inv_rope_fp8_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
                                              ctypes.c_float, _P, _P, _P, _P]),
+    "rq_inv_rope_fp8_quant_ex": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
+                                                ctypes.c_float, _P, _P, _P, _P, ctypes.c_int]),
     "rq_rope_fp8_quant_insert": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _P, _P, _I64,
                                                 _I64, _I64, ctypes.c_float, _P, _P]),
 }
@@ -95,13 +99,14 @@ def _stream(device: torch.device) -> int:
 def inv_rope_fp8_quant(x: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
                        heads_per_group: int, eps: float = DEFAULT_EPS,
                        out: torch.Tensor | None = None, scales: torch.Tensor | None = None,
-                       error_flags: torch.Tensor | None = None):
+                       error_flags: torch.Tensor | None = None, variant: int = VARIANT_AUTO):
     """Inverse GPT-J RoPE on dims 448..511 + block-128 e4m3 quant with power-of-two scales.
 
     x: [N, H, 512] bf16 on the GPU (token / head strides free, last dim
     contiguous). Returns ``(out, scales)``: ``out`` [N, G, hpg*512] as
     ``torch.float8_e4m3fn``, ``scales`` [N, G, hpg*4] fp32, G = H / hpg.
     Preallocated ``out`` (uint8 or float8_e4m3fn) / ``scales`` are written in place.
+    ``variant`` picks the kernel (VARIANT_*; the default chooses by size).
     Runs on the current CUDA stream, asynchronously.
     """
     _cuda(x, "x", torch.bfloat16)
@@ -137,10 +142,10 @@ def inv_rope_fp8_quant(x: torch.Tensor, positions: torch.Tensor, cos_sin_cache: 
         _cuda(error_flags, "error_flags", torch.int32)
         flags = error_flags.data_ptr()
     with torch.cuda.device(x.device):
-        st = lib().rq_inv_rope_fp8_quant(
+        st = lib().rq_inv_rope_fp8_quant_ex(
             x.data_ptr(), n, h, x.stride(0), x.stride(1), positions.data_ptr(),
             cos_sin_cache.data_ptr(), cos_sin_cache.shape[0], hpg, float(eps), out.data_ptr(),
-            scales.data_ptr(), flags, _stream(x.device))
+            scales.data_ptr(), flags, _stream(x.device), int(variant))
     _check(st, "rq_inv_rope_fp8_quant")
     return out.view(torch.float8_e4m3fn).view(n, g, hpg * HEAD_DIM), scales.view(n, g, hpg * BLOCKS_PER_HEAD)
 

@@ -61,19 +61,22 @@ RQ_EXPORT const char* rq_status_string(int status) {
         case RQ_ERR_ALIGN: return "a pointer or stride breaks the 16-byte alignment rule";
         case RQ_ERR_GROUPING: return "heads_per_group must be >= 1 and divide n_heads";
         case RQ_ERR_CUDA: return "the CUDA runtime reported an error";
-        case RQ_ERR_ARG: return "eps must be finite and within [2^-100, 2^100]";
+        case RQ_ERR_ARG: return "eps must be finite and within [2^-100, 2^100]; variant must be known";
         default: return "unknown status";
     }
 }
 
 RQ_EXPORT int rq_version(void) { return (kVersionMajor << 16) | kVersionMinor; }
 
-RQ_EXPORT rq_status rq_inv_rope_fp8_quant(const void* x_bf16, int64_t n_tokens, int64_t n_heads,
-                                          int64_t x_stride_token, int64_t x_stride_head,
-                                          const int64_t* positions, const float* cos_sin_cache,
-                                          int64_t cache_rows, int64_t heads_per_group, float eps,
-                                          uint8_t* out_fp8, float* out_scales,
-                                          uint32_t* error_flags, void* stream) {
+RQ_EXPORT rq_status rq_inv_rope_fp8_quant_ex(const void* x_bf16, int64_t n_tokens,
+                                             int64_t n_heads, int64_t x_stride_token,
+                                             int64_t x_stride_head, const int64_t* positions,
+                                             const float* cos_sin_cache, int64_t cache_rows,
+                                             int64_t heads_per_group, float eps, uint8_t* out_fp8,
+                                             float* out_scales, uint32_t* error_flags,
+                                             void* stream, int variant) {
+    if (variant != RQ_INV_AUTO && variant != RQ_INV_WARP_ROWS && variant != RQ_INV_TMA_PIPELINE)
+        return RQ_ERR_ARG;
     if (n_tokens < 0 || n_heads < 1 || cache_rows < 1) return RQ_ERR_SHAPE;
     if (heads_per_group < 1 || n_heads % heads_per_group != 0) return RQ_ERR_GROUPING;
     if (!eps_ok(eps)) return RQ_ERR_ARG;
@@ -95,6 +98,7 @@ RQ_EXPORT rq_status rq_inv_rope_fp8_quant(const void* x_bf16, int64_t n_tokens, 
     p.sx_h = x_stride_head;
     p.n_rows = static_cast<uint32_t>(n_tokens * n_heads);
     p.n_heads = static_cast<uint32_t>(n_heads);
+    p.n_tokens = static_cast<uint32_t>(n_tokens);
     p.positions = positions;
     p.cache = cos_sin_cache;
     p.cache_rows = cache_rows;
@@ -102,10 +106,19 @@ RQ_EXPORT rq_status rq_inv_rope_fp8_quant(const void* x_bf16, int64_t n_tokens, 
     p.out = out_fp8;
     p.scales = out_scales;
     p.error_flags = error_flags;
-    // Rows in flight per warp: two for large calls; one when the grid would
-    // not even fill the GPU once (decode-sized calls), to spread the rows.
-    const int rows = (int64_t(p.n_rows) >= int64_t(dev.sm_count) * (rq::kInvThreads / 32) * 4) ? 2 : 1;
-    return from_cuda(rq::launch_inv_rope_fp8_quant(p, dev, rows, static_cast<cudaStream_t>(stream)));
+    return from_cuda(
+        rq::launch_inv_rope_fp8_quant(p, dev, variant, static_cast<cudaStream_t>(stream)));
+}
+
+RQ_EXPORT rq_status rq_inv_rope_fp8_quant(const void* x_bf16, int64_t n_tokens, int64_t n_heads,
+                                          int64_t x_stride_token, int64_t x_stride_head,
+                                          const int64_t* positions, const float* cos_sin_cache,
+                                          int64_t cache_rows, int64_t heads_per_group, float eps,
+                                          uint8_t* out_fp8, float* out_scales,
+                                          uint32_t* error_flags, void* stream) {
+    return rq_inv_rope_fp8_quant_ex(x_bf16, n_tokens, n_heads, x_stride_token, x_stride_head,
+                                    positions, cos_sin_cache, cache_rows, heads_per_group, eps,
+                                    out_fp8, out_scales, error_flags, stream, RQ_INV_AUTO);
 }
 
 RQ_EXPORT rq_status rq_rope_fp8_quant_insert(const void* kv_bf16, int64_t n_tokens,

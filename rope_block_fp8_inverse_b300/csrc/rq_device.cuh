@@ -102,12 +102,17 @@ __device__ __forceinline__ float halfwarp_max(float m) {
     return m;
 }
 
-// Exponent e = ceil(log2(r)) of a positive normal fp32 r from its bits:
-// r = 1.m * 2^E; r is 2^E exactly when m == 0, else 2^E < r < 2^(E+1).
-__device__ __forceinline__ int ceil_log2_normal(float r) {
-    const uint32_t u = __float_as_uint(r);
+// Exponent of the block scale, e = ceil(log2(fl32(amax / 448))), read off
+// amax's bits without dividing. With amax = 1.m * 2^E normal and k an
+// integer, round-to-nearest-even gives fl32(amax/448) <= 2^k exactly when
+// amax/448 <= 2^k * (1 + 2^-24), and since no fp32 value lies in
+// (1.75 * 2^(k+8), 1.75 * 2^(k+8) * (1 + 2^-24)] that is amax <= 1.75 * 2^(k+8).
+// So e = E - 8 when 1.m <= 1.75 (mantissa field <= 0x600000), else E - 7.
+// Valid for normal amax (the ABI keeps amax >= eps >= 2^-100).
+__device__ __forceinline__ int scale_exponent(float amax) {
+    const uint32_t u = __float_as_uint(amax);
     const int E = static_cast<int>((u >> 23) & 0xffu) - 127;
-    return E + ((u & 0x7fffffu) != 0u ? 1 : 0);
+    return E - 8 + ((u & 0x7fffffu) > 0x600000u ? 1 : 0);
 }
 
 __device__ __forceinline__ float pow2f(int e) {  // e in [-126, 127]
@@ -154,8 +159,8 @@ __device__ __forceinline__ RowOut rope_quant_row(const RowRegs& in, int lane, fl
     float mb = halfwarp_max(absmax8(fb));
     ma = fmaxf(ma, eps);
     mb = fmaxf(mb, eps);
-    const int ea = ceil_log2_normal(__fdiv_rn(ma, 448.0f));
-    const int eb = ceil_log2_normal(__fdiv_rn(mb, 448.0f));
+    const int ea = scale_exponent(ma);
+    const int eb = scale_exponent(mb);
     RowOut o;
     o.qa = quant8(fa, pow2f(-ea));
     o.qb = quant8(fb, pow2f(-eb));

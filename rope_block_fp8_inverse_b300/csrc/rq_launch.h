@@ -24,6 +24,7 @@ struct InvParams {
     int64_t sx_t, sx_h;
     uint32_t n_rows;          // N * H (< 2^31)
     uint32_t n_heads;
+    uint32_t n_tokens;
     const int64_t* positions;
     const float* cache;       // [cache_rows, 64]
     int64_t cache_rows;
@@ -47,7 +48,14 @@ struct InsParams {
     uint32_t* error_flags;
 };
 
-cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev, int rows_per_warp,
+// Kernel variants of the inverse op (all bit-identical in output).
+enum InvVariant {
+    kInvAuto = 0,        // chosen from the problem size
+    kInvWarpRows = 1,    // persistent warps, register loads (rq_kernels.cu)
+    kInvTmaPipeline = 2  // bulk-copy (TMA) shared-memory pipeline (rq_kernels.cu)
+};
+
+cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev, int variant,
                                       cudaStream_t stream);
 cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& dev,
                                          cudaStream_t stream);

@@ -88,6 +88,15 @@ def test_inverse_rejects_bad_arguments(lib, kw, status):
     assert _inv(lib, **kw) == status
 
 
+def test_inverse_rejects_unknown_variant(lib):
+    args = (A16, 4, 8, 4096, 512, A16, A16, 16, 4, 1e-10, A16, A16, None, None)
+    assert lib.rq_inv_rope_fp8_quant_ex(*args, 3) == RQ_ERR_ARG
+    assert lib.rq_inv_rope_fp8_quant_ex(*args, -1) == RQ_ERR_ARG
+    bad = (None,) + args[1:]
+    for v in (0, 1, 2):   # known variants reach the pointer checks
+        assert lib.rq_inv_rope_fp8_quant_ex(*bad, v) == RQ_ERR_NULL
+
+
 def test_inverse_empty_batch_is_a_no_op(lib):
     # n_tokens == 0: OK with no launch, even with NULL buffers
     assert _inv(lib, n=0, x=None, pos=None, cs=None, out=None, sc=None) == RQ_OK

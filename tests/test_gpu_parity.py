@@ -57,12 +57,16 @@ def assert_parity(got_codes, got_scales, want_codes, want_scales, exact=False):
     return bad.size
 
 
-def run_inverse(rq, inp, eps=1e-10, x_override=None):
+VARIANTS = pytest.mark.parametrize("variant", [1, 2], ids=["warp_rows", "tma_pipeline"])
+
+
+def run_inverse(rq, inp, eps=1e-10, x_override=None, variant=0):
     dev = torch.device("cuda:0")
     x = (x_override if x_override is not None else inp["x"]).to(dev)
     pos = inp["positions"].to(dev)
     cache = inp["cos_sin_cache"].to(dev)
-    codes, scales = rq.inv_rope_fp8_quant(x, pos, cache, inp["heads_per_group"], eps=eps)
+    codes, scales = rq.inv_rope_fp8_quant(x, pos, cache, inp["heads_per_group"], eps=eps,
+                                          variant=variant)
     torch.cuda.synchronize()
     return codes.view(torch.uint8).cpu().numpy(), scales.cpu().numpy()
 
@@ -76,18 +80,20 @@ def oracle_inverse(inp, eps=1e-10, x=None):
 
 # ---------------------------------------------------------------- inverse op
 
-def test_tiny_workload_exact(rq):
+@VARIANTS
+def test_tiny_workload_exact(rq, variant):
     inp = W.inverse_inputs(W.TINY)
-    gc, gs = run_inverse(rq, inp)
+    gc, gs = run_inverse(rq, inp, variant=variant)
     wc, ws = oracle_inverse(inp)
     assert gc.shape == (64, 1, 8 * 512) and gs.shape == (64, 1, 32)
     assert_parity(gc, gs, wc, ws, exact=True)
 
 
 @pytest.mark.parametrize("n", W.DECODE_TOKENS)
-def test_decode_sweep_exact(rq, n):
+@VARIANTS
+def test_decode_sweep_exact(rq, variant, n):
     inp = W.inverse_inputs(W.decode_spec(n))
-    gc, gs = run_inverse(rq, inp)
+    gc, gs = run_inverse(rq, inp, variant=variant)
     wc, ws = oracle_inverse(inp)
     assert_parity(gc, gs, wc, ws, exact=True)
 
@@ -95,31 +101,34 @@ def test_decode_sweep_exact(rq, n):
 @pytest.mark.parametrize("h,groups", W.PAGE_TEST_SHAPES,
                          ids=[f"H{h}_G{g}" for h, g in W.PAGE_TEST_SHAPES])
 @pytest.mark.parametrize("n", [1, 37, 300])
-def test_page_test_shapes(rq, h, groups, n):
+@VARIANTS
+def test_page_test_shapes(rq, variant, h, groups, n):
     """The (H, groups) shapes of the inverse-RoPE page's test (S5), ragged N."""
     spec = W.InverseSpec(f"page{h}x{groups}", n, h, h // groups, 8192, "uniform", True, seed=n)
     inp = W.inverse_inputs(spec)
-    gc, gs = run_inverse(rq, inp)
+    gc, gs = run_inverse(rq, inp, variant=variant)
     wc, ws = oracle_inverse(inp)
     assert gc.shape == (n, groups, (h // groups) * 512)
     assert_parity(gc, gs, wc, ws, exact=True)
 
 
-def test_irregular_grouping_full(rq):
+@VARIANTS
+def test_irregular_grouping_full(rq, variant):
     """N=8192, H=24, heads_per_group=6: every output compared."""
     inp = W.inverse_inputs(W.IRREGULAR)
-    gc, gs = run_inverse(rq, inp)
+    gc, gs = run_inverse(rq, inp, variant=variant)
     wc, ws = oracle_inverse(inp)
     assert gc.shape == (8192, 4, 6 * 512)
     assert_parity(gc, gs, wc, ws, exact=True)
 
 
-def test_prefill16k_sampled_tokens(rq):
+@VARIANTS
+def test_prefill16k_sampled_tokens(rq, variant):
     """Full-size launch (N=16384, H=32, hpg=8, the benchmarked configuration);
     the oracle recomputes a sample of tokens one by one (batch invariance
     makes a token's output independent of the rest of the batch)."""
     inp = W.inverse_inputs(W.PREFILL16K)
-    gc, gs = run_inverse(rq, inp)
+    gc, gs = run_inverse(rq, inp, variant=variant)
     assert gc.shape == (16384, 4, 4096) and gs.shape == (16384, 4, 32)
     rng = np.random.default_rng(0)
     idx = np.unique(np.concatenate([[0, 1, 16383], rng.choice(16384, 1500, replace=False)]))
@@ -132,7 +141,8 @@ def test_prefill16k_sampled_tokens(rq):
     assert not np.any((gc & 0x7F) == 0x7F)
 
 
-def test_strided_inputs(rq):
+@VARIANTS
+def test_strided_inputs(rq, variant):
     """Token / head strides other than [N, H, 512] contiguous give the same bytes."""
     spec = W.InverseSpec("strided", 77, 16, 4, 4096, "uniform", True, seed=3)
     inp = W.inverse_inputs(spec)
@@ -141,8 +151,8 @@ def test_strided_inputs(rq):
     wide = torch.zeros(77, 21, 512, dtype=torch.bfloat16)
     wide[:, 3:19] = x
     head_major = x.transpose(0, 1).contiguous().transpose(0, 1)
-    for variant in (wide.cuda()[:, 3:19], head_major.cuda()):
-        gc, gs = run_inverse(rq, inp, x_override=variant)
+    for xv in (wide.cuda()[:, 3:19], head_major.cuda()):
+        gc, gs = run_inverse(rq, inp, x_override=xv, variant=variant)
         assert_parity(gc, gs, wc, ws, exact=True)
 
 
@@ -157,25 +167,37 @@ def test_batch_invariance_across_launch_shapes(rq):
         assert np.array_equal(gc[lo:hi], c2) and np.array_equal(gs[lo:hi], s2)
 
 
+def test_variants_identical_at_full_size(rq):
+    """Every kernel variant writes the same bytes on the benchmarked shape."""
+    inp = W.inverse_inputs(W.PREFILL16K)
+    ref = run_inverse(rq, inp, variant=1)
+    for v in (0, 2):
+        got = run_inverse(rq, inp, variant=v)
+        assert np.array_equal(ref[0], got[0]) and np.array_equal(ref[1], got[1]), v
+
+
 @pytest.mark.parametrize("eps", [1e-10, 1e-4, 2.0 ** -100, 3.5])
-def test_eps_and_special_values(rq, eps):
+@VARIANTS
+def test_eps_and_special_values(rq, variant, eps):
     """Zero blocks (scale from eps), subnormal bf16, exact saturation, signed zeros."""
     n, h = 6, 4
+    gen = torch.Generator().manual_seed(21)
     x = torch.zeros(n, h, 512, dtype=torch.float32)
-    x[1] = torch.randn(h, 512) * 1e-38                      # bf16 subnormals
+    x[1] = torch.randn(h, 512, generator=gen) * 1e-38       # bf16 subnormals
     x[2, :, ::7] = 448.0
     x[2, :, 1::7] = -448.0 * 2 ** -12
     x[3] = -0.0
-    x[4, :, 448:] = torch.randn(h, 64) * 3                  # only the rotated dims live
-    x[5] = torch.randn(h, 512) * 2.0 ** 60
+    x[4, :, 448:] = torch.randn(h, 64, generator=gen) * 3   # only the rotated dims live
+    x[5] = torch.randn(h, 512, generator=gen) * 2.0 ** 60
     spec_inp = {"x": x.to(torch.bfloat16), "positions": torch.tensor([0, 1, 2, 3, 4, 5]),
                 "cos_sin_cache": W.rope_cache(64), "heads_per_group": 2}
-    gc, gs = run_inverse(rq, spec_inp, eps=eps)
+    gc, gs = run_inverse(rq, spec_inp, eps=eps, variant=variant)
     wc, ws = oracle_inverse(spec_inp, eps=eps)
     assert_parity(gc, gs, wc, ws, exact=True)
 
 
-def test_position_out_of_range_flags_and_skips(rq):
+@VARIANTS
+def test_position_out_of_range_flags_and_skips(rq, variant):
     """The kernel's own bounds check: a bad position skips the token (outputs
     untouched) and sets RQ_FLAG_POSITION_RANGE; the other tokens are exact."""
     inp = W.inverse_inputs(W.InverseSpec("oob", 8, 8, 8, 100, "uniform", True, seed=9))
@@ -187,7 +209,7 @@ def test_position_out_of_range_flags_and_skips(rq):
     scales = torch.full((8, 1, 32), -7.0, device=dev)
     flags = torch.zeros(1, dtype=torch.int32, device=dev)
     rq.inv_rope_fp8_quant(inp["x"].to(dev), pos.to(dev), inp["cos_sin_cache"].to(dev), 8,
-                          out=out, scales=scales, error_flags=flags)
+                          out=out, scales=scales, error_flags=flags, variant=variant)
     torch.cuda.synchronize()
     assert int(flags.item()) == 1
     o = out.cpu().numpy()
@@ -256,10 +278,11 @@ def test_insert16k_full(rq):
 
 @pytest.mark.parametrize("n", [1, 5, 64, 1000])
 def test_insert_ragged_and_padded_blocks(rq, n):
-    spec = W.InsertSpec("ins", n, 4096, 32, 16, seed=n)
+    blocks = 2 * W.ceil_div(n, 16) + 1
+    spec = W.InsertSpec("ins", n, 4096, blocks, 16, seed=n)
     inp = W.insert_inputs(spec)
     pad = 16 * 528 + 48                          # block stride with padding bytes
-    kc = torch.full((32, pad), 0xA5, dtype=torch.uint8)
+    kc = torch.full((blocks, pad), 0xA5, dtype=torch.uint8)
     slots = inp["slot_mapping"].clone()
     if n > 3:
         slots[::3] = -1                          # skipped tokens
