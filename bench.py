@@ -43,7 +43,7 @@ STEP_BYTES = INV_BYTES + INS_BYTES
 L2_BYTES = 126 * 2 ** 20
 FALLBACK_HBM_GBS = 6400.0
 # the kernel the default (auto) variant launches at the benchmarked shape
-INV_KERNEL_NAME = "inv_rope_fp8_quant_tma_kernel"
+INV_KERNEL_NAME = "inv_rope_fp8_quant_stream_kernel"
 
 
 def parse():

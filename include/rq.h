@@ -111,11 +111,12 @@ rq_status rq_inv_rope_fp8_quant(const void *x_bf16, int64_t n_tokens, int64_t n_
 
 /* Kernel variants of rq_inv_rope_fp8_quant; all produce identical bytes. */
 typedef enum rq_inv_variant {
-    RQ_INV_AUTO = 0,          /* chosen from n_tokens * n_heads (the default)        */
-    RQ_INV_WARP_ROWS = 1,     /* persistent warps, two rows in flight per warp       */
-    RQ_INV_TMA_PIPELINE = 2   /* one producer warp streams 8-row tiles into a ring of
-                                 shared-memory stages with 1-D bulk copies (TMA);
-                                 eight consumer warps compute and store              */
+    RQ_INV_AUTO = 0,          /* chosen from n_tokens * n_heads (the default): the
+                                 stream kernel from 64 rows per SM up, else warp rows */
+    RQ_INV_WARP_ROWS = 1,     /* persistent warps, rows loaded straight to registers */
+    RQ_INV_STREAM = 2         /* every warp streams 8-head tiles through a private
+                                 two-stage ring of shared memory filled by 1-D bulk
+                                 copies (TMA), re-arming each stage once read        */
 } rq_inv_variant;
 
 /* rq_inv_rope_fp8_quant with an explicit kernel variant (rq_inv_variant);

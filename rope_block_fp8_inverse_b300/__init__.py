@@ -17,13 +17,13 @@ import threading
 
 import torch
 
-__all__ = ["VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_TMA_PIPELINE", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
+__all__ = ["VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
 
 HEAD_DIM = 512
 BLOCKS_PER_HEAD = 4
 # kernel variants of the inverse op (rq_inv_variant); all give identical bytes
-VARIANT_AUTO, VARIANT_WARP_ROWS, VARIANT_TMA_PIPELINE = 0, 1, 2
+VARIANT_AUTO, VARIANT_WARP_ROWS, VARIANT_STREAM = 0, 1, 2
 RECORD_BYTES = 528
 DEFAULT_EPS = 1e-10
 

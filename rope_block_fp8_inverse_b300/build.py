@@ -22,9 +22,9 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "librq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-Xptxas", "-v", *ARCH, f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["rq_kernels.cu", "rq_api.cpp"]
+SOURCES = ["rq_kernels.cu", "rq_stream.cu", "rq_api.cpp"]
 
 
 def nvcc() -> str:

@@ -75,8 +75,7 @@ RQ_EXPORT rq_status rq_inv_rope_fp8_quant_ex(const void* x_bf16, int64_t n_token
                                              int64_t heads_per_group, float eps, uint8_t* out_fp8,
                                              float* out_scales, uint32_t* error_flags,
                                              void* stream, int variant) {
-    if (variant != RQ_INV_AUTO && variant != RQ_INV_WARP_ROWS && variant != RQ_INV_TMA_PIPELINE)
-        return RQ_ERR_ARG;
+    if (variant < RQ_INV_AUTO || variant > RQ_INV_STREAM) return RQ_ERR_ARG;
     if (n_tokens < 0 || n_heads < 1 || cache_rows < 1) return RQ_ERR_SHAPE;
     if (heads_per_group < 1 || n_heads % heads_per_group != 0) return RQ_ERR_GROUPING;
     if (!eps_ok(eps)) return RQ_ERR_ARG;

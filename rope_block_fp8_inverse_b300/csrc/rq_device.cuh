@@ -1,16 +1,20 @@
-// rq_device.cuh -- per-row device arithmetic shared by the inverse and the
-// insert kernels (sm_103a).
+// rq_device.cuh -- per-row device arithmetic shared by every kernel of the
+// library (sm_103a).
 //
 // Work unit: one 512-wide head row (one (token, head) of the inverse op, one
-// token of the insert op), owned by one warp. Lane l holds elements
-// [8l, 8l+8) ("half A", blocks 0-1) and [256+8l, 256+8l+8) ("half B",
-// blocks 2-3), so each 16-byte load instruction of the warp reads 512
-// contiguous bytes and each 8-byte store writes 256 contiguous bytes. A
-// lane's 8 elements are 4 whole (even, odd) pairs, so the RoPE partner is
-// in the same thread's registers (no shuffle, no second read). Lanes 24-31
-// of half B hold dims 448..511, the 32 rotated pairs: lane l rotates pairs
-// 4(l-24) .. 4(l-24)+3. A 128-element block is 16 lanes of one half, so the
-// block amax is a 4-step xor-shuffle within 16 lanes.
+// token of the insert op), owned by one warp, in the "block-interleaved" lane
+// layout: lane l owns two 8-element chunks,
+//     A = 16 * (l / 8) + l % 8   and   B = A + 8,
+// both inside 128-element block l / 8. So
+//  * each lane has exactly one block scale, and a block's amax is a 3-step
+//    xor reduction over 8 lanes;
+//  * a warp-wide 16-byte access to every lane's A chunk (or B chunk) touches
+//    four whole 128-byte segments: coalesced in global memory, free of bank
+//    conflicts in shared memory;
+//  * dims 448..511 are the B chunks of lanes 24..31, and a chunk holds four
+//    whole (even, odd) pairs, so the RoPE partner is in the same thread's
+//    registers (no shuffle, no second read): lane l rotates pairs
+//    4(l-24) .. 4(l-24)+3.
 //
 // Arithmetic follows "[vllm] 한 프로그램이 4개 head를 처리하게 하라: DeepSeek-V4
 // inverse RoPE + FP8 quant 커널 3.5배 가속기" (vLLM PR #63540 analysis):
@@ -24,12 +28,14 @@
 namespace rq {
 
 constexpr int kHeadDim = 512;
-constexpr int kHalf = 256;          // elements per half-row
-constexpr int kRopeLane0 = 24;      // first lane whose half-B elements are >= 448
+constexpr int kRopeLane0 = 24;      // first lane whose B chunk is >= dim 448
 constexpr int kCacheWidth = 64;     // cos | sin
 constexpr int kHalfRope = 32;
 constexpr int kRecordBytes = 528;   // paged record: 512 codes + 4 fp32 scales
 constexpr unsigned kFull = 0xffffffffu;
+
+// Index (in 8-element chunks) of lane l's A chunk; its B chunk is A + 8.
+__device__ __forceinline__ int chunk_a(int lane) { return 16 * (lane >> 3) + (lane & 7); }
 
 // Streaming 16-byte read of data touched once: read-only path, no L1 line.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
@@ -41,82 +47,102 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 }
 
 // 16-byte read of data re-read by other warps (cos/sin rows): read-only path.
-__device__ __forceinline__ float4 ld_shared_ro16(const float* p) {
+__device__ __forceinline__ float4 ld_ro16(const float* p) {
     return __ldg(reinterpret_cast<const float4*>(p));
 }
 
-// Streaming 8-byte store (evict-first in L2: written once, read by a later op).
+// Streaming stores (evict-first in L2: written once, read by a later op).
 __device__ __forceinline__ void st_stream8(void* p, uint32_t lo, uint32_t hi) {
     asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(lo), "r"(hi) : "memory");
 }
 
-__device__ __forceinline__ void st_stream16f(void* p, float a, float b, float c, float d) {
-    asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
-                 : "memory");
+__device__ __forceinline__ void st_stream4f(void* p, float v) {
+    asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
-// bf16 pair in one 32-bit word -> two fp32 (exact: bf16 is the top half).
-__device__ __forceinline__ void unpack_bf16x8(const uint4 w, float (&f)[8]) {
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+// The lane's 16 elements as 8 (even, odd) pairs, two pairs per packed
+// register: ev[i] = (even of pair 2i, even of pair 2i+1), od[i] likewise.
+// Pairs 0-3 are chunk A, pairs 4-7 chunk B. bf16 -> fp32 is exact (bf16 is
+// the top half of an fp32).
+struct Pairs {
+    float2 ev[4], od[4];
+};
+
+__device__ __forceinline__ Pairs unpack(uint4 a, uint4 b) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    Pairs p;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(u[i] << 16);
-        f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+        p.ev[i] = make_float2(__uint_as_float(w[2 * i] << 16), __uint_as_float(w[2 * i + 1] << 16));
+        p.od[i] = make_float2(__uint_as_float(w[2 * i] & 0xffff0000u),
+                              __uint_as_float(w[2 * i + 1] & 0xffff0000u));
     }
+    return p;
 }
 
-// Rotate the 4 (even, odd) pairs of f with cos c[i], sin s[i]; every product
-// and every sum is rounded on its own (no FMA contraction).
+// Rotate the four pairs of chunk B with cos c4 and sin s4 (one value per
+// pair). Every product and every sum is rounded on its own, in the page's
+// order (S2): inverse  even' = even*c + odd*s,  odd' = odd*c - even*s;
+//             forward  even' = even*c - odd*s,  odd' = odd*c + even*s.
+// Scalar __fmul_rn / __fadd_rn / __fsub_rn are never contracted into an FMA;
+// packed fp32x2 arithmetic is not used here because ptxas may fuse it, which
+// moves values that sit exactly on an e4m3 rounding tie.
 template <bool kInverse>
-__device__ __forceinline__ void rotate4(float (&f)[8], const float4 c4, const float4 s4) {
+__device__ __forceinline__ void rotate_b(Pairs& p, float4 c4, float4 s4) {
     const float c[4] = {c4.x, c4.y, c4.z, c4.w};
     const float s[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float e = f[2 * i], o = f[2 * i + 1];
-        const float ec = __fmul_rn(e, c[i]), os = __fmul_rn(o, s[i]);
-        const float oc = __fmul_rn(o, c[i]), es = __fmul_rn(e, s[i]);
+    for (int k = 0; k < 4; ++k) {
+        float& e = (k & 1) ? p.ev[2 + k / 2].y : p.ev[2 + k / 2].x;
+        float& o = (k & 1) ? p.od[2 + k / 2].y : p.od[2 + k / 2].x;
+        const float ec = __fmul_rn(e, c[k]), os = __fmul_rn(o, s[k]);
+        const float oc = __fmul_rn(o, c[k]), es = __fmul_rn(e, s[k]);
         if (kInverse) {
-            f[2 * i] = __fadd_rn(ec, os);
-            f[2 * i + 1] = __fsub_rn(oc, es);
+            e = __fadd_rn(ec, os);
+            o = __fsub_rn(oc, es);
         } else {
-            f[2 * i] = __fsub_rn(ec, os);
-            f[2 * i + 1] = __fadd_rn(oc, es);
+            e = __fsub_rn(ec, os);
+            o = __fadd_rn(oc, es);
         }
     }
 }
 
-__device__ __forceinline__ float absmax8(const float (&f)[8]) {
-    float m = fabsf(f[0]);
+__device__ __forceinline__ float absmax(const Pairs& p) {
+    float m0 = fmaxf(fabsf(p.ev[0].x), fabsf(p.ev[0].y));
+    float m1 = fmaxf(fabsf(p.od[0].x), fabsf(p.od[0].y));
 #pragma unroll
-    for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    for (int i = 1; i < 4; ++i) {
+        m0 = fmaxf(m0, fmaxf(fabsf(p.ev[i].x), fabsf(p.ev[i].y)));
+        m1 = fmaxf(m1, fmaxf(fabsf(p.od[i].x), fabsf(p.od[i].y)));
+    }
+    return fmaxf(m0, m1);
+}
+
+// max over the 8 lanes of this lane's block (xor offsets stay in aligned
+// 8-lane groups)
+__device__ __forceinline__ float block_max(float m) {
+#pragma unroll
+    for (int off = 4; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
     return m;
 }
 
-// max over the 16 lanes of this lane's half-warp (xor offsets stay inside
-// aligned 16-lane groups).
-__device__ __forceinline__ float halfwarp_max(float m) {
-#pragma unroll
-    for (int off = 8; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-    return m;
+// Bit pattern of the block scale 2^e, e = ceil(log2(fl32(amax / 448))), read
+// off amax's bits without dividing. With amax = 1.m * 2^E normal, round-to-
+// nearest-even gives fl32(amax/448) <= 2^k exactly when amax/448 <=
+// 2^k (1 + 2^-24), and since no fp32 value lies in (1.75 * 2^(k+8),
+// 1.75 * 2^(k+8) (1 + 2^-24)] that is amax <= 1.75 * 2^(k+8). So e = E - 8
+// when the mantissa field is <= 0x600000 and E - 7 otherwise. Adding 0x1fffff
+// to amax's bits carries into the exponent field exactly when the mantissa
+// field exceeds 0x600000, so the masked sum holds the biased E or E + 1, and
+// subtracting 8 << 23 rebiases it to e. Valid for normal amax >= 0 (the ABI
+// keeps amax >= eps >= 2^-100, and e stays within [-108, 120]).
+__device__ __forceinline__ uint32_t scale_bits(float amax) {
+    return ((__float_as_uint(amax) + 0x1fffffu) & 0x7f800000u) - (8u << 23);
 }
 
-// Exponent of the block scale, e = ceil(log2(fl32(amax / 448))), read off
-// amax's bits without dividing. With amax = 1.m * 2^E normal and k an
-// integer, round-to-nearest-even gives fl32(amax/448) <= 2^k exactly when
-// amax/448 <= 2^k * (1 + 2^-24), and since no fp32 value lies in
-// (1.75 * 2^(k+8), 1.75 * 2^(k+8) * (1 + 2^-24)] that is amax <= 1.75 * 2^(k+8).
-// So e = E - 8 when 1.m <= 1.75 (mantissa field <= 0x600000), else E - 7.
-// Valid for normal amax (the ABI keeps amax >= eps >= 2^-100).
-__device__ __forceinline__ int scale_exponent(float amax) {
-    const uint32_t u = __float_as_uint(amax);
-    const int E = static_cast<int>((u >> 23) & 0xffu) - 127;
-    return E - 8 + ((u & 0x7fffffu) > 0x600000u ? 1 : 0);
-}
-
-__device__ __forceinline__ float pow2f(int e) {  // e in [-126, 127]
-    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+// 2^-e from the bits of 2^e (both normal for e in [-108, 120]).
+__device__ __forceinline__ float inv_scale(uint32_t sbits) {
+    return __uint_as_float((254u << 23) - sbits);
 }
 
 // cvt.rn.satfinite.e4m3x2.f32 d, a, b puts a in the upper byte and b in the
@@ -127,46 +153,45 @@ __device__ __forceinline__ uint32_t e4m3x2(float even, float odd) {
     return r;
 }
 
-// 8 fp32 values times an exact power-of-two inverse scale -> 8 e4m3 codes.
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float inv) {
-    uint2 q;
-    q.x = e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
-          (e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16);
-    q.y = e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
-          (e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16);
-    return q;
+// Exact power-of-two scaling of two values at once (mul.rn.f32x2). The result
+// feeds only the e4m3 conversion, so no contraction can change it.
+__device__ __forceinline__ float2 mul2_exact(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
+// 16 values times an exact power-of-two inverse scale -> 16 e4m3 codes in
+// element order (even of pair k at byte 2k, odd at byte 2k+1): x, y hold
+// chunk A's 8 codes, z, w chunk B's.
+__device__ __forceinline__ uint4 quant16(const Pairs& p, float inv) {
+    const float2 iv = make_float2(inv, inv);
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 e = mul2_exact(p.ev[i], iv);
+        const float2 o = mul2_exact(p.od[i], iv);
+        q[i] = e4m3x2(e.x, o.x) | (e4m3x2(e.y, o.y) << 16);
+    }
+    return make_uint4(q[0], q[1], q[2], q[3]);
 }
 
-// Loaded operands of one row for one lane.
-struct RowRegs {
-    uint4 a, b;      // half A / half B bf16 x8
-    float4 c, s;     // cos / sin of this lane's 4 pairs (lanes 24..31 only)
-};
-
-// Quantised result of one row for one lane.
-struct RowOut {
-    uint2 qa, qb;    // 8 codes of half A, 8 of half B
-    float sa, sb;    // this lane's block scales (block lane/16, 2 + lane/16)
-};
-
+// One row for one lane: chunks a (A) and b (B) as bf16 x8; rope lanes pass
+// the cos / sin of their four pairs. Returns the 16 codes and sets *scale to
+// the lane's block scale.
 template <bool kInverse>
-__device__ __forceinline__ RowOut rope_quant_row(const RowRegs& in, int lane, float eps) {
-    float fa[8], fb[8];
-    unpack_bf16x8(in.a, fa);
-    unpack_bf16x8(in.b, fb);
-    if (lane >= kRopeLane0) rotate4<kInverse>(fb, in.c, in.s);
-    float ma = halfwarp_max(absmax8(fa));
-    float mb = halfwarp_max(absmax8(fb));
-    ma = fmaxf(ma, eps);
-    mb = fmaxf(mb, eps);
-    const int ea = scale_exponent(ma);
-    const int eb = scale_exponent(mb);
-    RowOut o;
-    o.qa = quant8(fa, pow2f(-ea));
-    o.qb = quant8(fb, pow2f(-eb));
-    o.sa = pow2f(ea);
-    o.sb = pow2f(eb);
-    return o;
+__device__ __forceinline__ uint4 rope_quant_row(uint4 a, uint4 b, bool rope_lane, float4 c4,
+                                                float4 s4, float eps, float* scale) {
+    Pairs p = unpack(a, b);
+    if (rope_lane) rotate_b<kInverse>(p, c4, s4);
+    const uint32_t sb = scale_bits(fmaxf(block_max(absmax(p)), eps));
+    *scale = __uint_as_float(sb);
+    return quant16(p, inv_scale(sb));
+}
+
+// Store one quantised row: 8 codes of chunk A, 8 of chunk B, and (from the
+// first lane of each block) the block's fp32 scale.
+__device__ __forceinline__ void store_row(uint8_t* codes, float* scales4, int lane, int ca,
+                                          uint4 q, float scale) {
+    st_stream8(codes + 8 * ca, q.x, q.y);
+    st_stream8(codes + 8 * (ca + 8), q.z, q.w);
+    if ((lane & 7) == 0) st_stream4f(scales4 + (lane >> 3), scale);
 }
 
 }  // namespace rq

@@ -52,11 +52,16 @@ struct InsParams {
 enum InvVariant {
     kInvAuto = 0,        // chosen from the problem size
     kInvWarpRows = 1,    // persistent warps, register loads (rq_kernels.cu)
-    kInvTmaPipeline = 2  // bulk-copy (TMA) shared-memory pipeline (rq_kernels.cu)
+    kInvStream = 2       // one TMA ring per warp (rq_stream.cu)
 };
+
+// The automatic choice takes the stream kernel from this many rows per SM up.
+constexpr int64_t kStreamMinRowsPerSm = 64;
 
 cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev, int variant,
                                       cudaStream_t stream);
+cudaError_t launch_inv_rope_fp8_quant_stream(const InvParams& p, const DeviceInfo& dev,
+                                             cudaStream_t stream);
 cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& dev,
                                          cudaStream_t stream);
 

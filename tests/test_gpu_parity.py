@@ -57,7 +57,8 @@ def assert_parity(got_codes, got_scales, want_codes, want_scales, exact=False):
     return bad.size
 
 
-VARIANTS = pytest.mark.parametrize("variant", [1, 2], ids=["warp_rows", "tma_pipeline"])
+VARIANT_IDS = {1: "warp_rows", 2: "stream"}
+VARIANTS = pytest.mark.parametrize("variant", list(VARIANT_IDS), ids=list(VARIANT_IDS.values()))
 
 
 def run_inverse(rq, inp, eps=1e-10, x_override=None, variant=0):
@@ -151,7 +152,11 @@ def test_strided_inputs(rq, variant):
     wide = torch.zeros(77, 21, 512, dtype=torch.bfloat16)
     wide[:, 3:19] = x
     head_major = x.transpose(0, 1).contiguous().transpose(0, 1)
-    for xv in (wide.cuda()[:, 3:19], head_major.cuda()):
+    # head stride of 520 elements (a multiple of 8, not 16) and a base 16 bytes
+    # past a 32-byte boundary: kernels that read 32 bytes per lane must fall back
+    odd = torch.zeros(77, 16, 520, dtype=torch.bfloat16)
+    odd[:, :, 8:] = x
+    for xv in (wide.cuda()[:, 3:19], head_major.cuda(), odd.cuda()[:, :, 8:]):
         gc, gs = run_inverse(rq, inp, x_override=xv, variant=variant)
         assert_parity(gc, gs, wc, ws, exact=True)
 
@@ -193,6 +198,20 @@ def test_eps_and_special_values(rq, variant, eps):
                 "cos_sin_cache": W.rope_cache(64), "heads_per_group": 2}
     gc, gs = run_inverse(rq, spec_inp, eps=eps, variant=variant)
     wc, ws = oracle_inverse(spec_inp, eps=eps)
+    assert_parity(gc, gs, wc, ws, exact=True)
+
+
+@VARIANTS
+def test_rotation_tie_is_not_fused(rq, variant):
+    """A rotated value on an exact e4m3 rounding tie (the oracle pin's worked
+    case): an FMA anywhere in the rotation would flip its code."""
+    from test_oracle_pins import TIE_POSITION, tie_row
+    inp = {"x": torch.tensor(tie_row()).to(torch.bfloat16).expand(3, 4, 512).contiguous(),
+           "positions": torch.tensor([TIE_POSITION] * 3), "cos_sin_cache": W.rope_cache(8192),
+           "heads_per_group": 2}
+    gc, gs = run_inverse(rq, inp, variant=variant)
+    wc, ws = oracle_inverse(inp)
+    assert wc[0, 0, 494] == 4
     assert_parity(gc, gs, wc, ws, exact=True)
 
 

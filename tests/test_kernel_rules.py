@@ -1,20 +1,28 @@
 """CPU checks of the exact reformulations the CUDA kernels use, against the oracle.
 
-The kernels never divide amax by 448: they read the scale exponent off
-amax's bits (e = E - 8, plus one when the mantissa exceeds 1.75). That rule
-is equal to the oracle's definition, e = ceil(log2(fl32(amax / 448))), for
-every normal amax; this test restates the rule (it is the kernel's formula,
-not the oracle's) and compares it with the oracle at every binade boundary
-and over a dense stride of all normal fp32 values >= 2^-100 (the ABI's
-smallest eps, so the smallest possible amax).
+The kernels never divide amax by 448 nor take a logarithm: they build the
+scale's fp32 bit pattern from amax's bits, ((bits + 0x1fffff) & 0x7f800000) -
+(8 << 23), i.e. 2^(E-8) when amax's mantissa field is <= 0x600000 and
+2^(E-7) above it, and the inverse scale as (254 << 23) minus that pattern.
+This test restates that rule (it is the kernel's formula, not the oracle's)
+and compares it with the oracle's definition, 2^ceil(log2(fl32(amax / 448))),
+at every binade boundary and over a dense stride of all normal fp32 values
+>= 2^-100 (the ABI's smallest eps, so the smallest possible amax).
 """
 import numpy as np
 
 
+def kernel_scale_rule(amax: np.ndarray):
+    u = amax.view(np.uint32).astype(np.uint64)
+    sbits = (((u + 0x1FFFFF) & 0x7F800000) - (8 << 23)).astype(np.uint32)
+    inv = ((254 << 23) - sbits.astype(np.int64)).astype(np.uint32)
+    return sbits.view(np.float32), inv.view(np.float32)
+
+
 def kernel_exponent_rule(amax: np.ndarray) -> np.ndarray:
-    u = amax.view(np.uint32).astype(np.int64)
-    E = ((u >> 23) & 0xFF) - 127
-    return E - 8 + ((u & 0x7FFFFF) > 0x600000)
+    s, inv = kernel_scale_rule(amax)
+    assert np.all(s.astype(np.float64) * inv.astype(np.float64) == 1.0)
+    return ((s.view(np.uint32) >> 23) & 0xFF).astype(np.int64) - 127
 
 
 def _oracle_exponent(oracle_lib, amax):

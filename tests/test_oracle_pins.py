@@ -342,6 +342,40 @@ def test_worked_case_exact_grid_block(oracle_lib):
         assert np.array_equal(codes[0, 0, :448][zero[:448]], signs[:448][zero[:448]])
 
 
+# A rotated value that lands exactly on a round-to-nearest-even tie of the
+# e4m3 grid when each product and the sum are rounded on their own (the op
+# order of the inverse-RoPE page, S2): pair 23 of a row at position 5386 of
+# the 8192-row theta=10000 cache, block 3's scale fixed at 2^-2 by a 100.
+# A fused multiply-add would land just below the tie and give code 3.
+TIE_POSITION = 5386
+TIE_E, TIE_O = -0.4296875, 0.34375
+
+
+def tie_row():
+    x = np.zeros((1, 1, 512), np.float32)
+    x[0, 0, 384] = 100.0
+    x[0, 0, 494] = TIE_E
+    x[0, 0, 495] = TIE_O
+    return x
+
+
+def test_worked_case_rotation_tie(oracle_lib):
+    cache = W.rope_cache(8192)
+    c = np.float32(cache[TIE_POSITION, 23].item())
+    s = np.float32(cache[TIE_POSITION, 32 + 23].item())
+    e, o = np.float32(TIE_E), np.float32(TIE_O)
+    even = np.float32(np.float32(e * c) + np.float32(o * s))   # numpy fp32: each op rounded
+    scale = 0.25                                                 # 2^ceil(log2(100/448))
+    assert Fraction(float(even)) / Fraction(scale) == Fraction(7, 2) * Fraction(1, 2 ** 9)
+    fused = np.float32(np.float64(e) * np.float64(c) + np.float64(np.float32(o * s)))
+    assert float(fused) / scale < 3.5 * 2.0 ** -9                # the fused value is below the tie
+    codes, scales = oracle_lib.inv_rope_fp8_quant(
+        _bf16(tie_row()), torch.tensor([TIE_POSITION]), cache, 1)
+    assert scales[0, 0, 3] == np.float32(scale)
+    assert codes[0, 0, 494] == 4                                 # the tie goes to the even code
+    assert codes[0, 0, 384] == 0x7C                              # 100 * 4 = 400 = 1.5625 * 2^8
+
+
 def test_layout_fingerprint_groups(oracle_lib):
     """Token t, head h filled with 2^(h + 2t - 12): scale 2^(h + 2t - 20); codes all
     equal. The scale of every (t, g, hig*4+b) slot identifies which head landed there."""
