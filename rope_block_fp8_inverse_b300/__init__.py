@@ -176,6 +176,8 @@ def rope_fp8_quant_insert(kv: torch.Tensor, positions: torch.Tensor, cos_sin_cac
         raise ValueError("cos_sin_cache must be a contiguous [P, 64] fp32 tensor")
     if k_cache.dim() != 2 or k_cache.stride(1) != 1:
         raise ValueError("k_cache must be [num_blocks, block_bytes] with contiguous rows")
+    if k_cache.shape[1] < int(block_size) * RECORD_BYTES:
+        raise ValueError(f"k_cache rows must hold block_size * {RECORD_BYTES} bytes")
     for t in (positions, slot_mapping, cos_sin_cache, k_cache):
         if t.device != kv.device:
             raise ValueError("all tensors must be on the same device")

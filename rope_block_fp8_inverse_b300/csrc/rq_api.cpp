@@ -160,5 +160,7 @@ RQ_EXPORT rq_status rq_rope_fp8_quant_insert(const void* kv_bf16, int64_t n_toke
     p.block_stride = block_stride_bytes;
     p.eps = eps;
     p.error_flags = error_flags;
-    return from_cuda(rq::launch_rope_fp8_quant_insert(p, dev, static_cast<cudaStream_t>(stream)));
+    return from_cuda(
+        rq::launch_rope_fp8_quant_insert(p, dev, static_cast<cudaStream_t>(stream)));
 }
+

@@ -42,13 +42,14 @@ inv_rope_fp8_quant_kernel(InvParams p) {
             if (r < p.n_rows) {  // warp-uniform
                 const uint32_t t = r / p.n_heads;
                 const uint32_t h = r - t * p.n_heads;
+                // the row's reads do not wait for its position: only cos/sin do
+                const uint16_t* row = x + static_cast<int64_t>(t) * p.sx_t +
+                                      static_cast<int64_t>(h) * p.sx_h;
+                a[i] = ld_stream16(row + 8 * ca);
+                b[i] = ld_stream16(row + 8 * (ca + 8));
                 const int64_t pos = __ldg(p.positions + t);
                 live[i] = static_cast<uint64_t>(pos) < static_cast<uint64_t>(p.cache_rows);
                 if (live[i]) {
-                    const uint16_t* row = x + static_cast<int64_t>(t) * p.sx_t +
-                                          static_cast<int64_t>(h) * p.sx_h;
-                    a[i] = ld_stream16(row + 8 * ca);
-                    b[i] = ld_stream16(row + 8 * (ca + 8));
                     if (rope_lane) {
                         const float* cs = p.cache + pos * kCacheWidth + cs_col;
                         c[i] = ld_ro16(cs);
@@ -95,6 +96,10 @@ rope_fp8_quant_insert_kernel(InsParams p) {
             live[i] = false;
             slot[i] = -1;
             if (t < p.n_tokens) {
+                // the row's reads do not wait for its position or slot
+                const uint16_t* row = kv + static_cast<int64_t>(t) * p.skv;
+                a[i] = ld_stream16(row + 8 * ca);
+                b[i] = ld_stream16(row + 8 * (ca + 8));
                 const int64_t pos = __ldg(p.positions + t);
                 slot[i] = __ldg(p.slot_mapping + t);
                 const bool pos_ok =
@@ -102,9 +107,6 @@ rope_fp8_quant_insert_kernel(InsParams p) {
                 const bool slot_ok = slot[i] < n_slots;
                 live[i] = pos_ok && slot_ok && slot[i] >= 0;
                 if (live[i]) {
-                    const uint16_t* row = kv + static_cast<int64_t>(t) * p.skv;
-                    a[i] = ld_stream16(row + 8 * ca);
-                    b[i] = ld_stream16(row + 8 * (ca + 8));
                     if (rope_lane) {
                         const float* cs = p.cache + pos * kCacheWidth + cs_col;
                         c[i] = ld_ro16(cs);

@@ -55,8 +55,11 @@ enum InvVariant {
     kInvStream = 2       // one TMA ring per warp (rq_stream.cu)
 };
 
-// The automatic choice takes the stream kernel from this many rows per SM up.
-constexpr int64_t kStreamMinRowsPerSm = 64;
+// The automatic choice takes the inverse op's stream kernel from this many
+// rows per SM up (measured on B300: the warp-rows kernel is as fast or faster
+// up to 4096 tokens x 32 heads, the stream kernel faster at 16384 x 32).
+constexpr int64_t kStreamMinRowsPerSm = 2048;
+
 
 cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev, int variant,
                                       cudaStream_t stream);

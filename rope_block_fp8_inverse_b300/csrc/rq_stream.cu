@@ -7,6 +7,9 @@
 // cp.async.bulk) that complete on the stage's mbarrier. The warp keeps
 // kStages tiles in flight: it waits for the oldest stage, computes and
 // stores its rows, then re-arms that same stage with the tile kStages ahead.
+// A tile's codes and scales are gathered in one of two shared-memory output
+// buffers and leave with two bulk stores (4 KiB of codes and 128 bytes of
+// scales for an 8-head tile), so the writes too are large contiguous copies.
 // There is no producer warp and no barrier shared between warps, so the
 // bytes in flight per SM (resident warps x kStages x kRows KiB) cost no
 // registers and no cross-warp handshakes.
@@ -31,7 +34,10 @@ namespace rq {
 
 namespace {
 
-constexpr int kStreamWarps = 8;  // warps per CTA; each runs its own ring
+#ifndef RQ_STREAM_WARPS
+#define RQ_STREAM_WARPS 8
+#endif
+constexpr int kStreamWarps = RQ_STREAM_WARPS;  // warps per CTA; each runs its own ring
 
 template <int kRows, int kStages>
 struct Ring {
@@ -39,10 +45,12 @@ struct Ring {
     static constexpr uint32_t kCsBytes = kCacheWidth * 4;     // cos | sin row
     static constexpr uint32_t kStageBytes = kRows * kRowBytes + kCsBytes;
     static constexpr uint32_t kBarBytes = 128;                // the ring's mbarriers, padded
-    static constexpr uint32_t kWarpBytes = kBarBytes + kStages * kStageBytes;
+    static constexpr uint32_t kOutBytes = kRows * (kHeadDim + 16);  // a tile's codes + scales
+    static constexpr uint32_t kWarpBytes = kBarBytes + kStages * kStageBytes + 2 * kOutBytes;
     static constexpr uint32_t kCtaBytes = kStreamWarps * kWarpBytes;
     static_assert(kStages * 8 <= int(kBarBytes), "too many stages for the barrier block");
     static_assert(kStageBytes % 128 == 0, "stages must stay 128-byte aligned");
+    static_assert(kOutBytes % 16 == 0, "output buffers must stay 16-byte aligned");
 };
 
 // A warp's tiles are warp, warp + n_warps, warp + 2 n_warps, ...; this walks
@@ -83,6 +91,7 @@ inv_rope_fp8_quant_stream_kernel(InvParams p) {
     const uint32_t n_mine = (n_tiles - warp + n_warps - 1) / n_warps;
     const uint32_t bar0 = smem_addr(smem) + wib * R::kWarpBytes;
     const uint32_t stage0 = bar0 + R::kBarBytes;
+    const uint32_t out0 = stage0 + kStages * R::kStageBytes;
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
         mbar_init_fence();
@@ -156,6 +165,13 @@ inv_rope_fp8_quant_stream_kernel(InvParams p) {
                 s4 = lds16f(st + kRows * R::kRowBytes + kHalfRope * 4 + cs_off);
             }
             const int64_t r0 = int64_t(cw.t) * p.n_heads + h0;
+            // the tile's codes and scales are gathered in output buffer j % 2
+            // and written with two bulk stores: the buffer's previous store
+            // (tile j - 2, one commit group older than the newest) must have
+            // finished reading it
+            const uint32_t ob = out0 + (j & 1u) * R::kOutBytes;
+            if (lane == 0) bulk_wait_read_all_but_newest();
+            __syncwarp();
 #pragma unroll
             for (int i = 0; i < kRows; ++i) {
                 if (uint32_t(i) < nrows) {
@@ -164,15 +180,26 @@ inv_rope_fp8_quant_stream_kernel(InvParams p) {
                     const uint4 b = lds16(row + 16 * (ca + 8));
                     float scale;
                     const uint4 q = rope_quant_row<true>(a, b, rope_lane, c4, s4, p.eps, &scale);
-                    store_row(p.out + (r0 + i) * kHeadDim, p.scales + (r0 + i) * 4, lane, ca, q,
-                              scale);
+                    const uint32_t o = ob + i * kHeadDim;
+                    sts8(o + 8 * ca, q.x, q.y);
+                    sts8(o + 8 * (ca + 8), q.z, q.w);
+                    if ((lane & 7) == 0) sts4f(ob + kRows * kHeadDim + i * 16 + (lane >> 3) * 4, scale);
                 }
             }
+            fence_proxy_async_smem();  // this lane's writes, visible to the bulk stores
+            __syncwarp();
+            if (lane == 0) {
+                bulk_s2g(p.out + r0 * kHeadDim, ob, nrows * kHeadDim);
+                bulk_s2g(p.scales + r0 * 4, ob + kRows * kHeadDim, nrows * 16);
+            }
         }
+        if (lane == 0) bulk_commit();  // one group per tile (empty for a skipped tile)
         cw.next();
         __syncwarp();  // every lane has read stage s: it may be refilled
         if (j + kStages < n_mine) issue(j + kStages);
     }
+    if (lane == 0) bulk_wait_all();  // no bulk store may still read shared memory at exit
+    __syncwarp();
     if (!ok) {
         // a wait gave up (never expected): report it, and let no copy still
         // land in this warp's stages after the CTA exits

@@ -260,13 +260,15 @@ def test_preallocated_fp8_output_and_stream(rq):
 
 # ---------------------------------------------------------------- insert op
 
-def run_insert(rq, inp, k_cache=None, slots=None, eps=1e-10, flags=None):
+def run_insert(rq, inp, k_cache=None, slots=None, eps=1e-10, flags=None, kv=None,
+               positions=None):
     dev = torch.device("cuda:0")
     kc = (inp["k_cache"] if k_cache is None else k_cache).to(dev).contiguous()
     sl = (inp["slot_mapping"] if slots is None else slots).to(dev)
-    rq.rope_fp8_quant_insert(inp["kv"].to(dev), inp["positions"].to(dev),
-                             inp["cos_sin_cache"].to(dev), sl, kc, inp["block_size"], eps=eps,
-                             error_flags=flags)
+    kvd = (inp["kv"] if kv is None else kv).to(dev)
+    pos = (inp["positions"] if positions is None else positions).to(dev)
+    rq.rope_fp8_quant_insert(kvd, pos, inp["cos_sin_cache"].to(dev), sl, kc, inp["block_size"],
+                             eps=eps, error_flags=flags)
     torch.cuda.synchronize()
     return kc.cpu().numpy()
 
@@ -319,4 +321,31 @@ def test_insert_slot_out_of_range_flags(rq):
     assert int(flags.item()) == 2
     ok = torch.tensor([0, -1, 3, -1, -1, 7])
     want = oracle_insert(inp, slots=ok)
+    _assert_cache_parity(got, want)
+
+
+def test_insert_position_out_of_range_flags(rq):
+    """A bad position skips its token (record untouched) and sets the flag."""
+    spec = W.InsertSpec("ins-pos", 9, 64, 3, 4, seed=4)
+    inp = W.insert_inputs(spec)
+    pos = inp["positions"].clone()
+    pos[1] = 64
+    pos[6] = -3
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    got = run_insert(rq, inp, flags=flags, positions=pos)
+    assert int(flags.item()) == 1
+    slots = inp["slot_mapping"].clone()
+    slots[[1, 6]] = -1
+    want = oracle_insert(inp, slots=slots)
+    _assert_cache_parity(got, want)
+
+
+def test_insert_strided_kv(rq):
+    """kv rows with a token stride of 520 elements (not contiguous) give the same bytes."""
+    spec = W.InsertSpec("ins-strided", 300, 4096, 10, 32, seed=6)
+    inp = W.insert_inputs(spec)
+    wide = torch.zeros(300, 520, dtype=torch.bfloat16)
+    wide[:, :512] = inp["kv"]
+    got = run_insert(rq, inp, kv=wide.cuda()[:, :512])
+    want = oracle_insert(inp)
     _assert_cache_parity(got, want)
