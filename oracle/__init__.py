@@ -72,6 +72,11 @@ def _load():
                                                       ctypes.c_float, P, P, ctypes.c_int]),
             "rqo_rope_fp8_quant_insert": (ctypes.c_int, [P, i64, i64, P, P, i64, P, P, i64,
                                                          i64, i64, ctypes.c_float, ctypes.c_int]),
+            "rqo_f32_to_bf16": (ctypes.c_uint16, [ctypes.c_float]),
+            "rqo_ue8m0_of_scale": (ctypes.c_uint8, [ctypes.c_float]),
+            "rqo_f32_to_bf16_array": (None, [P, i64, P]),
+            "rqo_pack_ue8m0_array": (None, [P, i64, P]),
+            "rqo_inv_rope_bf16": (ctypes.c_int, [P, i64, i64, i64, i64, P, P, i64, i64, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -145,6 +150,25 @@ def block_scale(amax) -> np.ndarray:
     return out
 
 
+def f32_to_bf16(v) -> np.ndarray:
+    """bf16 bit patterns (uint16) of fp32 values, round to nearest, ties to even."""
+    v = _np(v, np.float32)
+    out = np.empty(v.shape, np.uint16)
+    _load().rqo_f32_to_bf16_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def pack_ue8m0(scales) -> np.ndarray:
+    """Pack [..., 4] power-of-two fp32 block scales into one uint32 per head:
+    byte b = UE8M0 code (exponent + 127) of block b's scale."""
+    s = _np(scales, np.float32)
+    if s.shape[-1] % BLOCKS_PER_HEAD:
+        raise OracleError("the last dim must hold whole heads (4 scales each)")
+    out = np.empty(s.shape[:-1] + (s.shape[-1] // BLOCKS_PER_HEAD,), np.uint32)
+    _load().rqo_pack_ue8m0_array(_ptr(s), out.size, _ptr(out))
+    return out
+
+
 # ------------------------------------------------------------------ row steps
 
 def rope_rows(rows, positions, cos_sin_cache, inverse: bool) -> np.ndarray:
@@ -207,6 +231,24 @@ def inv_rope_fp8_quant(x, positions, cos_sin_cache, heads_per_group: int,
     if rc:
         raise OracleError(f"rqo_inv_rope_fp8_quant status {rc}")
     return codes, scales
+
+
+def inv_rope_bf16(x, positions, cos_sin_cache, heads_per_group: int) -> np.ndarray:
+    """The non-quantising variant: inverse RoPE of x [N, H, 512] bf16 as bf16
+    bit patterns, [N, G, hpg*512] uint16."""
+    arr = _np(x, np.uint16)
+    n, h = arr.shape[0], arr.shape[1]
+    pos = _np(positions, np.int64)
+    cs = _np(cos_sin_cache, np.float32)
+    hpg = int(heads_per_group)
+    if hpg < 1 or h % hpg:
+        raise OracleError("heads_per_group must divide the head count")
+    out = np.empty((n, h // hpg, hpg * HEAD_DIM), np.uint16)
+    rc = _load().rqo_inv_rope_bf16(_ptr(arr), n, h, h * HEAD_DIM, HEAD_DIM, _ptr(pos), _ptr(cs),
+                                   cs.shape[0], hpg, _ptr(out))
+    if rc:
+        raise OracleError(f"rqo_inv_rope_bf16 status {rc}")
+    return out
 
 
 def rope_fp8_quant_insert(kv, positions, cos_sin_cache, slot_mapping, k_cache,

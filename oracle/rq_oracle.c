@@ -44,6 +44,13 @@
  *  - paged record of one token: 512 code bytes then the 4 fp32 block scales
  *    (528 bytes) at k_cache + (slot / block_size) * block_stride
  *    + (slot % block_size) * 528; a negative slot means "skip this token".
+ *  - UE8M0 scale packing ([INV] S3 mentions it without a layout): each
+ *    power-of-two block scale 2^e becomes the byte e + 127 (the OCP
+ *    Microscaling E8M0 encoding, value 2^(byte - 127)), and the four blocks
+ *    of a head are packed into one 32-bit word, block b in bits 8b..8b+7;
+ *  - the non-quantising variant ([INV] S4, CompileKey.quantize): the
+ *    inverse-rotated head is written as bf16, each fp32 value rounded to
+ *    the nearest bf16, ties to even, in the same [N, G, hpg*512] layout.
  */
 #include <math.h>
 #include <pthread.h>
@@ -81,6 +88,41 @@ float rqo_bf16_to_f32(uint16_t b)
 
 /* [OFP8] E4M3 decode: s eeee mmm; e == 0 is subnormal m/8 * 2^-6,
  * otherwise (1 + m/8) * 2^(e-7); s 1111 111 is NaN. */
+/* Nearest bf16 to an fp32 value, ties to even (IEEE-754 round to nearest on
+ * the 16 dropped bits; a carry out of the mantissa correctly moves to the
+ * next binade or to infinity). NaN stays NaN (sign kept, quiet bit set). */
+uint16_t rqo_f32_to_bf16(float f)
+{
+    uint32_t u, lo, hi;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    hi = u >> 16;
+    lo = u & 0xffffu;
+    if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u)))
+        hi += 1u;
+    return (uint16_t)hi;
+}
+
+/* OCP Microscaling E8M0 byte of a power-of-two scale 2^e (e in [-127, 127]):
+ * e + 127. frexp gives s = 0.5 * 2^E exactly for a power of two, so e = E - 1. */
+uint8_t rqo_ue8m0_of_scale(float s)
+{
+    int E;
+    (void)frexp((double)s, &E);
+    return (uint8_t)(E - 1 + 127);
+}
+
+/* Four block scales of a head packed as UE8M0 bytes, block b in bits 8b..8b+7. */
+uint32_t rqo_pack_ue8m0(const float *scales4)
+{
+    uint32_t w = 0;
+    int b;
+    for (b = 0; b < BLOCKS_PER_HEAD; ++b)
+        w |= (uint32_t)rqo_ue8m0_of_scale(scales4[b]) << (8 * b);
+    return w;
+}
+
 double rqo_e4m3_decode(uint8_t c)
 {
     int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
@@ -230,6 +272,20 @@ void rqo_block_scale_array(const float *amax, int64_t n, float *out)
 }
 
 /* rows: [R, 512] fp32, rotated in place with cache row pos[r] */
+void rqo_f32_to_bf16_array(const float *v, int64_t n, uint16_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = rqo_f32_to_bf16(v[i]);
+}
+
+void rqo_pack_ue8m0_array(const float *scales, int64_t heads, uint32_t *out)
+{
+    int64_t i;
+    for (i = 0; i < heads; ++i)
+        out[i] = rqo_pack_ue8m0(scales + i * BLOCKS_PER_HEAD);
+}
+
 int rqo_rope_rows(float *rows, int64_t R, const int64_t *pos,
                   const float *cache, int64_t cache_rows, int inverse)
 {
@@ -373,6 +429,43 @@ int rqo_inv_rope_fp8_quant(const uint16_t *x, int64_t n_tokens,
     a.t1 = n_tokens;
     return split_run(inv_worker, &a, sizeof a, n_tokens, nthreads,
                      inv_set_range);
+}
+
+/* The non-quantising variant: inverse RoPE of x [N, H, 512] bf16, written
+ * as bf16 into out [N, H/hpg, hpg*512] (contiguous; head hig of group g at
+ * [hig*512, hig*512 + 512) of row (t, g)). Single-threaded. */
+int rqo_inv_rope_bf16(const uint16_t *x, int64_t n_tokens, int64_t n_heads,
+                      int64_t sx_t, int64_t sx_h, const int64_t *pos,
+                      const float *cache, int64_t cache_rows, int64_t hpg,
+                      uint16_t *out)
+{
+    float row[HEAD_DIM];
+    int64_t t, h, G;
+    int k;
+    if (n_tokens < 0 || n_heads < 1 || cache_rows < 1)
+        return RQO_ERR_ARG;
+    if (hpg < 1 || n_heads % hpg != 0)
+        return RQO_ERR_GROUPING;
+    if (n_tokens == 0)
+        return RQO_OK;
+    if (!x || !pos || !cache || !out)
+        return RQO_ERR_ARG;
+    G = n_heads / hpg;
+    for (t = 0; t < n_tokens; ++t) {
+        if (pos[t] < 0 || pos[t] >= cache_rows)
+            return RQO_ERR_POSITION;
+        for (h = 0; h < n_heads; ++h) {
+            int64_t g = h / hpg, hig = h % hpg;
+            const uint16_t *src = x + t * sx_t + h * sx_h;
+            uint16_t *dst = out + ((t * G + g) * hpg + hig) * HEAD_DIM;
+            for (k = 0; k < HEAD_DIM; ++k)
+                row[k] = rqo_bf16_to_f32(src[k]);
+            rqo_rope_row(row, cache + pos[t] * CACHE_WIDTH, 1);
+            for (k = 0; k < HEAD_DIM; ++k)
+                dst[k] = rqo_f32_to_bf16(row[k]);
+        }
+    }
+    return RQO_OK;
 }
 
 /* ---------------------------------------------------------- insert op */

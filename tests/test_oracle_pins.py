@@ -499,3 +499,72 @@ def test_insert_placement_and_sentinel(oracle_lib):
     # the forward rotation is the +theta one (complex pin)
     ref = _complex_rotate(rows, inp["positions"].numpy(), inp["cos_sin_cache"].numpy(), False)
     assert np.allclose(y, ref, atol=1e-5, rtol=0)
+
+
+# ----------------------------------------------------------------- next rows: bf16 out, UE8M0
+
+def test_bf16_rounding_matches_torch_dense_sweep(oracle_lib):
+    """Round-to-nearest-even fp32 -> bf16 against torch's conversion (a library
+    routine) over every 97th fp32 bit pattern, both signs, NaN excluded."""
+    for sign in (0, 0x80000000):
+        bits = (np.arange(0, 0x7F800001, 97, dtype=np.uint64) | sign).astype(np.uint32)
+        v = bits.view(np.float32)
+        want = torch.from_numpy(v.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(oracle_lib.f32_to_bf16(v), want)
+
+
+@pytest.mark.parametrize("bits,want", [
+    (0x3F808000, 0x3F80),   # 1 + 2^-8: a tie, to the even neighbour 1.0
+    (0x3F818000, 0x3F82),   # 1 + 3*2^-8: a tie, to the even neighbour 1 + 2^-6
+    (0x3F808001, 0x3F81),   # just above the tie: up
+    (0x7F7FFFFF, 0x7F80),   # the largest finite fp32 rounds to +inf
+    (0x7F7F7FFF, 0x7F7F),   # below the last tie: the largest finite bf16
+    (0x80000000, 0x8000),   # -0 keeps its sign
+    (0x00008000, 0x0000),   # subnormal tie to even (0)
+    (0x00018000, 0x0002),   # subnormal tie to even (2)
+    (0xFF800000, 0xFF80),   # -inf
+])
+def test_bf16_rounding_worked_cases(oracle_lib, bits, want):
+    v = np.array([bits], np.uint32).view(np.float32)
+    assert int(oracle_lib.f32_to_bf16(v)[0]) == want
+
+
+def test_bf16_rounding_keeps_nan(oracle_lib):
+    v = np.array([0x7FC00000, 0xFF800001, 0x7F800001], np.uint32).view(np.float32)
+    out = oracle_lib.f32_to_bf16(v)
+    assert np.all((out & 0x7F80) == 0x7F80) and np.all((out & 0x007F) != 0)
+
+
+def test_ue8m0_packing_worked_case(oracle_lib):
+    """OCP Microscaling E8M0: value 2^(byte - 127); block b in bits 8b..8b+7."""
+    s = np.array([2.0 ** -3, 1.0, 2.0 ** 5, 2.0 ** -42], np.float32)
+    assert int(oracle_lib.pack_ue8m0(s)[0]) == (85 << 24) | (132 << 16) | (127 << 8) | 124
+
+
+def test_ue8m0_decodes_to_every_scale_of_a_run(oracle_lib):
+    inp = W.inverse_inputs(W.TINY)
+    codes, scales = oracle_lib.inv_rope_fp8_quant(inp["x"], inp["positions"],
+                                                  inp["cos_sin_cache"], 8)
+    packed = oracle_lib.pack_ue8m0(scales)
+    assert packed.shape == (64, 1, 8)
+    for b in range(4):
+        byte = ((packed >> (8 * b)) & 0xFF).astype(np.int64)
+        dec = np.ldexp(1.0, byte - 127)
+        assert np.array_equal(dec, scales[..., b::4].astype(np.float64))
+
+
+def test_inv_rope_bf16_is_the_rotation_rounded(oracle_lib):
+    """quantize=False: NoPE dims pass through bit-exactly; the rotated dims are
+    torch's bf16 rounding of the (separately pinned) fp32 rotation."""
+    spec = W.InverseSpec("bf16", 37, 12, 6, 8192, "uniform", True, seed=11)
+    inp = W.inverse_inputs(spec)
+    out = oracle_lib.inv_rope_bf16(inp["x"], inp["positions"], inp["cos_sin_cache"], 6)
+    assert out.shape == (37, 2, 6 * 512)
+    xb = inp["x"].view(torch.int16).numpy().view(np.uint16).reshape(37, 12, 512)
+    o = out.reshape(37, 12, 512)
+    assert np.array_equal(o[..., :448], xb[..., :448])
+    rows = oracle_lib.rope_rows(inp["x"].float().numpy().reshape(-1, 512),
+                                np.repeat(inp["positions"].numpy(), 12),
+                                inp["cos_sin_cache"], inverse=True)
+    want = torch.from_numpy(rows).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(o.reshape(-1, 512), want)
