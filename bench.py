@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="steps of the host-buffer end-to-end leg (default min(steps, 20))")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode-launches", type=int, default=300,
+                    help="launches timed per extra output kind / layout (0 skips them)")
     ap.add_argument("--ref-budget-s", type=float, default=60.0,
                     help="host seconds the reference arm's timed + warm-up steps aim to take")
     ap.add_argument("--inv-tokens", type=int, default=None,
@@ -296,6 +298,29 @@ def run_ours(args, world, rank, local):
     ins_ms = statistics.fmean(inv_ev[i][1].elapsed_time(ins_ev[i]) for i in range(args.steps))
     ms_step = total_ms / args.steps
 
+    # the "next" rows of the path (other output kinds and layouts), each timed
+    # like the inverse launch above, outside the step's timed region
+    modes = {}
+    for name, mode, gm in ((("fp8_group_major", "fp8", True), ("ue8m0", "ue8m0", False),
+                            ("ue8m0_group_major", "ue8m0", True), ("bf16", "bf16", False))
+                           if args.mode_launches > 0 else ()):
+        mo, ms = rq.empty_outputs(n, h // hpg, hpg, mode, group_major=gm, device=dev)
+        for _ in range(3):
+            rq.inv_rope_quant(x, pos, cache, hpg, mode=mode, out=mo, scales=ms)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.mode_launches)]
+        torch.cuda.synchronize(dev)
+        for a, b in evs:
+            a.record(stream)
+            rq.inv_rope_quant(x, pos, cache, hpg, mode=mode, out=mo, scales=ms)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+        mb = W.inverse_bytes(n, h, mode)
+        modes[name] = {"us": round(us, 2), "bytes": mb, "GBs": round(mb / us / 1e3, 1),
+                       "frac_of_measured_peak": round(mb / us / 1e3 / measured_peaks()[0], 4)}
+        del mo, ms
+
     # end to end through the public API from pinned host buffers
     e2e_steps = args.e2e_steps or min(args.steps, 20)
     x_host = inv_h["x"].pin_memory()
@@ -385,6 +410,8 @@ def run_ours(args, world, rank, local):
             "path": "pinned host -> device copies, both C-ABI calls, device -> pinned host",
         },
         "gpu_launches": 2 * args.steps,
+        "output_modes": {"kernel": "inv_rope_quant_layout_kernel", "launches_each": args.mode_launches,
+                         "results": modes},
         "clocks": sampler.summary(),
     }
     if args.inv_tokens and args.inv_tokens != INV_SPEC.n_tokens:

@@ -64,7 +64,8 @@ typedef enum rq_status {
     RQ_ERR_ALIGN = 3,    /* a pointer or stride breaks the 16-byte rule     */
     RQ_ERR_GROUPING = 4, /* heads_per_group < 1 or does not divide n_heads  */
     RQ_ERR_CUDA = 5,     /* the CUDA runtime reported an error              */
-    RQ_ERR_ARG = 6       /* eps outside [2^-100, 2^100], or a bad variant   */
+    RQ_ERR_ARG = 6       /* eps outside [2^-100, 2^100], or a bad variant or
+                            output mode                                     */
 } rq_status;
 
 /* device-side error bits (OR-ed into *error_flags) */
@@ -128,6 +129,52 @@ rq_status rq_inv_rope_fp8_quant_ex(const void *x_bf16, int64_t n_tokens, int64_t
                                    int64_t cache_rows, int64_t heads_per_group, float eps,
                                    uint8_t *out_fp8, float *out_scales,
                                    uint32_t *error_flags, void *stream, int variant);
+
+/* What rq_inv_rope_quant_layout writes for each head. */
+typedef enum rq_out_mode {
+    RQ_OUT_FP8_SCALE_F32 = 0,   /* 512 e4m3 codes + 4 fp32 block scales               */
+    RQ_OUT_FP8_SCALE_UE8M0 = 1, /* 512 e4m3 codes + one uint32 of packed UE8M0 scales:
+                                   byte b (bits 8b..8b+7) = the biased exponent of
+                                   block b's power-of-two scale (value 2^(byte-127))  */
+    RQ_OUT_BF16 = 2             /* no quantisation: the 512 inverse-rotated values as
+                                   bf16, each rounded to nearest even                 */
+} rq_out_mode;
+
+/*
+ * Inverse RoPE with a choice of output kind and any output layout ([INV]
+ * S1-S4: the page's kernel has a non-quantising variant (CompileKey.quantize,
+ * S4) and packs scales as UE8M0 as well (S3)). Inputs and numerics are those
+ * of rq_inv_rope_fp8_quant; only the outputs differ:
+ *
+ *  out        head i (0 <= i < heads_per_group) of group g of token t starts at
+ *               out + t*out_stride_token + g*out_stride_group + i*W  (bytes),
+ *             W = 512 (codes) or 1024 (bf16); its W bytes are contiguous.
+ *             16-byte aligned; both strides >= 0 and multiples of 16.
+ *             The contiguous [N, G, hpg*512] layout of rq_inv_rope_fp8_quant is
+ *             out_stride_token = G*hpg*W, out_stride_group = hpg*W; a
+ *             group-major [G, N, hpg*W] buffer is out_stride_group = N*hpg*W,
+ *             out_stride_token = hpg*W.
+ *  scales     element j of group g of token t sits at
+ *               scales + t*scale_stride_token + g*scale_stride_group
+ *                      + j*scale_stride_elem          (in elements),
+ *             j = 4i + b (fp32, RQ_OUT_FP8_SCALE_F32) or j = i (uint32,
+ *             RQ_OUT_FP8_SCALE_UE8M0). 4-byte aligned, strides >= 0.
+ *             Ignored (may be NULL) for RQ_OUT_BF16.
+ *  out_mode   an rq_out_mode; any other value returns RQ_ERR_ARG.
+ *
+ * Outputs that overlap give unspecified bytes. Positions outside
+ * [0, cache_rows) are skipped and flagged as in rq_inv_rope_fp8_quant.
+ * Runs one persistent warp-per-row kernel with per-thread stores.
+ */
+rq_status rq_inv_rope_quant_layout(const void *x_bf16, int64_t n_tokens, int64_t n_heads,
+                                   int64_t x_stride_token, int64_t x_stride_head,
+                                   const int64_t *positions, const float *cos_sin_cache,
+                                   int64_t cache_rows, int64_t heads_per_group, float eps,
+                                   int out_mode, void *out, int64_t out_stride_token,
+                                   int64_t out_stride_group, void *scales,
+                                   int64_t scale_stride_token, int64_t scale_stride_group,
+                                   int64_t scale_stride_elem, uint32_t *error_flags,
+                                   void *stream);
 
 /*
  * Forward RoPE + block-FP8 quant + paged insert ([KV] S1, numerics as above

@@ -17,7 +17,8 @@ import threading
 
 import torch
 
-__all__ = ["VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
+__all__ = ["VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
+           "empty_outputs", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
 
 HEAD_DIM = 512
@@ -25,6 +26,8 @@ BLOCKS_PER_HEAD = 4
 # kernel variants of the inverse op (rq_inv_variant); all give identical bytes
 VARIANT_AUTO, VARIANT_WARP_ROWS, VARIANT_STREAM = 0, 1, 2
 RECORD_BYTES = 528
+# output kinds of inv_rope_quant (rq_out_mode): fp32 scales, packed UE8M0 scales, bf16 (no quant)
+OUT_MODES = {"fp8": 0, "ue8m0": 1, "bf16": 2}
 DEFAULT_EPS = 1e-10
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librq.so")
@@ -41,6 +44,9 @@ ABI_SYMBOLS = {
                                                 ctypes.c_float, _P, _P, _P, _P, ctypes.c_int]),
     "rq_rope_fp8_quant_insert": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _P, _P, _I64,
                                                 _I64, _I64, ctypes.c_float, _P, _P]),
+    "rq_inv_rope_quant_layout": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
+                                                ctypes.c_float, ctypes.c_int, _P, _I64, _I64, _P,
+                                                _I64, _I64, _I64, _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -148,6 +154,93 @@ def inv_rope_fp8_quant(x: torch.Tensor, positions: torch.Tensor, cos_sin_cache: 
             scales.data_ptr(), flags, _stream(x.device), int(variant))
     _check(st, "rq_inv_rope_fp8_quant")
     return out.view(torch.float8_e4m3fn).view(n, g, hpg * HEAD_DIM), scales.view(n, g, hpg * BLOCKS_PER_HEAD)
+
+
+def empty_outputs(n: int, groups: int, heads_per_group: int, mode: str = "fp8",
+                  group_major: bool = False, device=None):
+    """Uninitialised ``(out, scales)`` for :func:`inv_rope_quant`, shaped
+    [N, G, hpg*512] / [N, G, hpg*4] (fp8), [N, G, hpg] int32 (ue8m0) or
+    [N, G, hpg*512] bf16 with ``scales`` None (bf16). With ``group_major`` the
+    storage is [G, N, ...] and the returned tensors are its [N, G, ...] views."""
+    if mode not in OUT_MODES:
+        raise ValueError(f"mode must be one of {sorted(OUT_MODES)}")
+    w = heads_per_group * HEAD_DIM
+    dt = torch.bfloat16 if mode == "bf16" else torch.uint8
+    sw, sdt = ((heads_per_group * BLOCKS_PER_HEAD, torch.float32) if mode == "fp8"
+               else (heads_per_group, torch.int32))
+
+    def alloc(width, dtype):
+        if group_major:
+            return torch.empty((groups, n, width), dtype=dtype, device=device).permute(1, 0, 2)
+        return torch.empty((n, groups, width), dtype=dtype, device=device)
+    return alloc(w, dt), (None if mode == "bf16" else alloc(sw, sdt))
+
+
+def inv_rope_quant(x: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                   heads_per_group: int, mode: str = "fp8", out: torch.Tensor | None = None,
+                   scales: torch.Tensor | None = None, eps: float = DEFAULT_EPS,
+                   error_flags: torch.Tensor | None = None):
+    """Inverse RoPE with a choice of output kind and layout (``rq_inv_rope_quant_layout``).
+
+    ``mode``: "fp8" (e4m3 codes + fp32 block scales), "ue8m0" (codes + one
+    int32 per head holding its four UE8M0 scale bytes, block b in bits
+    8b..8b+7) or "bf16" (no quantisation: the rotated head as bf16).
+    ``out`` is an [N, G, hpg*512] view (uint8 / float8_e4m3fn, or bf16) and
+    ``scales`` an [N, G, hpg*4] fp32 or [N, G, hpg] int32 view; any token /
+    group strides work (e.g. group-major storage, see :func:`empty_outputs`),
+    the last dim must be contiguous for ``out``. Returns ``(out, scales)``.
+    """
+    if mode not in OUT_MODES:
+        raise ValueError(f"mode must be one of {sorted(OUT_MODES)}")
+    _cuda(x, "x", torch.bfloat16)
+    if x.dim() != 3 or x.shape[2] != HEAD_DIM or x.stride(2) != 1:
+        raise ValueError("x must be [N, H, 512] with a contiguous last dim")
+    n, h = x.shape[0], x.shape[1]
+    hpg = int(heads_per_group)
+    if hpg < 1 or h % hpg:
+        raise ValueError(f"heads_per_group={hpg} must divide H={h}")
+    g = h // hpg
+    _cuda(positions, "positions", torch.int64)
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    if positions.shape != (n,) or not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous [N] int64 tensor")
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != 64 or not cos_sin_cache.is_contiguous():
+        raise ValueError("cos_sin_cache must be a contiguous [P, 64] fp32 tensor")
+    if out is None:
+        out, sc = empty_outputs(n, g, hpg, mode, device=x.device)
+        scales = sc if scales is None else scales
+    if mode != "bf16" and scales is None:
+        scales = empty_outputs(n, g, hpg, mode, device=x.device)[1]
+    want_out = (torch.bfloat16,) if mode == "bf16" else (torch.uint8, torch.float8_e4m3fn)
+    if not out.is_cuda or out.dtype not in want_out:
+        raise TypeError(f"out must be a CUDA tensor of {want_out}")
+    if tuple(out.shape) != (n, g, hpg * HEAD_DIM) or out.stride(2) != 1:
+        raise ValueError(f"out must be an [N, G, {hpg * HEAD_DIM}] view with a contiguous last dim")
+    isz = out.element_size()
+    o_t, o_g = out.stride(0) * isz, out.stride(1) * isz
+    s_t = s_g = s_e = 0
+    sptr = 0
+    if mode != "bf16":
+        sdt, sw = (torch.float32, hpg * BLOCKS_PER_HEAD) if mode == "fp8" else (torch.int32, hpg)
+        _cuda(scales, "scales", sdt)
+        if tuple(scales.shape) != (n, g, sw):
+            raise ValueError(f"scales must be an [N, G, {sw}] view")
+        s_t, s_g, s_e = scales.stride()
+        sptr = scales.data_ptr()
+    for t in (positions, cos_sin_cache, out) + ((scales,) if mode != "bf16" else ()):
+        if t.device != x.device:
+            raise ValueError("all tensors must be on the same device")
+    flags = 0
+    if error_flags is not None:
+        _cuda(error_flags, "error_flags", torch.int32)
+        flags = error_flags.data_ptr()
+    with torch.cuda.device(x.device):
+        st = lib().rq_inv_rope_quant_layout(
+            x.data_ptr(), n, h, x.stride(0), x.stride(1), positions.data_ptr(),
+            cos_sin_cache.data_ptr(), cos_sin_cache.shape[0], hpg, float(eps), OUT_MODES[mode],
+            out.data_ptr(), o_t, o_g, sptr, s_t, s_g, s_e, flags, _stream(x.device))
+    _check(st, "rq_inv_rope_quant_layout")
+    return out, scales
 
 
 def rope_fp8_quant_insert(kv: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,

@@ -120,6 +120,58 @@ RQ_EXPORT rq_status rq_inv_rope_fp8_quant(const void* x_bf16, int64_t n_tokens, 
                                     out_fp8, out_scales, error_flags, stream, RQ_INV_AUTO);
 }
 
+RQ_EXPORT rq_status rq_inv_rope_quant_layout(
+    const void* x_bf16, int64_t n_tokens, int64_t n_heads, int64_t x_stride_token,
+    int64_t x_stride_head, const int64_t* positions, const float* cos_sin_cache,
+    int64_t cache_rows, int64_t heads_per_group, float eps, int out_mode, void* out,
+    int64_t out_stride_token, int64_t out_stride_group, void* scales, int64_t scale_stride_token,
+    int64_t scale_stride_group, int64_t scale_stride_elem, uint32_t* error_flags, void* stream) {
+    if (out_mode < RQ_OUT_FP8_SCALE_F32 || out_mode > RQ_OUT_BF16) return RQ_ERR_ARG;
+    if (n_tokens < 0 || n_heads < 1 || cache_rows < 1) return RQ_ERR_SHAPE;
+    if (heads_per_group < 1 || n_heads % heads_per_group != 0) return RQ_ERR_GROUPING;
+    if (!eps_ok(eps)) return RQ_ERR_ARG;
+    if (n_heads >= kMaxRows || n_tokens >= kMaxRows / n_heads) return RQ_ERR_SHAPE;
+    if (out_stride_token < 0 || out_stride_group < 0 || scale_stride_token < 0 ||
+        scale_stride_group < 0 || scale_stride_elem < 0)
+        return RQ_ERR_SHAPE;
+    if (n_tokens == 0) return RQ_OK;
+    const bool quant = out_mode != RQ_OUT_BF16;
+    if (!x_bf16 || !positions || !cos_sin_cache || !out || (quant && !scales)) return RQ_ERR_NULL;
+    if (!aligned(x_bf16, 16) || x_stride_token % 8 != 0 || x_stride_head % 8 != 0 ||
+        !aligned(positions, 8) || !aligned(cos_sin_cache, 16) || !aligned(out, 16) ||
+        out_stride_token % 16 != 0 || out_stride_group % 16 != 0 ||
+        (quant && !aligned(scales, 4)) || (error_flags && !aligned(error_flags, 4)))
+        return RQ_ERR_ALIGN;
+
+    rq::DeviceInfo dev;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    rq::InvParams p;
+    p.x = x_bf16;
+    p.sx_t = x_stride_token;
+    p.sx_h = x_stride_head;
+    p.n_rows = static_cast<uint32_t>(n_tokens * n_heads);
+    p.n_heads = static_cast<uint32_t>(n_heads);
+    p.n_tokens = static_cast<uint32_t>(n_tokens);
+    p.positions = positions;
+    p.cache = cos_sin_cache;
+    p.cache_rows = cache_rows;
+    p.eps = eps;
+    p.out = static_cast<uint8_t*>(out);
+    p.scales = static_cast<float*>(scales);
+    p.error_flags = error_flags;
+    p.lay.mode = out_mode;
+    p.lay.hpg = static_cast<uint32_t>(heads_per_group);
+    p.lay.ot = out_stride_token;
+    p.lay.og = out_stride_group;
+    p.lay.st = scale_stride_token;
+    p.lay.sg = scale_stride_group;
+    p.lay.se = scale_stride_elem;
+    return from_cuda(
+        rq::launch_inv_rope_quant_layout(p, dev, static_cast<cudaStream_t>(stream)));
+}
+
 RQ_EXPORT rq_status rq_rope_fp8_quant_insert(const void* kv_bf16, int64_t n_tokens,
                                              int64_t kv_stride_token, const int64_t* positions,
                                              const float* cos_sin_cache, int64_t cache_rows,

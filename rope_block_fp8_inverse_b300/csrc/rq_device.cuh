@@ -185,6 +185,42 @@ __device__ __forceinline__ uint4 rope_quant_row(uint4 a, uint4 b, bool rope_lane
     return quant16(p, inv_scale(sb));
 }
 
+// Two fp32 values -> one bf16x2 word, each rounded to nearest even (the
+// first value at the lower address). cvt.rn.bf16x2.f32 d, a, b puts a in the
+// upper half.
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The non-quantising row: rotation only, then bf16. Returns chunk A's 8
+// values in *qa and chunk B's in *qb, in element order.
+template <bool kInverse>
+__device__ __forceinline__ void rope_row_bf16(uint4 a, uint4 b, bool rope_lane, float4 c4,
+                                              float4 s4, uint4* qa, uint4* qb) {
+    Pairs p = unpack(a, b);
+    if (rope_lane) rotate_b<kInverse>(p, c4, s4);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        w[2 * i] = bf16x2(p.ev[i].x, p.od[i].x);
+        w[2 * i + 1] = bf16x2(p.ev[i].y, p.od[i].y);
+    }
+    *qa = make_uint4(w[0], w[1], w[2], w[3]);
+    *qb = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__device__ __forceinline__ void st_stream16(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_stream4u(void* p, uint32_t v) {
+    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Store one quantised row: 8 codes of chunk A, 8 of chunk B, and (from the
 // first lane of each block) the block's fp32 scale.
 __device__ __forceinline__ void store_row(uint8_t* codes, float* scales4, int lane, int ca,

@@ -71,6 +71,94 @@ inv_rope_fp8_quant_kernel(InvParams p) {
     }
 }
 
+// ------------------------------------------------------------------ inverse, any output layout
+
+// The warp-rows kernel with the output addressed through OutLayout: fp32 or
+// packed UE8M0 scales, or (kMode == kOutBf16) the rotated head as bf16 with
+// no quantisation, into token-major, group-major or any other strided
+// layout. Loads and arithmetic are those of inv_rope_fp8_quant_kernel.
+template <int kRows, int kMode>
+__global__ void __launch_bounds__(kInvThreads)
+inv_rope_quant_layout_kernel(InvParams p) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
+    const uint16_t* __restrict__ x = static_cast<const uint16_t*>(p.x);
+    const int ca = chunk_a(lane);
+    const bool rope_lane = lane >= kRopeLane0;
+    const int cs_col = (rope_lane ? lane - kRopeLane0 : 0) * 4;
+    constexpr int64_t kHeadBytes = kMode == kOutBf16 ? 2 * kHeadDim : kHeadDim;
+
+    for (uint32_t r0 = warp * kRows; r0 < p.n_rows; r0 += n_warps * kRows) {
+        uint4 a[kRows], b[kRows];
+        float4 c[kRows], s[kRows];
+        uint32_t tt[kRows], hh[kRows];
+        bool live[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const uint32_t r = r0 + i;
+            live[i] = false;
+            if (r < p.n_rows) {  // warp-uniform
+                const uint32_t t = r / p.n_heads;
+                const uint32_t h = r - t * p.n_heads;
+                tt[i] = t;
+                hh[i] = h;
+                const uint16_t* row = x + static_cast<int64_t>(t) * p.sx_t +
+                                      static_cast<int64_t>(h) * p.sx_h;
+                a[i] = ld_stream16(row + 8 * ca);
+                b[i] = ld_stream16(row + 8 * (ca + 8));
+                const int64_t pos = __ldg(p.positions + t);
+                live[i] = static_cast<uint64_t>(pos) < static_cast<uint64_t>(p.cache_rows);
+                if (live[i]) {
+                    if (rope_lane) {
+                        const float* cs = p.cache + pos * kCacheWidth + cs_col;
+                        c[i] = ld_ro16(cs);
+                        s[i] = ld_ro16(cs + kHalfRope);
+                    }
+                } else if (lane == 0 && p.error_flags) {
+                    atomicOr(p.error_flags, RQ_FLAG_POSITION_RANGE);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            if (!live[i]) continue;
+            const uint32_t g = hh[i] / p.lay.hpg;
+            const uint32_t hig = hh[i] - g * p.lay.hpg;
+            uint8_t* head = p.out + int64_t(tt[i]) * p.lay.ot + int64_t(g) * p.lay.og +
+                            int64_t(hig) * kHeadBytes;
+            if (kMode == kOutBf16) {
+                uint4 qa, qb;
+                rope_row_bf16<true>(a[i], b[i], rope_lane, c[i], s[i], &qa, &qb);
+                st_stream16(head + 16 * ca, qa);
+                st_stream16(head + 16 * (ca + 8), qb);
+                continue;
+            }
+            float scale;
+            const uint4 q = rope_quant_row<true>(a[i], b[i], rope_lane, c[i], s[i], p.eps, &scale);
+            st_stream8(head + 8 * ca, q.x, q.y);
+            st_stream8(head + 8 * (ca + 8), q.z, q.w);
+            const int64_t sbase = int64_t(tt[i]) * p.lay.st + int64_t(g) * p.lay.sg;
+            if (kMode == kOutFp8F32) {
+                if ((lane & 7) == 0)
+                    st_stream4f(p.scales + sbase + (int64_t(hig) * 4 + (lane >> 3)) * p.lay.se,
+                                scale);
+            } else {
+                // UE8M0: the biased exponent of the power-of-two scale, one
+                // byte per block, block b in bits 8b..8b+7 of the head's word
+                const uint32_t e = __float_as_uint(scale) >> 23;
+                const uint32_t w = e | (__shfl_sync(kFull, e, 8) << 8) |
+                                   (__shfl_sync(kFull, e, 16) << 16) |
+                                   (__shfl_sync(kFull, e, 24) << 24);
+                if (lane == 0)
+                    st_stream4u(reinterpret_cast<uint32_t*>(p.scales) + sbase +
+                                    int64_t(hig) * p.lay.se,
+                                w);
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ insert
 
 template <int kRows>
@@ -139,7 +227,8 @@ namespace {
 // Resident CTAs per SM of each kernel variant, queried once per device and
 // variant (thread-local: no locking on the launch path).
 constexpr int kMaxDevices = 64;
-enum Variant { kInv1, kInv2, kIns2, kVariants };
+// (kLay: 2 entries per output mode, one row or two rows per warp)
+enum Variant { kInv1, kInv2, kIns2, kLay, kVariants = kLay + 6 };
 
 template <typename K>
 int resident_blocks(int device, Variant v, K kernel, int threads) {
@@ -182,6 +271,30 @@ cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev,
         k<<<grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
     }
     return cudaGetLastError();
+}
+
+template <int kMode>
+cudaError_t launch_layout(const InvParams& p, const DeviceInfo& dev, cudaStream_t stream) {
+    constexpr int kWarps = kInvThreads / 32;
+    if (int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4) {
+        auto k = inv_rope_quant_layout_kernel<2, kMode>;
+        const int res = resident_blocks(dev.ordinal, Variant(kLay + 2 * kMode + 1), k, kInvThreads);
+        k<<<grid_size(p.n_rows, kWarps * 2, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
+    } else {
+        auto k = inv_rope_quant_layout_kernel<1, kMode>;
+        const int res = resident_blocks(dev.ordinal, Variant(kLay + 2 * kMode), k, kInvThreads);
+        k<<<grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_inv_rope_quant_layout(const InvParams& p, const DeviceInfo& dev,
+                                         cudaStream_t stream) {
+    switch (p.lay.mode) {
+        case kOutFp8F32: return launch_layout<kOutFp8F32>(p, dev, stream);
+        case kOutFp8Ue8m0: return launch_layout<kOutFp8Ue8m0>(p, dev, stream);
+        default: return launch_layout<kOutBf16>(p, dev, stream);
+    }
 }
 
 cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& dev,

@@ -18,6 +18,19 @@ struct DeviceInfo {
     int sm_count;
 };
 
+// Output of the layout entry point (rq_inv_rope_quant_layout): what is written
+// and where. Head i of group g of token t starts at
+//   out + t*ot + g*og + i*head_bytes   (head_bytes 512 for codes, 1024 for bf16),
+// and scale element j of that group (j = 4i + b for fp32 scales, j = i for
+// packed UE8M0 words) sits at scales + t*st + g*sg + j*se.
+enum OutMode { kOutFp8F32 = 0, kOutFp8Ue8m0 = 1, kOutBf16 = 2 };
+struct OutLayout {
+    int mode;
+    uint32_t hpg;
+    int64_t ot, og;       // bytes
+    int64_t st, sg, se;   // scale elements (fp32 or uint32)
+};
+
 // Arguments of the inverse kernel, validated on the host (rq_api.cpp).
 struct InvParams {
     const void* x;            // bf16 [N, H, 512], strides sx_t / sx_h elements
@@ -32,6 +45,7 @@ struct InvParams {
     uint8_t* out;             // [N*H, 512] codes
     float* scales;            // [N*H, 4]
     uint32_t* error_flags;    // may be null
+    OutLayout lay;            // used by the layout kernel only
 };
 
 struct InsParams {
@@ -63,6 +77,8 @@ constexpr int64_t kStreamMinRowsPerSm = 2048;
 
 cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev, int variant,
                                       cudaStream_t stream);
+cudaError_t launch_inv_rope_quant_layout(const InvParams& p, const DeviceInfo& dev,
+                                         cudaStream_t stream);
 cudaError_t launch_inv_rope_fp8_quant_stream(const InvParams& p, const DeviceInfo& dev,
                                              cudaStream_t stream);
 cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& dev,

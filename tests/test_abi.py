@@ -137,3 +137,33 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(2, 8, 512, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         rq.inv_rope_fp8_quant(x, torch.zeros(2, dtype=torch.int64), torch.zeros(4, 64), 8)
+
+
+def _lay(lib, mode=0, out=A16, ot=4 * 4096, og=4096, sc=A16, st=128, sg=32, se=1, n=4, h=8,
+         hpg=4, x=A16, flags=None):
+    return lib.rq_inv_rope_quant_layout(x, n, h, 4096, 512, A16, A16, 16, hpg, 1e-10, mode, out,
+                                        ot, og, sc, st, sg, se, flags, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(mode=3), RQ_ERR_ARG),
+    (dict(mode=-1), RQ_ERR_ARG),
+    (dict(hpg=3), RQ_ERR_GROUPING),
+    (dict(ot=-16), RQ_ERR_SHAPE),
+    (dict(se=-1), RQ_ERR_SHAPE),
+    (dict(out=None), RQ_ERR_NULL),
+    (dict(sc=None), RQ_ERR_NULL),                 # fp32 scales are required
+    (dict(mode=1, sc=None), RQ_ERR_NULL),         # so are UE8M0 words
+    (dict(out=A8), RQ_ERR_ALIGN),
+    (dict(ot=4 * 4096 + 8), RQ_ERR_ALIGN),
+    (dict(og=4104), RQ_ERR_ALIGN),
+    (dict(sc=A16 + 2), RQ_ERR_ALIGN),
+])
+def test_layout_rejects_bad_arguments(lib, kw, status):
+    assert _lay(lib, **kw) == status
+
+
+def test_layout_bf16_needs_no_scales_and_empty_is_a_no_op(lib):
+    # bf16 mode ignores scales: with scales NULL it reaches the pointer checks of x
+    assert _lay(lib, mode=2, sc=None, x=None) == RQ_ERR_NULL
+    assert _lay(lib, n=0, out=None, sc=None, x=None) == RQ_OK

@@ -349,3 +349,117 @@ def test_insert_strided_kv(rq):
     got = run_insert(rq, inp, kv=wide.cuda()[:, :512])
     want = oracle_insert(inp)
     _assert_cache_parity(got, want)
+
+
+# ---------------------------------------------------------------- output kinds and layouts
+
+LAYOUTS = ["token_major", "group_major", "scales_transposed"]
+
+
+def _outputs(rq, n, g, hpg, mode, layout):
+    dev = torch.device("cuda:0")
+    out, sc = rq.empty_outputs(n, g, hpg, mode, group_major=(layout == "group_major"), device=dev)
+    if layout == "scales_transposed" and sc is not None:
+        w = sc.shape[2]
+        sc = torch.empty((g, w, n), dtype=sc.dtype, device=dev).permute(2, 0, 1)
+    return out, sc
+
+
+def run_layout(rq, inp, mode, layout):
+    dev = torch.device("cuda:0")
+    x = inp["x"].to(dev)
+    n, h = x.shape[0], x.shape[1]
+    hpg = inp["heads_per_group"]
+    out, sc = _outputs(rq, n, h // hpg, hpg, mode, layout)
+    if mode == "bf16":
+        out.view(torch.int16).fill_(0x5A5A)
+    else:
+        out.view(torch.uint8).fill_(0x5A)
+    rq.inv_rope_quant(x, inp["positions"].to(dev), inp["cos_sin_cache"].to(dev), hpg, mode=mode,
+                      out=out, scales=sc)
+    torch.cuda.synchronize()
+    if mode == "bf16":
+        return out.contiguous().view(torch.int16).cpu().numpy().view(np.uint16), None
+    return out.contiguous().view(torch.uint8).cpu().numpy(), sc.contiguous().cpu().numpy()
+
+
+def oracle_layout(inp, mode):
+    import oracle
+    if mode == "bf16":
+        return oracle.inv_rope_bf16(inp["x"], inp["positions"], inp["cos_sin_cache"],
+                                    inp["heads_per_group"]), None
+    codes, scales = oracle_inverse(inp)
+    if mode == "ue8m0":
+        return codes, oracle.pack_ue8m0(scales).view(np.int32)
+    return codes, scales
+
+
+def assert_layout_parity(mode, got, want):
+    if mode == "bf16":
+        assert np.array_equal(got[0], want[0]), f"{np.count_nonzero(got[0] != want[0])} bf16 differ"
+    elif mode == "ue8m0":
+        assert got[0].shape == want[0].shape and got[1].shape == want[1].shape
+        assert np.array_equal(got[1].view(np.uint32), want[1].view(np.uint32))
+        assert np.array_equal(got[0], want[0])
+    else:
+        assert_parity(got[0], got[1], want[0], want[1], exact=True)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("mode", list(["fp8", "ue8m0", "bf16"]))
+@pytest.mark.parametrize("case", ["tiny", "irregular_small", "decode1", "page24x4"])
+def test_layout_modes_exact(rq, case, mode, layout):
+    spec = {"tiny": W.TINY,
+            "irregular_small": W.InverseSpec("irr", 300, 24, 6, 32768, "uniform", True, seed=7),
+            "decode1": W.decode_spec(1),
+            "page24x4": W.InverseSpec("p24", 37, 24, 6, 8192, "uniform", True, seed=37)}[case]
+    inp = W.inverse_inputs(spec)
+    got = run_layout(rq, inp, mode, layout)
+    want = oracle_layout(inp, mode)
+    assert_layout_parity(mode, got, want)
+
+
+def test_layout_fp8_equals_the_plain_entry_at_full_size(rq):
+    """Token-major fp32-scale output of the layout entry is byte-identical to
+    rq_inv_rope_fp8_quant on the benchmarked shape; group-major holds the same
+    bytes permuted."""
+    inp = W.inverse_inputs(W.PREFILL16K)
+    ref = run_inverse(rq, inp)
+    for layout in ("token_major", "group_major"):
+        got = run_layout(rq, inp, "fp8", layout)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), layout
+
+
+@pytest.mark.parametrize("mode", ["ue8m0", "bf16"])
+def test_layout_full_size_sampled_tokens(rq, mode):
+    inp = W.inverse_inputs(W.PREFILL16K)
+    got = run_layout(rq, inp, mode, "group_major")
+    rng = np.random.default_rng(1)
+    idx = np.unique(np.concatenate([[0, 16383], rng.choice(16384, 600, replace=False)]))
+    sub = {"x": inp["x"][idx], "positions": inp["positions"][idx],
+           "cos_sin_cache": inp["cos_sin_cache"], "heads_per_group": 8}
+    want = oracle_layout(sub, mode)
+    assert_layout_parity(mode, (got[0][idx], None if got[1] is None else got[1][idx]), want)
+
+
+def test_layout_bad_position_flags_and_skips(rq):
+    inp = W.inverse_inputs(W.InverseSpec("lay-oob", 5, 8, 4, 100, "uniform", True, seed=9))
+    pos = inp["positions"].clone()
+    pos[3] = 100
+    dev = torch.device("cuda:0")
+    out, sc = rq.empty_outputs(5, 2, 4, "ue8m0", group_major=True, device=dev)
+    out.fill_(0x5A)
+    sc.fill_(-7)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    rq.inv_rope_quant(inp["x"].to(dev), pos.to(dev), inp["cos_sin_cache"].to(dev), 4,
+                      mode="ue8m0", out=out, scales=sc, error_flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 1
+    o, s = out.cpu().numpy(), sc.cpu().numpy()
+    assert np.all(o[3] == 0x5A) and np.all(s[3] == -7)
+    keep = [0, 1, 2, 4]
+    sub = {"x": inp["x"][keep], "positions": pos[keep], "cos_sin_cache": inp["cos_sin_cache"],
+           "heads_per_group": 4}
+    want = oracle_layout(sub, "ue8m0")
+    assert np.array_equal(o[keep], want[0]) and np.array_equal(s[keep].view(np.uint32),
+                                                               want[1].view(np.uint32))

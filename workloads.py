@@ -125,10 +125,13 @@ def insert_inputs(spec: InsertSpec, cache: torch.Tensor | None = None,
             "k_cache": k_cache, "block_size": spec.block_size}
 
 
-def inverse_bytes(n_tokens: int, n_heads: int) -> int:
-    """Algorithmic HBM bytes of one inverse op: x read, codes + scales written,
-    positions and one 256-byte cos/sin row read per token."""
-    per_head = HEAD_DIM * 2 + HEAD_DIM + 4 * 4
+def inverse_bytes(n_tokens: int, n_heads: int, mode: str = "fp8") -> int:
+    """Algorithmic HBM bytes of one inverse op: x read, the outputs written
+    (codes + 4 fp32 scales per head for "fp8", codes + one packed 4-byte word
+    per head for "ue8m0", 512 bf16 values per head for "bf16"), positions and
+    one 256-byte cos/sin row read per token."""
+    out_per_head = {"fp8": HEAD_DIM + 4 * 4, "ue8m0": HEAD_DIM + 4, "bf16": HEAD_DIM * 2}[mode]
+    per_head = HEAD_DIM * 2 + out_per_head
     per_token = 8 + CACHE_WIDTH * 4
     return n_tokens * (n_heads * per_head + per_token)
 
