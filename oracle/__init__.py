@@ -77,6 +77,11 @@ def _load():
             "rqo_f32_to_bf16_array": (None, [P, i64, P]),
             "rqo_pack_ue8m0_array": (None, [P, i64, P]),
             "rqo_inv_rope_bf16": (ctypes.c_int, [P, i64, i64, i64, i64, P, P, i64, i64, P]),
+            "rqo_f64_to_bf16_array": (None, [P, i64, P]),
+            "rqo_qnorm_rope_kv_rope_quant_insert": (ctypes.c_int, [P, i64, i64, i64, i64, P, i64, P,
+                                                                   i64, P, i64, i64, i64, P, P, P,
+                                                                   i64, ctypes.c_double,
+                                                                   ctypes.c_float]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -155,6 +160,14 @@ def f32_to_bf16(v) -> np.ndarray:
     v = _np(v, np.float32)
     out = np.empty(v.shape, np.uint16)
     _load().rqo_f32_to_bf16_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def f64_to_bf16(v) -> np.ndarray:
+    """bf16 bit patterns of float64 values, rounded once to nearest, ties to even."""
+    v = _np(v, np.float64)
+    out = np.empty(v.shape, np.uint16)
+    _load().rqo_f64_to_bf16_array(_ptr(v), v.size, _ptr(out))
     return out
 
 
@@ -273,3 +286,28 @@ def rope_fp8_quant_insert(kv, positions, cos_sin_cache, slot_mapping, k_cache,
     if rc:
         raise OracleError(f"rqo_rope_fp8_quant_insert status {rc}")
     return cache
+
+
+def qnorm_rope_kv_rope_quant_insert(q, kv, positions, cos_sin_cache, slot_mapping, k_cache,
+                                    block_size: int, q_head_padded: int, norm_eps: float = 1e-6,
+                                    quant_eps: float = 1e-10):
+    """The fused q/kv op: q [N, Hq, 512] bf16 is RMS-normalised per head (no
+    weight), forward-rotated and written into a zero-padded q_out
+    [N, q_head_padded, 512] (bf16 bit patterns, uint16); kv [N, 512] is
+    rotated, quantised and inserted into a copy of k_cache.
+    Returns (q_out, k_cache copy)."""
+    qa = _np(q, np.uint16)
+    n, hq = qa.shape[0], qa.shape[1]
+    a = _np(kv, np.uint16)
+    pos = _np(positions, np.int64)
+    cs = _np(cos_sin_cache, np.float32)
+    slots = _np(slot_mapping, np.int64)
+    cache = _np(k_cache, np.uint8).copy()
+    q_out = np.empty((n, int(q_head_padded), HEAD_DIM), np.uint16)
+    rc = _load().rqo_qnorm_rope_kv_rope_quant_insert(
+        _ptr(qa), n, hq, hq * HEAD_DIM, HEAD_DIM, _ptr(a), a.shape[1], _ptr(q_out),
+        int(q_head_padded), _ptr(cache), cache.shape[0], int(block_size), cache.shape[1],
+        _ptr(slots), _ptr(pos), _ptr(cs), cs.shape[0], float(norm_eps), float(quant_eps))
+    if rc:
+        raise OracleError(f"rqo_qnorm_rope_kv_rope_quant_insert status {rc}")
+    return q_out, cache

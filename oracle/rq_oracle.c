@@ -51,6 +51,12 @@
  *  - the non-quantising variant ([INV] S4, CompileKey.quantize): the
  *    inverse-rotated head is written as bf16, each fp32 value rounded to
  *    the nearest bf16, ties to even, in the same [N, G, hpg*512] layout.
+ *  - the fused q/kv op ([KV] S1): each q head (512 wide) is RMS-normalised
+ *    over its 512 values with no weight (the op takes none), x / sqrt(mean
+ *    (x^2) + eps), then forward-rotated like kv, and written as bf16 into a
+ *    q_out padded to q_head_padded heads, the pad heads all zero; kv is the
+ *    insert op above. The oracle computes the q part in double and rounds
+ *    the double result straight to bf16 (the pages fix no precision for it).
  */
 #include <math.h>
 #include <pthread.h>
@@ -102,6 +108,38 @@ uint16_t rqo_f32_to_bf16(float f)
     if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u)))
         hi += 1u;
     return (uint16_t)hi;
+}
+
+/* Nearest bf16 to a double, ties to even, rounded once (no detour through
+ * fp32): v = m * 2^E with 0.5 <= |m| < 1 keeps 8 significant bits (4 fewer
+ * below the bf16 normal range, down to the smallest subnormal 2^-133).
+ * Results beyond the largest finite bf16 become infinities. */
+uint16_t rqo_f64_to_bf16(double v)
+{
+    double m, r;
+    int E, keep;
+    float f;
+    uint32_t u;
+    if (v != v)
+        return 0x7fc0u;
+    if (v == 0.0 || isinf(v)) {
+        f = (float)v;               /* exact: zero or infinity keeps its sign */
+        memcpy(&u, &f, sizeof u);
+        return (uint16_t)(u >> 16);
+    }
+    m = frexp(v, &E);               /* v = m * 2^E, 0.5 <= |m| < 1 */
+    keep = 8;                       /* bf16: 8 significant bits when normal */
+    if (E - 1 < -126)               /* below 2^-126: subnormal spacing 2^-133 */
+        keep = 8 - (-126 - (E - 1));
+    if (keep < 0)
+        return (uint16_t)(v < 0 ? 0x8000u : 0u);
+    r = nearbyint(ldexp(m, keep));  /* default rounding mode: to nearest, ties to even */
+    r = ldexp(r, E - keep);
+    if (fabs(r) > 3.3895313892515355e38)  /* (2 - 2^-7) * 2^127, the largest bf16 */
+        return (uint16_t)(v < 0 ? 0xff80u : 0x7f80u);
+    f = (float)r;                   /* exact: r has at most 8 significant bits */
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
 }
 
 /* OCP Microscaling E8M0 byte of a power-of-two scale 2^e (e in [-127, 127]):
@@ -277,6 +315,13 @@ void rqo_f32_to_bf16_array(const float *v, int64_t n, uint16_t *out)
     int64_t i;
     for (i = 0; i < n; ++i)
         out[i] = rqo_f32_to_bf16(v[i]);
+}
+
+void rqo_f64_to_bf16_array(const double *v, int64_t n, uint16_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = rqo_f64_to_bf16(v[i]);
 }
 
 void rqo_pack_ue8m0_array(const float *scales, int64_t heads, uint32_t *out)
@@ -549,4 +594,65 @@ int rqo_rope_fp8_quant_insert(const uint16_t *kv, int64_t n_tokens,
     a.t1 = n_tokens;
     return split_run(ins_worker, &a, sizeof a, n_tokens, nthreads,
                      ins_set_range);
+}
+
+/* ------------------------------------------------- fused q + kv op ([KV] S1) */
+
+/* One q head: RMS norm over its 512 values (no weight), forward rotation of
+ * dims 448..511, rounded once to bf16. All in double. */
+void rqo_qnorm_rope_row(const uint16_t *src, const float *cs_row, double eps, uint16_t *dst)
+{
+    double y[HEAD_DIM], ss = 0.0, r;
+    int k, j;
+    for (k = 0; k < HEAD_DIM; ++k) {
+        y[k] = (double)rqo_bf16_to_f32(src[k]);
+        ss += y[k] * y[k];
+    }
+    r = 1.0 / sqrt(ss / HEAD_DIM + eps);
+    for (k = 0; k < HEAD_DIM; ++k)
+        y[k] *= r;
+    for (j = 0; j < HALF_ROPE; ++j) {
+        const double c = cs_row[j], s = cs_row[HALF_ROPE + j];
+        const double e = y[NOPE_DIM + 2 * j], o = y[NOPE_DIM + 2 * j + 1];
+        y[NOPE_DIM + 2 * j] = e * c - o * s;        /* forward: rotation by +theta */
+        y[NOPE_DIM + 2 * j + 1] = o * c + e * s;
+    }
+    for (k = 0; k < HEAD_DIM; ++k)
+        dst[k] = rqo_f64_to_bf16(y[k]);
+}
+
+/* q [N, Hq, 512] bf16 (strides sq_t, sq_h) -> q_out [N, Hpad, 512] bf16
+ * contiguous (heads Hq..Hpad-1 zero); kv [N, 512] -> paged k_cache as in
+ * rqo_rope_fp8_quant_insert (quant_eps is its block-amax clamp). */
+int rqo_qnorm_rope_kv_rope_quant_insert(const uint16_t *q, int64_t n_tokens, int64_t n_heads_q,
+                                        int64_t sq_t, int64_t sq_h, const uint16_t *kv,
+                                        int64_t skv, uint16_t *q_out, int64_t q_head_padded,
+                                        uint8_t *k_cache, int64_t num_blocks, int64_t block_size,
+                                        int64_t block_stride, const int64_t *slots,
+                                        const int64_t *pos, const float *cache,
+                                        int64_t cache_rows, double norm_eps, float quant_eps)
+{
+    int64_t t, h;
+    int rc;
+    if (n_tokens < 0 || n_heads_q < 1 || q_head_padded < n_heads_q || !(norm_eps >= 0.0))
+        return RQO_ERR_ARG;
+    if (n_tokens == 0)
+        return RQO_OK;
+    if (!q || !q_out)
+        return RQO_ERR_ARG;
+    for (t = 0; t < n_tokens; ++t) {
+        if (pos[t] < 0 || pos[t] >= cache_rows)
+            return RQO_ERR_POSITION;
+        for (h = 0; h < q_head_padded; ++h) {
+            uint16_t *dst = q_out + (t * q_head_padded + h) * HEAD_DIM;
+            if (h < n_heads_q)
+                rqo_qnorm_rope_row(q + t * sq_t + h * sq_h, cache + pos[t] * CACHE_WIDTH,
+                                   norm_eps, dst);
+            else
+                memset(dst, 0, HEAD_DIM * sizeof *dst);
+        }
+    }
+    rc = rqo_rope_fp8_quant_insert(kv, n_tokens, skv, pos, cache, cache_rows, slots, k_cache,
+                                   num_blocks, block_size, block_stride, quant_eps, 1);
+    return rc;
 }

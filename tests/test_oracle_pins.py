@@ -568,3 +568,108 @@ def test_inv_rope_bf16_is_the_rotation_rounded(oracle_lib):
                                 inp["cos_sin_cache"], inverse=True)
     want = torch.from_numpy(rows).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(o.reshape(-1, 512), want)
+
+
+# ----------------------------------------------------------------- next rows: fused q/kv op
+
+def _nearest_bf16_bruteforce(v: float) -> int:
+    """Exact nearest bf16 to a double (ties to even) by comparing the candidate
+    neighbours with exact rational distances."""
+    f = np.float32(v)  # a starting point; the answer is within one bf16 step of it
+    b = int(np.array([f], np.float32).view(np.uint32)[0] >> 16)
+    best = None
+    for c in {b - 1, b, b + 1}:
+        if c < 0 or c > 0xFFFF or (c & 0x7F80) == 0x7F80:
+            continue
+        if (c ^ b) & 0x8000:
+            continue
+        cv = Fraction(float(np.array([c << 16], np.uint32).view(np.float32)[0]))
+        d = abs(cv - Fraction(v))
+        key = (d, c & 1)            # nearer first, then the even one
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1]
+
+
+def test_f64_to_bf16_bruteforce_and_direct_rounding(oracle_lib):
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.standard_normal(1500) * 10.0 ** rng.integers(-30, 30, 1500),
+                        rng.standard_normal(200) * 1e-39])
+    # exact bf16 midpoints nudged by far less than an fp32 ulp: rounding through
+    # fp32 first would land on the midpoint and tie the wrong way
+    mids = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 3 * 2.0 ** -9, 1.5 + 2.0 ** -8])
+    v = np.concatenate([v, mids, mids + 2.0 ** -40, mids - 2.0 ** -40, -mids])
+    got = oracle_lib.f64_to_bf16(v)
+    want = np.array([_nearest_bf16_bruteforce(float(a)) for a in v], np.uint16)
+    assert np.array_equal(got, want)
+    assert int(oracle_lib.f64_to_bf16(np.array([1 + 2.0 ** -8 + 2.0 ** -40]))[0]) == 0x3F81
+
+
+def _qnorm_case(x_rows, pos, hq, hpad, cache_rows=64, eps=1e-6):
+    n = x_rows.shape[0]
+    q = torch.tensor(x_rows, dtype=torch.float32).to(torch.bfloat16)
+    kv = torch.zeros(n, 512, dtype=torch.bfloat16)
+    k_cache = torch.full((2, 4 * 528), 0xA5, dtype=torch.uint8)
+    slots = torch.full((n,), -1, dtype=torch.int64)
+    return q, kv, torch.tensor(pos), W.rope_cache(cache_rows), slots, k_cache, eps
+
+
+def test_qnorm_constant_row_is_unit_and_pads_are_zero(oracle_lib):
+    x = np.zeros((2, 3, 512), np.float32)
+    x[0, 0] = 0.75
+    x[0, 1] = -3.0
+    x[0, 2] = 2.0 ** -20
+    x[1] = 5.0
+    q, kv, pos, cache, slots, kc, eps = _qnorm_case(x, [0, 0], 3, 5, eps=0.0)
+    q_out, _ = oracle_lib.qnorm_rope_kv_rope_quant_insert(q, kv, pos, cache, slots, kc, 4, 5,
+                                                          norm_eps=0.0)
+    assert q_out.shape == (2, 5, 512)
+    assert np.all(q_out[0, 0] == 0x3F80) and np.all(q_out[0, 1] == 0xBF80)   # +1, -1
+    assert np.all(q_out[0, 2] == 0x3F80) and np.all(q_out[1, :3] == 0x3F80)
+    assert np.all(q_out[:, 3:] == 0)                                         # pad heads
+
+
+def test_qnorm_scale_invariance_and_unit_rms(oracle_lib):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((4, 2, 512)).astype(np.float32)
+    x = torch.tensor(x).to(torch.bfloat16).float().numpy()                   # bf16-exact
+    q1 = oracle_lib.qnorm_rope_kv_rope_quant_insert(*_qnorm_case(x, [0, 1, 2, 3], 2, 2)[:6], 4,
+                                                    2, norm_eps=0.0)[0]
+    q2 = oracle_lib.qnorm_rope_kv_rope_quant_insert(*_qnorm_case(x * 8.0, [0, 1, 2, 3], 2, 2)[:6],
+                                                    4, 2, norm_eps=0.0)[0]
+    assert np.array_equal(q1, q2)
+    y = torch.from_numpy(q1.view(np.int16)).view(torch.bfloat16).double().numpy()
+    rms = np.sqrt((y ** 2).mean(axis=-1))        # a rotation keeps the norm
+    assert np.all(np.abs(rms - 1.0) < 4e-3)
+
+
+def test_qnorm_rotated_tail_matches_complex_multiplication(oracle_lib):
+    rng = np.random.default_rng(9)
+    x = torch.tensor(rng.standard_normal((6, 1, 512)), dtype=torch.float32).to(torch.bfloat16)
+    pos = [0, 1, 7, 100, 1000, 4095]
+    cache = W.rope_cache(4096)
+    q, kv, p_, _, slots, kc, _ = _qnorm_case(x.float().numpy(), pos, 1, 1, cache_rows=4096)
+    q_out, _ = oracle_lib.qnorm_rope_kv_rope_quant_insert(x, kv, p_, cache, slots, kc, 4, 1,
+                                                          norm_eps=1e-6)
+    xd = x.double().numpy()[:, 0]
+    y = xd / np.sqrt((xd ** 2).mean(axis=-1, keepdims=True) + 1e-6)
+    c = cache.double().numpy()[pos]
+    z = (y[:, 448::2] + 1j * y[:, 449::2]) * (c[:, :32] + 1j * c[:, 32:])      # rotation by +theta
+    got = torch.from_numpy(q_out[:, 0].view(np.int16)).view(torch.bfloat16).double().numpy()
+    tol = 2.0 ** -8 * np.maximum(np.abs(z), 2.0 ** -120)                       # half a bf16 step + slack
+    assert np.all(np.abs(got[:, 448::2] - z.real) <= tol)
+    assert np.all(np.abs(got[:, 449::2] - z.imag) <= tol)
+    tol_n = 2.0 ** -8 * np.abs(y[:, :448]) + 1e-30
+    assert np.all(np.abs(got[:, :448] - y[:, :448]) <= tol_n)
+
+
+def test_fused_kv_part_is_the_insert_op(oracle_lib):
+    spec = W.InsertSpec("fused", 40, 4096, 4, 16, seed=12)
+    inp = W.insert_inputs(spec)
+    q = torch.randn(40, 3, 512, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    _, kc = oracle_lib.qnorm_rope_kv_rope_quant_insert(q, inp["kv"], inp["positions"],
+                                                       inp["cos_sin_cache"], inp["slot_mapping"],
+                                                       inp["k_cache"], 16, 4)
+    want = oracle_lib.rope_fp8_quant_insert(inp["kv"], inp["positions"], inp["cos_sin_cache"],
+                                            inp["slot_mapping"], inp["k_cache"], 16)
+    assert np.array_equal(kc, want)
