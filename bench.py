@@ -321,6 +321,36 @@ def run_ours(args, world, rank, local):
                        "frac_of_measured_peak": round(mb / us / 1e3 / measured_peaks()[0], 4)}
         del mo, ms
 
+    # the fused q/kv op (q RMS norm + RoPE into a padded q_out, with the kv insert)
+    fused = None
+    if args.mode_launches > 0:
+        fi = W.fused_inputs(W.FUSED16K, cache=inv_h["cos_sin_cache"])
+        fq, fkv = fi["q"].to(dev), fi["kv"].to(dev)
+        fpos, fsl, fkc = fi["positions"].to(dev), fi["slot_mapping"].to(dev), fi["k_cache"].to(dev)
+        fqo = torch.empty((fq.shape[0], fi["q_head_padded"], 512), dtype=torch.bfloat16, device=dev)
+
+        def fused_call():
+            rq.qnorm_rope_kv_rope_quant_insert(fq, fkv, fpos, cache, fsl, fkc, fi["block_size"],
+                                               fi["q_head_padded"], q_out=fqo)
+        for _ in range(3):
+            fused_call()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.mode_launches)]
+        torch.cuda.synchronize(dev)
+        for a, b in evs:
+            a.record(stream)
+            fused_call()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+        fb = W.fused_bytes(W.FUSED16K.n_tokens, W.FUSED16K.n_heads_q, W.FUSED16K.q_head_padded)
+        fused = {"kernel": "qnorm_rope_kv_insert_kernel", "workload": "fused16k (N=16384, Hq=32 "
+                 "padded to 64, kv into 512x64 slots)", "us": round(us, 2), "bytes": fb,
+                 "GBs": round(fb / us / 1e3, 1),
+                 "frac_of_measured_peak": round(fb / us / 1e3 / measured_peaks()[0], 4),
+                 "launches": args.mode_launches}
+        del fq, fkv, fpos, fsl, fkc, fqo
+
     # end to end through the public API from pinned host buffers
     e2e_steps = args.e2e_steps or min(args.steps, 20)
     x_host = inv_h["x"].pin_memory()
@@ -412,6 +442,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": 2 * args.steps,
         "output_modes": {"kernel": "inv_rope_quant_layout_kernel", "launches_each": args.mode_launches,
                          "results": modes},
+        "fused_qkv": fused,
         "clocks": sampler.summary(),
     }
     if args.inv_tokens and args.inv_tokens != INV_SPEC.n_tokens:

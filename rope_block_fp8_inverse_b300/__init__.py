@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
+__all__ = ["qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
            "empty_outputs", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
 
@@ -44,6 +44,10 @@ ABI_SYMBOLS = {
                                                 ctypes.c_float, _P, _P, _P, _P, ctypes.c_int]),
     "rq_rope_fp8_quant_insert": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _P, _P, _I64,
                                                 _I64, _I64, ctypes.c_float, _P, _P]),
+    "rq_qnorm_rope_kv_rope_quant_insert": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _I64, _P,
+                                                          _I64, _P, _P, _I64, _P, _P, _I64, _I64,
+                                                          _I64, ctypes.c_float, ctypes.c_float,
+                                                          _P, _P]),
     "rq_inv_rope_quant_layout": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
                                                 ctypes.c_float, ctypes.c_int, _P, _I64, _I64, _P,
                                                 _I64, _I64, _I64, _P, _P]),
@@ -284,3 +288,58 @@ def rope_fp8_quant_insert(kv: torch.Tensor, positions: torch.Tensor, cos_sin_cac
             cos_sin_cache.shape[0], slot_mapping.data_ptr(), k_cache.data_ptr(), k_cache.shape[0],
             int(block_size), k_cache.stride(0), float(eps), flags, _stream(kv.device))
     _check(st, "rq_rope_fp8_quant_insert")
+
+
+def qnorm_rope_kv_rope_quant_insert(q: torch.Tensor, kv: torch.Tensor, positions: torch.Tensor,
+                                    cos_sin_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                                    k_cache: torch.Tensor, block_size: int, q_head_padded: int,
+                                    norm_eps: float = 1e-6, quant_eps: float = DEFAULT_EPS,
+                                    q_out: torch.Tensor | None = None,
+                                    error_flags: torch.Tensor | None = None) -> torch.Tensor:
+    """The fused q/kv op (``rq_qnorm_rope_kv_rope_quant_insert``): q [N, Hq, 512]
+    bf16 is RMS-normalised per head (no weight), forward-rotated and written to
+    ``q_out`` [N, q_head_padded, 512] bf16 (pad heads zeroed); kv [N, 512] is
+    rotated, quantised and inserted into ``k_cache``. Returns ``q_out``."""
+    _cuda(q, "q", torch.bfloat16)
+    _cuda(kv, "kv", torch.bfloat16)
+    if q.dim() != 3 or q.shape[2] != HEAD_DIM or q.stride(2) != 1:
+        raise ValueError("q must be [N, Hq, 512] with a contiguous last dim")
+    n, hq = q.shape[0], q.shape[1]
+    hpad = int(q_head_padded)
+    if hpad < hq:
+        raise ValueError("q_head_padded must be >= the q head count")
+    if kv.dim() != 2 or kv.shape != (n, HEAD_DIM) or kv.stride(1) != 1:
+        raise ValueError("kv must be [N, 512] with a contiguous last dim")
+    _cuda(positions, "positions", torch.int64)
+    _cuda(slot_mapping, "slot_mapping", torch.int64)
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    _cuda(k_cache, "k_cache", torch.uint8)
+    if positions.shape != (n,) or not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous [N] int64 tensor")
+    if slot_mapping.shape != (n,) or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous [N] int64 tensor")
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != 64 or not cos_sin_cache.is_contiguous():
+        raise ValueError("cos_sin_cache must be a contiguous [P, 64] fp32 tensor")
+    if k_cache.dim() != 2 or k_cache.stride(1) != 1 or k_cache.shape[1] < int(block_size) * RECORD_BYTES:
+        raise ValueError("k_cache must be [num_blocks, >= block_size*528] with contiguous rows")
+    if q_out is None:
+        q_out = torch.empty((n, hpad, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
+    _cuda(q_out, "q_out", torch.bfloat16)
+    if tuple(q_out.shape) != (n, hpad, HEAD_DIM) or not q_out.is_contiguous():
+        raise ValueError("q_out must be a contiguous [N, q_head_padded, 512] bf16 tensor")
+    for t in (kv, positions, slot_mapping, cos_sin_cache, k_cache, q_out):
+        if t.device != q.device:
+            raise ValueError("all tensors must be on the same device")
+    flags = 0
+    if error_flags is not None:
+        _cuda(error_flags, "error_flags", torch.int32)
+        flags = error_flags.data_ptr()
+    with torch.cuda.device(q.device):
+        st = lib().rq_qnorm_rope_kv_rope_quant_insert(
+            q.data_ptr(), n, hq, q.stride(0), q.stride(1), kv.data_ptr(), kv.stride(0),
+            q_out.data_ptr(), hpad, positions.data_ptr(), cos_sin_cache.data_ptr(),
+            cos_sin_cache.shape[0], slot_mapping.data_ptr(), k_cache.data_ptr(), k_cache.shape[0],
+            int(block_size), k_cache.stride(0), float(norm_eps), float(quant_eps), flags,
+            _stream(q.device))
+    _check(st, "rq_qnorm_rope_kv_rope_quant_insert")
+    return q_out

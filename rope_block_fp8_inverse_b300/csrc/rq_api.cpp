@@ -216,3 +216,59 @@ RQ_EXPORT rq_status rq_rope_fp8_quant_insert(const void* kv_bf16, int64_t n_toke
         rq::launch_rope_fp8_quant_insert(p, dev, static_cast<cudaStream_t>(stream)));
 }
 
+RQ_EXPORT rq_status rq_qnorm_rope_kv_rope_quant_insert(
+    const void* q_bf16, int64_t n_tokens, int64_t n_heads_q, int64_t q_stride_token,
+    int64_t q_stride_head, const void* kv_bf16, int64_t kv_stride_token, void* q_out_bf16,
+    int64_t q_head_padded, const int64_t* positions, const float* cos_sin_cache,
+    int64_t cache_rows, const int64_t* slot_mapping, uint8_t* k_cache, int64_t num_blocks,
+    int64_t block_size, int64_t block_stride_bytes, float norm_eps, float quant_eps,
+    uint32_t* error_flags, void* stream) {
+    if (n_tokens < 0 || n_heads_q < 1 || q_head_padded < n_heads_q || cache_rows < 1 ||
+        num_blocks < 1 || block_size < 1 ||
+        block_size > (int64_t(1) << 40) / rq::kRecordBytesABI)
+        return RQ_ERR_SHAPE;
+    if (q_head_padded >= kMaxRows - 1 || n_tokens >= kMaxRows / (q_head_padded + 1))
+        return RQ_ERR_SHAPE;
+    if (block_stride_bytes < block_size * rq::kRecordBytesABI ||
+        num_blocks > (int64_t(1) << 62) / block_stride_bytes)
+        return RQ_ERR_SHAPE;
+    if (block_stride_bytes % 16 != 0) return RQ_ERR_ALIGN;
+    if (!std::isfinite(norm_eps) || norm_eps < 0.0f || !eps_ok(quant_eps)) return RQ_ERR_ARG;
+    if (n_tokens == 0) return RQ_OK;
+    if (!q_bf16 || !kv_bf16 || !q_out_bf16 || !positions || !cos_sin_cache || !slot_mapping ||
+        !k_cache)
+        return RQ_ERR_NULL;
+    if (!aligned(q_bf16, 16) || q_stride_token % 8 != 0 || q_stride_head % 8 != 0 ||
+        !aligned(kv_bf16, 16) || kv_stride_token % 8 != 0 || !aligned(q_out_bf16, 16) ||
+        !aligned(positions, 8) || !aligned(cos_sin_cache, 16) || !aligned(slot_mapping, 8) ||
+        !aligned(k_cache, 16) || (error_flags && !aligned(error_flags, 4)))
+        return RQ_ERR_ALIGN;
+
+    rq::DeviceInfo dev;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    rq::FusedParams p;
+    p.q = q_bf16;
+    p.sq_t = q_stride_token;
+    p.sq_h = q_stride_head;
+    p.n_heads_q = static_cast<uint32_t>(n_heads_q);
+    p.q_head_padded = static_cast<uint32_t>(q_head_padded);
+    p.kv = kv_bf16;
+    p.skv = kv_stride_token;
+    p.q_out = static_cast<uint16_t*>(q_out_bf16);
+    p.n_tokens = static_cast<uint32_t>(n_tokens);
+    p.n_units = static_cast<uint32_t>(n_tokens * (q_head_padded + 1));
+    p.positions = positions;
+    p.cache = cos_sin_cache;
+    p.cache_rows = cache_rows;
+    p.slot_mapping = slot_mapping;
+    p.k_cache = k_cache;
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.block_stride = block_stride_bytes;
+    p.norm_eps = norm_eps;
+    p.quant_eps = quant_eps;
+    p.error_flags = error_flags;
+    return from_cuda(rq::launch_qnorm_rope_kv_insert(p, dev, static_cast<cudaStream_t>(stream)));
+}

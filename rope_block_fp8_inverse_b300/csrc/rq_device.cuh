@@ -211,6 +211,48 @@ __device__ __forceinline__ void rope_row_bf16(uint4 a, uint4 b, bool rope_lane, 
     *qb = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// Sum over the whole warp (xor butterfly).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, off));
+    return v;
+}
+
+// One q head of the fused q/kv op: RMS norm over its 512 values (no weight),
+// then the forward rotation of the RoPE tail, then bf16 (round to nearest
+// even). fp32 throughout: sum of squares with fused multiply-adds, a
+// correctly rounded reciprocal square root. Returns chunk A's 8 values in
+// *qa and chunk B's in *qb.
+__device__ __forceinline__ void qnorm_rope_row_bf16(uint4 a, uint4 b, bool rope_lane, float4 c4,
+                                                    float4 s4, float eps, uint4* qa, uint4* qb) {
+    Pairs p = unpack(a, b);
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        ss = __fmaf_rn(p.ev[i].x, p.ev[i].x, ss);
+        ss = __fmaf_rn(p.ev[i].y, p.ev[i].y, ss);
+        ss = __fmaf_rn(p.od[i].x, p.od[i].x, ss);
+        ss = __fmaf_rn(p.od[i].y, p.od[i].y, ss);
+    }
+    ss = warp_sum(ss);
+    const float r = __frsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / kHeadDim), eps));
+    const float2 rr = make_float2(r, r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        p.ev[i] = __fmul2_rn(p.ev[i], rr);
+        p.od[i] = __fmul2_rn(p.od[i], rr);
+    }
+    if (rope_lane) rotate_b<false>(p, c4, s4);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        w[2 * i] = bf16x2(p.ev[i].x, p.od[i].x);
+        w[2 * i + 1] = bf16x2(p.ev[i].y, p.od[i].y);
+    }
+    *qa = make_uint4(w[0], w[1], w[2], w[3]);
+    *qb = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
 __device__ __forceinline__ void st_stream16(void* p, uint4 v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)

@@ -220,6 +220,98 @@ rope_fp8_quant_insert_kernel(InsParams p) {
     }
 }
 
+// ------------------------------------------------------------------ fused q + kv
+
+// The fused op of the Eager-Break workspace page (S1) in one launch: unit u
+// of token t = u / (Hpad + 1) is q head k = u % (Hpad + 1) for k < Hq (RMS
+// norm + forward RoPE -> bf16 into q_out), a pad head for Hq <= k < Hpad
+// (zeros), and the token's kv row for k == Hpad (forward RoPE + FP8 quant +
+// paged insert). A token whose position is out of range leaves its q heads
+// and its record untouched (pad heads are still zeroed) and sets the flag.
+template <int kRows>
+__global__ void __launch_bounds__(kInvThreads)
+qnorm_rope_kv_insert_kernel(FusedParams p) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
+    const uint16_t* __restrict__ q = static_cast<const uint16_t*>(p.q);
+    const uint16_t* __restrict__ kv = static_cast<const uint16_t*>(p.kv);
+    const int ca = chunk_a(lane);
+    const bool rope_lane = lane >= kRopeLane0;
+    const int cs_col = (rope_lane ? lane - kRopeLane0 : 0) * 4;
+    const uint32_t per_token = p.q_head_padded + 1;
+    const int64_t n_slots = p.num_blocks * p.block_size;
+
+    for (uint32_t u0 = warp * kRows; u0 < p.n_units; u0 += n_warps * kRows) {
+        uint4 a[kRows], b[kRows];
+        float4 c[kRows], s[kRows];
+        uint32_t tt[kRows], kk[kRows];
+        int64_t slot[kRows];
+        bool live[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const uint32_t u = u0 + i;
+            live[i] = false;
+            if (u >= p.n_units) continue;  // warp-uniform
+            const uint32_t t = u / per_token;
+            const uint32_t k = u - t * per_token;
+            tt[i] = t;
+            kk[i] = k;
+            const bool is_kv = k == p.q_head_padded;
+            if (!is_kv && k >= p.n_heads_q) {  // pad head: zeros, no input
+                live[i] = true;
+                continue;
+            }
+            const uint16_t* row = is_kv ? kv + int64_t(t) * p.skv
+                                        : q + int64_t(t) * p.sq_t + int64_t(k) * p.sq_h;
+            a[i] = ld_stream16(row + 8 * ca);
+            b[i] = ld_stream16(row + 8 * (ca + 8));
+            const int64_t pos = __ldg(p.positions + t);
+            const bool pos_ok = static_cast<uint64_t>(pos) < static_cast<uint64_t>(p.cache_rows);
+            bool slot_ok = true;
+            if (is_kv) {
+                slot[i] = __ldg(p.slot_mapping + t);
+                slot_ok = slot[i] < n_slots;
+                live[i] = pos_ok && slot_ok && slot[i] >= 0;
+            } else {
+                live[i] = pos_ok;
+            }
+            if (live[i]) {
+                if (rope_lane) {
+                    const float* cs = p.cache + pos * kCacheWidth + cs_col;
+                    c[i] = ld_ro16(cs);
+                    s[i] = ld_ro16(cs + kHalfRope);
+                }
+            } else if (lane == 0 && p.error_flags && (!pos_ok || !slot_ok)) {
+                atomicOr(p.error_flags, (pos_ok ? 0u : RQ_FLAG_POSITION_RANGE) |
+                                            (slot_ok ? 0u : RQ_FLAG_SLOT_RANGE));
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            if (!live[i]) continue;
+            const uint32_t t = tt[i], k = kk[i];
+            if (k == p.q_head_padded) {
+                float scale;
+                const uint4 qv =
+                    rope_quant_row<false>(a[i], b[i], rope_lane, c[i], s[i], p.quant_eps, &scale);
+                const int64_t blk = slot[i] / p.block_size;
+                const int64_t off = slot[i] - blk * p.block_size;
+                uint8_t* rec = p.k_cache + blk * p.block_stride + off * kRecordBytes;
+                store_row(rec, reinterpret_cast<float*>(rec + kHeadDim), lane, ca, qv, scale);
+                continue;
+            }
+            uint8_t* dst = reinterpret_cast<uint8_t*>(
+                p.q_out + (int64_t(t) * p.q_head_padded + k) * kHeadDim);
+            uint4 qa = make_uint4(0, 0, 0, 0), qb = qa;
+            if (k < p.n_heads_q)
+                qnorm_rope_row_bf16(a[i], b[i], rope_lane, c[i], s[i], p.norm_eps, &qa, &qb);
+            st_stream16(dst + 16 * ca, qa);
+            st_stream16(dst + 16 * (ca + 8), qb);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ launchers
 
 namespace {
@@ -228,7 +320,7 @@ namespace {
 // variant (thread-local: no locking on the launch path).
 constexpr int kMaxDevices = 64;
 // (kLay: 2 entries per output mode, one row or two rows per warp)
-enum Variant { kInv1, kInv2, kIns2, kLay, kVariants = kLay + 6 };
+enum Variant { kInv1, kInv2, kIns2, kFus1, kFus2, kLay, kVariants = kLay + 6 };
 
 template <typename K>
 int resident_blocks(int device, Variant v, K kernel, int threads) {
@@ -303,6 +395,21 @@ cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& d
     auto k = rope_fp8_quant_insert_kernel<2>;
     const int res = resident_blocks(dev.ordinal, kIns2, k, kInsThreads);
     k<<<grid_size(p.n_tokens, kWarps * 2, dev.sm_count, res), kInsThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qnorm_rope_kv_insert(const FusedParams& p, const DeviceInfo& dev,
+                                        cudaStream_t stream) {
+    constexpr int kWarps = kInvThreads / 32;
+    if (int64_t(p.n_units) >= int64_t(dev.sm_count) * kWarps * 4) {
+        auto k = qnorm_rope_kv_insert_kernel<2>;
+        const int res = resident_blocks(dev.ordinal, kFus2, k, kInvThreads);
+        k<<<grid_size(p.n_units, kWarps * 2, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
+    } else {
+        auto k = qnorm_rope_kv_insert_kernel<1>;
+        const int res = resident_blocks(dev.ordinal, kFus1, k, kInvThreads);
+        k<<<grid_size(p.n_units, kWarps * 1, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 

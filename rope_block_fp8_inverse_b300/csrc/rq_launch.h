@@ -62,6 +62,26 @@ struct InsParams {
     uint32_t* error_flags;
 };
 
+// Arguments of the fused q/kv kernel (rq_qnorm_rope_kv_rope_quant_insert).
+struct FusedParams {
+    const void* q;            // bf16 [N, Hq, 512], strides sq_t / sq_h elements
+    int64_t sq_t, sq_h;
+    uint32_t n_heads_q, q_head_padded;
+    const void* kv;           // bf16 [N, 512], token stride skv elements
+    int64_t skv;
+    uint16_t* q_out;          // bf16 [N, q_head_padded, 512] contiguous
+    uint32_t n_tokens;
+    uint32_t n_units;         // n_tokens * (q_head_padded + 1) < 2^31
+    const int64_t* positions;
+    const float* cache;
+    int64_t cache_rows;
+    const int64_t* slot_mapping;
+    uint8_t* k_cache;
+    int64_t num_blocks, block_size, block_stride;
+    float norm_eps, quant_eps;
+    uint32_t* error_flags;
+};
+
 // Kernel variants of the inverse op (all bit-identical in output).
 enum InvVariant {
     kInvAuto = 0,        // chosen from the problem size
@@ -83,5 +103,7 @@ cudaError_t launch_inv_rope_fp8_quant_stream(const InvParams& p, const DeviceInf
                                              cudaStream_t stream);
 cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& dev,
                                          cudaStream_t stream);
+cudaError_t launch_qnorm_rope_kv_insert(const FusedParams& p, const DeviceInfo& dev,
+                                        cudaStream_t stream);
 
 }  // namespace rq

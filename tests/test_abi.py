@@ -167,3 +167,32 @@ def test_layout_bf16_needs_no_scales_and_empty_is_a_no_op(lib):
     # bf16 mode ignores scales: with scales NULL it reaches the pointer checks of x
     assert _lay(lib, mode=2, sc=None, x=None) == RQ_ERR_NULL
     assert _lay(lib, n=0, out=None, sc=None, x=None) == RQ_OK
+
+
+def _fus(lib, q=A16, n=4, hq=8, sqt=4096, sqh=512, kv=A16, skv=512, qo=A16, hpad=8, pos=A16,
+         cs=A16, rows=16, slots=A16, cache=A16, nb=8, bs=64, stride=64 * 528, ne=1e-6, qe=1e-10):
+    return lib.rq_qnorm_rope_kv_rope_quant_insert(q, n, hq, sqt, sqh, kv, skv, qo, hpad, pos, cs,
+                                                  rows, slots, cache, nb, bs, stride, ne, qe,
+                                                  None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(hpad=7), RQ_ERR_SHAPE),
+    (dict(hq=0), RQ_ERR_SHAPE),
+    (dict(stride=64 * 528 - 16), RQ_ERR_SHAPE),
+    (dict(ne=-1.0), RQ_ERR_ARG),
+    (dict(ne=float("inf")), RQ_ERR_ARG),
+    (dict(qe=0.0), RQ_ERR_ARG),
+    (dict(qo=None), RQ_ERR_NULL),
+    (dict(kv=None), RQ_ERR_NULL),
+    (dict(qo=A8), RQ_ERR_ALIGN),
+    (dict(sqh=516), RQ_ERR_ALIGN),
+    (dict(stride=64 * 528 + 8), RQ_ERR_ALIGN),
+])
+def test_fused_rejects_bad_arguments(lib, kw, status):
+    assert _fus(lib, **kw) == status
+
+
+def test_fused_empty_batch_is_a_no_op(lib):
+    assert _fus(lib, n=0, q=None, kv=None, qo=None, pos=None, cs=None, slots=None,
+                cache=None) == RQ_OK

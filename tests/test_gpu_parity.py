@@ -463,3 +463,120 @@ def test_layout_bad_position_flags_and_skips(rq):
     want = oracle_layout(sub, "ue8m0")
     assert np.array_equal(o[keep], want[0]) and np.array_equal(s[keep].view(np.uint32),
                                                                want[1].view(np.uint32))
+
+
+# ---------------------------------------------------------------- fused q/kv op
+
+# q_out tolerance (fp32 kernel vs the fp64 oracle, both rounded to bf16):
+#   NoPE dims: within one bf16 step of the oracle;
+#   rotated dims: |got - want| <= ulp(got)/2 + ulp(want)/2 + 2^-16 * |pair|,
+#     |pair| = the oracle pair's Euclidean norm, covering the fp32 rounding of
+#     the norm factor and of the two products when they nearly cancel;
+#   and at most 1% of all values not bit-identical.
+BF16_INEXACT_FRACTION = 1e-2
+
+
+def _bf16_ordinal(u):
+    u = u.astype(np.int32)
+    mag = u & 0x7FFF
+    return np.where(u & 0x8000, -mag, mag)
+
+
+def _bf16_to_f64(u):
+    return torch.from_numpy(np.ascontiguousarray(u).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def _bf16_ulp(v):
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a >= 2.0 ** -126, np.exp2(e - 7), 2.0 ** -133)
+
+
+def run_fused(rq, inp, norm_eps=1e-6, q=None, positions=None, flags=None, q_out=None):
+    dev = torch.device("cuda:0")
+    kc = inp["k_cache"].to(dev).contiguous()
+    qd = (inp["q"] if q is None else q).to(dev)
+    pos = (inp["positions"] if positions is None else positions).to(dev)
+    out = rq.qnorm_rope_kv_rope_quant_insert(
+        qd, inp["kv"].to(dev), pos, inp["cos_sin_cache"].to(dev), inp["slot_mapping"].to(dev), kc,
+        inp["block_size"], inp["q_head_padded"], norm_eps=norm_eps, error_flags=flags,
+        q_out=q_out)
+    torch.cuda.synchronize()
+    return out.view(torch.int16).cpu().numpy().view(np.uint16), kc.cpu().numpy()
+
+
+def oracle_fused(inp, norm_eps=1e-6, positions=None, slots=None):
+    import oracle
+    return oracle.qnorm_rope_kv_rope_quant_insert(
+        inp["q"], inp["kv"], inp["positions"] if positions is None else positions,
+        inp["cos_sin_cache"], inp["slot_mapping"] if slots is None else slots, inp["k_cache"],
+        inp["block_size"], inp["q_head_padded"], norm_eps=norm_eps)
+
+
+def assert_fused_parity(got, want, n_heads_q):
+    gq, gc = got
+    wq, wc = want
+    assert np.array_equal(gc, wc), f"{np.count_nonzero(gc != wc)} cache bytes differ"
+    assert np.all(gq[:, n_heads_q:] == 0) and np.all(wq[:, n_heads_q:] == 0)
+    g, w = gq[:, :n_heads_q], wq[:, :n_heads_q]
+    steps = np.abs(_bf16_ordinal(g[..., :448]) - _bf16_ordinal(w[..., :448]))
+    assert steps.max() <= 1, f"NoPE dims: max bf16 step distance {steps.max()}"
+    gr, wr = _bf16_to_f64(g[..., 448:]), _bf16_to_f64(w[..., 448:])
+    pair = np.sqrt(wr[..., 0::2] ** 2 + wr[..., 1::2] ** 2).repeat(2, axis=-1)
+    tol = 0.5 * _bf16_ulp(gr) + 0.5 * _bf16_ulp(wr) + 2.0 ** -16 * pair
+    bad = np.abs(gr - wr) > tol
+    assert not bad.any(), f"{bad.sum()} rotated values beyond the bound"
+    inexact = np.count_nonzero(g != w)
+    assert inexact <= BF16_INEXACT_FRACTION * g.size, inexact
+    return inexact
+
+
+@pytest.mark.parametrize("n,hq,hpad", [(1, 1, 1), (7, 16, 64), (300, 32, 64), (64, 32, 32)])
+def test_fused_small_shapes(rq, n, hq, hpad):
+    spec = W.FusedSpec("f", n, hq, hpad, 4096, 2 * W.ceil_div(n, 16) + 1, 16, seed=n + hq)
+    inp = W.fused_inputs(spec)
+    assert_fused_parity(run_fused(rq, inp), oracle_fused(inp), hq)
+
+
+def test_fused16k_full(rq):
+    """The 16k-token shape, every output compared."""
+    inp = W.fused_inputs(W.FUSED16K)
+    got = run_fused(rq, inp)
+    assert got[0].shape == (16384, 64, 512)
+    assert_fused_parity(got, oracle_fused(inp), 32)
+
+
+@pytest.mark.parametrize("norm_eps", [0.0, 1e-6, 1.0])
+def test_fused_eps_zero_rows_and_strided_q(rq, norm_eps):
+    spec = W.FusedSpec("fe", 9, 4, 8, 256, 3, 8, seed=3)
+    inp = W.fused_inputs(spec)
+    q = inp["q"].clone()
+    q[2, 1] = 0.0 if norm_eps > 0 else 1.0          # a zero head needs eps > 0
+    q[4] = q[4] * 2.0 ** 40                          # large values: the norm removes the scale
+    q[5, :, 448:] = 0.0                              # only NoPE dims live
+    inp["q"] = q
+    wide = torch.zeros(9, 7, 512, dtype=torch.bfloat16)
+    wide[:, 2:6] = q
+    got = run_fused(rq, inp, norm_eps=norm_eps, q=wide.cuda()[:, 2:6])
+    assert_fused_parity(got, oracle_fused(inp, norm_eps=norm_eps), 4)
+
+
+def test_fused_bad_position_flags_and_skips(rq):
+    spec = W.FusedSpec("fb", 6, 2, 4, 64, 2, 8, seed=5)
+    inp = W.fused_inputs(spec)
+    pos = inp["positions"].clone()
+    pos[3] = 64
+    dev = torch.device("cuda:0")
+    q_out = torch.full((6, 4, 512), 7.0, dtype=torch.bfloat16, device=dev)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    gq, gc = run_fused(rq, inp, positions=pos, flags=flags, q_out=q_out)
+    assert int(flags.item()) == 1
+    seven = int(torch.tensor(7.0, dtype=torch.bfloat16).view(torch.int16).item())
+    assert np.all(gq[3, :2] == seven) and np.all(gq[3, 2:] == 0)
+    keep = [0, 1, 2, 4, 5]
+    slots = inp["slot_mapping"].clone()
+    slots[3] = -1
+    sub = dict(inp, q=inp["q"][keep], kv=inp["kv"][keep], positions=pos[keep],
+               slot_mapping=slots[keep])
+    wq, wc = oracle_fused(sub)
+    assert_fused_parity((gq[keep], gc), (wq, wc), 2)

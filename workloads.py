@@ -24,6 +24,9 @@ Workloads (named by what they are):
 * ``irregular``  N=8192, H=24, heads_per_group=6, positions U[0,32768), cache 32768.
 * ``insert16k``  kv [16384, 512], positions 0..16383, cache 65536,
                  slots = randperm(512*64)[:N], paged cache 512 blocks x 64 slots x 528 B.
+* ``fused16k``   the fused q/kv op: q [16384, 32, 512] (the 32 heads per rank of the
+                 DeepSeek-V4-Flash TP2 shape) padded to 64 heads in q_out, with the
+                 insert16k kv side; q is drawn before kv from the same generator.
 """
 from __future__ import annotations
 
@@ -66,6 +69,21 @@ PREFILL16K = InverseSpec("prefill16k", 16384, 32, 8, 65536, "arange", True)
 IRREGULAR = InverseSpec("irregular", 8192, 24, 6, 32768, "uniform", True)
 DECODE_TOKENS = (1, 2, 4, 8, 16, 32, 64)
 INSERT16K = InsertSpec("insert16k", 16384, 65536, 512, 64)
+
+
+@dataclass(frozen=True)
+class FusedSpec:
+    name: str
+    n_tokens: int
+    n_heads_q: int
+    q_head_padded: int
+    cache_rows: int
+    num_blocks: int
+    block_size: int
+    seed: int = 0
+
+
+FUSED16K = FusedSpec("fused16k", 16384, 32, 64, 65536, 512, 64)
 
 
 def decode_spec(n_tokens: int) -> InverseSpec:
@@ -123,6 +141,29 @@ def insert_inputs(spec: InsertSpec, cache: torch.Tensor | None = None,
     k_cache = torch.full((spec.num_blocks, block_bytes), fill, dtype=torch.uint8)
     return {"kv": kv, "positions": pos, "cos_sin_cache": cache, "slot_mapping": slots,
             "k_cache": k_cache, "block_size": spec.block_size}
+
+
+def fused_inputs(spec: FusedSpec, cache: torch.Tensor | None = None, fill: int = 0xA5) -> dict:
+    """q [N,Hq,512] bf16 (drawn first), then kv, positions 0..N-1, slots and a
+    ``fill``-ed paged cache as in insert_inputs."""
+    gen = torch.Generator().manual_seed(spec.seed)
+    q = _activations(gen, (spec.n_tokens, spec.n_heads_q, HEAD_DIM), False)
+    kv = _activations(gen, (spec.n_tokens, HEAD_DIM), False)
+    pos = torch.arange(spec.n_tokens, dtype=torch.int64)
+    n_slots = spec.num_blocks * spec.block_size
+    slots = torch.randperm(n_slots, generator=gen)[: spec.n_tokens].to(torch.int64)
+    if cache is None:
+        cache = rope_cache(spec.cache_rows)
+    k_cache = torch.full((spec.num_blocks, spec.block_size * RECORD_BYTES), fill, dtype=torch.uint8)
+    return {"q": q, "kv": kv, "positions": pos, "cos_sin_cache": cache, "slot_mapping": slots,
+            "k_cache": k_cache, "block_size": spec.block_size, "q_head_padded": spec.q_head_padded}
+
+
+def fused_bytes(n_tokens: int, n_heads_q: int, q_head_padded: int) -> int:
+    """Algorithmic bytes of one fused q/kv op: q read, every q_out head written
+    (pad heads too), plus the insert op's bytes (the cos/sin row serves q and kv)."""
+    return n_tokens * (n_heads_q * HEAD_DIM * 2 + q_head_padded * HEAD_DIM * 2) + \
+        insert_bytes(n_tokens)
 
 
 def inverse_bytes(n_tokens: int, n_heads: int, mode: str = "fp8") -> int:
