@@ -78,6 +78,9 @@ def _load():
             "rqo_pack_ue8m0_array": (None, [P, i64, P]),
             "rqo_inv_rope_bf16": (ctypes.c_int, [P, i64, i64, i64, i64, P, P, i64, i64, P]),
             "rqo_f64_to_bf16_array": (None, [P, i64, P]),
+            "rqo_indexer_q_rope_quant": (ctypes.c_int, [P, i64, i64, i64, i64, P, P, i64,
+                                                        ctypes.c_int, P, ctypes.c_float,
+                                                        ctypes.c_float, ctypes.c_float, P, P]),
             "rqo_qnorm_rope_kv_rope_quant_insert": (ctypes.c_int, [P, i64, i64, i64, i64, P, i64, P,
                                                                    i64, P, i64, i64, i64, P, P, P,
                                                                    i64, ctypes.c_double,
@@ -311,3 +314,26 @@ def qnorm_rope_kv_rope_quant_insert(q, kv, positions, cos_sin_cache, slot_mappin
     if rc:
         raise OracleError(f"rqo_qnorm_rope_kv_rope_quant_insert status {rc}")
     return q_out, cache
+
+
+def indexer_q_rope_quant(q, positions, cos_sin_cache, weights, softmax_scale: float,
+                         head_scale: float, neox: bool = True, eps: float = 1e-4):
+    """The indexer q op: q [N, H, 128] bf16 -> (codes [N, H, 128] uint8,
+    weights_out [N, H] fp32); dims 0..63 rotated (NeoX halves or GPT-J pairs),
+    rounded through bf16, one power-of-two scale per head folded into weights."""
+    a = _np(q, np.uint16)
+    n, h = a.shape[0], a.shape[1]
+    if a.shape[2] != 128:
+        raise OracleError("indexer heads are 128 wide")
+    pos = _np(positions, np.int64)
+    cs = _np(cos_sin_cache, np.float32)
+    w = _np(weights, np.float32)
+    codes = np.empty((n, h, 128), np.uint8)
+    wout = np.empty((n, h), np.float32)
+    rc = _load().rqo_indexer_q_rope_quant(_ptr(a), n, h, h * 128, 128, _ptr(pos), _ptr(cs),
+                                          cs.shape[0], 1 if neox else 0, _ptr(w),
+                                          float(softmax_scale), float(head_scale), float(eps),
+                                          _ptr(codes), _ptr(wout))
+    if rc:
+        raise OracleError(f"rqo_indexer_q_rope_quant status {rc}")
+    return codes, wout

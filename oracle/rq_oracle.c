@@ -28,6 +28,9 @@
  *  [IDX] "[vllm] vLLM의 GLM5.2 성능 최적화: Triton 커널 융합을 통한 E2E
  *        Throughput 향상" (analysis of vLLM PR #46862), S1: the power-of-two
  *        scale exp2(ceil(log2(raw scale))).
+ *  [IDX] S1 also shows the indexer kernel's steps: RoPE output rounded
+ *        through bf16, power-of-two FP8 scale, and the scale folded into the
+ *        indexer weights as weight * q_scale * softmax_scale * head_scale.
  *  [OFP8] OCP 8-bit Floating Point Specification (OFP8) rev 1.0: E4M3
  *        (bias 7, no infinities, S.1111.111 is NaN, max normal 448).
  *
@@ -57,6 +60,13 @@
  *    q_out padded to q_head_padded heads, the pad heads all zero; kv is the
  *    insert op above. The oracle computes the q part in double and rounds
  *    the double result straight to bf16 (the pages fix no precision for it).
+ *  - the indexer q op ([IDX] S1): q heads are 128 wide, dims 0..63 rotated
+ *    forward (NeoX halves: x0 = dim j, x1 = dim 32 + j; or GPT-J pairs:
+ *    x0 = dim 2j, x1 = dim 2j + 1), r0 = x0*c - x1*s, r1 = x1*c + x0*s with
+ *    every product and sum rounded to fp32, then rounded to bf16 and back;
+ *    one block per head: amax over its 128 values clamped by eps, the same
+ *    power-of-two scale, e4m3 codes; the scale is folded into the head's
+ *    weight, ((weight * q_scale) * softmax_scale) * head_scale in fp32.
  */
 #include <math.h>
 #include <pthread.h>
@@ -655,4 +665,65 @@ int rqo_qnorm_rope_kv_rope_quant_insert(const uint16_t *q, int64_t n_tokens, int
     rc = rqo_rope_fp8_quant_insert(kv, n_tokens, skv, pos, cache, cache_rows, slots, k_cache,
                                    num_blocks, block_size, block_stride, quant_eps, 1);
     return rc;
+}
+
+/* ---------------------------------------------- indexer q op ([IDX] S1) */
+
+#define IDX_HEAD_DIM 128
+#define IDX_ROPE_DIM 64
+
+/* q [N, H, 128] bf16 (strides sq_t, sq_h) -> codes [N, H, 128] e4m3 and
+ * weights_out [N, H] fp32 (weights [N, H] fp32 in). neox: 1 for NeoX halves,
+ * 0 for GPT-J pairs. */
+int rqo_indexer_q_rope_quant(const uint16_t *q, int64_t n_tokens, int64_t n_heads,
+                             int64_t sq_t, int64_t sq_h, const int64_t *pos, const float *cache,
+                             int64_t cache_rows, int neox, const float *weights,
+                             float softmax_scale, float head_scale, float eps, uint8_t *codes,
+                             float *weights_out)
+{
+    float y[IDX_HEAD_DIM];
+    int64_t t, h;
+    int k, j;
+    if (n_tokens < 0 || n_heads < 1 || cache_rows < 1 || !(eps > 0.0f))
+        return RQO_ERR_ARG;
+    if (n_tokens == 0)
+        return RQO_OK;
+    if (!q || !pos || !cache || !weights || !codes || !weights_out)
+        return RQO_ERR_ARG;
+    for (t = 0; t < n_tokens; ++t) {
+        const float *cs;
+        if (pos[t] < 0 || pos[t] >= cache_rows)
+            return RQO_ERR_POSITION;
+        cs = cache + pos[t] * CACHE_WIDTH;
+        for (h = 0; h < n_heads; ++h) {
+            const uint16_t *src = q + t * sq_t + h * sq_h;
+            float amax = 0.0f, scale, inv;
+            for (k = 0; k < IDX_HEAD_DIM; ++k)
+                y[k] = rqo_bf16_to_f32(src[k]);
+            for (j = 0; j < IDX_ROPE_DIM / 2; ++j) {
+                const int i0 = neox ? j : 2 * j, i1 = neox ? IDX_ROPE_DIM / 2 + j : 2 * j + 1;
+                const float c = cs[j], s = cs[HALF_ROPE + j];
+                const float x0 = y[i0], x1 = y[i1];
+                const float a0 = x0 * c, b0 = x1 * s, a1 = x1 * c, b1 = x0 * s;
+                const float r0 = a0 - b0, r1 = a1 + b1;
+                y[i0] = rqo_bf16_to_f32(rqo_f32_to_bf16(r0));   /* .to(bf16).to(fp32) */
+                y[i1] = rqo_bf16_to_f32(rqo_f32_to_bf16(r1));
+            }
+            for (k = 0; k < IDX_HEAD_DIM; ++k)
+                if (fabsf(y[k]) > amax)
+                    amax = fabsf(y[k]);
+            if (amax < eps)
+                amax = eps;
+            scale = rqo_block_scale(amax);
+            inv = 1.0f / scale;                        /* exact: a power of two */
+            for (k = 0; k < IDX_HEAD_DIM; ++k)
+                codes[(t * n_heads + h) * IDX_HEAD_DIM + k] = rqo_e4m3_encode((double)(y[k] * inv));
+            {
+                const float w0 = weights[t * n_heads + h] * scale;
+                const float w1 = w0 * softmax_scale;
+                weights_out[t * n_heads + h] = w1 * head_scale;
+            }
+        }
+    }
+    return RQO_OK;
 }

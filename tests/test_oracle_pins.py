@@ -673,3 +673,56 @@ def test_fused_kv_part_is_the_insert_op(oracle_lib):
     want = oracle_lib.rope_fp8_quant_insert(inp["kv"], inp["positions"], inp["cos_sin_cache"],
                                             inp["slot_mapping"], inp["k_cache"], 16)
     assert np.array_equal(kc, want)
+
+
+# ----------------------------------------------------------------- next rows: indexer q op
+
+def _idx_worked(oracle_lib, neox: bool, pos: int):
+    """One live pair (j = 5) plus a 224 that fixes the head's scale at 2^-1."""
+    j = 5
+    i0, i1 = (j, 32 + j) if neox else (2 * j, 2 * j + 1)
+    q = np.zeros((1, 1, 128), np.float32)
+    q[0, 0, i0] = 1.0
+    q[0, 0, 100] = 224.0
+    cache = W.rope_cache(4096)
+    codes, w = oracle_lib.indexer_q_rope_quant(
+        torch.tensor(q).to(torch.bfloat16), torch.tensor([pos]), cache,
+        torch.tensor([[3.0]]), 128 ** -0.5, 64 ** -0.5, neox=neox)
+    # expected: r0 = cos, r1 = sin of the textbook angle, rounded to fp32 (the
+    # cache), then to bf16 (the page's .to(bf16)), divided by the scale 1/2 and
+    # encoded by torch's float8 cast (all below 448)
+    ang = pos * 10000.0 ** (-j / 32)
+    cs = torch.tensor([np.cos(ang), np.sin(ang)], dtype=torch.float64).to(torch.float32)
+    vals = (cs.to(torch.bfloat16).float() * 2.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return codes[0, 0], w[0, 0], i0, i1, vals
+
+
+@pytest.mark.parametrize("neox", [True, False], ids=["neox", "gptj"])
+@pytest.mark.parametrize("pos", [0, 1, 3000])
+def test_indexer_worked_pair(oracle_lib, neox, pos):
+    codes, w, i0, i1, vals = _idx_worked(oracle_lib, neox, pos)
+    assert codes[i0] == vals[0] and codes[i1] == vals[1]
+    assert codes[100] == 0x7E                                   # 224 * 2 = 448
+    rest = np.ones(128, bool)
+    rest[[i0, i1, 100]] = False
+    assert np.all(codes[rest] & 0x7F == 0)      # zeros (a rotated 0 may carry a - sign)
+    exact = 3.0 * 0.5 * 128 ** -0.5 * 64 ** -0.5
+    assert abs(float(w) - exact) <= 2 * np.spacing(np.float32(exact))
+
+
+def test_indexer_scales_and_fold_invariants(oracle_lib):
+    gen = torch.Generator().manual_seed(4)
+    q = (torch.randn(50, 8, 128, generator=gen) * 3).to(torch.bfloat16)
+    pos = torch.randint(0, 4096, (50,), generator=gen)
+    wts = torch.rand(50, 8, generator=gen) + 0.5
+    codes, w = oracle_lib.indexer_q_rope_quant(q, pos, W.rope_cache(4096), wts, 0.125, 0.25)
+    q_scale = w.astype(np.float64) / (wts.double().numpy() * 0.125 * 0.25)
+    e = np.round(np.log2(q_scale))
+    assert np.allclose(q_scale, 2.0 ** e, rtol=2 ** -22)        # a power of two per head
+    dec = oracle_lib.e4m3_decode(codes).reshape(50, 8, 128)
+    amax_over_scale = np.abs(dec).max(axis=-1)
+    assert np.all(amax_over_scale <= 448) and np.all(amax_over_scale >= 224 - 16)
+    # NoPE dims 64..127 are the input exactly scaled: decode * scale == x rounded to e4m3
+    x = q.float().numpy()[..., 64:] / (2.0 ** e)[..., None]
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes[..., 64:], want)
