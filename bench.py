@@ -351,6 +351,37 @@ def run_ours(args, world, rank, local):
                  "launches": args.mode_launches}
         del fq, fkv, fpos, fsl, fkc, fqo
 
+    # the indexer q op (RoPE through bf16 + per-head FP8 + scale fold)
+    indexer = None
+    if args.mode_launches > 0:
+        ii = W.indexer_inputs(W.INDEXER16K, cache=inv_h["cos_sin_cache"])
+        iq, iw, ipos = ii["q"].to(dev), ii["weights"].to(dev), ii["positions"].to(dev)
+        ico = torch.empty((iq.shape[0], iq.shape[1], 128), dtype=torch.uint8, device=dev)
+        iwo = torch.empty((iq.shape[0], iq.shape[1]), dtype=torch.float32, device=dev)
+        indexer = {}
+        for style in ("neox", "gptj"):
+            def idx_call():
+                rq.indexer_q_rope_quant(iq, ipos, cache, iw, ii["softmax_scale"], ii["head_scale"],
+                                        rope_style=style, out=ico, weights_out=iwo)
+            for _ in range(3):
+                idx_call()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.mode_launches)]
+            torch.cuda.synchronize(dev)
+            for a, b in evs:
+                a.record(stream)
+                idx_call()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+            ib = W.indexer_bytes(W.INDEXER16K.n_tokens, W.INDEXER16K.n_heads)
+            indexer[style] = {"us": round(us, 2), "bytes": ib, "GBs": round(ib / us / 1e3, 1),
+                              "frac_of_measured_peak": round(ib / us / 1e3 / measured_peaks()[0], 4)}
+        indexer = {"kernel": "indexer_q_rope_quant_kernel", "workload": "indexer16k (N=16384, "
+                   "H=64, head 128, dims 0..63 rotary)", "launches_each": args.mode_launches,
+                   "results": indexer}
+        del iq, iw, ipos, ico, iwo
+
     # end to end through the public API from pinned host buffers
     e2e_steps = args.e2e_steps or min(args.steps, 20)
     x_host = inv_h["x"].pin_memory()
@@ -443,6 +474,7 @@ def run_ours(args, world, rank, local):
         "output_modes": {"kernel": "inv_rope_quant_layout_kernel", "launches_each": args.mode_launches,
                          "results": modes},
         "fused_qkv": fused,
+        "indexer_q": indexer,
         "clocks": sampler.summary(),
     }
     if args.inv_tokens and args.inv_tokens != INV_SPEC.n_tokens:

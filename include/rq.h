@@ -231,6 +231,41 @@ rq_status rq_qnorm_rope_kv_rope_quant_insert(
     int64_t block_size, int64_t block_stride_bytes, float norm_eps, float quant_eps,
     uint32_t *error_flags, void *stream);
 
+/* Which dims of the indexer head's rotary part form a rotation pair. */
+typedef enum rq_rope_style {
+    RQ_ROPE_NEOX = 0,   /* dim j with dim 32 + j, j = 0..31 (halves)        */
+    RQ_ROPE_GPTJ = 1    /* dim 2j with dim 2j + 1, j = 0..31 (interleaved)  */
+} rq_rope_style;
+
+/*
+ * The indexer q op of [IDX] S1 (RoPE + FP8 quant + scale fold in one pass).
+ * For every 128-wide head (t, h) of q:
+ *  - dims 0..63 are rotated forward with row positions[t] of the [P, 64]
+ *    cache (cos in columns 0..31, sin in 32..63, pair j uses column j):
+ *    r0 = x0*c - x1*s, r1 = x1*c + x0*s, each product and sum rounded to
+ *    fp32, then rounded to bf16 and back to fp32 (round to nearest even);
+ *  - one block per head: amax = max(max|y|, eps), q_scale =
+ *    2^ceil(log2(fl32(amax / 448))), out_fp8[t, h, k] = e4m3(y_k / q_scale);
+ *  - out_weights[t, h] = ((weights[t, h] * q_scale) * softmax_scale)
+ *    * head_scale, in fp32, in that order.
+ *  q_bf16       [N, H, 128] bf16, strides in elements (multiples of 8), base
+ *               16-byte aligned.
+ *  rope_style   an rq_rope_style; any other value returns RQ_ERR_ARG.
+ *  weights      [N, H] fp32, contiguous.
+ *  eps          in [2^-100, 2^100].
+ *  out_fp8      [N, H, 128] e4m3 codes, contiguous, 16-byte aligned.
+ *  out_weights  [N, H] fp32, contiguous.
+ * A head whose position is outside [0, cache_rows) is skipped (outputs
+ * untouched) and RQ_FLAG_POSITION_RANGE is set. N * H must be below 2^31.
+ */
+rq_status rq_indexer_q_rope_fp8_quant(const void *q_bf16, int64_t n_tokens, int64_t n_heads,
+                                      int64_t q_stride_token, int64_t q_stride_head,
+                                      const int64_t *positions, const float *cos_sin_cache,
+                                      int64_t cache_rows, int rope_style, const float *weights,
+                                      float softmax_scale, float head_scale, float eps,
+                                      uint8_t *out_fp8, float *out_weights,
+                                      uint32_t *error_flags, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

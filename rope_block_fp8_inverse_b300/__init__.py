@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
+__all__ = ["indexer_q_rope_quant", "qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
            "empty_outputs", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
 
@@ -48,6 +48,9 @@ ABI_SYMBOLS = {
                                                           _I64, _P, _P, _I64, _P, _P, _I64, _I64,
                                                           _I64, ctypes.c_float, ctypes.c_float,
                                                           _P, _P]),
+    "rq_indexer_q_rope_fp8_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64,
+                                                   ctypes.c_int, _P, ctypes.c_float, ctypes.c_float,
+                                                   ctypes.c_float, _P, _P, _P, _P]),
     "rq_inv_rope_quant_layout": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
                                                 ctypes.c_float, ctypes.c_int, _P, _I64, _I64, _P,
                                                 _I64, _I64, _I64, _P, _P]),
@@ -343,3 +346,59 @@ def qnorm_rope_kv_rope_quant_insert(q: torch.Tensor, kv: torch.Tensor, positions
             _stream(q.device))
     _check(st, "rq_qnorm_rope_kv_rope_quant_insert")
     return q_out
+
+
+ROPE_STYLES = {"neox": 0, "gptj": 1}
+
+
+def indexer_q_rope_quant(q: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                         weights: torch.Tensor, softmax_scale: float, head_scale: float,
+                         rope_style: str = "neox", eps: float = 1e-4,
+                         out: torch.Tensor | None = None, weights_out: torch.Tensor | None = None,
+                         error_flags: torch.Tensor | None = None):
+    """The indexer q op (``rq_indexer_q_rope_fp8_quant``): q [N, H, 128] bf16 ->
+    (codes [N, H, 128] float8_e4m3fn, weights_out [N, H] fp32). Dims 0..63 are
+    rotated forward ("neox": dim j with 32 + j, "gptj": 2j with 2j + 1) and
+    rounded through bf16; one power-of-two scale per head is folded into
+    weights_out = weights * q_scale * softmax_scale * head_scale."""
+    if rope_style not in ROPE_STYLES:
+        raise ValueError(f"rope_style must be one of {sorted(ROPE_STYLES)}")
+    _cuda(q, "q", torch.bfloat16)
+    if q.dim() != 3 or q.shape[2] != 128 or q.stride(2) != 1:
+        raise ValueError("q must be [N, H, 128] with a contiguous last dim")
+    n, h = q.shape[0], q.shape[1]
+    _cuda(positions, "positions", torch.int64)
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    _cuda(weights, "weights", torch.float32)
+    if positions.shape != (n,) or not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous [N] int64 tensor")
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != 64 or not cos_sin_cache.is_contiguous():
+        raise ValueError("cos_sin_cache must be a contiguous [P, 64] fp32 tensor")
+    if tuple(weights.shape) != (n, h) or not weights.is_contiguous():
+        raise ValueError("weights must be a contiguous [N, H] fp32 tensor")
+    if out is None:
+        out = torch.empty((n, h, 128), dtype=torch.uint8, device=q.device)
+    if weights_out is None:
+        weights_out = torch.empty((n, h), dtype=torch.float32, device=q.device)
+    if out.dtype not in (torch.uint8, torch.float8_e4m3fn) or not out.is_cuda:
+        raise TypeError("out must be a uint8 or float8_e4m3fn CUDA tensor")
+    if tuple(out.shape) != (n, h, 128) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [N, H, 128] tensor")
+    _cuda(weights_out, "weights_out", torch.float32)
+    if tuple(weights_out.shape) != (n, h) or not weights_out.is_contiguous():
+        raise ValueError("weights_out must be a contiguous [N, H] fp32 tensor")
+    for t in (positions, cos_sin_cache, weights, out, weights_out):
+        if t.device != q.device:
+            raise ValueError("all tensors must be on the same device")
+    flags = 0
+    if error_flags is not None:
+        _cuda(error_flags, "error_flags", torch.int32)
+        flags = error_flags.data_ptr()
+    with torch.cuda.device(q.device):
+        st = lib().rq_indexer_q_rope_fp8_quant(
+            q.data_ptr(), n, h, q.stride(0), q.stride(1), positions.data_ptr(),
+            cos_sin_cache.data_ptr(), cos_sin_cache.shape[0], ROPE_STYLES[rope_style],
+            weights.data_ptr(), float(softmax_scale), float(head_scale), float(eps),
+            out.data_ptr(), weights_out.data_ptr(), flags, _stream(q.device))
+    _check(st, "rq_indexer_q_rope_fp8_quant")
+    return out.view(torch.float8_e4m3fn), weights_out

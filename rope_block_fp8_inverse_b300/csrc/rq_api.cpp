@@ -272,3 +272,47 @@ RQ_EXPORT rq_status rq_qnorm_rope_kv_rope_quant_insert(
     p.error_flags = error_flags;
     return from_cuda(rq::launch_qnorm_rope_kv_insert(p, dev, static_cast<cudaStream_t>(stream)));
 }
+
+RQ_EXPORT rq_status rq_indexer_q_rope_fp8_quant(
+    const void* q_bf16, int64_t n_tokens, int64_t n_heads, int64_t q_stride_token,
+    int64_t q_stride_head, const int64_t* positions, const float* cos_sin_cache,
+    int64_t cache_rows, int rope_style, const float* weights, float softmax_scale,
+    float head_scale, float eps, uint8_t* out_fp8, float* out_weights, uint32_t* error_flags,
+    void* stream) {
+    if (rope_style != RQ_ROPE_NEOX && rope_style != RQ_ROPE_GPTJ) return RQ_ERR_ARG;
+    if (n_tokens < 0 || n_heads < 1 || cache_rows < 1) return RQ_ERR_SHAPE;
+    if (n_heads >= kMaxRows || n_tokens >= kMaxRows / n_heads) return RQ_ERR_SHAPE;
+    if (!eps_ok(eps) || !std::isfinite(softmax_scale) || !std::isfinite(head_scale))
+        return RQ_ERR_ARG;
+    if (n_tokens == 0) return RQ_OK;
+    if (!q_bf16 || !positions || !cos_sin_cache || !weights || !out_fp8 || !out_weights)
+        return RQ_ERR_NULL;
+    if (!aligned(q_bf16, 16) || q_stride_token % 8 != 0 || q_stride_head % 8 != 0 ||
+        !aligned(positions, 8) || !aligned(cos_sin_cache, 16) || !aligned(weights, 4) ||
+        !aligned(out_fp8, 16) || !aligned(out_weights, 4) ||
+        (error_flags && !aligned(error_flags, 4)))
+        return RQ_ERR_ALIGN;
+
+    rq::DeviceInfo dev;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    rq::IdxParams p;
+    p.q = q_bf16;
+    p.sq_t = q_stride_token;
+    p.sq_h = q_stride_head;
+    p.n_rows = static_cast<uint32_t>(n_tokens * n_heads);
+    p.n_heads = static_cast<uint32_t>(n_heads);
+    p.positions = positions;
+    p.cache = cos_sin_cache;
+    p.cache_rows = cache_rows;
+    p.neox = rope_style == RQ_ROPE_NEOX;
+    p.weights = weights;
+    p.softmax_scale = softmax_scale;
+    p.head_scale = head_scale;
+    p.eps = eps;
+    p.out = out_fp8;
+    p.weights_out = out_weights;
+    p.error_flags = error_flags;
+    return from_cuda(rq::launch_indexer_q_rope_quant(p, dev, static_cast<cudaStream_t>(stream)));
+}

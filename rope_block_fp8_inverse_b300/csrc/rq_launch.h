@@ -82,6 +82,22 @@ struct FusedParams {
     uint32_t* error_flags;
 };
 
+// Arguments of the indexer q kernel (rq_indexer_q_rope_fp8_quant).
+struct IdxParams {
+    const void* q;            // bf16 [N, H, 128], strides sq_t / sq_h elements
+    int64_t sq_t, sq_h;
+    uint32_t n_rows, n_heads; // n_rows = N * H < 2^31
+    const int64_t* positions;
+    const float* cache;       // [cache_rows, 64]
+    int64_t cache_rows;
+    bool neox;                // NeoX halves (true) or GPT-J pairs of dims 0..63
+    const float* weights;     // [N, H] fp32
+    float softmax_scale, head_scale, eps;
+    uint8_t* out;             // [N, H, 128] e4m3 codes
+    float* weights_out;       // [N, H] fp32
+    uint32_t* error_flags;
+};
+
 // Kernel variants of the inverse op (all bit-identical in output).
 enum InvVariant {
     kInvAuto = 0,        // chosen from the problem size
@@ -104,6 +120,8 @@ cudaError_t launch_inv_rope_fp8_quant_stream(const InvParams& p, const DeviceInf
 cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& dev,
                                          cudaStream_t stream);
 cudaError_t launch_qnorm_rope_kv_insert(const FusedParams& p, const DeviceInfo& dev,
+                                        cudaStream_t stream);
+cudaError_t launch_indexer_q_rope_quant(const IdxParams& p, const DeviceInfo& dev,
                                         cudaStream_t stream);
 
 }  // namespace rq

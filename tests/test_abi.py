@@ -196,3 +196,23 @@ def test_fused_rejects_bad_arguments(lib, kw, status):
 def test_fused_empty_batch_is_a_no_op(lib):
     assert _fus(lib, n=0, q=None, kv=None, qo=None, pos=None, cs=None, slots=None,
                 cache=None) == RQ_OK
+
+
+def _idx(lib, q=A16, n=4, h=8, sqt=1024, sqh=128, style=0, w=A16, ss=0.1, hs=0.2, eps=1e-4,
+         out=A16, wo=A16):
+    return lib.rq_indexer_q_rope_fp8_quant(q, n, h, sqt, sqh, A16, A16, 16, style, w, ss, hs,
+                                           eps, out, wo, None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(style=2), RQ_ERR_ARG),
+    (dict(eps=0.0), RQ_ERR_ARG),
+    (dict(ss=float("nan")), RQ_ERR_ARG),
+    (dict(h=0), RQ_ERR_SHAPE),
+    (dict(w=None), RQ_ERR_NULL),
+    (dict(wo=None), RQ_ERR_NULL),
+    (dict(out=A8), RQ_ERR_ALIGN),
+    (dict(sqh=132), RQ_ERR_ALIGN),
+])
+def test_indexer_rejects_bad_arguments(lib, kw, status):
+    assert _idx(lib, **kw) == status

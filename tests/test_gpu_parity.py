@@ -580,3 +580,63 @@ def test_fused_bad_position_flags_and_skips(rq):
                slot_mapping=slots[keep])
     wq, wc = oracle_fused(sub)
     assert_fused_parity((gq[keep], gc), (wq, wc), 2)
+
+
+# ---------------------------------------------------------------- indexer q op
+
+def run_indexer(rq, inp, style, q=None, positions=None, flags=None, out=None):
+    dev = torch.device("cuda:0")
+    qd = (inp["q"] if q is None else q).to(dev)
+    pos = (inp["positions"] if positions is None else positions).to(dev)
+    codes, w = rq.indexer_q_rope_quant(qd, pos, inp["cos_sin_cache"].to(dev),
+                                       inp["weights"].to(dev), inp["softmax_scale"],
+                                       inp["head_scale"], rope_style=style, error_flags=flags,
+                                       out=out)
+    torch.cuda.synchronize()
+    return codes.view(torch.uint8).cpu().numpy(), w.cpu().numpy()
+
+
+def oracle_indexer(inp, style, positions=None):
+    import oracle
+    return oracle.indexer_q_rope_quant(inp["q"], inp["positions"] if positions is None else positions,
+                                       inp["cos_sin_cache"], inp["weights"], inp["softmax_scale"],
+                                       inp["head_scale"], neox=(style == "neox"))
+
+
+@pytest.mark.parametrize("style", ["neox", "gptj"])
+@pytest.mark.parametrize("n,h", [(1, 1), (3, 64), (37, 7), (500, 64)])
+def test_indexer_exact(rq, style, n, h):
+    spec = W.IndexerSpec("idx", n, h, 4096, seed=n + h)
+    inp = W.indexer_inputs(spec)
+    inp["positions"] = torch.randint(0, 4096, (n,), generator=torch.Generator().manual_seed(n))
+    gc, gw = run_indexer(rq, inp, style)
+    wc, ww = oracle_indexer(inp, style)
+    assert np.array_equal(gc, wc), f"{np.count_nonzero(gc != wc)} codes differ"
+    assert np.array_equal(gw.view(np.uint32), ww.view(np.uint32))
+
+
+@pytest.mark.parametrize("style", ["neox", "gptj"])
+def test_indexer16k_sampled_tokens(rq, style):
+    inp = W.indexer_inputs(W.INDEXER16K)
+    gc, gw = run_indexer(rq, inp, style)
+    rng = np.random.default_rng(2)
+    idx = np.unique(np.concatenate([[0, 16383], rng.choice(16384, 800, replace=False)]))
+    sub = dict(inp, q=inp["q"][idx], weights=inp["weights"][idx], positions=inp["positions"][idx])
+    wc, ww = oracle_indexer(sub, style)
+    assert np.array_equal(gc[idx], wc) and np.array_equal(gw[idx].view(np.uint32),
+                                                          ww.view(np.uint32))
+
+
+def test_indexer_bad_position_flags_and_skips(rq):
+    inp = W.indexer_inputs(W.IndexerSpec("idx-oob", 5, 6, 64, seed=1))
+    pos = inp["positions"].clone()
+    pos[2] = -1
+    dev = torch.device("cuda:0")
+    out = torch.full((5, 6, 128), 0x5A, dtype=torch.uint8, device=dev)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    gc, gw = run_indexer(rq, inp, "neox", positions=pos, flags=flags, out=out)
+    assert int(flags.item()) == 1 and np.all(gc[2] == 0x5A)
+    keep = [0, 1, 3, 4]
+    sub = dict(inp, q=inp["q"][keep], weights=inp["weights"][keep], positions=pos[keep])
+    wc, ww = oracle_indexer(sub, "neox")
+    assert np.array_equal(gc[keep], wc) and np.array_equal(gw[keep], ww)

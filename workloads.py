@@ -86,6 +86,19 @@ class FusedSpec:
 FUSED16K = FusedSpec("fused16k", 16384, 32, 64, 65536, 512, 64)
 
 
+@dataclass(frozen=True)
+class IndexerSpec:
+    name: str
+    n_tokens: int
+    n_heads: int
+    cache_rows: int
+    seed: int = 0
+
+
+# the sparse-attention indexer's q: 64 heads of 128 per token (dims 0..63 rotary)
+INDEXER16K = IndexerSpec("indexer16k", 16384, 64, 65536)
+
+
 def decode_spec(n_tokens: int) -> InverseSpec:
     return InverseSpec(f"decode{n_tokens}", n_tokens, 32, 8, 65536, "uniform", False)
 
@@ -157,6 +170,26 @@ def fused_inputs(spec: FusedSpec, cache: torch.Tensor | None = None, fill: int =
     k_cache = torch.full((spec.num_blocks, spec.block_size * RECORD_BYTES), fill, dtype=torch.uint8)
     return {"q": q, "kv": kv, "positions": pos, "cos_sin_cache": cache, "slot_mapping": slots,
             "k_cache": k_cache, "block_size": spec.block_size, "q_head_padded": spec.q_head_padded}
+
+
+def indexer_inputs(spec: IndexerSpec, cache: torch.Tensor | None = None) -> dict:
+    """q [N,H,128] bf16 N(0,1) + 1% x50 outliers (drawn first), weights [N,H]
+    fp32 uniform in [0.5, 1.5), positions 0..N-1."""
+    gen = torch.Generator().manual_seed(spec.seed)
+    q = _activations(gen, (spec.n_tokens, spec.n_heads, 128), True)
+    w = torch.rand((spec.n_tokens, spec.n_heads), generator=gen) + 0.5
+    if cache is None:
+        cache = rope_cache(spec.cache_rows)
+    return {"q": q, "weights": w, "positions": torch.arange(spec.n_tokens, dtype=torch.int64),
+            "cos_sin_cache": cache, "softmax_scale": 128 ** -0.5,
+            "head_scale": spec.n_heads ** -0.5}
+
+
+def indexer_bytes(n_tokens: int, n_heads: int) -> int:
+    """Algorithmic bytes of one indexer q op: q read (256 B per head), codes
+    written (128 B), weight read and written (4 + 4 B), position and one cos/sin
+    row read per token."""
+    return n_tokens * (n_heads * (256 + 128 + 8) + 8 + CACHE_WIDTH * 4)
 
 
 def fused_bytes(n_tokens: int, n_heads_q: int, q_head_padded: int) -> int:
