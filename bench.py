@@ -294,7 +294,11 @@ def run_ours(args, world, rank, local):
     barrier(world)
     total_ms = max_over_ranks(start.elapsed_time(end), world)
     inv_ms = statistics.fmean(a.elapsed_time(b) for a, b in inv_ev)
-    inv_ms_med = statistics.median(a.elapsed_time(b) for a, b in inv_ev)
+    inv_all = sorted(a.elapsed_time(b) for a, b in inv_ev)
+    inv_ms_med = statistics.median(inv_all)
+    inv_pct = {f"p{q}": round(inv_all[min(len(inv_all) - 1, int(len(inv_all) * q / 100))] * 1e3, 2)
+               for q in (10, 50, 90, 99)}
+    inv_pct["max"] = round(inv_all[-1] * 1e3, 2)
     ins_ms = statistics.fmean(inv_ev[i][1].elapsed_time(ins_ev[i]) for i in range(args.steps))
     ms_step = total_ms / args.steps
 
@@ -432,6 +436,7 @@ def run_ours(args, world, rank, local):
         "us_per_step": round(ms_step * 1e3, 2),
         "inverse_us": round(inv_ms * 1e3, 2),
         "inverse_us_median": round(inv_ms_med * 1e3, 2),
+        "inverse_us_percentiles": inv_pct,
         "insert_us": round(ins_ms * 1e3, 2),
         "frac_of_nominal_8tbs": round(step_bytes / (ms_step * 1e-3) / 8e12, 4),
         "higher_is_better": True,

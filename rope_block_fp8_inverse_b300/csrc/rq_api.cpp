@@ -105,6 +105,14 @@ RQ_EXPORT rq_status rq_inv_rope_fp8_quant_ex(const void* x_bf16, int64_t n_token
     p.out = out_fp8;
     p.scales = out_scales;
     p.error_flags = error_flags;
+    // contiguous [N, G, hpg*512] output is [N, 1, H*512]: one group per token
+    p.lay.mode = rq::kOutFp8F32;
+    p.lay.hpg = static_cast<uint32_t>(n_heads);
+    p.lay.ot = n_heads * rq::kHeadDimABI;
+    p.lay.og = 0;
+    p.lay.st = n_heads * 4;
+    p.lay.sg = 0;
+    p.lay.se = 1;
     return from_cuda(
         rq::launch_inv_rope_fp8_quant(p, dev, variant, static_cast<cudaStream_t>(stream)));
 }
@@ -168,8 +176,13 @@ RQ_EXPORT rq_status rq_inv_rope_quant_layout(
     p.lay.st = scale_stride_token;
     p.lay.sg = scale_stride_group;
     p.lay.se = scale_stride_elem;
-    return from_cuda(
-        rq::launch_inv_rope_quant_layout(p, dev, static_cast<cudaStream_t>(stream)));
+    // large calls whose tiles fit the layout take the TMA-ring kernel
+    const bool stream_it = int64_t(p.n_rows) >= int64_t(dev.sm_count) * rq::kStreamMinRowsPerSm &&
+                           rq::stream_layout_ok(p);
+    return from_cuda(stream_it ? rq::launch_inv_rope_fp8_quant_stream(
+                                     p, dev, static_cast<cudaStream_t>(stream))
+                               : rq::launch_inv_rope_quant_layout(
+                                     p, dev, static_cast<cudaStream_t>(stream)));
 }
 
 RQ_EXPORT rq_status rq_rope_fp8_quant_insert(const void* kv_bf16, int64_t n_tokens,

@@ -259,8 +259,8 @@ __device__ __forceinline__ void st_stream16(void* p, uint4 v) {
                  : "memory");
 }
 
-__device__ __forceinline__ void st_stream4u(void* p, uint32_t v) {
-    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_stream1(void* p, uint32_t v) {
+    asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Store one quantised row: 8 codes of chunk A, 8 of chunk B, and (from the

@@ -143,17 +143,15 @@ inv_rope_quant_layout_kernel(InvParams p) {
                 if ((lane & 7) == 0)
                     st_stream4f(p.scales + sbase + (int64_t(hig) * 4 + (lane >> 3)) * p.lay.se,
                                 scale);
-            } else {
+            } else if ((lane & 7) == 0) {
                 // UE8M0: the biased exponent of the power-of-two scale, one
                 // byte per block, block b in bits 8b..8b+7 of the head's word
+                // (little-endian: byte b), written by block b's first lane
                 const uint32_t e = __float_as_uint(scale) >> 23;
-                const uint32_t w = e | (__shfl_sync(kFull, e, 8) << 8) |
-                                   (__shfl_sync(kFull, e, 16) << 16) |
-                                   (__shfl_sync(kFull, e, 24) << 24);
-                if (lane == 0)
-                    st_stream4u(reinterpret_cast<uint32_t*>(p.scales) + sbase +
-                                    int64_t(hig) * p.lay.se,
-                                w);
+                st_stream1(reinterpret_cast<uint8_t*>(reinterpret_cast<uint32_t*>(p.scales) +
+                                                      sbase + int64_t(hig) * p.lay.se) +
+                               (lane >> 3),
+                           e);
             }
         }
     }

@@ -12,6 +12,7 @@ namespace rq {
 constexpr int kInvThreads = 256;  // 8 warps per CTA
 constexpr int kInsThreads = 256;
 constexpr int64_t kRecordBytesABI = 528;  // paged record: 512 codes + 4 fp32 scales
+constexpr int64_t kHeadDimABI = 512;
 
 struct DeviceInfo {
     int ordinal;
@@ -117,6 +118,8 @@ cudaError_t launch_inv_rope_quant_layout(const InvParams& p, const DeviceInfo& d
                                          cudaStream_t stream);
 cudaError_t launch_inv_rope_fp8_quant_stream(const InvParams& p, const DeviceInfo& dev,
                                              cudaStream_t stream);
+// Whether the stream kernel can write p's output layout (tiles within a group).
+bool stream_layout_ok(const InvParams& p);
 cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& dev,
                                          cudaStream_t stream);
 cudaError_t launch_qnorm_rope_kv_insert(const FusedParams& p, const DeviceInfo& dev,

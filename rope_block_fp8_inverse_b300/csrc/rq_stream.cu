@@ -76,7 +76,10 @@ struct TileWalk {
 
 }  // namespace
 
-template <int kRows, int kStages>
+// kMode: what is written per head (OutMode); kScaleBulk: the tile's scales are
+// contiguous and 16-byte aligned, so they leave with one bulk store too
+// (otherwise each goes out with its own store, at any element stride).
+template <int kRows, int kStages, int kMode, bool kScaleBulk>
 __global__ void __launch_bounds__(kStreamWarps * 32)
 inv_rope_fp8_quant_stream_kernel(InvParams p) {
     using R = Ring<kRows, kStages>;
@@ -164,41 +167,92 @@ inv_rope_fp8_quant_stream_kernel(InvParams p) {
                 c4 = lds16f(st + kRows * R::kRowBytes + cs_off);
                 s4 = lds16f(st + kRows * R::kRowBytes + kHalfRope * 4 + cs_off);
             }
-            const int64_t r0 = int64_t(cw.t) * p.n_heads + h0;
-            // the tile's codes and scales are gathered in output buffer j % 2
-            // and written with two bulk stores: the buffer's previous store
-            // (tile j - 2, one commit group older than the newest) must have
-            // finished reading it
-            const uint32_t ob = out0 + (j & 1u) * R::kOutBytes;
-            if (lane == 0) bulk_wait_read_all_but_newest();
-            __syncwarp();
+            // the tile's heads h0 .. h0 + nrows - 1 lie in one output group
+            // (heads_per_group is a multiple of kRows): head hig0 + i of group g
+            const uint32_t g = h0 / p.lay.hpg;
+            const uint32_t hig0 = h0 - g * p.lay.hpg;
+            constexpr int64_t kHeadBytes = kMode == kOutBf16 ? 2 * kHeadDim : kHeadDim;
+            uint8_t* head0 = p.out + int64_t(cw.t) * p.lay.ot + int64_t(g) * p.lay.og +
+                             int64_t(hig0) * kHeadBytes;
+            const int64_t sbase = int64_t(cw.t) * p.lay.st + int64_t(g) * p.lay.sg;
+            if (kMode == kOutBf16) {
+                // no quantisation: each lane writes its 2 x 16 bytes directly
 #pragma unroll
-            for (int i = 0; i < kRows; ++i) {
-                if (uint32_t(i) < nrows) {
-                    const uint32_t row = st + i * R::kRowBytes;
-                    const uint4 a = lds16(row + 16 * ca);
-                    const uint4 b = lds16(row + 16 * (ca + 8));
-                    float scale;
-                    const uint4 q = rope_quant_row<true>(a, b, rope_lane, c4, s4, p.eps, &scale);
-                    const uint32_t o = ob + i * kHeadDim;
-                    sts8(o + 8 * ca, q.x, q.y);
-                    sts8(o + 8 * (ca + 8), q.z, q.w);
-                    if ((lane & 7) == 0) sts4f(ob + kRows * kHeadDim + i * 16 + (lane >> 3) * 4, scale);
+                for (int i = 0; i < kRows; ++i) {
+                    if (uint32_t(i) < nrows) {
+                        const uint32_t row = st + i * R::kRowBytes;
+                        uint4 qa, qb;
+                        rope_row_bf16<true>(lds16(row + 16 * ca), lds16(row + 16 * (ca + 8)),
+                                            rope_lane, c4, s4, &qa, &qb);
+                        st_stream16(head0 + i * kHeadBytes + 16 * ca, qa);
+                        st_stream16(head0 + i * kHeadBytes + 16 * (ca + 8), qb);
+                    }
+                }
+            } else {
+                // the tile's codes (and, with kScaleBulk, its scales) are
+                // gathered in output buffer j % 2 and leave with bulk stores:
+                // the buffer's previous store (tile j - 2, one commit group
+                // older than the newest) must have finished reading it
+                const uint32_t ob = out0 + (j & 1u) * R::kOutBytes;
+                const uint32_t osc = ob + kRows * kHeadDim;
+                if (lane == 0) bulk_wait_read_all_but_newest();
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < kRows; ++i) {
+                    if (uint32_t(i) < nrows) {
+                        const uint32_t row = st + i * R::kRowBytes;
+                        const uint4 a = lds16(row + 16 * ca);
+                        const uint4 b = lds16(row + 16 * (ca + 8));
+                        float scale;
+                        const uint4 q =
+                            rope_quant_row<true>(a, b, rope_lane, c4, s4, p.eps, &scale);
+                        const uint32_t o = ob + i * kHeadDim;
+                        sts8(o + 8 * ca, q.x, q.y);
+                        sts8(o + 8 * (ca + 8), q.z, q.w);
+                        const int64_t hig = int64_t(hig0) + i;
+                        if (kMode == kOutFp8F32) {
+                            if ((lane & 7) == 0) {
+                                if (kScaleBulk)
+                                    sts4f(osc + i * 16 + (lane >> 3) * 4, scale);
+                                else
+                                    st_stream4f(p.scales + sbase + (hig * 4 + (lane >> 3)) * p.lay.se,
+                                                scale);
+                            }
+                        } else if ((lane & 7) == 0) {
+                            // UE8M0: the first lane of block b writes byte b of
+                            // the head's word, the scale's biased exponent
+                            const uint32_t e = __float_as_uint(scale) >> 23;
+                            if (kScaleBulk)
+                                sts1(osc + i * 4 + (lane >> 3), e);
+                            else
+                                st_stream1(reinterpret_cast<uint8_t*>(
+                                               reinterpret_cast<uint32_t*>(p.scales) + sbase +
+                                               hig * p.lay.se) +
+                                               (lane >> 3),
+                                           e);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();  // this lane's writes, visible to the bulk stores
+                __syncwarp();
+                if (lane == 0) {
+                    bulk_s2g(head0, ob, nrows * kHeadDim);
+                    if (kScaleBulk) {
+                        if (kMode == kOutFp8F32)
+                            bulk_s2g(p.scales + sbase + int64_t(hig0) * 4, osc, nrows * 16);
+                        else
+                            bulk_s2g(reinterpret_cast<uint32_t*>(p.scales) + sbase + hig0, osc,
+                                     nrows * 4);
+                    }
                 }
             }
-            fence_proxy_async_smem();  // this lane's writes, visible to the bulk stores
-            __syncwarp();
-            if (lane == 0) {
-                bulk_s2g(p.out + r0 * kHeadDim, ob, nrows * kHeadDim);
-                bulk_s2g(p.scales + r0 * 4, ob + kRows * kHeadDim, nrows * 16);
-            }
         }
-        if (lane == 0) bulk_commit();  // one group per tile (empty for a skipped tile)
+        if (kMode != kOutBf16 && lane == 0) bulk_commit();  // one group per tile (empty if skipped)
         cw.next();
         __syncwarp();  // every lane has read stage s: it may be refilled
         if (j + kStages < n_mine) issue(j + kStages);
     }
-    if (lane == 0) bulk_wait_all();  // no bulk store may still read shared memory at exit
+    if (kMode != kOutBf16 && lane == 0) bulk_wait_all();  // no bulk store may read smem at exit
     __syncwarp();
     if (!ok) {
         // a wait gave up (never expected): report it, and let no copy still
@@ -216,26 +270,24 @@ inv_rope_fp8_quant_stream_kernel(InvParams p) {
 namespace {
 
 using StreamRing = Ring<RQ_STREAM_ROWS, RQ_STREAM_STAGES>;
-#define RQ_STREAM_KERNEL inv_rope_fp8_quant_stream_kernel<RQ_STREAM_ROWS, RQ_STREAM_STAGES>
-
 constexpr int kMaxDevices = 64;
 
-// Opt in to more than 48 KiB of dynamic shared memory (once per device) and
-// read the resulting residency.
+// Opt in to more than 48 KiB of dynamic shared memory (once per device and
+// kernel instance) and read the resulting residency.
+template <int kMode, bool kScaleBulk>
 cudaError_t stream_setup(int device, int* resident) {
+    auto kernel = inv_rope_fp8_quant_stream_kernel<RQ_STREAM_ROWS, RQ_STREAM_STAGES, kMode, kScaleBulk>;
     static thread_local int cache[kMaxDevices] = {0};
     const int d = (device >= 0 && device < kMaxDevices) ? device : 0;
     if (cache[d] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(RQ_STREAM_KERNEL,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(StreamRing::kCtaBytes));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(RQ_STREAM_KERNEL,
-                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      int(cudaSharedmemCarveoutMaxShared));
         if (e != cudaSuccess) return e;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, RQ_STREAM_KERNEL, kStreamWarps * 32,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kStreamWarps * 32,
                                                           StreamRing::kCtaBytes) != cudaSuccess ||
             n < 1)
             n = 1;
@@ -245,20 +297,50 @@ cudaError_t stream_setup(int device, int* resident) {
     return cudaSuccess;
 }
 
-}  // namespace
-
-cudaError_t launch_inv_rope_fp8_quant_stream(const InvParams& p, const DeviceInfo& dev,
-                                             cudaStream_t stream) {
+template <int kMode, bool kScaleBulk>
+cudaError_t launch_stream(const InvParams& p, const DeviceInfo& dev, cudaStream_t stream) {
     int resident = 1;
-    cudaError_t e = stream_setup(dev.ordinal, &resident);
+    cudaError_t e = stream_setup<kMode, kScaleBulk>(dev.ordinal, &resident);
     if (e != cudaSuccess) return e;
     const int64_t chunks = (p.n_heads + RQ_STREAM_ROWS - 1) / RQ_STREAM_ROWS;
     const int64_t warps_needed = int64_t(p.n_tokens) * chunks;
     const int64_t ctas_needed = (warps_needed + kStreamWarps - 1) / kStreamWarps;
     const int64_t cap = int64_t(dev.sm_count) * resident;
     const int grid = static_cast<int>(ctas_needed < cap ? ctas_needed : cap);
-    RQ_STREAM_KERNEL<<<grid, kStreamWarps * 32, StreamRing::kCtaBytes, stream>>>(p);
+    inv_rope_fp8_quant_stream_kernel<RQ_STREAM_ROWS, RQ_STREAM_STAGES, kMode, kScaleBulk>
+        <<<grid, kStreamWarps * 32, StreamRing::kCtaBytes, stream>>>(p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+bool stream_layout_ok(const InvParams& p) {
+    // a tile of RQ_STREAM_ROWS heads must stay inside one output group
+    return p.lay.hpg % RQ_STREAM_ROWS == 0;
+}
+
+bool stream_scale_bulk_ok(const InvParams& p) {
+    if (p.lay.mode == kOutBf16) return false;
+    // scales contiguous within the group, and every tile's run 16-byte aligned
+    // and a multiple of 16 bytes long (UE8M0: 4 bytes per head)
+    const bool full_tiles = p.lay.mode == kOutFp8F32 || p.n_heads % 4 == 0;
+    return p.lay.se == 1 && p.lay.st % 4 == 0 && p.lay.sg % 4 == 0 &&
+           (reinterpret_cast<uintptr_t>(p.scales) & 15) == 0 && full_tiles;
+}
+
+cudaError_t launch_inv_rope_fp8_quant_stream(const InvParams& p, const DeviceInfo& dev,
+                                             cudaStream_t stream) {
+    const bool bulk = stream_scale_bulk_ok(p);
+    switch (p.lay.mode) {
+        case kOutFp8F32:
+            return bulk ? launch_stream<kOutFp8F32, true>(p, dev, stream)
+                        : launch_stream<kOutFp8F32, false>(p, dev, stream);
+        case kOutFp8Ue8m0:
+            return bulk ? launch_stream<kOutFp8Ue8m0, true>(p, dev, stream)
+                        : launch_stream<kOutFp8Ue8m0, false>(p, dev, stream);
+        default:
+            return launch_stream<kOutBf16, false>(p, dev, stream);
+    }
 }
 
 }  // namespace rq

@@ -112,6 +112,10 @@ __device__ __forceinline__ void sts4f(uint32_t addr, float v) {
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ void sts1(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (bulk copy) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {

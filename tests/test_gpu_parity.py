@@ -430,16 +430,27 @@ def test_layout_fp8_equals_the_plain_entry_at_full_size(rq):
         assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), layout
 
 
-@pytest.mark.parametrize("mode", ["ue8m0", "bf16"])
-def test_layout_full_size_sampled_tokens(rq, mode):
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("mode", ["fp8", "ue8m0", "bf16"])
+def test_layout_full_size_sampled_tokens(rq, mode, layout):
+    """Full-size calls take the TMA-ring kernel (bulk or per-lane scale stores)."""
     inp = W.inverse_inputs(W.PREFILL16K)
-    got = run_layout(rq, inp, mode, "group_major")
+    got = run_layout(rq, inp, mode, layout)
     rng = np.random.default_rng(1)
     idx = np.unique(np.concatenate([[0, 16383], rng.choice(16384, 600, replace=False)]))
     sub = {"x": inp["x"][idx], "positions": inp["positions"][idx],
            "cos_sin_cache": inp["cos_sin_cache"], "heads_per_group": 8}
     want = oracle_layout(sub, mode)
     assert_layout_parity(mode, (got[0][idx], None if got[1] is None else got[1][idx]), want)
+
+
+@pytest.mark.parametrize("mode", ["fp8", "ue8m0"])
+def test_layout_irregular_full(rq, mode):
+    """heads_per_group = 6 at full size: tiles of 8 heads would cross groups, so
+    the warp-rows layout kernel runs; every output compared."""
+    inp = W.inverse_inputs(W.IRREGULAR)
+    got = run_layout(rq, inp, mode, "group_major")
+    assert_layout_parity(mode, got, oracle_layout(inp, mode))
 
 
 def test_layout_bad_position_flags_and_skips(rq):
