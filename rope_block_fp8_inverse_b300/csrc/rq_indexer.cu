@@ -4,13 +4,14 @@
 // bf16, one power-of-two FP8 scale per head, and that scale folded into the
 // head's indexer weight, weight * q_scale * softmax_scale * head_scale.
 //
-// Lane layout: a head is 16 chunks of 8 elements; 8 lanes own one head and a
-// warp holds 4 heads. Lane m (0..7) of a head owns chunks A = m and B = m + 4
-// when m < 4 (the 64 rotary dims) and A = m + 4, B = m + 8 when m >= 4, so
-//  * NeoX pairs (dim j with dim 32 + j) are element k of A and element k of
-//    B of the same lane (j = 8m + k), and GPT-J pairs (2j, 2j + 1) sit inside
-//    one chunk: the partner is always in the thread's registers;
-//  * the head's amax is a 3-step xor reduction over its 8 lanes.
+// Lane layout: 8 lanes own one head and a warp holds 4 heads. Half of a
+// head's 128 dims are rotary (dims 0..63, 32 pairs), so the rotation is
+// spread over all 8 lanes: lane m (0..7) owns the four pairs j = 4m .. 4m+3
+// (NeoX: dims j and 32 + j, two 8-byte pieces; GPT-J: dims 2j and 2j + 1,
+// one 16-byte chunk) and the 8 non-rotary dims 64 + 8m .. 64 + 8m + 7. Every
+// lane rotates the same number of pairs (no divergence) with the partner in
+// its own registers, and the head's amax is a 3-step xor reduction over its
+// 8 lanes.
 #include "rq_device.cuh"
 #include "rq_launch.h"
 
@@ -55,84 +56,133 @@ __device__ __forceinline__ uint2 quant8(const float (&v)[8], float inv) {
 
 }  // namespace
 
+// A warp takes kIdxGroups x 4 consecutive heads per iteration and issues all
+// their loads and position reads before computing any; cos/sin rows are read
+// in the compute phase (after the first head of a token they hit L1).
+constexpr int kIdxGroups = 4;
+
+__device__ __forceinline__ uint2 ld_stream8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream4(void* p, uint32_t v) {
+    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 template <bool kNeox>
 __global__ void __launch_bounds__(kInvThreads)
 indexer_q_rope_quant_kernel(IdxParams p) {
     const int lane = threadIdx.x & 31;
-    const int rs = lane >> 3;           // head slot within the warp
-    const int m = lane & 7;             // lane within the head
-    const bool rope_lane = m < 4;
-    const int ca = rope_lane ? m : m + 4;
-    const int cb = ca + 4;
+    const int rs = lane >> 3;           // head slot within a group of 4
+    const int m = lane & 7;             // lane within the head: pairs 4m .. 4m+3
+    const int nc = 8 + m;               // the lane's non-rotary chunk
     const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
     const uint16_t* __restrict__ q = static_cast<const uint16_t*>(p.q);
-    const uint32_t n_groups = (p.n_rows + 3) / 4;
+    constexpr uint32_t kRowsPerIter = 4 * kIdxGroups;
 
-    for (uint32_t g0 = warp; g0 < n_groups; g0 += n_warps) {
-        const uint32_t r = g0 * 4 + rs;
-        const bool row_ok = r < p.n_rows;  // uniform within the head's 8 lanes
-        uint4 a = make_uint4(0, 0, 0, 0), b = a;
-        float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0, s0 = c0, s1 = c0;
-        bool live = false;
-        if (row_ok) {
-            const uint32_t t = r / p.n_heads;
-            const uint32_t h = r - t * p.n_heads;
-            const uint16_t* row = q + int64_t(t) * p.sq_t + int64_t(h) * p.sq_h;
-            a = ld_stream16(row + 8 * ca);
-            b = ld_stream16(row + 8 * cb);
-            const int64_t pos = __ldg(p.positions + t);
-            live = static_cast<uint64_t>(pos) < static_cast<uint64_t>(p.cache_rows);
-            if (live && rope_lane) {
-                const float* cs = p.cache + pos * kCacheWidth;
-                // NeoX: pairs j = 8m .. 8m+7; GPT-J: chunk A pairs 4m .. 4m+3,
-                // chunk B pairs 16 + 4m .. 16 + 4m + 3
-                const int j0 = kNeox ? 8 * m : 4 * m;
-                const int j1 = kNeox ? 8 * m + 4 : 16 + 4 * m;
-                c0 = ld_ro16(cs + j0);
-                c1 = ld_ro16(cs + j1);
-                s0 = ld_ro16(cs + kHalfRope + j0);
-                s1 = ld_ro16(cs + kHalfRope + j1);
-            } else if (!live && m == 0 && p.error_flags) {
-                atomicOr(p.error_flags, RQ_FLAG_POSITION_RANGE);
+    for (uint32_t base = warp * kRowsPerIter; base < p.n_rows; base += n_warps * kRowsPerIter) {
+        uint4 rp[kIdxGroups], np[kIdxGroups];  // rotary words (NeoX: x = lo, y = hi), other chunk
+        int64_t pos[kIdxGroups];
+        bool live[kIdxGroups];
+#pragma unroll
+        for (int k = 0; k < kIdxGroups; ++k) {
+            const uint32_t r = base + 4 * k + rs;
+            rp[k] = make_uint4(0, 0, 0, 0);
+            np[k] = rp[k];
+            pos[k] = 0;
+            live[k] = false;
+            if (r < p.n_rows) {  // uniform within the head's 8 lanes
+                const uint32_t t = r / p.n_heads;
+                const uint32_t h = r - t * p.n_heads;
+                const uint16_t* row = q + int64_t(t) * p.sq_t + int64_t(h) * p.sq_h;
+                if (kNeox) {
+                    const uint2 lo = ld_stream8(row + 4 * m);          // dims 4m .. 4m+3
+                    const uint2 hi = ld_stream8(row + 32 + 4 * m);     // dims 32+4m .. 32+4m+3
+                    rp[k] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                } else {
+                    rp[k] = ld_stream16(row + 8 * m);                  // dims 8m .. 8m+7
+                }
+                np[k] = ld_stream16(row + 8 * nc);
+                pos[k] = __ldg(p.positions + t);
+                live[k] = static_cast<uint64_t>(pos[k]) < static_cast<uint64_t>(p.cache_rows);
+                if (!live[k] && m == 0 && p.error_flags)
+                    atomicOr(p.error_flags, RQ_FLAG_POSITION_RANGE);
             }
         }
-        float va[8], vb[8];
-        unpack8(a, va);
-        unpack8(b, vb);
-        if (rope_lane) {
-            const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-            if (kNeox) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    rot(va[k], vb[k], c[k], s[k]);
-                    round_bf16_pair(va[k], vb[k]);
+        for (int k = 0; k < kIdxGroups; ++k) {
+            const uint32_t r = base + 4 * k + rs;
+            // the four pairs (x0[i], x1[i]), i = 0..3, pair j = 4m + i
+            float x0[4], x1[4], nv[8];
+            if (kNeox) {
+                float lo[4], hi[4];
+                const uint32_t w[4] = {rp[k].x, rp[k].y, rp[k].z, rp[k].w};
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    lo[2 * i] = __uint_as_float(w[i] << 16);
+                    lo[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+                    hi[2 * i] = __uint_as_float(w[2 + i] << 16);
+                    hi[2 * i + 1] = __uint_as_float(w[2 + i] & 0xffff0000u);
                 }
-            } else {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    rot(va[2 * i], va[2 * i + 1], c[i], s[i]);
-                    rot(vb[2 * i], vb[2 * i + 1], c[4 + i], s[4 + i]);
-                    round_bf16_pair(va[2 * i], va[2 * i + 1]);
-                    round_bf16_pair(vb[2 * i], vb[2 * i + 1]);
+                    x0[i] = lo[i];
+                    x1[i] = hi[i];
+                }
+            } else {
+                float v[8];
+                unpack8(rp[k], v);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    x0[i] = v[2 * i];
+                    x1[i] = v[2 * i + 1];
                 }
             }
-        }
-        float amax = 0.f;
+            unpack8(np[k], nv);
+            if (live[k]) {
+                const float* cs = p.cache + pos[k] * kCacheWidth + 4 * m;
+                const float4 c4 = ld_ro16(cs), s4 = ld_ro16(cs + kHalfRope);
+                const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+                const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fmaxf(fabsf(va[k]), fabsf(vb[k])));
-        const uint32_t sb = scale_bits(fmaxf(block_max(amax), p.eps));
-        const float inv = inv_scale(sb);
-        const uint2 qa = quant8(va, inv), qb = quant8(vb, inv);
-        if (live) {
-            uint8_t* dst = p.out + int64_t(r) * kIdxDim;
-            st_stream8(dst + 8 * ca, qa.x, qa.y);
-            st_stream8(dst + 8 * cb, qb.x, qb.y);
-            if (m == 0) {
-                const float w0 = __fmul_rn(__ldg(p.weights + r), __uint_as_float(sb));
-                st_stream4f(p.weights_out + r,
-                            __fmul_rn(__fmul_rn(w0, p.softmax_scale), p.head_scale));
+                for (int i = 0; i < 4; ++i) {
+                    rot(x0[i], x1[i], c[i], sn[i]);
+                    round_bf16_pair(x0[i], x1[i]);
+                }
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(x0[i]), fabsf(x1[i])));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(nv[i]));
+            const uint32_t sb = scale_bits(fmaxf(block_max(amax), p.eps));
+            const float inv = inv_scale(sb);
+            const uint2 qn = quant8(nv, inv);
+            if (live[k]) {
+                uint8_t* dst = p.out + int64_t(r) * kIdxDim;
+                if (kNeox) {
+                    const uint32_t q0 = e4m3x2(__fmul_rn(x0[0], inv), __fmul_rn(x0[1], inv)) |
+                                        (e4m3x2(__fmul_rn(x0[2], inv), __fmul_rn(x0[3], inv)) << 16);
+                    const uint32_t q1 = e4m3x2(__fmul_rn(x1[0], inv), __fmul_rn(x1[1], inv)) |
+                                        (e4m3x2(__fmul_rn(x1[2], inv), __fmul_rn(x1[3], inv)) << 16);
+                    st_stream4(dst + 4 * m, q0);
+                    st_stream4(dst + 32 + 4 * m, q1);
+                } else {
+                    const float v[8] = {x0[0], x1[0], x0[1], x1[1], x0[2], x1[2], x0[3], x1[3]};
+                    const uint2 qr = quant8(v, inv);
+                    st_stream8(dst + 8 * m, qr.x, qr.y);
+                }
+                st_stream8(dst + 8 * nc, qn.x, qn.y);
+                if (m == 0) {
+                    const float w0 = __fmul_rn(__ldg(p.weights + r), __uint_as_float(sb));
+                    st_stream4f(p.weights_out + r,
+                                __fmul_rn(__fmul_rn(w0, p.softmax_scale), p.head_scale));
+                }
             }
         }
     }
@@ -162,8 +212,9 @@ int idx_resident(int device, bool neox) {
 cudaError_t launch_indexer_q_rope_quant(const IdxParams& p, const DeviceInfo& dev,
                                         cudaStream_t stream) {
     constexpr int kWarps = kInvThreads / 32;
-    const int64_t groups = (int64_t(p.n_rows) + 3) / 4;
-    const int64_t need = (groups + kWarps - 1) / kWarps;
+    const int64_t per_warp = 4 * kIdxGroups;
+    const int64_t warps = (int64_t(p.n_rows) + per_warp - 1) / per_warp;
+    const int64_t need = (warps + kWarps - 1) / kWarps;
     const int64_t cap = int64_t(dev.sm_count) * idx_resident(dev.ordinal, p.neox);
     const int grid = static_cast<int>(need < cap ? need : cap);
     if (p.neox)
