@@ -386,6 +386,37 @@ def run_ours(args, world, rank, local):
                    "results": indexer}
         del iq, iw, ipos, ico, iwo
 
+    # decode-sized calls (N tokens x 32 heads): device time per call, taken from
+    # CUDA-graph replays of 100 back-to-back calls (host launch cost excluded)
+    decode = None
+    if args.mode_launches > 0:
+        decode = {}
+        for nt in W.DECODE_TOKENS:
+            di = W.inverse_inputs(W.decode_spec(nt), cache=inv_h["cos_sin_cache"])
+            dx, dp = di["x"].to(dev), di["positions"].to(dev)
+            do = torch.empty((nt, 4, 4096), dtype=torch.uint8, device=dev)
+            ds = torch.empty((nt, 4, 32), dtype=torch.float32, device=dev)
+            rq.inv_rope_fp8_quant(dx, dp, cache, 8, out=do, scales=ds)
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            gs = torch.cuda.Stream(dev)
+            gs.wait_stream(stream)
+            with torch.cuda.stream(gs):
+                with torch.cuda.graph(g, stream=gs):
+                    for _ in range(100):
+                        rq.inv_rope_fp8_quant(dx, dp, cache, 8, out=do, scales=ds)
+            g.replay()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(5):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            decode[str(nt)] = round(e0.elapsed_time(e1) * 1e3 / 500, 2)
+        decode = {"workload": "decode: N tokens x 32 heads, heads_per_group 8, positions "
+                  "U[0,65536); graph of 100 calls, 5 replays", "us_per_call": decode}
+
     # end to end through the public API from pinned host buffers
     e2e_steps = args.e2e_steps or min(args.steps, 20)
     x_host = inv_h["x"].pin_memory()
@@ -480,6 +511,7 @@ def run_ours(args, world, rank, local):
                          "results": modes},
         "fused_qkv": fused,
         "indexer_q": indexer,
+        "decode_latency": decode,
         "clocks": sampler.summary(),
     }
     if args.inv_tokens and args.inv_tokens != INV_SPEC.n_tokens:

@@ -651,3 +651,66 @@ def test_indexer_bad_position_flags_and_skips(rq):
     sub = dict(inp, q=inp["q"][keep], weights=inp["weights"][keep], positions=pos[keep])
     wc, ww = oracle_indexer(sub, "neox")
     assert np.array_equal(gc[keep], wc) and np.array_equal(gw[keep], ww)
+
+
+# ---------------------------------------------------------------- CUDA graphs
+
+def test_every_entry_point_replays_in_a_cuda_graph(rq):
+    """Every call is stream-ordered with no host synchronisation and no
+    allocation inside the library, so it can be captured in a CUDA graph; the
+    replayed bytes equal an eager run's."""
+    dev = torch.device("cuda:0")
+    inv = W.inverse_inputs(W.InverseSpec("g", 300, 32, 8, 4096, "uniform", True, seed=8))
+    ins = W.insert_inputs(W.InsertSpec("g", 300, 4096, 10, 32, seed=8), cache=inv["cos_sin_cache"])
+    fus = W.fused_inputs(W.FusedSpec("g", 300, 16, 32, 4096, 10, 32, seed=8), cache=inv["cos_sin_cache"])
+    idx = W.indexer_inputs(W.IndexerSpec("g", 300, 8, 4096, seed=8), cache=inv["cos_sin_cache"])
+    x, pos, cache = inv["x"].to(dev), inv["positions"].to(dev), inv["cos_sin_cache"].to(dev)
+    kv, kpos, sl = ins["kv"].to(dev), ins["positions"].to(dev), ins["slot_mapping"].to(dev)
+    fq, fkv, fsl = fus["q"].to(dev), fus["kv"].to(dev), fus["slot_mapping"].to(dev)
+    iq, iw = idx["q"].to(dev), idx["weights"].to(dev)
+    bufs = {}
+
+    def outputs():
+        bufs["codes"] = torch.empty(300, 4, 4096, dtype=torch.uint8, device=dev)
+        bufs["scales"] = torch.empty(300, 4, 32, device=dev)
+        bufs["lay"] = rq.empty_outputs(300, 4, 8, "ue8m0", group_major=True, device=dev)
+        bufs["kc"] = ins["k_cache"].to(dev)
+        bufs["fkc"] = fus["k_cache"].to(dev)
+        bufs["qo"] = torch.empty(300, 32, 512, dtype=torch.bfloat16, device=dev)
+        bufs["ic"] = torch.empty(300, 8, 128, dtype=torch.uint8, device=dev)
+        bufs["iw"] = torch.empty(300, 8, device=dev)
+
+    def step():
+        rq.inv_rope_fp8_quant(x, pos, cache, 8, out=bufs["codes"], scales=bufs["scales"])
+        rq.inv_rope_quant(x, pos, cache, 8, mode="ue8m0", out=bufs["lay"][0], scales=bufs["lay"][1])
+        rq.rope_fp8_quant_insert(kv, kpos, cache, sl, bufs["kc"], 32)
+        rq.qnorm_rope_kv_rope_quant_insert(fq, fkv, kpos, cache, fsl, bufs["fkc"], 32, 32,
+                                           q_out=bufs["qo"])
+        rq.indexer_q_rope_quant(iq, kpos, cache, iw, idx["softmax_scale"], idx["head_scale"],
+                                out=bufs["ic"], weights_out=bufs["iw"])
+
+    def snapshot():
+        return {k: (tuple(t.clone() for t in v) if isinstance(v, tuple) else v.clone())
+                for k, v in bufs.items()}
+
+    outputs()
+    step()
+    torch.cuda.synchronize()
+    eager = snapshot()
+    outputs()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    got = snapshot()
+    for k in eager:
+        a, b = eager[k], got[k]
+        if isinstance(a, tuple):
+            assert all(torch.equal(u, v) for u, v in zip(a, b)), k
+        else:
+            assert torch.equal(a, b), k
