@@ -106,6 +106,18 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak_fp8():
+    """Dense fp8 tensor peak: the measured cuBLAS bf16 burst figure times the
+    nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s = 2)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return round(2.0 * float(d["bf16_tflops"]), 1), "measured bf16 burst x 2 (nominal ratio)"
+    except Exception:
+        return 3600.0, "fallback 1.8 PFLOP/s bf16 x 2"
+
+
 class ClockSampler:
     """Samples the SM clock and clock-event (throttle) reasons of one GPU during
     the timed region: through NVML when pynvml imports, else by running
@@ -386,6 +398,47 @@ def run_ours(args, world, rank, local):
                    "results": indexer}
         del iq, iw, ipos, ico, iwo
 
+    # the consumer: grouped FP8 GEMM (wo_a-style) on the inverse op's own output,
+    # 4 groups x K = 4096, n_out = 1024 per group, tensor cores (tcgen05)
+    gemm = None
+    if args.mode_launches > 0:
+        g_out = 1024
+        gen = torch.Generator().manual_seed(7)
+        wc = torch.randint(0, 256, (h // hpg, g_out, hpg * 512), generator=gen,
+                           dtype=torch.int32).to(torch.uint8)
+        wc[(wc & 0x7F) == 0x7F] = 0x38
+        wc = wc.to(dev)
+        ws = (2.0 ** torch.randint(-10, -6, (h // hpg, g_out // 128, hpg * 4), generator=gen)
+              .float()).to(dev)
+        gy = torch.empty((n, h // hpg, g_out), dtype=torch.bfloat16, device=dev)
+        rq.inv_rope_fp8_quant(x, pos, cache, hpg, out=out, scales=scales)
+
+        def gemm_call():
+            rq.grouped_fp8_gemm(out, scales, wc, ws, out=gy)
+        for _ in range(3):
+            gemm_call()
+        gl = max(10, args.mode_launches // 6)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(gl)]
+        torch.cuda.synchronize(dev)
+        for a, b in evs:
+            a.record(stream)
+            gemm_call()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+        flop = 2.0 * n * h * 512 * g_out
+        tf = flop / us / 1e6
+        fp8_peak, fp8_src = measured_tensor_peak_fp8()
+        gemm = {"kernel": "grouped_fp8_gemm_kernel", "workload": f"grouped FP8 GEMM: M={n}, "
+                f"G={h // hpg}, K={hpg * 512}, n_out={g_out} per group, block scales 1x128 / "
+                "128x128", "us": round(us, 2), "flop": flop,
+                "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": fp8_peak,
+                             "unit": "TFLOP/s", "frac": round(tf / fp8_peak, 4),
+                             "peak_source": fp8_src},
+                "launches": gl}
+        del wc, ws, gy
+
     # decode-sized calls (N tokens x 32 heads): device time per call, taken from
     # CUDA-graph replays of 100 back-to-back calls (host launch cost excluded)
     decode = None
@@ -512,6 +565,7 @@ def run_ours(args, world, rank, local):
         "fused_qkv": fused,
         "indexer_q": indexer,
         "decode_latency": decode,
+        "consumer_gemm": gemm,
         "clocks": sampler.summary(),
     }
     if args.inv_tokens and args.inv_tokens != INV_SPEC.n_tokens:

@@ -266,6 +266,30 @@ rq_status rq_indexer_q_rope_fp8_quant(const void *q_bf16, int64_t n_tokens, int6
                                       uint8_t *out_fp8, float *out_weights,
                                       uint32_t *error_flags, void *stream);
 
+/*
+ * The consumer of the block-FP8 output: a grouped FP8 GEMM on the tensor
+ * cores ([INV] intro: each output group's quantised attention output feeds
+ * that group's wo_a projection). For every group g and token m:
+ *   y[m, g, n] = sum over 128-wide K blocks kt of
+ *                a_scales[m, g, kt] * w_scales[g, n / 128, kt]
+ *                * sum_{k in kt} e4m3(a_codes[m, g, k]) * e4m3(w_codes[g, n, k])
+ * in fp32, written as bf16 (round to nearest even).
+ *  a_codes     [n_tokens, groups, k_per_group] e4m3 codes (the layout
+ *              rq_inv_rope_fp8_quant writes), 16-byte aligned.
+ *  a_scales    [n_tokens, groups, k_per_group / 128] fp32 (idem).
+ *  w_codes     [groups, n_out, k_per_group] e4m3 codes (K contiguous),
+ *              16-byte aligned.
+ *  w_scales    [groups, n_out / 128, k_per_group / 128] fp32, one per
+ *              128 x 128 block.
+ *  y_bf16      [n_tokens, groups, n_out] bf16, 16-byte aligned.
+ *  k_per_group, n_out: multiples of 128. Any n_tokens >= 0.
+ * A bounded wait that gives up sets RQ_FLAG_TIMEOUT (never expected).
+ */
+rq_status rq_grouped_fp8_gemm(const uint8_t *a_codes, const float *a_scales, int64_t n_tokens,
+                              int64_t groups, int64_t k_per_group, const uint8_t *w_codes,
+                              const float *w_scales, int64_t n_out, uint16_t *y_bf16,
+                              uint32_t *error_flags, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

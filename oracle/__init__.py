@@ -337,3 +337,25 @@ def indexer_q_rope_quant(q, positions, cos_sin_cache, weights, softmax_scale: fl
     if rc:
         raise OracleError(f"rqo_indexer_q_rope_quant status {rc}")
     return codes, wout
+
+
+def grouped_fp8_gemm(a_codes, a_scales, w_codes, w_scales) -> np.ndarray:
+    """The grouped FP8 GEMM, exactly in float64: for every group g,
+    y[:, g] = sum over 128-wide K blocks of (decode(A) * a_scale) @ (decode(W) * w_scale).T,
+    with a_codes [N, G, K], a_scales [N, G, K/128], w_codes [G, n_out, K] and
+    w_scales [G, n_out/128, K/128] (one scale per 128 x 128 weight block).
+    Decoding uses the oracle's e4m3 decoder; the products and sums use numpy
+    float64 matmul (every e4m3 product and the scaled sums of up to 2^22 of
+    them are exact or within float64 rounding). Returns [N, G, n_out] float64."""
+    ac = _np(a_codes, np.uint8)
+    wc = _np(w_codes, np.uint8)
+    sa = _np(a_scales, np.float32).astype(np.float64)
+    sw = _np(w_scales, np.float32).astype(np.float64)
+    n, g, k = ac.shape
+    n_out = wc.shape[1]
+    a = e4m3_decode(ac).reshape(n, g, k // 128, 128) * sa[..., None]
+    w = e4m3_decode(wc).reshape(g, n_out // 128, 128, k // 128, 128) * \
+        sw[:, :, None, :, None]
+    a = a.reshape(n, g, k)
+    w = w.reshape(g, n_out, k)
+    return np.einsum("ngk,gok->ngo", a, w)

@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["indexer_q_rope_quant", "qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
+__all__ = ["grouped_fp8_gemm", "indexer_q_rope_quant", "qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
            "empty_outputs", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
 
@@ -51,6 +51,7 @@ ABI_SYMBOLS = {
     "rq_indexer_q_rope_fp8_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64,
                                                    ctypes.c_int, _P, ctypes.c_float, ctypes.c_float,
                                                    ctypes.c_float, _P, _P, _P, _P]),
+    "rq_grouped_fp8_gemm": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _P]),
     "rq_inv_rope_quant_layout": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
                                                 ctypes.c_float, ctypes.c_int, _P, _I64, _I64, _P,
                                                 _I64, _I64, _I64, _P, _P]),
@@ -402,3 +403,48 @@ def indexer_q_rope_quant(q: torch.Tensor, positions: torch.Tensor, cos_sin_cache
             out.data_ptr(), weights_out.data_ptr(), flags, _stream(q.device))
     _check(st, "rq_indexer_q_rope_fp8_quant")
     return out.view(torch.float8_e4m3fn), weights_out
+
+
+def grouped_fp8_gemm(a_codes: torch.Tensor, a_scales: torch.Tensor, w_codes: torch.Tensor,
+                     w_scales: torch.Tensor, out: torch.Tensor | None = None,
+                     error_flags: torch.Tensor | None = None) -> torch.Tensor:
+    """Grouped FP8 GEMM on the tensor cores (``rq_grouped_fp8_gemm``): for every
+    group g, ``y[:, g] = dequant(a_codes[:, g]) @ dequant(w_codes[g]).T`` in
+    fp32, written as bf16 [N, G, n_out]. ``a_codes`` [N, G, K] e4m3 (uint8 or
+    float8) with ``a_scales`` [N, G, K/128] fp32 (what inv_rope_fp8_quant
+    returns); ``w_codes`` [G, n_out, K] with ``w_scales`` [G, n_out/128, K/128]."""
+    for t, name in ((a_codes, "a_codes"), (w_codes, "w_codes")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn) or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous uint8 / float8_e4m3fn tensor")
+    if a_codes.dim() != 3 or w_codes.dim() != 3:
+        raise ValueError("a_codes must be [N, G, K] and w_codes [G, n_out, K]")
+    n, g, k = a_codes.shape
+    if w_codes.shape[0] != g or w_codes.shape[2] != k:
+        raise ValueError("w_codes must be [G, n_out, K] with the codes' G and K")
+    n_out = w_codes.shape[1]
+    _cuda(a_scales, "a_scales", torch.float32)
+    _cuda(w_scales, "w_scales", torch.float32)
+    if tuple(a_scales.shape) != (n, g, k // 128) or not a_scales.is_contiguous():
+        raise ValueError("a_scales must be a contiguous [N, G, K/128] fp32 tensor")
+    if tuple(w_scales.shape) != (g, n_out // 128, k // 128) or not w_scales.is_contiguous():
+        raise ValueError("w_scales must be a contiguous [G, n_out/128, K/128] fp32 tensor")
+    if out is None:
+        out = torch.empty((n, g, n_out), dtype=torch.bfloat16, device=a_codes.device)
+    _cuda(out, "out", torch.bfloat16)
+    if tuple(out.shape) != (n, g, n_out) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [N, G, n_out] bf16 tensor")
+    for t in (a_scales, w_codes, w_scales, out):
+        if t.device != a_codes.device:
+            raise ValueError("all tensors must be on the same device")
+    flags = 0
+    if error_flags is not None:
+        _cuda(error_flags, "error_flags", torch.int32)
+        flags = error_flags.data_ptr()
+    with torch.cuda.device(a_codes.device):
+        st = lib().rq_grouped_fp8_gemm(a_codes.data_ptr(), a_scales.data_ptr(), n, g, k,
+                                       w_codes.data_ptr(), w_scales.data_ptr(), n_out,
+                                       out.data_ptr(), flags, _stream(a_codes.device))
+    _check(st, "rq_grouped_fp8_gemm")
+    return out

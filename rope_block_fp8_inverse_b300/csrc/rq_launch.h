@@ -99,6 +99,15 @@ struct IdxParams {
     uint32_t* error_flags;
 };
 
+// Arguments of the grouped FP8 GEMM (rq_grouped_fp8_gemm).
+struct GemmParams {
+    int m, groups, k, n_out;  // k = per-group K (multiple of 128), n_out multiple of 128
+    const float* a_scales;    // [m, groups, k / 128]
+    const float* w_scales;    // [groups, n_out / 128, k / 128]
+    uint16_t* y;              // bf16 [m, groups, n_out]
+    uint32_t* error_flags;
+};
+
 // Kernel variants of the inverse op (all bit-identical in output).
 enum InvVariant {
     kInvAuto = 0,        // chosen from the problem size
@@ -126,5 +135,7 @@ cudaError_t launch_qnorm_rope_kv_insert(const FusedParams& p, const DeviceInfo& 
                                         cudaStream_t stream);
 cudaError_t launch_indexer_q_rope_quant(const IdxParams& p, const DeviceInfo& dev,
                                         cudaStream_t stream);
+cudaError_t launch_grouped_fp8_gemm(const GemmParams& p, const uint8_t* a_codes,
+                                    const uint8_t* w_codes, int dev_ordinal, cudaStream_t stream);
 
 }  // namespace rq

@@ -1,0 +1,122 @@
+// rq_umma.cuh -- 5th-generation tensor core (tcgen05) and tensor-map TMA
+// primitives for sm_103a, as inline PTX, plus the two descriptors the MMA
+// takes. Used by the grouped FP8 GEMM (rq_gemm.cu).
+//
+// Shared-memory matrix descriptor (64 bits) for an operand tile stored
+// K-major with the 128-byte swizzle (each row of the tile is 128 bytes of K;
+// 8-row groups of 1024 bytes; inside a group the 16-byte chunk c of row r sits
+// at chunk position c ^ (r % 8), which is what a TMA load with
+// CU_TENSOR_MAP_SWIZZLE_128B writes into a 1024-byte aligned buffer):
+//   bits  0..13  start address >> 4
+//   bits 16..29  leading-dimension byte offset >> 4 (unused for this layout: 1)
+//   bits 32..45  stride byte offset >> 4 (distance between 8-row groups: 1024)
+//   bits 46..47  descriptor version (1)
+//   bits 49..51  base offset (0: the buffer is 1024-byte aligned)
+//   bit  52      leading-dimension offset mode (0)
+//   bits 61..63  layout: 2 = 128-byte swizzle
+// Instruction descriptor (32 bits) of kind::f8f6f4:
+//   bits 4..5 D format (1 = f32), 7..9 A format (0 = e4m3), 10..12 B format
+//   (0 = e4m3), 15 / 16 A / B major (0 = K-major), 17..22 N >> 3,
+//   24..28 M >> 4; all other bits 0 (dense, no negation, no saturation).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rq {
+namespace umma {
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_byte_addr) {
+    uint64_t d = 0;
+    d |= uint64_t((smem_byte_addr >> 4) & 0x3fffu);
+    d |= uint64_t(1u) << 16;                 // leading byte offset (unused) = 16 B
+    d |= uint64_t(1024u >> 4) << 32;         // stride byte offset = 1024 B
+    d |= uint64_t(1u) << 46;                 // version
+    d |= uint64_t(2u) << 61;                 // 128-byte swizzle
+    return d;
+}
+
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
+    return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+// TMEM allocation: one full warp executes these.
+__device__ __forceinline__ void tmem_alloc(uint32_t smem_dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_dst),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T; accumulate when `acc` != 0.
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// Arrive once on the mbarrier when every tcgen05 operation this thread
+// issued so far has completed.
+__device__ __forceinline__ void commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
+// 32*(w%4) .. 32*(w%4)+31; the address carries the lane in bits 16..31).
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+        "%30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 2-D tensor-map TMA load of one box into this CTA's shared memory,
+// completing on mbarrier `bar`. x is the innermost coordinate.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+}  // namespace umma
+}  // namespace rq

@@ -216,3 +216,24 @@ def _idx(lib, q=A16, n=4, h=8, sqt=1024, sqh=128, style=0, w=A16, ss=0.1, hs=0.2
 ])
 def test_indexer_rejects_bad_arguments(lib, kw, status):
     assert _idx(lib, **kw) == status
+
+
+def _gemm(lib, a=A16, sa=A16, n=4, g=2, k=512, w=A16, sw=A16, no=256, y=A16):
+    return lib.rq_grouped_fp8_gemm(a, sa, n, g, k, w, sw, no, y, None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=500), RQ_ERR_SHAPE),
+    (dict(no=200), RQ_ERR_SHAPE),
+    (dict(g=0), RQ_ERR_SHAPE),
+    (dict(n=-1), RQ_ERR_SHAPE),
+    (dict(w=None), RQ_ERR_NULL),
+    (dict(y=A8), RQ_ERR_ALIGN),
+    (dict(a=A8), RQ_ERR_ALIGN),
+])
+def test_gemm_rejects_bad_arguments(lib, kw, status):
+    assert _gemm(lib, **kw) == status
+
+
+def test_gemm_empty_is_a_no_op(lib):
+    assert _gemm(lib, n=0, a=None, sa=None, w=None, sw=None, y=None) == RQ_OK

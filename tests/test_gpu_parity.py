@@ -714,3 +714,57 @@ def test_every_entry_point_replays_in_a_cuda_graph(rq):
             assert all(torch.equal(u, v) for u, v in zip(a, b)), k
         else:
             assert torch.equal(a, b), k
+
+
+# ---------------------------------------------------------------- grouped FP8 GEMM (tensor cores)
+
+def _rand_codes(shape, gen):
+    c = torch.randint(0, 256, shape, generator=gen, dtype=torch.int32).to(torch.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x38              # no NaN codes
+    return c
+
+
+def _gemm_bound(a, sa, w, sw, want):
+    """|got - want| <= 2^-8 |want| (bf16 output) + 2^-20 sum_k |a_k w_k| (fp32
+    accumulation inside the MMA and across K blocks)."""
+    import oracle
+    mag = oracle.grouped_fp8_gemm(a.numpy() & 0x7F, sa, w.numpy() & 0x7F, sw)
+    return 2.0 ** -8 * np.abs(want) + 2.0 ** -20 * mag
+
+
+def assert_gemm_parity(got, a, sa, w, sw):
+    import oracle
+    want = oracle.grouped_fp8_gemm(a, sa, w, sw)
+    bound = _gemm_bound(a, sa, w, sw, want)
+    err = np.abs(got.double().cpu().numpy() - want)
+    assert np.all(err <= bound), f"{np.count_nonzero(err > bound)} outputs beyond the bound"
+
+
+@pytest.mark.parametrize("m,g,k,n_out", [(1, 1, 128, 128), (128, 1, 128, 128), (300, 2, 512, 256),
+                                         (257, 4, 4096, 128), (130, 1, 1024, 384)])
+def test_gemm_random_codes(rq, m, g, k, n_out):
+    gen = torch.Generator().manual_seed(m + k)
+    a, w = _rand_codes((m, g, k), gen), _rand_codes((g, n_out, k), gen)
+    sa = 2.0 ** torch.randint(-8, 4, (m, g, k // 128), generator=gen).float()
+    sw = 2.0 ** torch.randint(-12, -4, (g, n_out // 128, k // 128), generator=gen).float()
+    dev = torch.device("cuda:0")
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = rq.grouped_fp8_gemm(a.to(dev), sa.to(dev), w.to(dev), sw.to(dev), error_flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    assert_gemm_parity(y, a, sa, w, sw)
+
+
+def test_gemm_consumes_the_inverse_op_output(rq):
+    """The op's own codes and scales (bit-exact with the oracle) feed the GEMM."""
+    inp = W.inverse_inputs(W.InverseSpec("gemm", 200, 16, 8, 4096, "uniform", True, seed=4))
+    dev = torch.device("cuda:0")
+    codes, scales = rq.inv_rope_fp8_quant(inp["x"].to(dev), inp["positions"].to(dev),
+                                          inp["cos_sin_cache"].to(dev), 8)
+    gen = torch.Generator().manual_seed(5)
+    w = _rand_codes((2, 256, 4096), gen)
+    sw = 2.0 ** torch.randint(-10, -6, (2, 2, 32), generator=gen).float()
+    y = rq.grouped_fp8_gemm(codes, scales, w.to(dev), sw.to(dev))
+    torch.cuda.synchronize()
+    wc, ws = oracle_inverse(inp)
+    assert_gemm_parity(y, torch.from_numpy(wc), ws, w, sw)

@@ -726,3 +726,34 @@ def test_indexer_scales_and_fold_invariants(oracle_lib):
     x = q.float().numpy()[..., 64:] / (2.0 ** e)[..., None]
     want = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(codes[..., 64:], want)
+
+
+# ----------------------------------------------------------------- next rows: grouped FP8 GEMM
+
+def test_gemm_oracle_identity_weights(oracle_lib):
+    """Weights = 1.0 (e4m3 0x38) on the diagonal, scale 2^-3: y = dequant(A)[:, :, :n_out] / 8."""
+    rng = np.random.default_rng(1)
+    a = rng.integers(0, 256, (5, 2, 256)).astype(np.uint8)
+    a[(a & 0x7F) == 0x7F] = 0x38
+    sa = np.ldexp(1.0, rng.integers(-4, 4, (5, 2, 2))).astype(np.float32)
+    w = np.zeros((2, 128, 256), np.uint8)
+    w[:, np.arange(128), np.arange(128)] = 0x38
+    sw = np.full((2, 1, 2), 0.125, np.float32)
+    y = oracle_lib.grouped_fp8_gemm(a, sa, w, sw)
+    want = oracle_lib.e4m3_decode(a[..., :128]) * sa[..., :1] / 8
+    assert np.array_equal(y, want)
+
+
+def test_gemm_oracle_brute_force(oracle_lib):
+    rng = np.random.default_rng(2)
+    a = rng.integers(0, 0x7F, (3, 1, 256)).astype(np.uint8) | (rng.integers(0, 2, (3, 1, 256)) << 7).astype(np.uint8)
+    w = rng.integers(0, 0x7F, (1, 128, 256)).astype(np.uint8)
+    sa = np.ldexp(1.0, rng.integers(-3, 3, (3, 1, 2))).astype(np.float32)
+    sw = np.ldexp(1.0, rng.integers(-3, 3, (1, 1, 2))).astype(np.float32)
+    y = oracle_lib.grouped_fp8_gemm(a, sa, w, sw)
+    dec = {c: oracle_lib.e4m3_decode(np.array([c], np.uint8))[0] for c in range(256)}
+    for m in range(3):
+        for n in (0, 5, 127):
+            s = sum(dec[int(a[m, 0, k])] * float(sa[m, 0, k // 128]) * dec[int(w[0, n, k])] *
+                    float(sw[0, 0, k // 128]) for k in range(256))
+            assert y[m, 0, n] == s
