@@ -427,6 +427,18 @@ def run_ours(args, world, rank, local):
             b.record(stream)
         torch.cuda.synchronize(dev)
         us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+
+        def fused_gemm_call():
+            rq.inv_rope_fp8_quant_gemm(x, pos, cache, hpg, wc, ws, out=gy)
+        for _ in range(3):
+            fused_gemm_call()
+        torch.cuda.synchronize(dev)
+        for a, b in evs:
+            a.record(stream)
+            fused_gemm_call()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        us_fused = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
         flop = 2.0 * n * h * 512 * g_out
         tf = flop / us / 1e6
         fp8_peak, fp8_src = measured_tensor_peak_fp8()
@@ -436,6 +448,13 @@ def run_ours(args, world, rank, local):
                 "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": fp8_peak,
                              "unit": "TFLOP/s", "frac": round(tf / fp8_peak, 4),
                              "peak_source": fp8_src},
+                "fused": {"kernel": "fused_inv_rope_quant_gemm_kernel",
+                          "what": "inverse RoPE + block-FP8 quant produced inside the GEMM "
+                                  "from bf16 x (codes never reach HBM)",
+                          "us": round(us_fused, 2),
+                          "tflops": round(flop / us_fused / 1e6, 1),
+                          "frac": round(flop / us_fused / 1e6 / fp8_peak, 4),
+                          "unfused_op_plus_gemm_us": round(inv_ms * 1e3 + us, 2)},
                 "launches": gl}
         del wc, ws, gy
 

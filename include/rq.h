@@ -290,6 +290,28 @@ rq_status rq_grouped_fp8_gemm(const uint8_t *a_codes, const float *a_scales, int
                               const float *w_scales, int64_t n_out, uint16_t *y_bf16,
                               uint32_t *error_flags, void *stream);
 
+/*
+ * The inverse RoPE + block-FP8 quant fused into its consumer: the grouped
+ * FP8 GEMM of rq_grouped_fp8_gemm, whose A operand (group g's 128-wide K
+ * blocks = its heads' quantisation blocks) is produced inside the GEMM from
+ * x with exactly the arithmetic of rq_inv_rope_fp8_quant; the codes and
+ * scales never reach HBM. The result equals rq_inv_rope_fp8_quant followed
+ * by rq_grouped_fp8_gemm, bit for bit.
+ *  x_bf16 .. eps   as in rq_inv_rope_fp8_quant, with heads_per_group <= 8
+ *                  and both strides > 0 (the input is read by tensor-map TMA).
+ *  w_codes, w_scales, n_out, y_bf16   as in rq_grouped_fp8_gemm, with
+ *                  groups = n_heads / heads_per_group and
+ *                  K = heads_per_group * 512.
+ * A token whose position is outside [0, cache_rows) sets
+ * RQ_FLAG_POSITION_RANGE; its y rows are then unspecified.
+ */
+rq_status rq_inv_rope_fp8_quant_gemm(const void *x_bf16, int64_t n_tokens, int64_t n_heads,
+                                     int64_t x_stride_token, int64_t x_stride_head,
+                                     const int64_t *positions, const float *cos_sin_cache,
+                                     int64_t cache_rows, int64_t heads_per_group, float eps,
+                                     const uint8_t *w_codes, const float *w_scales, int64_t n_out,
+                                     uint16_t *y_bf16, uint32_t *error_flags, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["grouped_fp8_gemm", "indexer_q_rope_quant", "qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
+__all__ = ["inv_rope_fp8_quant_gemm", "grouped_fp8_gemm", "indexer_q_rope_quant", "qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
            "empty_outputs", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
 
@@ -52,6 +52,8 @@ ABI_SYMBOLS = {
                                                    ctypes.c_int, _P, ctypes.c_float, ctypes.c_float,
                                                    ctypes.c_float, _P, _P, _P, _P]),
     "rq_grouped_fp8_gemm": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _P]),
+    "rq_inv_rope_fp8_quant_gemm": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
+                                                  ctypes.c_float, _P, _P, _I64, _P, _P, _P]),
     "rq_inv_rope_quant_layout": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
                                                 ctypes.c_float, ctypes.c_int, _P, _I64, _I64, _P,
                                                 _I64, _I64, _I64, _P, _P]),
@@ -447,4 +449,54 @@ def grouped_fp8_gemm(a_codes: torch.Tensor, a_scales: torch.Tensor, w_codes: tor
                                        w_codes.data_ptr(), w_scales.data_ptr(), n_out,
                                        out.data_ptr(), flags, _stream(a_codes.device))
     _check(st, "rq_grouped_fp8_gemm")
+    return out
+
+
+def inv_rope_fp8_quant_gemm(x: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                            heads_per_group: int, w_codes: torch.Tensor, w_scales: torch.Tensor,
+                            eps: float = DEFAULT_EPS, out: torch.Tensor | None = None,
+                            error_flags: torch.Tensor | None = None) -> torch.Tensor:
+    """Inverse RoPE + block-FP8 quant fused into the grouped FP8 GEMM
+    (``rq_inv_rope_fp8_quant_gemm``): y [N, G, n_out] bf16, bit-identical to
+    ``grouped_fp8_gemm(*inv_rope_fp8_quant(x, ...), w_codes, w_scales)``."""
+    _cuda(x, "x", torch.bfloat16)
+    if x.dim() != 3 or x.shape[2] != HEAD_DIM or x.stride(2) != 1:
+        raise ValueError("x must be [N, H, 512] with a contiguous last dim")
+    n, h = x.shape[0], x.shape[1]
+    hpg = int(heads_per_group)
+    if hpg < 1 or h % hpg:
+        raise ValueError(f"heads_per_group={hpg} must divide H={h}")
+    g, k = h // hpg, hpg * HEAD_DIM
+    _cuda(positions, "positions", torch.int64)
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    if positions.shape != (n,) or not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous [N] int64 tensor")
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != 64 or not cos_sin_cache.is_contiguous():
+        raise ValueError("cos_sin_cache must be a contiguous [P, 64] fp32 tensor")
+    if w_codes.dtype not in (torch.uint8, torch.float8_e4m3fn) or not w_codes.is_cuda or \
+            not w_codes.is_contiguous() or w_codes.dim() != 3 or w_codes.shape[0] != g or \
+            w_codes.shape[2] != k:
+        raise ValueError(f"w_codes must be a contiguous [G={g}, n_out, K={k}] e4m3 CUDA tensor")
+    n_out = w_codes.shape[1]
+    _cuda(w_scales, "w_scales", torch.float32)
+    if tuple(w_scales.shape) != (g, n_out // 128, k // 128) or not w_scales.is_contiguous():
+        raise ValueError("w_scales must be a contiguous [G, n_out/128, K/128] fp32 tensor")
+    if out is None:
+        out = torch.empty((n, g, n_out), dtype=torch.bfloat16, device=x.device)
+    _cuda(out, "out", torch.bfloat16)
+    if tuple(out.shape) != (n, g, n_out) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [N, G, n_out] bf16 tensor")
+    for t in (positions, cos_sin_cache, w_codes, w_scales, out):
+        if t.device != x.device:
+            raise ValueError("all tensors must be on the same device")
+    flags = 0
+    if error_flags is not None:
+        _cuda(error_flags, "error_flags", torch.int32)
+        flags = error_flags.data_ptr()
+    with torch.cuda.device(x.device):
+        st = lib().rq_inv_rope_fp8_quant_gemm(
+            x.data_ptr(), n, h, x.stride(0), x.stride(1), positions.data_ptr(),
+            cos_sin_cache.data_ptr(), cos_sin_cache.shape[0], hpg, float(eps), w_codes.data_ptr(),
+            w_scales.data_ptr(), n_out, out.data_ptr(), flags, _stream(x.device))
+    _check(st, "rq_inv_rope_fp8_quant_gemm")
     return out

@@ -360,3 +360,48 @@ RQ_EXPORT rq_status rq_grouped_fp8_gemm(const uint8_t* a_codes, const float* a_s
     return from_cuda(rq::launch_grouped_fp8_gemm(p, a_codes, w_codes, dev.ordinal,
                                                  static_cast<cudaStream_t>(stream)));
 }
+
+RQ_EXPORT rq_status rq_inv_rope_fp8_quant_gemm(
+    const void* x_bf16, int64_t n_tokens, int64_t n_heads, int64_t x_stride_token,
+    int64_t x_stride_head, const int64_t* positions, const float* cos_sin_cache,
+    int64_t cache_rows, int64_t heads_per_group, float eps, const uint8_t* w_codes,
+    const float* w_scales, int64_t n_out, uint16_t* y_bf16, uint32_t* error_flags, void* stream) {
+    if (n_tokens < 0 || n_heads < 1 || cache_rows < 1 || n_out < 128 || n_out % 128 != 0)
+        return RQ_ERR_SHAPE;
+    if (heads_per_group < 1 || n_heads % heads_per_group != 0) return RQ_ERR_GROUPING;
+    if (heads_per_group > 8) return RQ_ERR_SHAPE;  // K = heads_per_group * 512 <= 4096
+    if (!eps_ok(eps)) return RQ_ERR_ARG;
+    const int64_t groups = n_heads / heads_per_group;
+    if (n_tokens >= kMaxRows || groups * n_out >= kMaxRows ||
+        n_tokens * groups >= kMaxRows / n_out)
+        return RQ_ERR_SHAPE;
+    if (n_tokens == 0) return RQ_OK;
+    if (!x_bf16 || !positions || !cos_sin_cache || !w_codes || !w_scales || !y_bf16)
+        return RQ_ERR_NULL;
+    if (!aligned(x_bf16, 16) || x_stride_token % 8 != 0 || x_stride_head % 8 != 0 ||
+        x_stride_token <= 0 || x_stride_head <= 0 || !aligned(positions, 8) ||
+        !aligned(cos_sin_cache, 16) || !aligned(w_codes, 16) || !aligned(w_scales, 4) ||
+        !aligned(y_bf16, 16) || (error_flags && !aligned(error_flags, 4)))
+        return RQ_ERR_ALIGN;
+    rq::DeviceInfo dev;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return from_cuda(e);
+    rq::FusedGemmParams p;
+    p.x = x_bf16;
+    p.sx_t = x_stride_token;
+    p.sx_h = x_stride_head;
+    p.positions = positions;
+    p.cache = cos_sin_cache;
+    p.cache_rows = cache_rows;
+    p.m = static_cast<int>(n_tokens);
+    p.groups = static_cast<int>(groups);
+    p.hpg = static_cast<int>(heads_per_group);
+    p.k = static_cast<int>(heads_per_group * 512);
+    p.n_out = static_cast<int>(n_out);
+    p.eps = eps;
+    p.w_scales = w_scales;
+    p.y = y_bf16;
+    p.error_flags = error_flags;
+    return from_cuda(rq::launch_fused_inv_rope_quant_gemm(p, w_codes, dev.ordinal,
+                                                          static_cast<cudaStream_t>(stream)));
+}

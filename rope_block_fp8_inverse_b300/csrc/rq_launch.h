@@ -108,6 +108,20 @@ struct GemmParams {
     uint32_t* error_flags;
 };
 
+// Arguments of the fused inverse-RoPE + quant + grouped GEMM.
+struct FusedGemmParams {
+    const void* x;            // bf16 [m, groups * hpg, 512], strides sx_t / sx_h elements
+    int64_t sx_t, sx_h;
+    const int64_t* positions;
+    const float* cache;
+    int64_t cache_rows;
+    int m, groups, hpg, k, n_out;   // k = hpg * 512
+    float eps;
+    const float* w_scales;    // [groups, n_out / 128, k / 128]
+    uint16_t* y;              // bf16 [m, groups, n_out]
+    uint32_t* error_flags;
+};
+
 // Kernel variants of the inverse op (all bit-identical in output).
 enum InvVariant {
     kInvAuto = 0,        // chosen from the problem size
@@ -137,5 +151,7 @@ cudaError_t launch_indexer_q_rope_quant(const IdxParams& p, const DeviceInfo& de
                                         cudaStream_t stream);
 cudaError_t launch_grouped_fp8_gemm(const GemmParams& p, const uint8_t* a_codes,
                                     const uint8_t* w_codes, int dev_ordinal, cudaStream_t stream);
+cudaError_t launch_fused_inv_rope_quant_gemm(const FusedGemmParams& p, const uint8_t* w_codes,
+                                             int dev_ordinal, cudaStream_t stream);
 
 }  // namespace rq

@@ -768,3 +768,41 @@ def test_gemm_consumes_the_inverse_op_output(rq):
     torch.cuda.synchronize()
     wc, ws = oracle_inverse(inp)
     assert_gemm_parity(y, torch.from_numpy(wc), ws, w, sw)
+
+
+@pytest.mark.parametrize("n,h,hpg,n_out", [(1, 8, 8, 128), (200, 16, 8, 256), (300, 24, 6, 128),
+                                           (129, 32, 8, 384)])
+def test_fused_gemm_equals_op_then_gemm(rq, n, h, hpg, n_out):
+    """The fused kernel produces the A operand in shared memory with the op's
+    arithmetic, so its output equals the op followed by the GEMM bit for bit;
+    the GEMM part is also checked against the float64 oracle."""
+    inp = W.inverse_inputs(W.InverseSpec("fg", n, h, hpg, 4096, "uniform", True, seed=n))
+    dev = torch.device("cuda:0")
+    x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
+    g, k = h // hpg, hpg * 512
+    gen = torch.Generator().manual_seed(h)
+    w = _rand_codes((g, n_out, k), gen)
+    sw = 2.0 ** torch.randint(-10, -6, (g, n_out // 128, k // 128), generator=gen).float()
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = rq.inv_rope_fp8_quant_gemm(x, pos, cache, hpg, w.to(dev), sw.to(dev), error_flags=flags)
+    codes, scales = rq.inv_rope_fp8_quant(x, pos, cache, hpg)
+    y2 = rq.grouped_fp8_gemm(codes, scales, w.to(dev), sw.to(dev))
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    wc, ws = oracle_inverse(inp)
+    assert_gemm_parity(y, torch.from_numpy(wc), ws, w, sw)
+
+
+def test_fused_gemm_full_size_matches_op_then_gemm(rq):
+    inp = W.inverse_inputs(W.PREFILL16K)
+    dev = torch.device("cuda:0")
+    x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
+    gen = torch.Generator().manual_seed(3)
+    w = _rand_codes((4, 256, 4096), gen).to(dev)
+    sw = (2.0 ** torch.randint(-10, -6, (4, 2, 32), generator=gen).float()).to(dev)
+    y = rq.inv_rope_fp8_quant_gemm(x, pos, cache, 8, w, sw)
+    codes, scales = rq.inv_rope_fp8_quant(x, pos, cache, 8)
+    y2 = rq.grouped_fp8_gemm(codes, scales, w, sw)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
