@@ -34,6 +34,18 @@ constexpr int kHalfRope = 32;
 constexpr int kRecordBytes = 528;   // paged record: 512 codes + 4 fp32 scales
 constexpr unsigned kFull = 0xffffffffu;
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream drains;
+// pdl_wait() blocks until that kernel has completed and its memory is
+// visible, so it must come before the first global access. Without PDL
+// both are no-ops. pdl_launch_dependents() lets the next such kernel be
+// scheduled (its own pdl_wait() still waits for this one to finish).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Index (in 8-element chunks) of lane l's A chunk; its B chunk is A + 8.
 __device__ __forceinline__ int chunk_a(int lane) { return 16 * (lane >> 3) + (lane & 7); }
 

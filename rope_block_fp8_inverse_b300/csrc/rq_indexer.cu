@@ -76,6 +76,8 @@ __device__ __forceinline__ void st_stream4(void* p, uint32_t v) {
 template <bool kNeox>
 __global__ void __launch_bounds__(kInvThreads)
 indexer_q_rope_quant_kernel(IdxParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int rs = lane >> 3;           // head slot within a group of 4
     const int m = lane & 7;             // lane within the head: pairs 4m .. 4m+3
@@ -217,11 +219,8 @@ cudaError_t launch_indexer_q_rope_quant(const IdxParams& p, const DeviceInfo& de
     const int64_t need = (warps + kWarps - 1) / kWarps;
     const int64_t cap = int64_t(dev.sm_count) * idx_resident(dev.ordinal, p.neox);
     const int grid = static_cast<int>(need < cap ? need : cap);
-    if (p.neox)
-        indexer_q_rope_quant_kernel<true><<<grid, kInvThreads, 0, stream>>>(p);
-    else
-        indexer_q_rope_quant_kernel<false><<<grid, kInvThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    if (p.neox) return launch_pdl(indexer_q_rope_quant_kernel<true>, grid, kInvThreads, 0, stream, p);
+    return launch_pdl(indexer_q_rope_quant_kernel<false>, grid, kInvThreads, 0, stream, p);
 }
 
 }  // namespace rq

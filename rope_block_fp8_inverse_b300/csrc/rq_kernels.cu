@@ -23,6 +23,8 @@ namespace rq {
 template <int kRows>
 __global__ void __launch_bounds__(kInvThreads)
 inv_rope_fp8_quant_kernel(InvParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
@@ -80,6 +82,8 @@ inv_rope_fp8_quant_kernel(InvParams p) {
 template <int kRows, int kMode>
 __global__ void __launch_bounds__(kInvThreads)
 inv_rope_quant_layout_kernel(InvParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
@@ -162,6 +166,8 @@ inv_rope_quant_layout_kernel(InvParams p) {
 template <int kRows>
 __global__ void __launch_bounds__(kInsThreads)
 rope_fp8_quant_insert_kernel(InsParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
@@ -229,6 +235,8 @@ rope_fp8_quant_insert_kernel(InsParams p) {
 template <int kRows>
 __global__ void __launch_bounds__(kInvThreads)
 qnorm_rope_kv_insert_kernel(FusedParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
@@ -354,13 +362,13 @@ cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev,
     if (int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4) {
         auto k = inv_rope_fp8_quant_kernel<2>;
         const int res = resident_blocks(dev.ordinal, kInv2, k, kInvThreads);
-        k<<<grid_size(p.n_rows, kWarps * 2, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
-    } else {
-        auto k = inv_rope_fp8_quant_kernel<1>;
-        const int res = resident_blocks(dev.ordinal, kInv1, k, kInvThreads);
-        k<<<grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
+        return launch_pdl(k, grid_size(p.n_rows, kWarps * 2, dev.sm_count, res), kInvThreads, 0,
+                          stream, p);
     }
-    return cudaGetLastError();
+    auto k = inv_rope_fp8_quant_kernel<1>;
+    const int res = resident_blocks(dev.ordinal, kInv1, k, kInvThreads);
+    return launch_pdl(k, grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0, stream,
+                      p);
 }
 
 template <int kMode>
@@ -369,13 +377,13 @@ cudaError_t launch_layout(const InvParams& p, const DeviceInfo& dev, cudaStream_
     if (int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4) {
         auto k = inv_rope_quant_layout_kernel<2, kMode>;
         const int res = resident_blocks(dev.ordinal, Variant(kLay + 2 * kMode + 1), k, kInvThreads);
-        k<<<grid_size(p.n_rows, kWarps * 2, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
-    } else {
-        auto k = inv_rope_quant_layout_kernel<1, kMode>;
-        const int res = resident_blocks(dev.ordinal, Variant(kLay + 2 * kMode), k, kInvThreads);
-        k<<<grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
+        return launch_pdl(k, grid_size(p.n_rows, kWarps * 2, dev.sm_count, res), kInvThreads, 0,
+                          stream, p);
     }
-    return cudaGetLastError();
+    auto k = inv_rope_quant_layout_kernel<1, kMode>;
+    const int res = resident_blocks(dev.ordinal, Variant(kLay + 2 * kMode), k, kInvThreads);
+    return launch_pdl(k, grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0,
+                      stream, p);
 }
 
 cudaError_t launch_inv_rope_quant_layout(const InvParams& p, const DeviceInfo& dev,
@@ -392,8 +400,8 @@ cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& d
     constexpr int kWarps = kInsThreads / 32;
     auto k = rope_fp8_quant_insert_kernel<2>;
     const int res = resident_blocks(dev.ordinal, kIns2, k, kInsThreads);
-    k<<<grid_size(p.n_tokens, kWarps * 2, dev.sm_count, res), kInsThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k, grid_size(p.n_tokens, kWarps * 2, dev.sm_count, res), kInsThreads, 0,
+                      stream, p);
 }
 
 cudaError_t launch_qnorm_rope_kv_insert(const FusedParams& p, const DeviceInfo& dev,
@@ -402,13 +410,13 @@ cudaError_t launch_qnorm_rope_kv_insert(const FusedParams& p, const DeviceInfo& 
     if (int64_t(p.n_units) >= int64_t(dev.sm_count) * kWarps * 4) {
         auto k = qnorm_rope_kv_insert_kernel<2>;
         const int res = resident_blocks(dev.ordinal, kFus2, k, kInvThreads);
-        k<<<grid_size(p.n_units, kWarps * 2, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
-    } else {
-        auto k = qnorm_rope_kv_insert_kernel<1>;
-        const int res = resident_blocks(dev.ordinal, kFus1, k, kInvThreads);
-        k<<<grid_size(p.n_units, kWarps * 1, dev.sm_count, res), kInvThreads, 0, stream>>>(p);
+        return launch_pdl(k, grid_size(p.n_units, kWarps * 2, dev.sm_count, res), kInvThreads, 0,
+                          stream, p);
     }
-    return cudaGetLastError();
+    auto k = qnorm_rope_kv_insert_kernel<1>;
+    const int res = resident_blocks(dev.ordinal, kFus1, k, kInvThreads);
+    return launch_pdl(k, grid_size(p.n_units, kWarps * 1, dev.sm_count, res), kInvThreads, 0,
+                      stream, p);
 }
 
 }  // namespace rq

@@ -82,6 +82,8 @@ struct TileWalk {
 template <int kRows, int kStages, int kMode, bool kScaleBulk>
 __global__ void __launch_bounds__(kStreamWarps * 32)
 inv_rope_fp8_quant_stream_kernel(InvParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
     using R = Ring<kRows, kStages>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31;
@@ -307,9 +309,9 @@ cudaError_t launch_stream(const InvParams& p, const DeviceInfo& dev, cudaStream_
     const int64_t ctas_needed = (warps_needed + kStreamWarps - 1) / kStreamWarps;
     const int64_t cap = int64_t(dev.sm_count) * resident;
     const int grid = static_cast<int>(ctas_needed < cap ? ctas_needed : cap);
-    inv_rope_fp8_quant_stream_kernel<RQ_STREAM_ROWS, RQ_STREAM_STAGES, kMode, kScaleBulk>
-        <<<grid, kStreamWarps * 32, StreamRing::kCtaBytes, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(
+        inv_rope_fp8_quant_stream_kernel<RQ_STREAM_ROWS, RQ_STREAM_STAGES, kMode, kScaleBulk>, grid,
+        kStreamWarps * 32, StreamRing::kCtaBytes, stream, p);
 }
 
 }  // namespace
