@@ -359,3 +359,29 @@ def grouped_fp8_gemm(a_codes, a_scales, w_codes, w_scales) -> np.ndarray:
     a = a.reshape(n, g, k)
     w = w.reshape(g, n_out, k)
     return np.einsum("ngk,gok->ngo", a, w)
+
+
+def ue8m0_decode(codes) -> np.ndarray:
+    """Values of UE8M0 scale codes (OCP MX: an 8-bit biased exponent, no sign,
+    no mantissa): code e is 2^(e - 127); code 255 is NaN. Returns float64."""
+    e = _np(codes, np.uint8).astype(np.int64)
+    out = np.ldexp(1.0, e - 127)
+    return np.where(e == 255, np.nan, out)
+
+
+def grouped_fp8_gemm_ue8m0(a_codes, a_sf_words, w_codes, w_sf) -> np.ndarray:
+    """The grouped FP8 GEMM with UE8M0 block scales (the scale encoding of the
+    inverse-RoPE page's packed-scale output, S3, on both operands):
+      a_sf_words [N, G, K/512] uint32: byte b of word (n, g, h) is the code of
+                 K block 4h + b of row n in group g (one word per 512-wide head,
+                 exactly what the op writes in its UE8M0 mode);
+      w_sf       [G, n_out/128, K/128] uint8: one code per 128 x 128 weight block.
+    The codes are decoded to their powers of two and the GEMM is then the
+    definition of grouped_fp8_gemm. Returns [N, G, n_out] float64."""
+    words = _np(a_sf_words, np.uint32)
+    n, g, heads = words.shape
+    shifts = (8 * np.arange(BLOCKS_PER_HEAD, dtype=np.uint32))
+    a_bytes = ((words[..., None] >> shifts) & 0xFF).astype(np.uint8)   # [N, G, heads, 4]
+    a_scales = ue8m0_decode(a_bytes.reshape(n, g, heads * BLOCKS_PER_HEAD))
+    w_scales = ue8m0_decode(w_sf)
+    return grouped_fp8_gemm(a_codes, a_scales, w_codes, w_scales)

@@ -16,6 +16,7 @@ head / group index) fails at least one of them:
   spec by hand, layout fingerprints per (token, group, head), the block-amax
   invariant 224 <= amax/scale <= 448, the dequantisation error bound.
 """
+import math
 import os
 from fractions import Fraction
 
@@ -757,3 +758,58 @@ def test_gemm_oracle_brute_force(oracle_lib):
             s = sum(dec[int(a[m, 0, k])] * float(sa[m, 0, k // 128]) * dec[int(w[0, n, k])] *
                     float(sw[0, 0, k // 128]) for k in range(256))
             assert y[m, 0, n] == s
+
+
+def test_ue8m0_decode_special_codes(oracle_lib):
+    """OCP MX UE8M0: code 127 is 1.0, 0 is 2^-127, 254 is 2^127, 255 is NaN."""
+    v = oracle_lib.ue8m0_decode(np.array([0, 1, 126, 127, 128, 254, 255], np.uint8))
+    assert v[0] == math.ldexp(1.0, -127) and v[1] == math.ldexp(1.0, -126)
+    assert v[2] == 0.5 and v[3] == 1.0 and v[4] == 2.0 and v[5] == math.ldexp(1.0, 127)
+    assert math.isnan(v[6])
+
+
+def test_gemm_ue8m0_oracle_brute_force(oracle_lib):
+    """Scales given as UE8M0 codes: every (row, K block) of A has a distinct
+    exponent, so a wrong byte inside the packed word or a wrong word (head) shows.
+    Decoding here goes through torch's float8_e4m3fn, not the oracle's decoder."""
+    rng = np.random.default_rng(3)
+    n, k, n_out = 3, 1024, 256              # two heads of 4 blocks per row, 2 weight row blocks
+    a = rng.integers(0, 256, (n, 1, k)).astype(np.uint8)
+    a[(a & 0x7F) == 0x7F] = 0x30             # no NaN codes
+    w = rng.integers(0, 256, (1, n_out, k)).astype(np.uint8)
+    w[(w & 0x7F) == 0x7F] = 0x40
+    a_exp = (120 + rng.permutation(8 * n).reshape(n, 1, 8)).astype(np.uint32)   # per (row, block)
+    words = np.zeros((n, 1, 2), np.uint32)
+    for b in range(4):
+        words |= a_exp[..., b::4] << (8 * b)   # block 4h + b in byte b of word h
+    w_sf = rng.integers(124, 131, (1, n_out // 128, k // 128)).astype(np.uint8)
+    y = oracle_lib.grouped_fp8_gemm_ue8m0(a, words, w, w_sf)
+    dec = torch.from_numpy(np.arange(256, dtype=np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+    for m in range(n):
+        for o in (0, 77, 128, 255):
+            terms = []
+            for kk in range(k):
+                kt = kk // 128
+                sa = math.ldexp(1.0, int(a_exp[m, 0, kt]) - 127)
+                sw = math.ldexp(1.0, int(w_sf[0, o // 128, kt]) - 127)
+                terms.append(dec[a[m, 0, kk]] * sa * dec[w[0, o, kk]] * sw)   # each exact
+            # fsum is the correctly rounded sum; the oracle's float64 matmul may
+            # round each of its 1024 additions
+            exact = math.fsum(terms)
+            assert abs(y[m, 0, o] - exact) <= 2.0 ** -42 * math.fsum(abs(t) for t in terms)
+
+
+def test_gemm_ue8m0_oracle_matches_fp32_scales_of_the_op(oracle_lib):
+    """The op's UE8M0 output and its fp32 scales are the same powers of two, so
+    the GEMM over either scale encoding gives the same float64 result."""
+    spec = W.InverseSpec("g", 6, 8, 8, 4096, "uniform", True, seed=4)
+    inp = W.inverse_inputs(spec)
+    codes, scales = oracle_lib.inv_rope_fp8_quant(inp["x"], inp["positions"], inp["cos_sin_cache"], 8)
+    words = oracle_lib.pack_ue8m0(scales.reshape(6, 1, 32))
+    rng = np.random.default_rng(5)
+    w = rng.integers(0, 0x7F, (1, 128, 4096)).astype(np.uint8)
+    e = rng.integers(122, 132, (1, 1, 32)).astype(np.uint8)
+    y_ue = oracle_lib.grouped_fp8_gemm_ue8m0(codes.reshape(6, 1, 4096), words, w, e)
+    y_f32 = oracle_lib.grouped_fp8_gemm(codes.reshape(6, 1, 4096), scales.reshape(6, 1, 32), w,
+                                        np.ldexp(1.0, e.astype(np.int64) - 127).astype(np.float32))
+    assert np.array_equal(y_ue, y_f32)
