@@ -439,6 +439,26 @@ def run_ours(args, world, rank, local):
             b.record(stream)
         torch.cuda.synchronize(dev)
         us_fused = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+
+        # the same GEMM on the block-scaled MMA, fed by the op's UE8M0 mode
+        # (token-major packed words) and the weight scales as UE8M0 codes
+        mx_codes = torch.empty_like(out)
+        mx_words = torch.empty((n, h // hpg, hpg), dtype=torch.int32, device=dev)
+        rq.inv_rope_quant(x, pos, cache, hpg, mode="ue8m0", out=mx_codes, scales=mx_words)
+        w_sf = (torch.log2(ws).round().to(torch.int32) + 127).to(torch.uint8)
+
+        def mx_call():
+            rq.grouped_fp8_gemm_ue8m0(mx_codes, mx_words, wc, w_sf, out=gy)
+        for _ in range(3):
+            mx_call()
+        torch.cuda.synchronize(dev)
+        for a, b in evs:
+            a.record(stream)
+            mx_call()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        us_mx = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+        del mx_codes, mx_words
         flop = 2.0 * n * h * 512 * g_out
         tf = flop / us / 1e6
         fp8_peak, fp8_src = measured_tensor_peak_fp8()
@@ -455,6 +475,14 @@ def run_ours(args, world, rank, local):
                           "tflops": round(flop / us_fused / 1e6, 1),
                           "frac": round(flop / us_fused / 1e6 / fp8_peak, 4),
                           "unfused_op_plus_gemm_us": round(inv_ms * 1e3 + us, 2)},
+                "ue8m0": {"kernel": "grouped_fp8_gemm_ue8m0_kernel",
+                          "what": "UE8M0 block scales (the op's packed-scale output) applied "
+                                  "inside the block-scaled MMA (tcgen05 kind::mxf8f6f4)",
+                          "us": round(us_mx, 2),
+                          "roofline": {"bound": "tensor", "achieved": round(flop / us_mx / 1e6, 1),
+                                       "peak": fp8_peak, "unit": "TFLOP/s",
+                                       "frac": round(flop / us_mx / 1e6 / fp8_peak, 4),
+                                       "peak_source": fp8_src}},
                 "launches": gl}
         del wc, ws, gy
 

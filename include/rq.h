@@ -291,6 +291,37 @@ rq_status rq_grouped_fp8_gemm(const uint8_t *a_codes, const float *a_scales, int
                               uint32_t *error_flags, void *stream);
 
 /*
+ * The same grouped FP8 GEMM with UE8M0 block scales (power-of-two scales
+ * stored as 8-bit biased exponents, the encoding of the op's packed-scale
+ * output, [INV] S3), computed by the block-scaled tensor-core MMA, which
+ * applies both scales inside the K loop:
+ *   y[m, g, n] = sum over 128-wide K blocks kt of
+ *                2^(ea(m, g, kt) - 127) * 2^(ew(g, n / 128, kt) - 127)
+ *                * sum_{k in kt} e4m3(a_codes[m, g, k]) * e4m3(w_codes[g, n, k])
+ * accumulated in fp32 by the tensor cores, written as bf16 (round to
+ * nearest even). The order of the fp32 additions is the hardware's, so
+ * results agree with rq_grouped_fp8_gemm to fp32 accumulation error, not
+ * bit for bit.
+ *  a_codes     [n_tokens, groups, k_per_group] e4m3 codes, 16-byte aligned.
+ *  a_sf        [n_tokens, groups, k_per_group / 512] uint32, 4-byte aligned:
+ *              byte b (bits 8b..8b+7) of word (m, g, h) is ea(m, g, 4h + b),
+ *              i.e. the token-major scales of rq_inv_rope_quant_layout in
+ *              RQ_OUT_FP8_SCALE_UE8M0 mode (one word per 512-wide head).
+ *  w_codes     [groups, n_out, k_per_group] e4m3 codes, 16-byte aligned.
+ *  w_sf        [groups, n_out / 128, k_per_group / 128] uint8, one code ew
+ *              per 128 x 128 block.
+ *  y_bf16      [n_tokens, groups, n_out] bf16, 16-byte aligned.
+ *  k_per_group a multiple of 512, at most 4096; n_out a multiple of 128.
+ * Code 255 (NaN in the UE8M0 encoding) gives unspecified outputs. Any
+ * n_tokens >= 0. A bounded wait that gives up sets RQ_FLAG_TIMEOUT (never
+ * expected).
+ */
+rq_status rq_grouped_fp8_gemm_ue8m0(const uint8_t *a_codes, const uint32_t *a_sf,
+                                    int64_t n_tokens, int64_t groups, int64_t k_per_group,
+                                    const uint8_t *w_codes, const uint8_t *w_sf, int64_t n_out,
+                                    uint16_t *y_bf16, uint32_t *error_flags, void *stream);
+
+/*
  * The inverse RoPE + block-FP8 quant fused into its consumer: the grouped
  * FP8 GEMM of rq_grouped_fp8_gemm, whose A operand (group g's 128-wide K
  * blocks = its heads' quantisation blocks) is produced inside the GEMM from

@@ -17,7 +17,8 @@ import threading
 
 import torch
 
-__all__ = ["inv_rope_fp8_quant_gemm", "grouped_fp8_gemm", "indexer_q_rope_quant", "qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
+__all__ = ["inv_rope_fp8_quant_gemm", "grouped_fp8_gemm", "grouped_fp8_gemm_ue8m0",
+           "indexer_q_rope_quant", "qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
            "empty_outputs", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
 
@@ -52,6 +53,8 @@ ABI_SYMBOLS = {
                                                    ctypes.c_int, _P, ctypes.c_float, ctypes.c_float,
                                                    ctypes.c_float, _P, _P, _P, _P]),
     "rq_grouped_fp8_gemm": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _P]),
+    "rq_grouped_fp8_gemm_ue8m0": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P,
+                                                 _P]),
     "rq_inv_rope_fp8_quant_gemm": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
                                                   ctypes.c_float, _P, _P, _I64, _P, _P, _P]),
     "rq_inv_rope_quant_layout": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
@@ -449,6 +452,54 @@ def grouped_fp8_gemm(a_codes: torch.Tensor, a_scales: torch.Tensor, w_codes: tor
                                        w_codes.data_ptr(), w_scales.data_ptr(), n_out,
                                        out.data_ptr(), flags, _stream(a_codes.device))
     _check(st, "rq_grouped_fp8_gemm")
+    return out
+
+
+def grouped_fp8_gemm_ue8m0(a_codes: torch.Tensor, a_sf: torch.Tensor, w_codes: torch.Tensor,
+                           w_sf: torch.Tensor, out: torch.Tensor | None = None,
+                           error_flags: torch.Tensor | None = None) -> torch.Tensor:
+    """Grouped FP8 GEMM with UE8M0 block scales on the block-scaled tensor-core
+    MMA (``rq_grouped_fp8_gemm_ue8m0``). ``a_codes`` [N, G, K] e4m3 with
+    ``a_sf`` [N, G, K/512] packed UE8M0 words (int32 / uint32: byte b of word h
+    = K block 4h + b, what ``inv_rope_quant(mode="ue8m0")`` writes token-major);
+    ``w_codes`` [G, n_out, K] with ``w_sf`` [G, n_out/128, K/128] uint8 codes.
+    K a multiple of 512, at most 4096. Returns bf16 [N, G, n_out]."""
+    for t, name in ((a_codes, "a_codes"), (w_codes, "w_codes")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn) or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous uint8 / float8_e4m3fn tensor")
+    if a_codes.dim() != 3 or w_codes.dim() != 3:
+        raise ValueError("a_codes must be [N, G, K] and w_codes [G, n_out, K]")
+    n, g, k = a_codes.shape
+    if w_codes.shape[0] != g or w_codes.shape[2] != k:
+        raise ValueError("w_codes must be [G, n_out, K] with the codes' G and K")
+    n_out = w_codes.shape[1]
+    if not isinstance(a_sf, torch.Tensor) or not a_sf.is_cuda or \
+            a_sf.dtype not in (torch.int32, torch.uint32):
+        raise TypeError("a_sf must be an int32 / uint32 CUDA tensor")
+    _cuda(w_sf, "w_sf", torch.uint8)
+    if tuple(a_sf.shape) != (n, g, k // 512) or not a_sf.is_contiguous():
+        raise ValueError("a_sf must be a contiguous [N, G, K/512] tensor of packed words")
+    if tuple(w_sf.shape) != (g, n_out // 128, k // 128) or not w_sf.is_contiguous():
+        raise ValueError("w_sf must be a contiguous [G, n_out/128, K/128] uint8 tensor")
+    if out is None:
+        out = torch.empty((n, g, n_out), dtype=torch.bfloat16, device=a_codes.device)
+    _cuda(out, "out", torch.bfloat16)
+    if tuple(out.shape) != (n, g, n_out) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [N, G, n_out] bf16 tensor")
+    for t in (a_sf, w_codes, w_sf, out):
+        if t.device != a_codes.device:
+            raise ValueError("all tensors must be on the same device")
+    flags = 0
+    if error_flags is not None:
+        _cuda(error_flags, "error_flags", torch.int32)
+        flags = error_flags.data_ptr()
+    with torch.cuda.device(a_codes.device):
+        st = lib().rq_grouped_fp8_gemm_ue8m0(a_codes.data_ptr(), a_sf.data_ptr(), n, g, k,
+                                             w_codes.data_ptr(), w_sf.data_ptr(), n_out,
+                                             out.data_ptr(), flags, _stream(a_codes.device))
+    _check(st, "rq_grouped_fp8_gemm_ue8m0")
     return out
 
 

@@ -24,7 +24,8 @@ LIB_PATH = os.path.join(PKG, "librq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-Xptxas", "-v", *ARCH, f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["rq_kernels.cu", "rq_stream.cu", "rq_indexer.cu", "rq_gemm.cu", "rq_api.cpp"]
+SOURCES = ["rq_kernels.cu", "rq_stream.cu", "rq_indexer.cu", "rq_gemm.cu", "rq_gemm_mx.cu",
+           "rq_api.cpp"]
 
 
 def nvcc() -> str:

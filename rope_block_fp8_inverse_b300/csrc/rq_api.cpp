@@ -361,6 +361,39 @@ RQ_EXPORT rq_status rq_grouped_fp8_gemm(const uint8_t* a_codes, const float* a_s
                                                  static_cast<cudaStream_t>(stream)));
 }
 
+RQ_EXPORT rq_status rq_grouped_fp8_gemm_ue8m0(const uint8_t* a_codes, const uint32_t* a_sf,
+                                              int64_t n_tokens, int64_t groups,
+                                              int64_t k_per_group, const uint8_t* w_codes,
+                                              const uint8_t* w_sf, int64_t n_out,
+                                              uint16_t* y_bf16, uint32_t* error_flags,
+                                              void* stream) {
+    if (n_tokens < 0 || groups < 1 || k_per_group < 512 || k_per_group > 4096 || n_out < 128)
+        return RQ_ERR_SHAPE;
+    if (k_per_group % 512 != 0 || n_out % 128 != 0) return RQ_ERR_SHAPE;
+    if (n_tokens >= kMaxRows || groups * k_per_group >= kMaxRows || groups * n_out >= kMaxRows ||
+        n_tokens * groups >= kMaxRows / n_out)
+        return RQ_ERR_SHAPE;
+    if (n_tokens == 0) return RQ_OK;
+    if (!a_codes || !a_sf || !w_codes || !w_sf || !y_bf16) return RQ_ERR_NULL;
+    if (!aligned(a_codes, 16) || !aligned(w_codes, 16) || !aligned(y_bf16, 16) ||
+        !aligned(a_sf, 4) || (error_flags && !aligned(error_flags, 4)))
+        return RQ_ERR_ALIGN;
+    rq::DeviceInfo dev;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return from_cuda(e);
+    rq::MxGemmParams p;
+    p.m = static_cast<int>(n_tokens);
+    p.groups = static_cast<int>(groups);
+    p.k = static_cast<int>(k_per_group);
+    p.n_out = static_cast<int>(n_out);
+    p.a_sf = a_sf;
+    p.w_sf = w_sf;
+    p.y = y_bf16;
+    p.error_flags = error_flags;
+    return from_cuda(rq::launch_grouped_fp8_gemm_ue8m0(p, a_codes, w_codes, dev,
+                                                       static_cast<cudaStream_t>(stream)));
+}
+
 RQ_EXPORT rq_status rq_inv_rope_fp8_quant_gemm(
     const void* x_bf16, int64_t n_tokens, int64_t n_heads, int64_t x_stride_token,
     int64_t x_stride_head, const int64_t* positions, const float* cos_sin_cache,

@@ -489,10 +489,10 @@ EncodeTiled encode_fn() {
     return fn;
 }
 
-// 2-D uint8 tensor [rows, inner] with row stride `stride` bytes, boxes of
-// 128 bytes x box_rows rows, 128-byte swizzle; rows past the end read as zeros.
+}  // namespace
+
 bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t stride,
-              uint32_t box_rows = 128) {
+              uint32_t box_rows) {
     EncodeTiled fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {inner, rows};
@@ -503,6 +503,8 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 // The bf16 input as a 3-D tensor [tokens, heads, 512] with free token / head
 // strides; boxes of 128 elements x 1 head x 128 tokens, no swizzle.
@@ -523,7 +525,8 @@ bool make_x_map(CUtensorMap* map, const FusedGemmParams& p) {
 cudaError_t launch_grouped_fp8_gemm(const GemmParams& p, const uint8_t* a_codes,
                                     const uint8_t* w_codes, int dev_ordinal, cudaStream_t stream) {
     CUtensorMap ma, mw;
-    if (!make_map(&ma, a_codes, uint64_t(p.groups) * p.k, uint64_t(p.m), uint64_t(p.groups) * p.k) ||
+    if (!make_map(&ma, a_codes, uint64_t(p.groups) * p.k, uint64_t(p.m), uint64_t(p.groups) * p.k,
+                  128) ||
         !make_map(&mw, w_codes, uint64_t(p.k), uint64_t(p.groups) * p.n_out, uint64_t(p.k), kGBN))
         return cudaErrorInvalidValue;
     constexpr int kMax = 64;
@@ -543,7 +546,7 @@ cudaError_t launch_grouped_fp8_gemm(const GemmParams& p, const uint8_t* a_codes,
 cudaError_t launch_fused_inv_rope_quant_gemm(const FusedGemmParams& p, const uint8_t* w_codes,
                                              int dev_ordinal, cudaStream_t stream) {
     CUtensorMap mw, mx;
-    if (!make_map(&mw, w_codes, uint64_t(p.k), uint64_t(p.groups) * p.n_out, uint64_t(p.k)) ||
+    if (!make_map(&mw, w_codes, uint64_t(p.k), uint64_t(p.groups) * p.n_out, uint64_t(p.k), 128) ||
         !make_x_map(&mx, p))
         return cudaErrorInvalidValue;
     constexpr int kMax = 64;

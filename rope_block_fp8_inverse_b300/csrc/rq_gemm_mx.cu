@@ -1,0 +1,323 @@
+// rq_gemm_mx.cu -- the consumer grouped FP8 GEMM with UE8M0 block scales on
+// the block-scaled 5th-generation tensor-core MMA (tcgen05.mma
+// kind::mxf8f6f4, one UE8M0 scale code per row and 32-wide K step).
+//
+// The inverse-RoPE page's packed-scale output ("[vllm] 한 프로그램이 4개 head를
+// 처리하게 하라: DeepSeek-V4 inverse RoPE + FP8 quant 커널 3.5배 가속기", S3:
+// four UE8M0 codes per head in one 32-bit word) is exactly the scale operand
+// this MMA reads: the word of head h covers the group's K blocks 4h..4h+3,
+// and the instruction descriptor's scale-factor byte (kt % 4) picks block kt's
+// code out of it. Weight scales are one code per 128 x 128 block. The tensor
+// cores apply both scales inside the K loop, so the whole K reduction of a
+// tile accumulates in TMEM and is read back once, by the epilogue: nothing is
+// folded in registers per K tile (which is what bounds the fp32-scale GEMM of
+// rq_gemm.cu).
+//
+// For every group g:  Y[:, g, :] = (A_g * 2^(sa - 127)) @ (W_g * 2^(sw - 127))^T,
+// Y bf16 [M, G, n_out].
+//
+// Persistent CTAs (one per SM) walk the 128 x 256 output tiles t = blockIdx.x,
+// blockIdx.x + gridDim.x, ...; the N tiles of one (M tile, group) are
+// neighbours, so concurrent CTAs read the same A rows from L2.
+//   warp 0   one lane: tensor-map TMA of each 128-wide K step of A (16 KiB)
+//            and W (32 KiB) into a 4-stage ring;
+//   warp 1   allocates TMEM; one lane copies each tile's scale codes from
+//            shared memory to TMEM (tcgen05.cp) and issues the MMAs
+//            (M = 128, N = 256, 4 x K = 32 per K step);
+//   warp 2   builds each tile's scale-code atoms in shared memory (double
+//            buffered), one tile ahead of the MMA;
+//   warps 4..11  epilogue: thread = output row (TMEM lane 32 * (warp % 4) +
+//            lane), 128 of the 256 columns; reads the finished accumulator,
+//            releases it to the next tile's MMAs, then stores bf16.
+// TMEM (512 columns): accumulator 0..255, A scale codes 256..319 (two tiles),
+// W scale codes 320..447 (two tiles). Every wait is bounded; a role that gives
+// up raises a shared abort flag that the others poll, so the CTA still drains
+// its copies, frees TMEM and exits, and the call reports RQ_FLAG_TIMEOUT.
+#include "rq_device.cuh"
+#include "rq_launch.h"
+#include "rq_tma.cuh"
+#include "rq_umma.cuh"
+
+namespace rq {
+
+namespace {
+
+constexpr int kMxBM = 128, kMxBN = 256, kMxBK = 128;
+constexpr int kMxStages = 4;
+constexpr int kMxMaxHeads = 8;                                  // K up to 8 x 512 = 4096
+constexpr uint32_t kMxATile = kMxBM * kMxBK;                    // 16 KiB
+constexpr uint32_t kMxWTile = kMxBN * kMxBK;                    // 32 KiB
+constexpr uint32_t kSfAtom = 512;                               // 32 rows x 16 bytes
+constexpr uint32_t kSfaBytes = kMxMaxHeads * kSfAtom;           // one atom per head
+constexpr uint32_t kSfbBytes = 2 * kMxMaxHeads * kSfAtom;       // per head: two N halves
+constexpr uint32_t kSfBufBytes = kSfaBytes + kSfbBytes;
+constexpr uint32_t kMxOffW = kMxStages * kMxATile;
+constexpr uint32_t kMxOffSf = kMxOffW + kMxStages * kMxWTile;
+constexpr uint32_t kMxOffBar = kMxOffSf + 2 * kSfBufBytes;
+// full[S], empty[S], sf_full[2], sf_empty[2], tfull, tempty, done
+constexpr uint32_t kMxNumBars = 2 * kMxStages + 4 + 3;
+constexpr uint32_t kMxOffSlot = kMxOffBar + 8 * kMxNumBars;     // TMEM base, abort flag
+constexpr uint32_t kMxSmem = kMxOffSlot + 16 + 1024;            // + room to align to 1 KiB
+constexpr int kMxThreads = 384;
+constexpr int kMxEpiWarp0 = 4;
+constexpr int kMxEpiThreads = kMxThreads - 32 * kMxEpiWarp0;    // 256
+constexpr uint32_t kTmemSfa = 256;     // + 32 per buffer: 4 columns per head word
+constexpr uint32_t kTmemSfb = 320;     // + 64 per buffer: 8 columns per head word
+constexpr uint32_t kMxTmemCols = 512;
+constexpr uint32_t kUe8m0One4 = 0x7f7f7f7fu;                    // four codes of 1.0
+
+static_assert(kMxSmem <= 232448, "shared memory per CTA");
+static_assert(kTmemSfb + 2 * 8 * kMxMaxHeads <= kMxTmemCols, "TMEM columns");
+
+// Poll an mbarrier phase; give up after kSpinLimit polls (raising `abort`)
+// or as soon as another role has raised it.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile uint32_t* abort) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && *abort) return false;
+    }
+    *abort = 1u;
+    return false;
+}
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                      uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+struct MxTile {
+    int mt, g, nt;
+};
+
+__device__ __forceinline__ MxTile mx_tile(int t, int n_nt, int groups) {
+    MxTile x;
+    x.nt = t % n_nt;
+    const int r = t / n_nt;
+    x.g = r % groups;
+    x.mt = r / groups;
+    return x;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kMxThreads, 1)
+grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
+                              const __grid_constant__ CUtensorMap tma_w, MxGemmParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t a0 = base, w0 = base + kMxOffW, sf0 = base + kMxOffSf, bar0 = base + kMxOffBar;
+    const uint32_t full0 = bar0, empty0 = bar0 + 8 * kMxStages;
+    const uint32_t sfull0 = bar0 + 16 * kMxStages, sempty0 = sfull0 + 16;
+    const uint32_t tfull = sempty0 + 16, tempty = tfull + 8, done = tempty + 8;
+    uint8_t* slot = smem_raw + (base + kMxOffSlot - raw);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(slot);
+    volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(slot + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_kt = p.k / kMxBK, n_heads = p.k / 512;
+    const int n_nt = (p.n_out + kMxBN - 1) / kMxBN;
+    const int n_tiles = ((p.m + kMxBM - 1) / kMxBM) * p.groups * n_nt;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMxStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sfull0 + 8 * b, 1);
+            mbar_init(sempty0 + 8 * b, 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty, kMxEpiThreads);
+        mbar_init(done, 1);
+        *abort = 0u;
+        mbar_init_fence();
+    }
+    if (warp == 1) {
+        umma::tmem_alloc(base + kMxOffSlot, kMxTmemCols);
+        umma::tmem_relinquish();
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;  // K steps issued
+            bool ok = true;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                const MxTile x = mx_tile(t, n_nt, p.groups);
+                for (int kt = 0; kt < n_kt; ++kt) {
+                    const uint32_t s = it % kMxStages, ph = (it / kMxStages) & 1u;
+                    if (!wait_or_abort(empty0 + 8 * s, ph ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full0 + 8 * s, kMxATile + kMxWTile);
+                    umma::tma_load_2d(a0 + s * kMxATile, &tma_a, x.g * p.k + kt * kMxBK,
+                                      x.mt * kMxBM, full0 + 8 * s);
+                    umma::tma_load_2d(w0 + s * kMxWTile, &tma_w, kt * kMxBK,
+                                      x.g * p.n_out + x.nt * kMxBN, full0 + 8 * s);
+                    ++it;
+                }
+            }
+            // Let the copies still in flight land before the CTA exits (on the
+            // normal path every one of them was already consumed).
+            for (uint32_t j = it > uint32_t(kMxStages) ? it - kMxStages : 0u; j < it; ++j)
+                if (!mbar_wait(full0 + 8 * (j % kMxStages), (j / kMxStages) & 1u)) *abort = 1u;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t it = 0, i = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++i) {
+                const uint32_t b = i & 1u;
+                if (!wait_or_abort(sfull0 + 8 * b, (i >> 1) & 1u, abort) ||
+                    !wait_or_abort(tempty, (i & 1u) ^ 1u, abort))
+                    break;
+                umma::fence_after_sync();
+                const uint32_t sfa_t = tmem + kTmemSfa + 32 * b, sfb_t = tmem + kTmemSfb + 64 * b;
+                const uint32_t sfa = sf0 + b * kSfBufBytes, sfb = sfa + kSfaBytes;
+                for (int h = 0; h < n_heads; ++h) {
+                    umma::cp_32x128b_warpx4(sfa_t + 4 * h, umma::smem_desc_plain(sfa + h * kSfAtom));
+                    umma::cp_32x128b_warpx4(sfb_t + 8 * h,
+                                            umma::smem_desc_plain(sfb + 2 * h * kSfAtom));
+                    umma::cp_32x128b_warpx4(sfb_t + 8 * h + 4,
+                                            umma::smem_desc_plain(sfb + (2 * h + 1) * kSfAtom));
+                }
+                umma::commit(sempty0 + 8 * b);  // the atoms are free once copied
+                for (int kt = 0; kt < n_kt; ++kt) {
+                    const uint32_t s = it % kMxStages, ph = (it / kMxStages) & 1u;
+                    if (!wait_or_abort(full0 + 8 * s, ph, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    umma::fence_after_sync();
+                    const uint64_t ad = umma::smem_desc_sw128(a0 + s * kMxATile);
+                    const uint64_t wd = umma::smem_desc_sw128(w0 + s * kMxWTile);
+                    const uint32_t idesc = umma::idesc_mx_e4m3_ue8m0(kMxBM, kMxBN, uint32_t(kt & 3));
+                    const uint32_t h = uint32_t(kt >> 2);
+#pragma unroll
+                    for (int k = 0; k < kMxBK / 32; ++k)  // K = 32 bytes of e4m3 per MMA
+                        umma::mma_mxf8f6f4(tmem, ad + 2 * k, wd + 2 * k, idesc, sfa_t + 4 * h,
+                                           sfb_t + 8 * h, (kt | k) != 0);
+                    umma::commit(empty0 + 8 * s);
+                    ++it;
+                }
+                if (ok) umma::commit(tfull);
+            }
+            umma::commit(done);
+            if (!mbar_wait(done, 0)) *abort = 1u;  // nothing in flight before teardown
+        }
+    } else if (warp == 2) {
+        uint32_t i = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
+            const MxTile x = mx_tile(t, n_nt, p.groups);
+            const uint32_t b = i & 1u;
+            if (!__all_sync(kFull, wait_or_abort(sempty0 + 8 * b, ((i >> 1) & 1u) ^ 1u, abort)))
+                break;
+            const uint32_t sfa = sf0 + b * kSfBufBytes, sfb = sfa + kSfaBytes;
+            // A: atom h, 16-byte row `lane` = the words of rows lane + 32c, c = 0..3
+            uint32_t wa[kMxMaxHeads][4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int row = x.mt * kMxBM + lane + 32 * c;
+                const uint32_t* src = p.a_sf + (int64_t(row) * p.groups + x.g) * n_heads;
+#pragma unroll
+                for (int h = 0; h < kMxMaxHeads; ++h)
+                    wa[h][c] = (h < n_heads && row < p.m) ? __ldg(src + h) : kUe8m0One4;
+            }
+#pragma unroll
+            for (int h = 0; h < kMxMaxHeads; ++h)
+                if (h < n_heads)
+                    sts16(sfa + h * kSfAtom + 16 * lane, wa[h][0], wa[h][1], wa[h][2], wa[h][3]);
+            // W: one code per 128 x 128 block, the same for every row of an atom;
+            // bytes b of the word = K blocks 4h + b
+            const int n_blk = p.n_out / 128;
+            for (int h = 0; h < n_heads; ++h) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int nb = 2 * x.nt + half;
+                    uint32_t w = kUe8m0One4;
+                    if (nb < n_blk) {
+                        const uint8_t* src = p.w_sf + (int64_t(x.g) * n_blk + nb) * n_kt + 4 * h;
+                        w = uint32_t(__ldg(src)) | (uint32_t(__ldg(src + 1)) << 8) |
+                            (uint32_t(__ldg(src + 2)) << 16) | (uint32_t(__ldg(src + 3)) << 24);
+                    }
+                    sts16(sfb + (2 * h + half) * kSfAtom + 16 * lane, w, w, w, w);
+                }
+            }
+            fence_proxy_async_smem();  // generic-proxy writes -> tcgen05.cp reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sfull0 + 8 * b);
+        }
+    } else if (warp >= kMxEpiWarp0) {
+        const int quad = warp & 3;
+        const int half = (warp - kMxEpiWarp0) >> 2;
+        uint32_t i = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
+            const MxTile x = mx_tile(t, n_nt, p.groups);
+            // the warp leaves together: the TMEM loads below are warp-collective
+            if (!__all_sync(kFull, wait_or_abort(tfull, i & 1u, abort))) break;
+            umma::fence_after_sync();
+            uint32_t packed[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float d[32];
+                umma::ld32(tmem + (uint32_t(quad * 32) << 16) + half * 128 + c * 32, d);
+                umma::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) packed[c * 16 + j] = bf16x2(d[2 * j], d[2 * j + 1]);
+            }
+            umma::fence_before_sync();
+            mbar_arrive(tempty);  // the accumulator may take the next tile's MMAs
+            const int row = x.mt * kMxBM + quad * 32 + lane;
+            const int col = x.nt * kMxBN + half * 128;
+            if (row < p.m && col < p.n_out) {
+                uint16_t* y = p.y + (int64_t(row) * p.groups + x.g) * p.n_out + col;
+#pragma unroll
+                for (int j = 0; j < 64; j += 4)
+                    *reinterpret_cast<uint4*>(y + 2 * j) =
+                        make_uint4(packed[j], packed[j + 1], packed[j + 2], packed[j + 3]);
+            }
+        }
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort && p.error_flags) atomicOr(p.error_flags, RQ_FLAG_TIMEOUT);
+    if (warp == 1) {
+        umma::fence_after_sync();
+        umma::tmem_dealloc(tmem, kMxTmemCols);
+    }
+}
+
+cudaError_t launch_grouped_fp8_gemm_ue8m0(const MxGemmParams& p, const uint8_t* a_codes,
+                                          const uint8_t* w_codes, const DeviceInfo& dev,
+                                          cudaStream_t stream) {
+    CUtensorMap ma, mw;
+    if (!make_map(&ma, a_codes, uint64_t(p.groups) * p.k, uint64_t(p.m), uint64_t(p.groups) * p.k,
+                  kMxBM) ||
+        !make_map(&mw, w_codes, uint64_t(p.k), uint64_t(p.groups) * p.n_out, uint64_t(p.k), kMxBN))
+        return cudaErrorInvalidValue;
+    constexpr int kMax = 64;
+    static thread_local bool attr_done[kMax] = {};
+    const int d = (dev.ordinal >= 0 && dev.ordinal < kMax) ? dev.ordinal : 0;
+    if (!attr_done[d]) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            grouped_fp8_gemm_ue8m0_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMxSmem));
+        if (e != cudaSuccess) return e;
+        attr_done[d] = true;
+    }
+    const int64_t tiles = int64_t((p.m + kMxBM - 1) / kMxBM) * p.groups *
+                          ((p.n_out + kMxBN - 1) / kMxBN);
+    if (tiles == 0) return cudaSuccess;
+    const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
+    grouped_fp8_gemm_ue8m0_kernel<<<grid, kMxThreads, kMxSmem, stream>>>(ma, mw, p);
+    return cudaGetLastError();
+}
+
+}  // namespace rq

@@ -2,6 +2,7 @@
 // the kernel launchers (rq_kernels.cu). Not installed, not part of the ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -129,6 +130,15 @@ struct GemmParams {
     uint32_t* error_flags;
 };
 
+// Arguments of the grouped FP8 GEMM with UE8M0 block scales.
+struct MxGemmParams {
+    int m, groups, k, n_out;  // k = per-group K (multiple of 512, at most 4096), n_out % 128 == 0
+    const uint32_t* a_sf;     // [m, groups, k / 512] packed UE8M0 words (byte b = block 4h + b)
+    const uint8_t* w_sf;      // [groups, n_out / 128, k / 128] UE8M0 codes
+    uint16_t* y;              // bf16 [m, groups, n_out]
+    uint32_t* error_flags;
+};
+
 // Arguments of the fused inverse-RoPE + quant + grouped GEMM.
 struct FusedGemmParams {
     const void* x;            // bf16 [m, groups * hpg, 512], strides sx_t / sx_h elements
@@ -174,5 +184,14 @@ cudaError_t launch_grouped_fp8_gemm(const GemmParams& p, const uint8_t* a_codes,
                                     const uint8_t* w_codes, int dev_ordinal, cudaStream_t stream);
 cudaError_t launch_fused_inv_rope_quant_gemm(const FusedGemmParams& p, const uint8_t* w_codes,
                                              int dev_ordinal, cudaStream_t stream);
+cudaError_t launch_grouped_fp8_gemm_ue8m0(const MxGemmParams& p, const uint8_t* a_codes,
+                                          const uint8_t* w_codes, const DeviceInfo& dev,
+                                          cudaStream_t stream);
+
+// Tensor map of a 2-D uint8 tensor [rows, inner] with row stride `stride`
+// bytes: boxes of 128 bytes x box_rows rows, 128-byte swizzle, rows past the
+// end read as zeros. False when the driver rejects it (or has no encoder).
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t stride,
+              uint32_t box_rows);
 
 }  // namespace rq

@@ -18,6 +18,18 @@
 //   bits 4..5 D format (1 = f32), 7..9 A format (0 = e4m3), 10..12 B format
 //   (0 = e4m3), 15 / 16 A / B major (0 = K-major), 17..22 N >> 3,
 //   24..28 M >> 4; all other bits 0 (dense, no negation, no saturation).
+// Instruction descriptor of kind::mxf8f6f4 (block-scaled, D always f32):
+//   bits 4..5 B scale-factor byte, 7..9 / 10..12 A / B format (0 = e4m3),
+//   17..22 N >> 3, 23 scale format (1 = UE8M0), 24..28 M >> 4, 29..30 A
+//   scale-factor byte.
+// Scale factors in tensor memory (scale_vec::1X: one UE8M0 code per row and
+// 32-wide K step): a 32-bit TMEM cell holds four codes and the descriptor's
+// scale-factor byte picks one. For 128 rows (of A, or a 128-row slice of B)
+// the codes sit in 4 consecutive columns: column c, byte b, in every lane
+// quadrant at lane 32q + i, holds the code of row i + 32c. That is what
+// tcgen05.cp .32x128b.warpx4 writes from a 512-byte shared-memory atom whose
+// 16-byte row i holds words (row i, i+32, i+64, i+96); B rows 128..255 use
+// the next 4 columns.
 #pragma once
 
 #include <cuda.h>
@@ -39,6 +51,22 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_byte_addr) {
 
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
     return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3_ue8m0(int m, int n, uint32_t sf_byte) {
+    return (sf_byte << 4) | (uint32_t(n >> 3) << 17) | (1u << 23) | (uint32_t(m >> 4) << 24) |
+           (sf_byte << 29);
+}
+
+// Shared-memory descriptor of an unswizzled K-major operand made of 8-row x
+// 16-byte core matrices stored one after the other (rows 16 bytes apart):
+// stride byte offset 128, leading byte offset unused, layout 0 = no swizzle.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t smem_byte_addr) {
+    uint64_t d = 0;
+    d |= uint64_t((smem_byte_addr >> 4) & 0x3fffu);
+    d |= uint64_t(128u >> 4) << 32;
+    d |= uint64_t(1u) << 46;
+    return d;
 }
 
 // TMEM allocation: one full warp executes these.
@@ -74,6 +102,30 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
         : "memory");
+}
+
+// Block-scaled D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T, e4m3 operands, UE8M0
+// scale factors read from TMEM columns sfa_tmem / sfb_tmem (byte chosen by
+// the instruction descriptor).
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                             uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+        "[%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(acc)
+        : "memory");
+}
+
+// Copy a 512-byte shared-memory atom (32 rows x 16 bytes) into 4 TMEM columns
+// of all four lane quadrants (lane 32q + i, column c = bytes 4c..4c+3 of row
+// i). Ordered with this thread's later tcgen05.mma; completion is tracked by
+// tcgen05.commit like an MMA.
+__device__ __forceinline__ void cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
 }
 
 // Arrive once on the mbarrier when every tcgen05 operation this thread

@@ -237,3 +237,28 @@ def test_gemm_rejects_bad_arguments(lib, kw, status):
 
 def test_gemm_empty_is_a_no_op(lib):
     assert _gemm(lib, n=0, a=None, sa=None, w=None, sw=None, y=None) == RQ_OK
+
+
+def _gemm_mx(lib, a=A16, sa=A16, n=4, g=2, k=512, w=A16, sw=A16, no=256, y=A16):
+    return lib.rq_grouped_fp8_gemm_ue8m0(a, sa, n, g, k, w, sw, no, y, None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=128), RQ_ERR_SHAPE),        # K must hold whole 512-wide heads (one scale word each)
+    (dict(k=640), RQ_ERR_SHAPE),
+    (dict(k=4608), RQ_ERR_SHAPE),       # at most 4096 (the scale codes' TMEM budget)
+    (dict(no=200), RQ_ERR_SHAPE),
+    (dict(g=0), RQ_ERR_SHAPE),
+    (dict(n=-1), RQ_ERR_SHAPE),
+    (dict(sa=None), RQ_ERR_NULL),
+    (dict(sw=None), RQ_ERR_NULL),
+    (dict(y=A8), RQ_ERR_ALIGN),
+    (dict(a=A8), RQ_ERR_ALIGN),
+    (dict(sa=A16 + 2), RQ_ERR_ALIGN),
+])
+def test_gemm_ue8m0_rejects_bad_arguments(lib, kw, status):
+    assert _gemm_mx(lib, **kw) == status
+
+
+def test_gemm_ue8m0_empty_is_a_no_op(lib):
+    assert _gemm_mx(lib, n=0, a=None, sa=None, w=None, sw=None, y=None) == RQ_OK

@@ -806,3 +806,94 @@ def test_fused_gemm_full_size_matches_op_then_gemm(rq):
     y2 = rq.grouped_fp8_gemm(codes, scales, w, sw)
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+# ---------------------------------------------------------------- grouped FP8 GEMM, UE8M0 scales
+
+def _ue8m0_case(m, g, k, n_out, seed):
+    """Random codes, A scale codes per (row, 128-block) in [118, 134), packed
+    four to a word, and W codes per 128 x 128 block in [120, 130)."""
+    gen = torch.Generator().manual_seed(seed)
+    a, w = _rand_codes((m, g, k), gen), _rand_codes((g, n_out, k), gen)
+    ea = torch.randint(118, 134, (m, g, k // 128), generator=gen, dtype=torch.int64)
+    words = (ea.view(m, g, k // 512, 4) << torch.tensor([0, 8, 16, 24])).sum(-1)
+    a_sf = words.to(torch.uint32).view(torch.int32) if hasattr(torch, "uint32") else \
+        words.to(torch.int64).to(torch.int32)
+    w_sf = torch.randint(120, 130, (g, n_out // 128, k // 128), generator=gen,
+                         dtype=torch.int32).to(torch.uint8)
+    sa = torch.ldexp(torch.ones(()), (ea - 127).float()).float()
+    sw = torch.ldexp(torch.ones(()), (w_sf.long() - 127).float()).float()
+    return a, a_sf, w, w_sf, sa, sw
+
+
+@pytest.mark.parametrize("m,g,k,n_out", [(1, 1, 512, 128), (128, 1, 512, 256), (300, 2, 1024, 384),
+                                         (257, 4, 4096, 1024), (1000, 1, 2048, 640),
+                                         (5, 3, 4096, 128)])
+def test_gemm_ue8m0_random_codes(rq, m, g, k, n_out):
+    """Every row and K block has its own scale code, so a wrong scale-factor
+    layout (row, K block or N half) fails the float64 oracle's bound."""
+    import oracle
+    a, a_sf, w, w_sf, sa, sw = _ue8m0_case(m, g, k, n_out, seed=m * 7 + k)
+    dev = torch.device("cuda:0")
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = rq.grouped_fp8_gemm_ue8m0(a.to(dev), a_sf.to(dev), w.to(dev), w_sf.to(dev),
+                                  error_flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    want = oracle.grouped_fp8_gemm_ue8m0(a.numpy(), a_sf.numpy().view(np.uint32), w.numpy(),
+                                         w_sf.numpy())
+    bound = _gemm_bound(a, sa.numpy(), w, sw.numpy(), want)
+    err = np.abs(y.double().cpu().numpy() - want)
+    assert np.all(err <= bound), f"{np.count_nonzero(err > bound)} outputs beyond the bound"
+
+
+def test_gemm_ue8m0_consumes_the_op_ue8m0_output(rq):
+    """The op's UE8M0 mode (packed words, token-major) feeds the block-scaled
+    GEMM directly; the result matches the fp32-scale GEMM on the op's fp32
+    scales within the same bound (both are the same powers of two)."""
+    import oracle
+    inp = W.inverse_inputs(W.InverseSpec("gemm", 300, 16, 8, 4096, "uniform", True, seed=6))
+    dev = torch.device("cuda:0")
+    x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
+    codes, words = rq.inv_rope_quant(x, pos, cache, 8, mode="ue8m0")
+    gen = torch.Generator().manual_seed(7)
+    w = _rand_codes((2, 384, 4096), gen)
+    w_sf = torch.randint(120, 126, (2, 3, 32), generator=gen, dtype=torch.int32).to(torch.uint8)
+    y = rq.grouped_fp8_gemm_ue8m0(codes, words, w.to(dev), w_sf.to(dev))
+    torch.cuda.synchronize()
+    wc, ws = oracle_inverse(inp)
+    sw = np.ldexp(1.0, w_sf.numpy().astype(np.int64) - 127).astype(np.float32)
+    want = oracle.grouped_fp8_gemm(wc, ws, w.numpy(), sw)
+    bound = _gemm_bound(torch.from_numpy(wc), ws, w, sw, want)
+    err = np.abs(y.double().cpu().numpy() - want)
+    assert np.all(err <= bound), f"{np.count_nonzero(err > bound)} outputs beyond the bound"
+
+
+def test_gemm_ue8m0_full_size_sampled_rows(rq):
+    """prefill16k's op output (16384 tokens, 4 groups, K = 4096) through the
+    block-scaled GEMM with 1024 outputs per group, in the bench's launch
+    configuration; 64 sampled rows against the float64 oracle."""
+    import oracle
+    inp = W.inverse_inputs(W.PREFILL16K)
+    dev = torch.device("cuda:0")
+    x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
+    codes, words = rq.inv_rope_quant(x, pos, cache, 8, mode="ue8m0")
+    gen = torch.Generator().manual_seed(11)
+    w = _rand_codes((4, 1024, 4096), gen)
+    w_sf = torch.randint(118, 124, (4, 8, 32), generator=gen, dtype=torch.int32).to(torch.uint8)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = rq.grouped_fp8_gemm_ue8m0(codes, words, w.to(dev), w_sf.to(dev), error_flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    rows = torch.randperm(16384, generator=gen)[:64].sort().values
+    rows[-1] = 16383
+    a = codes[rows].cpu()
+    sf = words[rows].cpu().numpy().view(np.uint32)
+    want = oracle.grouped_fp8_gemm_ue8m0(a.numpy(), sf, w.numpy(), w_sf.numpy())
+    shifts = np.array([0, 8, 16, 24], np.uint32)
+    sa = np.ldexp(1.0, ((sf[..., None] >> shifts) & 0xFF).reshape(64, 4, 32).astype(np.int64)
+                  - 127).astype(np.float32)
+    sw = np.ldexp(1.0, w_sf.numpy().astype(np.int64) - 127).astype(np.float32)
+    bound = _gemm_bound(a, sa, w, sw, want)
+    err = np.abs(y[rows].double().cpu().numpy() - want)
+    assert np.all(err <= bound), f"{np.count_nonzero(err > bound)} outputs beyond the bound"
