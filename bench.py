@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="steps of the host-buffer end-to-end leg (default min(steps, 20))")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-chunk", type=int, default=512,
+                    help="tokens per chunk of the host-buffer pipeline in the e2e leg")
     ap.add_argument("--mode-launches", type=int, default=300,
                     help="launches timed per extra output kind / layout (0 skips them)")
     ap.add_argument("--ref-budget-s", type=float, default=60.0,
@@ -530,16 +532,19 @@ def run_ours(args, world, rank, local):
     h2d = sum(t.numel() * t.element_size() for t in (x_host, pos_host, kv_host, kpos_host, slots_host))
     d2h = sum(t.numel() * t.element_size() for t in (out_host, scales_host, kc_host))
 
+    # the inverse op goes through the host-buffer C-ABI call (chunked copy-in /
+    # kernel / copy-out pipeline inside the library); the insert's inputs are
+    # copied in and the paged cache read back around its device call
+    ws = torch.empty(rq.host_workspace_bytes(h, args.e2e_chunk), dtype=torch.uint8, device=dev)
+
     def e2e_step():
-        x.copy_(x_host, non_blocking=True)
-        pos.copy_(pos_host, non_blocking=True)
         kv.copy_(kv_host, non_blocking=True)
         kpos.copy_(kpos_host, non_blocking=True)
         slots.copy_(slots_host, non_blocking=True)
-        step()
-        out_host.copy_(out, non_blocking=True)
-        scales_host.copy_(scales, non_blocking=True)
+        rq.rope_fp8_quant_insert(kv, kpos, cache, slots, k_cache, bs)
         kc_host.copy_(k_cache, non_blocking=True)
+        rq.inv_rope_fp8_quant_host(x_host, pos_host, cache, hpg, out=out_host, scales=scales_host,
+                                   workspace=ws, chunk_tokens=args.e2e_chunk)
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -604,7 +609,10 @@ def run_ours(args, world, rank, local):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "steps": e2e_steps,
-            "path": "pinned host -> device copies, both C-ABI calls, device -> pinned host",
+            "path": "inverse: rq_inv_rope_fp8_quant_host (pinned host buffers; chunked copy-in / "
+                    "kernels / copy-out pipeline over a device workspace, "
+                    f"{args.e2e_chunk} tokens per chunk); insert: pinned host -> device copies, "
+                    "the device call, paged cache -> pinned host",
         },
         "gpu_launches": 2 * args.steps,
         "output_modes": {"kernel": "inv_rope_quant_layout_kernel", "launches_each": args.mode_launches,

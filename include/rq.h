@@ -110,6 +110,50 @@ rq_status rq_inv_rope_fp8_quant(const void *x_bf16, int64_t n_tokens, int64_t n_
                                 uint8_t *out_fp8, float *out_scales,
                                 uint32_t *error_flags, void *stream);
 
+/*
+ * Device workspace, in bytes, that rq_inv_rope_fp8_quant_host needs for
+ * chunks of chunk_tokens tokens of n_heads heads (three chunk slots, each
+ * holding x, positions, codes and scales). -1 for n_heads < 1,
+ * chunk_tokens < 1 or chunk_tokens * n_heads >= 2^31.
+ */
+int64_t rq_inv_rope_fp8_quant_host_workspace(int64_t n_heads, int64_t chunk_tokens);
+
+/*
+ * rq_inv_rope_fp8_quant over HOST buffers (same op, same bytes). The tokens go
+ * through the device in chunks of chunk_tokens: each chunk is copied into a
+ * slot of the caller's device workspace, processed by the op's kernels on
+ * `stream` and copied back. Two copy streams owned by the library run the
+ * copies: while one chunk is processed, the next is copied in and the
+ * previous one out, so both directions of the host link are busy at once.
+ * The call is stream-ordered on `stream` like every other: the copies start
+ * after the work enqueued on `stream` before the call, and work enqueued
+ * after it starts once the last copy-out has finished. The host outputs are
+ * complete when `stream` has synchronised.
+ *  x_bf16_host      [N, H, 512] bf16, contiguous, host memory (page-locked
+ *                   for the copies to overlap; pageable memory works, slowly).
+ *  positions_host   [N] int64, host memory.
+ *  cos_sin_cache    [cache_rows, 64] fp32, DEVICE memory (as in
+ *                   rq_inv_rope_fp8_quant).
+ *  out_fp8_host     [N, G, hpg*512] uint8, host memory.
+ *  out_scales_host  [N, G, hpg*4] fp32, host memory.
+ *  workspace        device memory, 256-byte aligned, owned by the caller, at
+ *                   least rq_inv_rope_fp8_quant_host_workspace(H, chunk_tokens)
+ *                   bytes (else RQ_ERR_SHAPE); must not be reused until `stream`
+ *                   passes this call.
+ *  error_flags      device memory or NULL, as in rq_inv_rope_fp8_quant.
+ * Other arguments and errors as in rq_inv_rope_fp8_quant, except that the
+ * host outputs of a token whose position is out of range are unspecified
+ * (chunks are copied back whole; the flag is still set). On an RQ_ERR_CUDA
+ * return part of the pipeline may have been enqueued; the outputs are then
+ * unspecified. Calls from several host threads are serialised per device.
+ */
+rq_status rq_inv_rope_fp8_quant_host(const void *x_bf16_host, int64_t n_tokens, int64_t n_heads,
+                                     const int64_t *positions_host, const float *cos_sin_cache,
+                                     int64_t cache_rows, int64_t heads_per_group, float eps,
+                                     uint8_t *out_fp8_host, float *out_scales_host,
+                                     void *workspace, int64_t workspace_bytes,
+                                     int64_t chunk_tokens, uint32_t *error_flags, void *stream);
+
 /* Kernel variants of rq_inv_rope_fp8_quant; all produce identical bytes. */
 typedef enum rq_inv_variant {
     RQ_INV_AUTO = 0,          /* chosen from n_tokens * n_heads (the default): the

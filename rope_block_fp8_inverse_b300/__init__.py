@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["inv_rope_fp8_quant_gemm", "grouped_fp8_gemm", "grouped_fp8_gemm_ue8m0",
+__all__ = ["inv_rope_fp8_quant_host", "host_workspace_bytes", "inv_rope_fp8_quant_gemm", "grouped_fp8_gemm", "grouped_fp8_gemm_ue8m0",
            "indexer_q_rope_quant", "qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
            "empty_outputs", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
@@ -53,6 +53,9 @@ ABI_SYMBOLS = {
                                                    ctypes.c_int, _P, ctypes.c_float, ctypes.c_float,
                                                    ctypes.c_float, _P, _P, _P, _P]),
     "rq_grouped_fp8_gemm": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _P]),
+    "rq_inv_rope_fp8_quant_host_workspace": (ctypes.c_int64, [_I64, _I64]),
+    "rq_inv_rope_fp8_quant_host": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, ctypes.c_float,
+                                                  _P, _P, _P, _I64, _I64, _P, _P]),
     "rq_grouped_fp8_gemm_ue8m0": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P,
                                                  _P]),
     "rq_inv_rope_fp8_quant_gemm": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64,
@@ -453,6 +456,73 @@ def grouped_fp8_gemm(a_codes: torch.Tensor, a_scales: torch.Tensor, w_codes: tor
                                        out.data_ptr(), flags, _stream(a_codes.device))
     _check(st, "rq_grouped_fp8_gemm")
     return out
+
+
+def host_workspace_bytes(n_heads: int, chunk_tokens: int) -> int:
+    """Device workspace bytes ``inv_rope_fp8_quant_host`` needs (three chunk slots)."""
+    n = lib().rq_inv_rope_fp8_quant_host_workspace(n_heads, chunk_tokens)
+    if n < 0:
+        raise ValueError("n_heads and chunk_tokens must be >= 1 with chunk_tokens * n_heads < 2^31")
+    return int(n)
+
+
+def inv_rope_fp8_quant_host(x: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                            heads_per_group: int, eps: float = DEFAULT_EPS,
+                            out: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                            workspace: torch.Tensor | None = None, chunk_tokens: int = 512,
+                            error_flags: torch.Tensor | None = None):
+    """The inverse op over HOST tensors (``rq_inv_rope_fp8_quant_host``): x [N, H, 512]
+    bf16 and positions [N] int64 on the CPU (pinned for the copies to overlap),
+    the cos/sin cache on the GPU. The library streams chunks of ``chunk_tokens``
+    tokens through ``workspace`` (a CUDA uint8 tensor of at least
+    ``host_workspace_bytes(H, chunk_tokens)`` bytes; allocated when None), with
+    copy-in, kernels and copy-out of consecutive chunks overlapped. Returns the
+    CPU (pinned) ``(out, scales)``, complete once the current CUDA stream of
+    the cache's device has synchronised."""
+    if not isinstance(x, torch.Tensor) or x.is_cuda or x.dtype != torch.bfloat16:
+        raise TypeError("x must be a CPU bf16 tensor")
+    if x.dim() != 3 or x.shape[-1] != HEAD_DIM or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [N, H, 512] tensor")
+    n, h, _ = x.shape
+    if not isinstance(positions, torch.Tensor) or positions.is_cuda or \
+            positions.dtype != torch.int64 or tuple(positions.shape) != (n,) or \
+            not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous CPU int64 tensor [N]")
+    _cuda(cos_sin_cache, "cos_sin_cache", torch.float32)
+    dev = cos_sin_cache.device
+    if heads_per_group < 1 or h % heads_per_group:
+        raise ValueError("heads_per_group must divide the head count")
+    g = h // heads_per_group
+    if out is None:
+        out = torch.empty((n, g, heads_per_group * HEAD_DIM), dtype=torch.float8_e4m3fn,
+                          pin_memory=True)
+    if scales is None:
+        scales = torch.empty((n, g, heads_per_group * BLOCKS_PER_HEAD), dtype=torch.float32,
+                             pin_memory=True)
+    for t, name, dts, shape in ((out, "out", (torch.uint8, torch.float8_e4m3fn),
+                                 (n, g, heads_per_group * HEAD_DIM)),
+                                (scales, "scales", (torch.float32,),
+                                 (n, g, heads_per_group * BLOCKS_PER_HEAD))):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype not in dts or \
+                tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU {dts[0]} tensor of shape {shape}")
+    need = host_workspace_bytes(h, chunk_tokens)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _cuda(workspace, "workspace", torch.uint8)
+    if workspace.device != dev:
+        raise ValueError("workspace must be on the cache's device")
+    flags = 0
+    if error_flags is not None:
+        _cuda(error_flags, "error_flags", torch.int32)
+        flags = error_flags.data_ptr()
+    with torch.cuda.device(dev):
+        st = lib().rq_inv_rope_fp8_quant_host(
+            x.data_ptr(), n, h, positions.data_ptr(), cos_sin_cache.data_ptr(),
+            cos_sin_cache.shape[0], heads_per_group, eps, out.data_ptr(), scales.data_ptr(),
+            workspace.data_ptr(), workspace.numel(), chunk_tokens, flags, _stream(dev))
+    _check(st, "rq_inv_rope_fp8_quant_host")
+    return out, scales
 
 
 def grouped_fp8_gemm_ue8m0(a_codes: torch.Tensor, a_sf: torch.Tensor, w_codes: torch.Tensor,

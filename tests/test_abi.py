@@ -262,3 +262,36 @@ def test_gemm_ue8m0_rejects_bad_arguments(lib, kw, status):
 
 def test_gemm_ue8m0_empty_is_a_no_op(lib):
     assert _gemm_mx(lib, n=0, a=None, sa=None, w=None, sw=None, y=None) == RQ_OK
+
+
+def _host(lib, x=A16, n=4, h=8, pos=A16, cache=A16, rows=64, hpg=8, out=A16, sc=A16, ws=A16,
+          wsb=1 << 40, chunk=2):
+    return lib.rq_inv_rope_fp8_quant_host(x, n, h, pos, cache, rows, hpg, 1e-10, out, sc, ws, wsb,
+                                          chunk, None, None)
+
+
+def test_host_workspace_size_is_three_aligned_slots(lib):
+    a = lambda b: (b + 255) // 256 * 256
+    for h, ct in ((8, 1), (32, 1024), (24, 7)):
+        slot = a(ct * h * 1024) + a(ct * 8) + a(ct * h * 512) + a(ct * h * 16)
+        assert lib.rq_inv_rope_fp8_quant_host_workspace(h, ct) == 3 * slot
+    assert lib.rq_inv_rope_fp8_quant_host_workspace(0, 4) == -1
+    assert lib.rq_inv_rope_fp8_quant_host_workspace(8, 0) == -1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(chunk=0), RQ_ERR_SHAPE),
+    (dict(n=-1), RQ_ERR_SHAPE),
+    (dict(hpg=3), RQ_ERR_GROUPING),
+    (dict(wsb=1000), RQ_ERR_SHAPE),     # smaller than the three slots
+    (dict(x=None), RQ_ERR_NULL),
+    (dict(ws=None), RQ_ERR_NULL),
+    (dict(sc=None), RQ_ERR_NULL),
+    (dict(ws=A16 + 16), RQ_ERR_ALIGN),
+])
+def test_host_rejects_bad_arguments(lib, kw, status):
+    assert _host(lib, **kw) == status
+
+
+def test_host_empty_batch_is_a_no_op(lib):
+    assert _host(lib, n=0, x=None, pos=None, out=None, sc=None, ws=None) == RQ_OK

@@ -668,6 +668,10 @@ def test_every_entry_point_replays_in_a_cuda_graph(rq):
     kv, kpos, sl = ins["kv"].to(dev), ins["positions"].to(dev), ins["slot_mapping"].to(dev)
     fq, fkv, fsl = fus["q"].to(dev), fus["kv"].to(dev), fus["slot_mapping"].to(dev)
     iq, iw = idx["q"].to(dev), idx["weights"].to(dev)
+    gen = torch.Generator().manual_seed(8)
+    gw = _rand_codes((4, 256, 4096), gen).to(dev)
+    gsw = (2.0 ** torch.randint(-10, -6, (4, 2, 32), generator=gen).float()).to(dev)
+    gsf = (torch.log2(gsw).round().to(torch.int32) + 127).to(torch.uint8)
     bufs = {}
 
     def outputs():
@@ -679,6 +683,11 @@ def test_every_entry_point_replays_in_a_cuda_graph(rq):
         bufs["qo"] = torch.empty(300, 32, 512, dtype=torch.bfloat16, device=dev)
         bufs["ic"] = torch.empty(300, 8, 128, dtype=torch.uint8, device=dev)
         bufs["iw"] = torch.empty(300, 8, device=dev)
+        bufs["mx"] = (torch.empty(300, 4, 4096, dtype=torch.uint8, device=dev),
+                      torch.empty(300, 4, 8, dtype=torch.int32, device=dev))
+        bufs["y"] = torch.empty(300, 4, 256, dtype=torch.bfloat16, device=dev)
+        bufs["ymx"] = torch.empty(300, 4, 256, dtype=torch.bfloat16, device=dev)
+        bufs["yfused"] = torch.empty(300, 4, 256, dtype=torch.bfloat16, device=dev)
 
     def step():
         rq.inv_rope_fp8_quant(x, pos, cache, 8, out=bufs["codes"], scales=bufs["scales"])
@@ -688,6 +697,10 @@ def test_every_entry_point_replays_in_a_cuda_graph(rq):
                                            q_out=bufs["qo"])
         rq.indexer_q_rope_quant(iq, kpos, cache, iw, idx["softmax_scale"], idx["head_scale"],
                                 out=bufs["ic"], weights_out=bufs["iw"])
+        rq.grouped_fp8_gemm(bufs["codes"], bufs["scales"], gw, gsw, out=bufs["y"])
+        rq.inv_rope_quant(x, pos, cache, 8, mode="ue8m0", out=bufs["mx"][0], scales=bufs["mx"][1])
+        rq.grouped_fp8_gemm_ue8m0(bufs["mx"][0], bufs["mx"][1], gw, gsf, out=bufs["ymx"])
+        rq.inv_rope_fp8_quant_gemm(x, pos, cache, 8, gw, gsw, out=bufs["yfused"])
 
     def snapshot():
         return {k: (tuple(t.clone() for t in v) if isinstance(v, tuple) else v.clone())
@@ -897,3 +910,52 @@ def test_gemm_ue8m0_full_size_sampled_rows(rq):
     bound = _gemm_bound(a, sa, w, sw, want)
     err = np.abs(y[rows].double().cpu().numpy() - want)
     assert np.all(err <= bound), f"{np.count_nonzero(err > bound)} outputs beyond the bound"
+
+
+# ---------------------------------------------------------------- host-buffer pipeline
+
+@pytest.mark.parametrize("n,h,hpg,chunk", [(5, 8, 8, 1024), (1000, 32, 8, 256), (2049, 32, 8, 1024),
+                                           (5000, 24, 6, 512), (700, 16, 16, 1)])
+def test_host_pipeline_equals_device_call(rq, n, h, hpg, chunk):
+    """Chunks pass through three workspace slots (every slot reused, a ragged
+    last chunk); the host outputs equal the device call's bytes, which the
+    other tests pin to the oracle."""
+    inp = W.inverse_inputs(W.InverseSpec("host", n, h, hpg, 4096, "uniform", True, seed=n))
+    dev = torch.device("cuda:0")
+    cache = inp["cos_sin_cache"].to(dev)
+    x_h, pos_h = inp["x"].pin_memory(), inp["positions"].pin_memory()
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    out_h, sc_h = rq.inv_rope_fp8_quant_host(x_h, pos_h, cache, hpg, chunk_tokens=chunk,
+                                             error_flags=flags)
+    codes, scales = rq.inv_rope_fp8_quant(x_h.to(dev), pos_h.to(dev), cache, hpg)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    assert out_h.dtype == codes.dtype
+    assert torch.equal(out_h.view(torch.uint8), codes.cpu().view(torch.uint8))
+    assert torch.equal(sc_h, scales.cpu())
+
+
+def test_host_pipeline_is_stream_ordered_and_flags_bad_positions(rq):
+    """Work enqueued before the call is seen by its copies (the cache is
+    written on the stream just before), work after it sees its outputs, and a
+    bad position is flagged as in the device call (its host outputs are
+    unspecified: the chunk's device slot, stale there, is copied back whole)."""
+    inp = W.inverse_inputs(W.InverseSpec("host", 600, 8, 8, 4096, "uniform", True, seed=3))
+    dev = torch.device("cuda:0")
+    cache = torch.zeros_like(inp["cos_sin_cache"]).to(dev)
+    pos = inp["positions"].clone()
+    pos[123] = 4096
+    x_h, pos_h = inp["x"].pin_memory(), pos.pin_memory()
+    out_h = torch.empty((600, 1, 4096), dtype=torch.uint8).pin_memory()
+    sc_h = torch.empty((600, 1, 32)).pin_memory()
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    cache.copy_(inp["cos_sin_cache"], non_blocking=True)
+    rq.inv_rope_fp8_quant_host(x_h, pos_h, cache, 8, out=out_h, scales=sc_h, chunk_tokens=64,
+                               error_flags=flags)
+    after = flags.clone()
+    torch.cuda.current_stream().synchronize()
+    assert int(after.item()) == 1
+    keep = torch.tensor([i for i in range(600) if i != 123])
+    sub = dict(inp, x=inp["x"][keep], positions=inp["positions"][keep])
+    wc, ws = oracle_inverse(sub)
+    assert np.array_equal(out_h[keep].numpy(), wc) and np.array_equal(sc_h[keep].numpy(), ws)
