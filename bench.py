@@ -43,7 +43,7 @@ STEP_BYTES = INV_BYTES + INS_BYTES
 L2_BYTES = 126 * 2 ** 20
 FALLBACK_HBM_GBS = 6400.0
 # the kernel the default (auto) variant launches at the benchmarked shape
-INV_KERNEL_NAME = "inv_rope_fp8_quant_stream_kernel"
+INV_KERNEL_NAME = "inv_rope_fp8_quant_kernel"
 
 
 def parse():
@@ -645,17 +645,21 @@ def run_ours(args, world, rank, local):
 
 def _committed_traffic():
     """dram bytes per launch of the inverse kernel from the committed ncu summary
-    (profiles/inv_rope_fp8_quant_prefill16k.md), or None when absent."""
+    (profiles/inv_rope_fp8_quant_prefill16k.md), or None when absent or taken
+    on another kernel than the one the bench times."""
     path = os.path.join(ROOT, "profiles", "inv_rope_fp8_quant_prefill16k.md")
+    kernel, value = None, None
     try:
         with open(path) as f:
             for line in f:
+                if line.startswith("traffic_kernel:"):
+                    kernel = line.split(":", 1)[1].strip()
                 if line.startswith("traffic_bytes_per_launch:"):
                     v = line.split(":", 1)[1].strip()
-                    return None if v in ("", "null") else int(float(v))
+                    value = None if v in ("", "null") else int(float(v))
     except OSError:
-        pass
-    return None
+        return None
+    return value if kernel == INV_KERNEL_NAME else None
 
 
 # ------------------------------------------------------------------ reference arm

@@ -156,9 +156,8 @@ rq_status rq_inv_rope_fp8_quant_host(const void *x_bf16_host, int64_t n_tokens, 
 
 /* Kernel variants of rq_inv_rope_fp8_quant; all produce identical bytes. */
 typedef enum rq_inv_variant {
-    RQ_INV_AUTO = 0,          /* chosen from n_tokens * n_heads (the default): the
-                                 stream kernel from 2048 rows per SM up (303,104 rows
-                                 on 148 SMs), else warp rows                          */
+    RQ_INV_AUTO = 0,          /* the default: warp rows (measured the faster of the
+                                 two at every size on B300)                          */
     RQ_INV_WARP_ROWS = 1,     /* persistent warps, rows loaded straight to registers */
     RQ_INV_STREAM = 2         /* every warp streams 8-head tiles through a private
                                  two-stage ring of shared memory filled by 1-D bulk

@@ -58,8 +58,13 @@ __device__ __forceinline__ uint2 quant8(const float (&v)[8], float inv) {
 
 // A warp takes kIdxGroups x 4 consecutive heads per iteration and issues all
 // their loads and position reads before computing any; cos/sin rows are read
-// in the compute phase (after the first head of a token they hit L1).
-constexpr int kIdxGroups = 4;
+// in the compute phase (after the first head of a token they hit L1). Memory
+// parallelism comes from occupancy rather than depth: one group per warp
+// keeps the kernel at 32 registers, so 8 CTAs (64 warps) fit on an SM, which
+// measured faster than 2 or 4 groups at lower occupancy (every such variant
+// wrote the same bytes).
+constexpr int kIdxGroups = 1;
+constexpr int kIdxMinBlocks = 8;
 
 __device__ __forceinline__ uint2 ld_stream8(const void* p) {
     uint2 v;
@@ -74,7 +79,7 @@ __device__ __forceinline__ void st_stream4(void* p, uint32_t v) {
 }
 
 template <bool kNeox>
-__global__ void __launch_bounds__(kInvThreads)
+__global__ void __launch_bounds__(kInvThreads, kIdxMinBlocks)
 indexer_q_rope_quant_kernel(IdxParams p) {
     pdl_wait();
     pdl_launch_dependents();
