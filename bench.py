@@ -324,24 +324,29 @@ def run_ours(args, world, rank, local):
     ins_ms = statistics.fmean(inv_ev[i][1].elapsed_time(ins_ev[i]) for i in range(args.steps))
     ms_step = total_ms / args.steps
 
-    # the "next" rows of the path (other output kinds and layouts), each timed
-    # like the inverse launch above, outside the step's timed region
+    def span_us(fn, launches):
+        """Mean µs per launch of `launches` back-to-back calls, one event pair
+        around all of them on the launching stream (after 3 warm calls)."""
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(launches):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) * 1e3 / launches
+
+    # the "next" rows of the path (other output kinds and layouts), outside the
+    # step's timed region, each as back-to-back launches
     modes = {}
     for name, mode, gm in ((("fp8_group_major", "fp8", True), ("ue8m0", "ue8m0", False),
                             ("ue8m0_group_major", "ue8m0", True), ("bf16", "bf16", False))
                            if args.mode_launches > 0 else ()):
         mo, ms = rq.empty_outputs(n, h // hpg, hpg, mode, group_major=gm, device=dev)
-        for _ in range(3):
-            rq.inv_rope_quant(x, pos, cache, hpg, mode=mode, out=mo, scales=ms)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.mode_launches)]
-        torch.cuda.synchronize(dev)
-        for a, b in evs:
-            a.record(stream)
-            rq.inv_rope_quant(x, pos, cache, hpg, mode=mode, out=mo, scales=ms)
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+        us = span_us(lambda: rq.inv_rope_quant(x, pos, cache, hpg, mode=mode, out=mo, scales=ms),
+                     args.mode_launches)
         mb = W.inverse_bytes(n, h, mode)
         modes[name] = {"us": round(us, 2), "bytes": mb, "GBs": round(mb / us / 1e3, 1),
                        "frac_of_measured_peak": round(mb / us / 1e3 / measured_peaks()[0], 4)}
@@ -358,17 +363,7 @@ def run_ours(args, world, rank, local):
         def fused_call():
             rq.qnorm_rope_kv_rope_quant_insert(fq, fkv, fpos, cache, fsl, fkc, fi["block_size"],
                                                fi["q_head_padded"], q_out=fqo)
-        for _ in range(3):
-            fused_call()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.mode_launches)]
-        torch.cuda.synchronize(dev)
-        for a, b in evs:
-            a.record(stream)
-            fused_call()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+        us = span_us(fused_call, args.mode_launches)
         fb = W.fused_bytes(W.FUSED16K.n_tokens, W.FUSED16K.n_heads_q, W.FUSED16K.q_head_padded)
         fused = {"kernel": "qnorm_rope_kv_insert_kernel", "workload": "fused16k (N=16384, Hq=32 "
                  "padded to 64, kv into 512x64 slots)", "us": round(us, 2), "bytes": fb,
@@ -389,17 +384,7 @@ def run_ours(args, world, rank, local):
             def idx_call():
                 rq.indexer_q_rope_quant(iq, ipos, cache, iw, ii["softmax_scale"], ii["head_scale"],
                                         rope_style=style, out=ico, weights_out=iwo)
-            for _ in range(3):
-                idx_call()
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(args.mode_launches)]
-            torch.cuda.synchronize(dev)
-            for a, b in evs:
-                a.record(stream)
-                idx_call()
-                b.record(stream)
-            torch.cuda.synchronize(dev)
-            us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+            us = span_us(idx_call, args.mode_launches)
             ib = W.indexer_bytes(W.INDEXER16K.n_tokens, W.INDEXER16K.n_heads)
             indexer[style] = {"us": round(us, 2), "bytes": ib, "GBs": round(ib / us / 1e3, 1),
                               "frac_of_measured_peak": round(ib / us / 1e3 / measured_peaks()[0], 4)}
@@ -425,30 +410,12 @@ def run_ours(args, world, rank, local):
 
         def gemm_call():
             rq.grouped_fp8_gemm(out, scales, wc, ws, out=gy)
-        for _ in range(3):
-            gemm_call()
         gl = max(10, args.mode_launches // 6)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(gl)]
-        torch.cuda.synchronize(dev)
-        for a, b in evs:
-            a.record(stream)
-            gemm_call()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+        us = span_us(gemm_call, gl)
 
         def fused_gemm_call():
             rq.inv_rope_fp8_quant_gemm(x, pos, cache, hpg, wc, ws, out=gy)
-        for _ in range(3):
-            fused_gemm_call()
-        torch.cuda.synchronize(dev)
-        for a, b in evs:
-            a.record(stream)
-            fused_gemm_call()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        us_fused = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+        us_fused = span_us(fused_gemm_call, gl)
 
         # the same GEMM on the block-scaled MMA, fed by the op's UE8M0 mode
         # (token-major packed words) and the weight scales as UE8M0 codes
@@ -459,15 +426,7 @@ def run_ours(args, world, rank, local):
 
         def mx_call():
             rq.grouped_fp8_gemm_ue8m0(mx_codes, mx_words, wc, w_sf, out=gy)
-        for _ in range(3):
-            mx_call()
-        torch.cuda.synchronize(dev)
-        for a, b in evs:
-            a.record(stream)
-            mx_call()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        us_mx = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+        us_mx = span_us(mx_call, gl)
         del mx_codes, mx_words
         flop = 2.0 * n * h * 512 * g_out
         tf = flop / us / 1e6
@@ -627,7 +586,10 @@ def run_ours(args, world, rank, local):
                     "the device call, paged cache -> pinned host",
         },
         "gpu_launches": 2 * args.steps,
-        "output_modes": {"kernel": "inv_rope_quant_layout_kernel", "launches_each": args.mode_launches,
+        "secondary_timing": "output_modes, fused_qkv, indexer_q and consumer_gemm: one event pair "
+                            "around N back-to-back launches, mean per launch",
+        "output_modes": {"kernel": "inv_rope_fp8_quant_stream_kernel (rq_inv_rope_quant_layout, "
+                                   "heads_per_group 8)", "launches_each": args.mode_launches,
                          "results": modes},
         "fused_qkv": fused,
         "indexer_q": indexer,

@@ -46,6 +46,50 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Position of row r = t * n_heads + h of the [N, H] row space, with head h =
+// g * hpg + i (group g, head i within it), advanced by a fixed row stride with
+// no division: the persistent warp-rows kernels step every warp by the same
+// stride, so only the set-up divides.
+struct RowPos {
+    uint32_t t, h, g, i;
+};
+
+struct RowStride {
+    uint32_t dt, dh, dg, di;
+};
+
+__device__ __forceinline__ RowPos row_pos(uint32_t r, uint32_t n_heads, uint32_t hpg) {
+    RowPos w;
+    w.t = r / n_heads;
+    w.h = r - w.t * n_heads;
+    w.g = w.h / hpg;
+    w.i = w.h - w.g * hpg;
+    return w;
+}
+
+__device__ __forceinline__ RowStride row_stride(uint32_t d, uint32_t n_heads, uint32_t hpg) {
+    const RowPos q = row_pos(d, n_heads, hpg);
+    return RowStride{q.t, q.h, q.g, q.i};
+}
+
+// w += s rows (n_heads = groups * hpg).
+__device__ __forceinline__ void row_advance(RowPos& w, const RowStride& s, uint32_t n_heads,
+                                            uint32_t hpg, uint32_t groups) {
+    w.t += s.dt;
+    w.h += s.dh;
+    w.g += s.dg;
+    w.i += s.di;
+    if (w.i >= hpg) {
+        w.i -= hpg;
+        ++w.g;
+    }
+    if (w.h >= n_heads) {
+        w.h -= n_heads;
+        ++w.t;
+        w.g -= groups;
+    }
+}
+
 // Index (in 8-element chunks) of lane l's A chunk; its B chunk is A + 8.
 __device__ __forceinline__ int chunk_a(int lane) { return 16 * (lane >> 3) + (lane & 7); }
 

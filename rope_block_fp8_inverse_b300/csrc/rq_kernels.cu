@@ -20,8 +20,10 @@ namespace rq {
 // [N, G, hpg*4] outputs this is exactly the grouped layout of the inverse
 // RoPE page, S1 (head h = g*hpg + i of token t at row (t, g), offset i*512),
 // so the grouping never changes an address.
+// Held to 4 CTAs per SM (64 registers), measured 1% faster than the
+// compiler's free choice of 73 registers (3 CTAs).
 template <int kRows>
-__global__ void __launch_bounds__(kInvThreads)
+__global__ void __launch_bounds__(kInvThreads, 4)
 inv_rope_fp8_quant_kernel(InvParams p) {
     pdl_wait();
     pdl_launch_dependents();
@@ -32,18 +34,25 @@ inv_rope_fp8_quant_kernel(InvParams p) {
     const int ca = chunk_a(lane);
     const bool rope_lane = lane >= kRopeLane0;
     const int cs_col = (rope_lane ? lane - kRopeLane0 : 0) * 4;
+    // rows walked without division (one group of all heads: g = 0, i = h)
+    const RowStride step = row_stride(n_warps * kRows, p.n_heads, p.n_heads);
+    const RowStride next = row_stride(1, p.n_heads, p.n_heads);
+    RowPos base = row_pos(warp * kRows, p.n_heads, p.n_heads);
 
-    for (uint32_t r0 = warp * kRows; r0 < p.n_rows; r0 += n_warps * kRows) {
+    for (uint32_t r0 = warp * kRows; r0 < p.n_rows;
+         r0 += n_warps * kRows, row_advance(base, step, p.n_heads, p.n_heads, 1)) {
         uint4 a[kRows], b[kRows];
         float4 c[kRows], s[kRows];
         bool live[kRows];
+        RowPos w = base;
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             const uint32_t r = r0 + i;
+            if (i > 0) row_advance(w, next, p.n_heads, p.n_heads, 1);
             live[i] = false;
             if (r < p.n_rows) {  // warp-uniform
-                const uint32_t t = r / p.n_heads;
-                const uint32_t h = r - t * p.n_heads;
+                const uint32_t t = w.t;
+                const uint32_t h = w.h;
                 // the row's reads do not wait for its position: only cos/sin do
                 const uint16_t* row = x + static_cast<int64_t>(t) * p.sx_t +
                                       static_cast<int64_t>(h) * p.sx_h;
@@ -78,9 +87,12 @@ inv_rope_fp8_quant_kernel(InvParams p) {
 // The warp-rows kernel with the output addressed through OutLayout: fp32 or
 // packed UE8M0 scales, or (kMode == kOutBf16) the rotated head as bf16 with
 // no quantisation, into token-major, group-major or any other strided
-// layout. Loads and arithmetic are those of inv_rope_fp8_quant_kernel.
+// layout. Loads and arithmetic are those of inv_rope_fp8_quant_kernel. Rows
+// are walked without division (RowPos), and the kernel is held to 4 CTAs per
+// SM (64 registers): on B300 that took the fp8 layouts from 0.86 to 0.92 of
+// the copy peak.
 template <int kRows, int kMode>
-__global__ void __launch_bounds__(kInvThreads)
+__global__ void __launch_bounds__(kInvThreads, 4)
 inv_rope_quant_layout_kernel(InvParams p) {
     pdl_wait();
     pdl_launch_dependents();
@@ -92,23 +104,30 @@ inv_rope_quant_layout_kernel(InvParams p) {
     const bool rope_lane = lane >= kRopeLane0;
     const int cs_col = (rope_lane ? lane - kRopeLane0 : 0) * 4;
     constexpr int64_t kHeadBytes = kMode == kOutBf16 ? 2 * kHeadDim : kHeadDim;
+    const uint32_t hpg = p.lay.hpg, groups = p.n_heads / hpg;
+    const RowStride step = row_stride(n_warps * kRows, p.n_heads, hpg);
+    const RowStride next = row_stride(1, p.n_heads, hpg);
+    RowPos base = row_pos(warp * kRows, p.n_heads, hpg);
 
-    for (uint32_t r0 = warp * kRows; r0 < p.n_rows; r0 += n_warps * kRows) {
+    for (uint32_t r0 = warp * kRows; r0 < p.n_rows;
+         r0 += n_warps * kRows, row_advance(base, step, p.n_heads, hpg, groups)) {
         uint4 a[kRows], b[kRows];
         float4 c[kRows], s[kRows];
-        uint32_t tt[kRows], hh[kRows];
+        RowPos w[kRows];
         bool live[kRows];
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             const uint32_t r = r0 + i;
+            w[i] = base;
+            if (i > 0) {
+                w[i] = w[i - 1];
+                row_advance(w[i], next, p.n_heads, hpg, groups);
+            }
             live[i] = false;
             if (r < p.n_rows) {  // warp-uniform
-                const uint32_t t = r / p.n_heads;
-                const uint32_t h = r - t * p.n_heads;
-                tt[i] = t;
-                hh[i] = h;
+                const uint32_t t = w[i].t;
                 const uint16_t* row = x + static_cast<int64_t>(t) * p.sx_t +
-                                      static_cast<int64_t>(h) * p.sx_h;
+                                      static_cast<int64_t>(w[i].h) * p.sx_h;
                 a[i] = ld_stream16(row + 8 * ca);
                 b[i] = ld_stream16(row + 8 * (ca + 8));
                 const int64_t pos = __ldg(p.positions + t);
@@ -127,9 +146,8 @@ inv_rope_quant_layout_kernel(InvParams p) {
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             if (!live[i]) continue;
-            const uint32_t g = hh[i] / p.lay.hpg;
-            const uint32_t hig = hh[i] - g * p.lay.hpg;
-            uint8_t* head = p.out + int64_t(tt[i]) * p.lay.ot + int64_t(g) * p.lay.og +
+            const uint32_t g = w[i].g, hig = w[i].i;
+            uint8_t* head = p.out + int64_t(w[i].t) * p.lay.ot + int64_t(g) * p.lay.og +
                             int64_t(hig) * kHeadBytes;
             if (kMode == kOutBf16) {
                 uint4 qa, qb;
@@ -142,7 +160,7 @@ inv_rope_quant_layout_kernel(InvParams p) {
             const uint4 q = rope_quant_row<true>(a[i], b[i], rope_lane, c[i], s[i], p.eps, &scale);
             st_stream8(head + 8 * ca, q.x, q.y);
             st_stream8(head + 8 * (ca + 8), q.z, q.w);
-            const int64_t sbase = int64_t(tt[i]) * p.lay.st + int64_t(g) * p.lay.sg;
+            const int64_t sbase = int64_t(w[i].t) * p.lay.st + int64_t(g) * p.lay.sg;
             if (kMode == kOutFp8F32) {
                 if ((lane & 7) == 0)
                     st_stream4f(p.scales + sbase + (int64_t(hig) * 4 + (lane >> 3)) * p.lay.se,
