@@ -265,20 +265,27 @@ qnorm_rope_kv_insert_kernel(FusedParams p) {
     const int cs_col = (rope_lane ? lane - kRopeLane0 : 0) * 4;
     const uint32_t per_token = p.q_head_padded + 1;
     const int64_t n_slots = p.num_blocks * p.block_size;
+    // units walked without division (unit u = t * per_token + k)
+    const RowStride step = row_stride(n_warps * kRows, per_token, per_token);
+    const RowStride next = row_stride(1, per_token, per_token);
+    RowPos base = row_pos(warp * kRows, per_token, per_token);
 
-    for (uint32_t u0 = warp * kRows; u0 < p.n_units; u0 += n_warps * kRows) {
+    for (uint32_t u0 = warp * kRows; u0 < p.n_units;
+         u0 += n_warps * kRows, row_advance(base, step, per_token, per_token, 1)) {
         uint4 a[kRows], b[kRows];
         float4 c[kRows], s[kRows];
         uint32_t tt[kRows], kk[kRows];
         int64_t slot[kRows];
         bool live[kRows];
+        RowPos w = base;
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             const uint32_t u = u0 + i;
+            if (i > 0) row_advance(w, next, per_token, per_token, 1);
             live[i] = false;
             if (u >= p.n_units) continue;  // warp-uniform
-            const uint32_t t = u / per_token;
-            const uint32_t k = u - t * per_token;
+            const uint32_t t = w.t;
+            const uint32_t k = w.h;
             tt[i] = t;
             kk[i] = k;
             const bool is_kv = k == p.q_head_padded;
@@ -344,7 +351,7 @@ namespace {
 // variant (thread-local: no locking on the launch path).
 constexpr int kMaxDevices = 64;
 // (kLay: 2 entries per output mode, one row or two rows per warp)
-enum Variant { kInv1, kInv2, kIns2, kFus1, kFus2, kLay, kVariants = kLay + 6 };
+enum Variant { kInv1, kInv2, kIns1, kFus1, kLay, kVariants = kLay + 6 };
 
 template <typename K>
 int resident_blocks(int device, Variant v, K kernel, int threads) {
@@ -419,21 +426,20 @@ cudaError_t launch_inv_rope_quant_layout(const InvParams& p, const DeviceInfo& d
 cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& dev,
                                          cudaStream_t stream) {
     constexpr int kWarps = kInsThreads / 32;
-    auto k = rope_fp8_quant_insert_kernel<2>;
-    const int res = resident_blocks(dev.ordinal, kIns2, k, kInsThreads);
-    return launch_pdl(k, grid_size(p.n_tokens, kWarps * 2, dev.sm_count, res), kInsThreads, 0,
+    // one token per warp and iteration (44 registers, more CTAs per SM): the
+    // 30 MB op is latency-bound, and on B300 this ran it in 4.9 us against
+    // 5.7 us with two tokens per warp (CUDA-graph replays)
+    auto k = rope_fp8_quant_insert_kernel<1>;
+    const int res = resident_blocks(dev.ordinal, kIns1, k, kInsThreads);
+    return launch_pdl(k, grid_size(p.n_tokens, kWarps * 1, dev.sm_count, res), kInsThreads, 0,
                       stream, p);
 }
 
 cudaError_t launch_qnorm_rope_kv_insert(const FusedParams& p, const DeviceInfo& dev,
                                         cudaStream_t stream) {
     constexpr int kWarps = kInvThreads / 32;
-    if (int64_t(p.n_units) >= int64_t(dev.sm_count) * kWarps * 4) {
-        auto k = qnorm_rope_kv_insert_kernel<2>;
-        const int res = resident_blocks(dev.ordinal, kFus2, k, kInvThreads);
-        return launch_pdl(k, grid_size(p.n_units, kWarps * 2, dev.sm_count, res), kInvThreads, 0,
-                          stream, p);
-    }
+    // one unit per warp and iteration at every size: 63 registers, 4 CTAs per
+    // SM; two units per warp need 80 registers (3 CTAs) and measured 7% slower
     auto k = qnorm_rope_kv_insert_kernel<1>;
     const int res = resident_blocks(dev.ordinal, kFus1, k, kInvThreads);
     return launch_pdl(k, grid_size(p.n_units, kWarps * 1, dev.sm_count, res), kInvThreads, 0,
