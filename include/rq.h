@@ -154,6 +154,25 @@ rq_status rq_inv_rope_fp8_quant_host(const void *x_bf16_host, int64_t n_tokens, 
                                      void *workspace, int64_t workspace_bytes,
                                      int64_t chunk_tokens, uint32_t *error_flags, void *stream);
 
+/*
+ * TEST ONLY: fault injection for the bounded waits of the TMA / tensor-core
+ * kernels, for calls made afterwards from the calling host thread. Each
+ * selected kernel skips one of its own copies, so a wait on a barrier that
+ * nothing will complete runs out after spin_limit polls (0 = the default,
+ * 2^22); the kernel then sets RQ_FLAG_TIMEOUT in error_flags, lets its
+ * copies in flight land, frees what it holds and exits, leaving the context
+ * usable. Outputs of an injected call are unspecified. mask 0 and
+ * spin_limit 0 restore normal operation.
+ *   RQ_DEBUG_STREAM_STAGE  the TMA-ring inverse kernel (RQ_INV_STREAM and the
+ *                          layout call's large heads_per_group % 8 == 0 case):
+ *                          warp 0 leaves its first tile unarmed
+ *   RQ_DEBUG_GEMM_LOADS    rq_grouped_fp8_gemm and rq_grouped_fp8_gemm_ue8m0:
+ *                          the first CTA's TMA producer issues no copy
+ */
+#define RQ_DEBUG_STREAM_STAGE 1u
+#define RQ_DEBUG_GEMM_LOADS 2u
+void rq_debug_inject(uint32_t mask, uint32_t spin_limit);
+
 /* Kernel variants of rq_inv_rope_fp8_quant; all produce identical bytes. */
 typedef enum rq_inv_variant {
     RQ_INV_AUTO = 0,          /* the default: warp rows (measured the faster of the

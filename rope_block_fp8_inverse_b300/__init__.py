@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["inv_rope_fp8_quant_host", "host_workspace_bytes", "inv_rope_fp8_quant_gemm", "grouped_fp8_gemm", "grouped_fp8_gemm_ue8m0",
+__all__ = ["debug_inject", "DEBUG_STREAM_STAGE", "DEBUG_GEMM_LOADS", "inv_rope_fp8_quant_host", "host_workspace_bytes", "inv_rope_fp8_quant_gemm", "grouped_fp8_gemm", "grouped_fp8_gemm_ue8m0",
            "indexer_q_rope_quant", "qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
            "empty_outputs", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
@@ -30,6 +30,8 @@ RECORD_BYTES = 528
 # output kinds of inv_rope_quant (rq_out_mode): fp32 scales, packed UE8M0 scales, bf16 (no quant)
 OUT_MODES = {"fp8": 0, "ue8m0": 1, "bf16": 2}
 DEFAULT_EPS = 1e-10
+# test-only fault injection (rq_debug_inject)
+DEBUG_STREAM_STAGE, DEBUG_GEMM_LOADS = 1, 2
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librq.so")
 
@@ -53,6 +55,7 @@ ABI_SYMBOLS = {
                                                    ctypes.c_int, _P, ctypes.c_float, ctypes.c_float,
                                                    ctypes.c_float, _P, _P, _P, _P]),
     "rq_grouped_fp8_gemm": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _P]),
+    "rq_debug_inject": (None, [ctypes.c_uint32, ctypes.c_uint32]),
     "rq_inv_rope_fp8_quant_host_workspace": (ctypes.c_int64, [_I64, _I64]),
     "rq_inv_rope_fp8_quant_host": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, ctypes.c_float,
                                                   _P, _P, _P, _I64, _I64, _P, _P]),
@@ -456,6 +459,14 @@ def grouped_fp8_gemm(a_codes: torch.Tensor, a_scales: torch.Tensor, w_codes: tor
                                        out.data_ptr(), flags, _stream(a_codes.device))
     _check(st, "rq_grouped_fp8_gemm")
     return out
+
+
+def debug_inject(mask: int = 0, spin_limit: int = 0) -> None:
+    """TEST ONLY (``rq_debug_inject``): make the selected kernels skip one of
+    their own copies so that a bounded wait runs out after ``spin_limit`` polls
+    and ``RQ_FLAG_TIMEOUT`` is reported; ``debug_inject()`` restores normal
+    operation. Applies to later calls from this thread."""
+    lib().rq_debug_inject(mask, spin_limit)
 
 
 def host_workspace_bytes(n_heads: int, chunk_tokens: int) -> int:

@@ -18,6 +18,9 @@ constexpr int kVersionMajor = 1;
 constexpr int kVersionMinor = 0;
 constexpr int64_t kMaxRows = int64_t(1) << 31;
 
+// rq_debug_inject's settings for calls from this host thread.
+thread_local rq::WaitCtl g_wait;
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool eps_ok(float eps) {
@@ -68,6 +71,11 @@ RQ_EXPORT const char* rq_status_string(int status) {
 
 RQ_EXPORT int rq_version(void) { return (kVersionMajor << 16) | kVersionMinor; }
 
+RQ_EXPORT void rq_debug_inject(uint32_t mask, uint32_t spin_limit) {
+    g_wait.inject = mask;
+    g_wait.spin_limit = spin_limit ? spin_limit : rq::kSpinLimit;
+}
+
 RQ_EXPORT rq_status rq_inv_rope_fp8_quant_ex(const void* x_bf16, int64_t n_tokens,
                                              int64_t n_heads, int64_t x_stride_token,
                                              int64_t x_stride_head, const int64_t* positions,
@@ -92,6 +100,7 @@ RQ_EXPORT rq_status rq_inv_rope_fp8_quant_ex(const void* x_bf16, int64_t n_token
     if (e != cudaSuccess) return from_cuda(e);
 
     rq::InvParams p;
+    p.wait = g_wait;
     p.x = x_bf16;
     p.sx_t = x_stride_token;
     p.sx_h = x_stride_head;
@@ -156,6 +165,7 @@ RQ_EXPORT rq_status rq_inv_rope_quant_layout(
     if (e != cudaSuccess) return from_cuda(e);
 
     rq::InvParams p;
+    p.wait = g_wait;
     p.x = x_bf16;
     p.sx_t = x_stride_token;
     p.sx_h = x_stride_head;
@@ -349,6 +359,7 @@ RQ_EXPORT rq_status rq_grouped_fp8_gemm(const uint8_t* a_codes, const float* a_s
     cudaError_t e = current_device(&dev);
     if (e != cudaSuccess) return from_cuda(e);
     rq::GemmParams p;
+    p.wait = g_wait;
     p.m = static_cast<int>(n_tokens);
     p.groups = static_cast<int>(groups);
     p.k = static_cast<int>(k_per_group);
@@ -382,6 +393,7 @@ RQ_EXPORT rq_status rq_grouped_fp8_gemm_ue8m0(const uint8_t* a_codes, const uint
     cudaError_t e = current_device(&dev);
     if (e != cudaSuccess) return from_cuda(e);
     rq::MxGemmParams p;
+    p.wait = g_wait;
     p.m = static_cast<int>(n_tokens);
     p.groups = static_cast<int>(groups);
     p.k = static_cast<int>(k_per_group);
@@ -420,6 +432,7 @@ RQ_EXPORT rq_status rq_inv_rope_fp8_quant_gemm(
     cudaError_t e = current_device(&dev);
     if (e != cudaSuccess) return from_cuda(e);
     rq::FusedGemmParams p;
+    p.wait = g_wait;
     p.x = x_bf16;
     p.sx_t = x_stride_token;
     p.sx_h = x_stride_head;

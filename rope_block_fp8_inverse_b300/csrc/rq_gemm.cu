@@ -91,12 +91,16 @@ grouped_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
     const uint32_t tmem = *tmem_slot_ptr;
 
     bool ok = true;
+    const uint32_t lim = p.wait.spin_limit;
+    // test-only fault injection: CTA 0's producer issues nothing
+    const bool starve = (p.wait.inject & kInjectGemmLoads) && blockIdx.x == 0 && blockIdx.y == 0 &&
+                        blockIdx.z == 0;
     if (warp == 0) {
-        if (lane == 0) {
+        if (lane == 0 && !starve) {
             for (int kt = 0; kt < n_kt; ++kt) {
                 const int s = kt % kGemmStages;
                 const uint32_t ph = (kt / kGemmStages) & 1;
-                if (!mbar_wait(empty0 + 8 * s, ph ^ 1u)) {
+                if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, lim)) {
                     ok = false;
                     break;
                 }
@@ -114,7 +118,7 @@ grouped_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                 const uint32_t ph = (kt / kGemmStages) & 1;
                 const int buf = kt & 1;
                 const uint32_t bph = (kt >> 1) & 1;
-                if (!mbar_wait(full0 + 8 * s, ph) || !mbar_wait(tempty0 + 8 * buf, bph ^ 1u)) {
+                if (!mbar_wait(full0 + 8 * s, ph, lim) || !mbar_wait(tempty0 + 8 * buf, bph ^ 1u, lim)) {
                     ok = false;
                     break;
                 }
@@ -128,7 +132,7 @@ grouped_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                 umma::commit(tfull0 + 8 * buf); // and the accumulator is ready
             }
             umma::commit(done);
-            if (!mbar_wait(done, 0)) ok = false;  // nothing in flight before teardown
+            if (!mbar_wait(done, 0, lim)) ok = false;  // nothing in flight before teardown
         }
     } else {
         // epilogue (warps 2..9): thread = output row = TMEM lane 32 * (warp % 4) + lane,
@@ -154,7 +158,7 @@ grouped_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
             const uint32_t bph = (kt >> 1) & 1;
             const float sc = __fmul_rn(__ldg(sa + kt), __ldg(sw + kt));
             // the warp leaves together: the TMEM loads below are warp-collective
-            if (!__all_sync(kFull, mbar_wait(tfull0 + 8 * buf, bph))) {
+            if (!__all_sync(kFull, mbar_wait(tfull0 + 8 * buf, bph, lim))) {
                 ok = false;
                 break;
             }
@@ -267,11 +271,12 @@ fused_inv_rope_quant_gemm_kernel(const __grid_constant__ CUtensorMap tma_x,
     const uint32_t tmem = *tmem_slot_ptr;
 
     bool ok = true;
+    const uint32_t lim = p.wait.spin_limit;
     if (warp == 0) {
         if (lane == 0) {
             for (int kt = 0; kt < n_kt; ++kt) {
                 const int sx = kt & 1;
-                if (!mbar_wait(xempty0 + 8 * sx, ((kt >> 1) & 1) ^ 1u)) {
+                if (!mbar_wait(xempty0 + 8 * sx, ((kt >> 1) & 1) ^ 1u, lim)) {
                     ok = false;
                     break;
                 }
@@ -279,7 +284,7 @@ fused_inv_rope_quant_gemm_kernel(const __grid_constant__ CUtensorMap tma_x,
                 umma::tma_load_3d(x0 + sx * kXTileBytes, &tma_x, (kt & 3) * kBK, g * p.hpg + kt / 4,
                                   m0, xfull0 + 8 * sx);
                 const int s = kt % kGemmStages;
-                if (!mbar_wait(empty0 + 8 * s, ((kt / kGemmStages) & 1) ^ 1u)) {
+                if (!mbar_wait(empty0 + 8 * s, ((kt / kGemmStages) & 1) ^ 1u, lim)) {
                     ok = false;
                     break;
                 }
@@ -294,8 +299,8 @@ fused_inv_rope_quant_gemm_kernel(const __grid_constant__ CUtensorMap tma_x,
             for (int kt = 0; kt < n_kt; ++kt) {
                 const int s = kt % kGemmStages;
                 const int buf = kt & 1;
-                if (!mbar_wait(full0 + 8 * s, (kt / kGemmStages) & 1) ||
-                    !mbar_wait(tempty0 + 8 * buf, ((kt >> 1) & 1) ^ 1u)) {
+                if (!mbar_wait(full0 + 8 * s, (kt / kGemmStages) & 1, lim) ||
+                    !mbar_wait(tempty0 + 8 * buf, ((kt >> 1) & 1) ^ 1u, lim)) {
                     ok = false;
                     break;
                 }
@@ -309,7 +314,7 @@ fused_inv_rope_quant_gemm_kernel(const __grid_constant__ CUtensorMap tma_x,
                 umma::commit(tfull0 + 8 * buf);
             }
             umma::commit(done);
-            if (!mbar_wait(done, 0)) ok = false;
+            if (!mbar_wait(done, 0, lim)) ok = false;
         }
     } else if (warp < kFusProdWarp0) {
         // epilogue: row = TMEM lane, 64 of the tile's 128 columns
@@ -324,7 +329,7 @@ fused_inv_rope_quant_gemm_kernel(const __grid_constant__ CUtensorMap tma_x,
         for (int kt = 0; kt < n_kt; ++kt) {
             const int buf = kt & 1;
             const float swk = __ldg(sw + kt);
-            if (!__all_sync(kFull, mbar_wait(tfull0 + 8 * buf, (kt >> 1) & 1))) {
+            if (!__all_sync(kFull, mbar_wait(tfull0 + 8 * buf, (kt >> 1) & 1, lim))) {
                 ok = false;
                 break;
             }
@@ -367,8 +372,8 @@ fused_inv_rope_quant_gemm_kernel(const __grid_constant__ CUtensorMap tma_x,
         for (int kt = 0; kt < n_kt; ++kt) {
             const int s = kt % kGemmStages;
             const int sx = kt & 1;
-            if (!__all_sync(kFull, mbar_wait(xfull0 + 8 * sx, (kt >> 1) & 1) &&
-                                       mbar_wait(empty0 + 8 * s, ((kt / kGemmStages) & 1) ^ 1u))) {
+            if (!__all_sync(kFull, mbar_wait(xfull0 + 8 * sx, (kt >> 1) & 1, lim) &&
+                                       mbar_wait(empty0 + 8 * s, ((kt / kGemmStages) & 1) ^ 1u, lim))) {
                 ok = false;
                 break;
             }

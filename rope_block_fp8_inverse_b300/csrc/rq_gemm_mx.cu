@@ -81,11 +81,11 @@ constexpr uint32_t kUe8m0One4 = 0x7f7f7f7fu;                    // four codes of
 static_assert(kMxSmem <= 232448, "shared memory per CTA");
 static_assert(kTmemSfb + 2 * 8 * kMxMaxHeads <= kMxTmemCols, "TMEM columns");
 
-// Poll an mbarrier phase; give up after kSpinLimit polls (raising `abort`)
+// Poll an mbarrier phase; give up after `limit` polls (raising `abort`)
 // or as soon as another role has raised it.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile uint32_t* abort) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+                                              volatile uint32_t* abort, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 255u && *abort) return false;
     }
@@ -135,6 +135,7 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
     const int n_pairs = ((p.m + kMxBM * kMxCluster - 1) / (kMxBM * kMxCluster)) * p.groups * n_nt;
     const uint32_t rank = umma::cluster_ctarank();
     const int cluster = blockIdx.x / kMxCluster, n_clusters = gridDim.x / kMxCluster;
+    const uint32_t lim = p.wait.spin_limit;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMxStages; ++s) {
@@ -161,14 +162,16 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
+        // test-only fault injection: CTA 0's producer issues nothing
+        const bool starve = (p.wait.inject & kInjectGemmLoads) && blockIdx.x == 0;
+        if (lane == 0 && !starve) {
             uint32_t it = 0;  // K steps issued
             bool ok = true;
             for (int t = cluster; t < n_pairs && ok; t += n_clusters) {
                 const MxTile x = mx_tile(t, n_nt, p.groups, rank);
                 for (int kt = 0; kt < n_kt; ++kt) {
                     const uint32_t s = it % kMxStages, ph = (it / kMxStages) & 1u;
-                    if (!wait_or_abort(empty0 + 8 * s, ph ^ 1u, abort)) {
+                    if (!wait_or_abort(empty0 + 8 * s, ph ^ 1u, abort, lim)) {
                         ok = false;
                         break;
                     }
@@ -185,7 +188,7 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
             // Let the copies still in flight land before the CTA exits (on the
             // normal path every one of them was already consumed).
             for (uint32_t j = it > uint32_t(kMxStages) ? it - kMxStages : 0u; j < it; ++j)
-                if (!mbar_wait(full0 + 8 * (j % kMxStages), (j / kMxStages) & 1u)) *abort = 1u;
+                if (!mbar_wait(full0 + 8 * (j % kMxStages), (j / kMxStages) & 1u, lim)) *abort = 1u;
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -193,8 +196,8 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
             bool ok = true;
             for (int t = cluster; t < n_pairs && ok; t += n_clusters, ++i) {
                 const uint32_t b = i & 1u;
-                if (!wait_or_abort(sfull0 + 8 * b, (i >> 1) & 1u, abort) ||
-                    !wait_or_abort(tempty, (i & 1u) ^ 1u, abort))
+                if (!wait_or_abort(sfull0 + 8 * b, (i >> 1) & 1u, abort, lim) ||
+                    !wait_or_abort(tempty, (i & 1u) ^ 1u, abort, lim))
                     break;
                 umma::fence_after_sync();
                 const uint32_t sfa_t = tmem + kTmemSfa + 32 * b, sfb_t = tmem + kTmemSfb + 64 * b;
@@ -209,7 +212,7 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
                 umma::commit(sempty0 + 8 * b);  // the atoms are free once copied
                 for (int kt = 0; kt < n_kt; ++kt) {
                     const uint32_t s = it % kMxStages, ph = (it / kMxStages) & 1u;
-                    if (!wait_or_abort(full0 + 8 * s, ph, abort)) {
+                    if (!wait_or_abort(full0 + 8 * s, ph, abort, lim)) {
                         ok = false;
                         break;
                     }
@@ -228,14 +231,14 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
                 if (ok) umma::commit(tfull);
             }
             umma::commit(done);
-            if (!mbar_wait(done, 0)) *abort = 1u;  // nothing in flight before teardown
+            if (!mbar_wait(done, 0, lim)) *abort = 1u;  // nothing in flight before teardown
         }
     } else if (warp == 2) {
         uint32_t i = 0;
         for (int t = cluster; t < n_pairs; t += n_clusters, ++i) {
             const MxTile x = mx_tile(t, n_nt, p.groups, rank);
             const uint32_t b = i & 1u;
-            if (!__all_sync(kFull, wait_or_abort(sempty0 + 8 * b, ((i >> 1) & 1u) ^ 1u, abort)))
+            if (!__all_sync(kFull, wait_or_abort(sempty0 + 8 * b, ((i >> 1) & 1u) ^ 1u, abort, lim)))
                 break;
             const uint32_t sfa = sf0 + b * kSfBufBytes, sfb = sfa + kSfaBytes;
             // A: atom h, 16-byte row `lane` = the words of rows lane + 32c, c = 0..3
@@ -279,7 +282,7 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
         for (int t = cluster; t < n_pairs; t += n_clusters, ++i) {
             const MxTile x = mx_tile(t, n_nt, p.groups, rank);
             // the warp leaves together: the TMEM loads below are warp-collective
-            if (!__all_sync(kFull, wait_or_abort(tfull, i & 1u, abort))) break;
+            if (!__all_sync(kFull, wait_or_abort(tfull, i & 1u, abort, lim))) break;
             umma::fence_after_sync();
             uint32_t packed[64];
 #pragma unroll

@@ -31,6 +31,20 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Polls of an mbarrier before a wait gives up and the kernel reports
+// RQ_FLAG_TIMEOUT (never expected in normal operation).
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+// Test-only fault injection (rq_debug_inject): a kernel skips one of its own
+// copies so that a bounded wait runs out; the values are RQ_DEBUG_* of rq.h.
+constexpr uint32_t kInjectStreamStage = 1u;  // TMA-ring inverse: warp 0 leaves tile 0 unarmed
+constexpr uint32_t kInjectGemmLoads = 2u;    // grouped GEMMs: CTA 0's producer issues nothing
+
+struct WaitCtl {
+    uint32_t spin_limit = kSpinLimit;  // polls per wait
+    uint32_t inject = 0;               // kInject* bits
+};
+
 constexpr int kInvThreads = 256;  // 8 warps per CTA
 constexpr int kInsThreads = 256;
 constexpr int64_t kRecordBytesABI = 528;  // paged record: 512 codes + 4 fp32 scales
@@ -69,6 +83,7 @@ struct InvParams {
     float* scales;            // [N*H, 4]
     uint32_t* error_flags;    // may be null
     OutLayout lay;            // used by the layout kernel only
+    WaitCtl wait;             // used by the stream kernel only
 };
 
 struct InsParams {
@@ -128,6 +143,7 @@ struct GemmParams {
     const float* w_scales;    // [groups, n_out / 128, k / 128]
     uint16_t* y;              // bf16 [m, groups, n_out]
     uint32_t* error_flags;
+    WaitCtl wait;
 };
 
 // Arguments of the grouped FP8 GEMM with UE8M0 block scales.
@@ -137,6 +153,7 @@ struct MxGemmParams {
     const uint8_t* w_sf;      // [groups, n_out / 128, k / 128] UE8M0 codes
     uint16_t* y;              // bf16 [m, groups, n_out]
     uint32_t* error_flags;
+    WaitCtl wait;
 };
 
 // Arguments of the fused inverse-RoPE + quant + grouped GEMM.
@@ -151,6 +168,7 @@ struct FusedGemmParams {
     const float* w_scales;    // [groups, n_out / 128, k / 128]
     uint16_t* y;              // bf16 [m, groups, n_out]
     uint32_t* error_flags;
+    WaitCtl wait;             // spin limit only
 };
 
 // Kernel variants of the inverse op (all bit-identical in output).

@@ -120,7 +120,10 @@ inv_rope_fp8_quant_stream_kernel(InvParams p) {
         const uint32_t s = j % kStages;
         const bool ok = static_cast<uint64_t>(pos) < static_cast<uint64_t>(p.cache_rows);
         valid = ok ? (valid | (1u << s)) : (valid & ~(1u << s));
-        if (lane == 0) {
+        // test-only fault injection: warp 0 leaves its first tile's stage
+        // unarmed, so the wait for it runs out
+        const bool starve = (p.wait.inject & kInjectStreamStage) && warp == 0 && j == 0;
+        if (lane == 0 && !starve) {
             const uint32_t bar = bar0 + 8 * s;
             if (ok) {
                 const uint32_t h0 = iw.c * kRows;
@@ -155,7 +158,7 @@ inv_rope_fp8_quant_stream_kernel(InvParams p) {
     bool ok = true;
     for (; j < n_mine; ++j) {
         const uint32_t s = j % kStages;
-        ok = mbar_wait(bar0 + 8 * s, (j / kStages) & 1u);
+        ok = mbar_wait(bar0 + 8 * s, (j / kStages) & 1u, p.wait.spin_limit);
         if (!__all_sync(kFull, ok)) {
             ok = false;
             break;
@@ -263,7 +266,7 @@ inv_rope_fp8_quant_stream_kernel(InvParams p) {
             if (p.error_flags) atomicOr(p.error_flags, RQ_FLAG_TIMEOUT);
             const uint32_t end = j + kStages < n_mine ? j + kStages : n_mine;
             for (uint32_t d = j; d < end; ++d)
-                (void)mbar_wait(bar0 + 8 * (d % kStages), (d / kStages) & 1u);
+                (void)mbar_wait(bar0 + 8 * (d % kStages), (d / kStages) & 1u, p.wait.spin_limit);
         }
         __syncwarp();
     }

@@ -6,12 +6,13 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "rq_launch.h"  // kSpinLimit
+
 namespace rq {
 
 // Each failed try_wait may suspend the thread for a hardware-chosen time
-// (well under a microsecond when the phase is pending); 2^22 polls bound a
-// wait to a few seconds at most.
-constexpr uint32_t kSpinLimit = 1u << 22;
+// (well under a microsecond when the phase is pending); kSpinLimit = 2^22
+// polls bound a wait to a few seconds at most.
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -53,9 +54,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase of the given parity to complete; false after kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
+// Wait for the phase of the given parity to complete; false after `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint32_t limit = kSpinLimit) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }

@@ -959,3 +959,72 @@ def test_host_pipeline_is_stream_ordered_and_flags_bad_positions(rq):
     sub = dict(inp, x=inp["x"][keep], positions=inp["positions"][keep])
     wc, ws = oracle_inverse(sub)
     assert np.array_equal(out_h[keep].numpy(), wc) and np.array_equal(sc_h[keep].numpy(), ws)
+
+
+# ---------------------------------------------------------------- bounded waits run out
+
+RQ_FLAG_TIMEOUT = 4
+
+
+def _injected(rq, mask, call):
+    """Run `call` with the test-only fault injection on (short waits), always
+    switching it off again; returns after the device has finished."""
+    rq.debug_inject(mask, 1 << 12)
+    try:
+        call()
+        torch.cuda.synchronize()
+    finally:
+        rq.debug_inject()
+
+
+def test_stream_kernel_wait_runs_out_reports_timeout_and_context_stays_usable(rq):
+    """Warp 0 of the TMA-ring kernel leaves its first stage unarmed: its wait
+    gives up, RQ_FLAG_TIMEOUT is set, the kernel exits; the next normal call on
+    the same context is exact."""
+    inp = W.inverse_inputs(W.InverseSpec("to", 2048, 32, 8, 4096, "uniform", True, seed=2))
+    dev = torch.device("cuda:0")
+    x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    _injected(rq, rq.DEBUG_STREAM_STAGE,
+              lambda: rq.inv_rope_fp8_quant(x, pos, cache, 8, error_flags=flags,
+                                            variant=rq.VARIANT_STREAM))
+    assert int(flags.item()) & RQ_FLAG_TIMEOUT
+    flags.zero_()
+    codes, scales = rq.inv_rope_fp8_quant(x, pos, cache, 8, error_flags=flags,
+                                          variant=rq.VARIANT_STREAM)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    wc, ws = oracle_inverse(inp)
+    assert np.array_equal(codes.view(torch.uint8).cpu().numpy(), wc)
+    assert np.array_equal(scales.cpu().numpy(), ws)
+
+
+@pytest.mark.parametrize("kind", ["fp32", "ue8m0"])
+def test_gemm_wait_runs_out_reports_timeout_and_context_stays_usable(rq, kind):
+    """The first CTA's TMA producer issues nothing: its MMA (and, for the
+    clustered kernel, its peer's) waits give up, RQ_FLAG_TIMEOUT is set, TMEM
+    is freed and the kernel exits; the next normal call is within the
+    oracle's bound."""
+    import oracle
+    dev = torch.device("cuda:0")
+    m, g, k, n_out = 300, 2, 1024, 256
+    a, a_sf, w, w_sf, sa, sw = _ue8m0_case(m, g, k, n_out, seed=9)
+    ad, wd = a.to(dev), w.to(dev)
+    if kind == "fp32":
+        sad, swd = sa.to(dev), sw.to(dev)
+        call = lambda fl: rq.grouped_fp8_gemm(ad, sad, wd, swd, error_flags=fl)
+        want = oracle.grouped_fp8_gemm(a.numpy(), sa.numpy(), w.numpy(), sw.numpy())
+    else:
+        asd, wsd = a_sf.to(dev), w_sf.to(dev)
+        call = lambda fl: rq.grouped_fp8_gemm_ue8m0(ad, asd, wd, wsd, error_flags=fl)
+        want = oracle.grouped_fp8_gemm_ue8m0(a.numpy(), a_sf.numpy().view(np.uint32), w.numpy(),
+                                             w_sf.numpy())
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    _injected(rq, rq.DEBUG_GEMM_LOADS, lambda: call(flags))
+    assert int(flags.item()) & RQ_FLAG_TIMEOUT
+    flags.zero_()
+    y = call(flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    bound = _gemm_bound(a, sa.numpy(), w, sw.numpy(), want)
+    assert np.all(np.abs(y.double().cpu().numpy() - want) <= bound)
