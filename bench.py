@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--inv-tokens", type=int, default=None,
                     help="tokens of the inverse op (default 16384; smaller cases are for "
                          "profiling captures and are not bench lines)")
+    ap.add_argument("--profile-op", choices=sorted(PROFILE_OPS), default=None,
+                    help="run only this op, 3 times, on --inv-tokens tokens (default 4096), "
+                         "then exit: the small case an ncu capture runs; prints no bench line")
     return ap.parse_args()
 
 
@@ -687,8 +690,72 @@ def run_reference(args, world, rank):
     }
 
 
+# ops --profile-op can run alone (kernel each one launches at these sizes)
+PROFILE_OPS = {
+    "inverse": "inv_rope_fp8_quant_kernel (warp rows)",
+    "inverse_stream": "inv_rope_fp8_quant_stream_kernel (RQ_INV_STREAM)",
+    "gemm": "grouped_fp8_gemm_kernel (M = tokens, G 4, K 4096, n_out 1024)",
+    "gemm_ue8m0": "grouped_fp8_gemm_ue8m0_kernel (same shape)",
+    "indexer": "indexer_q_rope_quant_kernel (tokens x 64 heads of 128, NeoX)",
+    "fused_qkv": "qnorm_rope_kv_insert_kernel (tokens x 32 q heads padded to 64 + kv)",
+}
+
+
+def run_profile_op(args):
+    """One op, 3 launches, nothing else: the small case of an ncu capture."""
+    import rope_block_fp8_inverse_b300 as rq
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n = args.inv_tokens or 4096
+    spec = W.InverseSpec(f"profile{n}", n, INV_SPEC.n_heads, INV_SPEC.heads_per_group,
+                         INV_SPEC.cache_rows, "arange", True)
+    op = args.profile_op
+    if op in ("inverse", "inverse_stream", "gemm", "gemm_ue8m0"):
+        inp = W.inverse_inputs(spec)
+        x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
+        hpg = spec.heads_per_group
+        variant = rq.VARIANT_STREAM if op == "inverse_stream" else rq.VARIANT_AUTO
+        if op.startswith("inverse"):
+            call = lambda: rq.inv_rope_fp8_quant(x, pos, cache, hpg, variant=variant)
+        else:
+            g = spec.n_heads // hpg
+            gen = torch.Generator().manual_seed(7)
+            wc = torch.randint(0, 256, (g, 1024, hpg * 512), generator=gen, dtype=torch.int32)
+            wc = wc.to(torch.uint8)
+            wc[(wc & 0x7F) == 0x7F] = 0x38
+            wc = wc.to(dev)
+            e = torch.randint(117, 121, (g, 8, hpg * 4), generator=gen, dtype=torch.int32)
+            if op == "gemm":
+                codes, scales = rq.inv_rope_fp8_quant(x, pos, cache, hpg)
+                ws = torch.ldexp(torch.ones(()), (e - 127).float()).float().to(dev)
+                call = lambda: rq.grouped_fp8_gemm(codes, scales, wc, ws)
+            else:
+                codes, words = rq.inv_rope_quant(x, pos, cache, hpg, mode="ue8m0")
+                wsf = e.to(torch.uint8).to(dev)
+                call = lambda: rq.grouped_fp8_gemm_ue8m0(codes, words, wc, wsf)
+    elif op == "indexer":
+        ii = W.indexer_inputs(W.IndexerSpec(f"profile{n}", n, 64, 65536))
+        q, w, pos, cache = (ii[k].to(dev) for k in ("q", "weights", "positions", "cos_sin_cache"))
+        call = lambda: rq.indexer_q_rope_quant(q, pos, cache, w, ii["softmax_scale"],
+                                               ii["head_scale"], rope_style="neox")
+    else:
+        fi = W.fused_inputs(W.FusedSpec(f"profile{n}", n, 32, 64, 65536, 512, 64))
+        fq, fkv, fpos, cache, fsl, fkc = (fi[k].to(dev) for k in
+                                          ("q", "kv", "positions", "cos_sin_cache",
+                                           "slot_mapping", "k_cache"))
+        call = lambda: rq.qnorm_rope_kv_rope_quant_insert(fq, fkv, fpos, cache, fsl, fkc,
+                                                          fi["block_size"], fi["q_head_padded"])
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    print(f"profile-op {op}: 3 launches of {PROFILE_OPS[op]} at {n} tokens", flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.profile_op:
+        return run_profile_op(args)
     if args.impl == "reference":
         # CPU arm: rank 0 alone times the oracle; other ranks exit without work
         world = int(os.environ.get("WORLD_SIZE", "1"))

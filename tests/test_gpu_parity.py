@@ -1028,3 +1028,42 @@ def test_gemm_wait_runs_out_reports_timeout_and_context_stays_usable(rq, kind):
     assert int(flags.item()) == 0
     bound = _gemm_bound(a, sa.numpy(), w, sw.numpy(), want)
     assert np.all(np.abs(y.double().cpu().numpy() - want) <= bound)
+
+
+def test_gemm_fp32_scales_full_size_sampled_rows(rq):
+    """The fp32-scale consumer GEMM in the bench's configuration (prefill16k's
+    op output, 4 groups, K = 4096, 1024 outputs per group); 64 sampled rows
+    against the float64 oracle."""
+    import oracle
+    inp = W.inverse_inputs(W.PREFILL16K)
+    dev = torch.device("cuda:0")
+    x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
+    codes, scales = rq.inv_rope_fp8_quant(x, pos, cache, 8)
+    gen = torch.Generator().manual_seed(12)
+    w = _rand_codes((4, 1024, 4096), gen)
+    sw = 2.0 ** torch.randint(-10, -6, (4, 8, 32), generator=gen).float()
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = rq.grouped_fp8_gemm(codes, scales, w.to(dev), sw.to(dev), error_flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    rows = torch.randperm(16384, generator=gen)[:64].sort().values
+    rows[0] = 0
+    a = codes[rows].view(torch.uint8).cpu()
+    sa = scales[rows].cpu().numpy()
+    want = oracle.grouped_fp8_gemm(a.numpy(), sa, w.numpy(), sw.numpy())
+    bound = _gemm_bound(a, sa, w, sw.numpy(), want)
+    assert np.all(np.abs(y[rows].double().cpu().numpy() - want) <= bound)
+
+
+def test_host_pipeline_full_size_in_the_bench_configuration(rq):
+    """prefill16k through the host-buffer call with 512-token chunks (the
+    bench's e2e leg): the same bytes as the device call."""
+    inp = W.inverse_inputs(W.PREFILL16K)
+    dev = torch.device("cuda:0")
+    cache = inp["cos_sin_cache"].to(dev)
+    x_h, pos_h = inp["x"].pin_memory(), inp["positions"].pin_memory()
+    out_h, sc_h = rq.inv_rope_fp8_quant_host(x_h, pos_h, cache, 8, chunk_tokens=512)
+    codes, scales = rq.inv_rope_fp8_quant(x_h.to(dev), pos_h.to(dev), cache, 8)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h.view(torch.uint8), codes.cpu().view(torch.uint8))
+    assert torch.equal(sc_h, scales.cpu())
