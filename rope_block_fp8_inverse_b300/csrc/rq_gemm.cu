@@ -42,7 +42,18 @@ constexpr uint32_t kTmemCols = 2 * kBN;
 // the unfused kernel's tile: 128 x 256 (one MMA of N = 256 per K = 32 step),
 // two 256-column accumulators = all 512 TMEM columns
 constexpr int kGBN = 256;
-constexpr int kGemmThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+// epilogue warps: a multiple of 4 (one per TMEM lane quadrant per column slice).
+// 8 warps of 128 columns; 16 warps of 64 columns measured slower on B300 (436
+// vs 294 us at M = 16384: 96 registers with spills at 576 threads, and the
+// same 128 KiB TMEM readback per K tile)
+#ifndef RQ_GEMM_EPI_WARPS
+#define RQ_GEMM_EPI_WARPS 8
+#endif
+constexpr int kGEpiWarps = RQ_GEMM_EPI_WARPS;
+constexpr int kGEpiCols = kGBN / (kGEpiWarps / 4);          // accumulator columns per warp
+constexpr int kGemmThreads = 64 + 32 * kGEpiWarps;          // warp 0 TMA, warp 1 MMA, epilogue
+static_assert(kGEpiWarps % 4 == 0 && kGEpiCols % 32 == 0 && 128 % kGEpiCols == 0,
+              "epilogue slices must tile the 256 columns in 32-column loads within 128-blocks");
 constexpr uint32_t kGWTile = kGBN * kBK;                     // 256 rows x 128 bytes
 constexpr uint32_t kGOffW = kGemmStages * kTileBytes;
 constexpr uint32_t kGOffBar = kGOffW + kGemmStages * kGWTile;
@@ -76,7 +87,7 @@ grouped_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8 * b, 1);
-            mbar_init(tempty0 + 8 * b, 256);
+            mbar_init(tempty0 + 8 * b, 32 * kGEpiWarps);
         }
         mbar_init(done, 1);
         mbar_init_fence();
@@ -135,24 +146,23 @@ grouped_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
             if (!mbar_wait(done, 0, lim)) ok = false;  // nothing in flight before teardown
         }
     } else {
-        // epilogue (warps 2..9): thread = output row = TMEM lane 32 * (warp % 4) + lane,
-        // columns 128 * half .. 128 * half + 127 of the tile, half = (warp - 2) / 4
+        // epilogue (warps 2 ..): thread = output row = TMEM lane 32 * (warp % 4) + lane,
+        // columns col0 .. col0 + kGEpiCols - 1 of the tile, col0 = kGEpiCols * ((warp - 2) / 4)
         const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int col0 = kGEpiCols * ((warp - 2) >> 2);
         const int row = quad * 32 + lane;
         const int gm = m0 + row;
         const int cm = gm < p.m ? gm : p.m - 1;  // rows past M hold zeros; read a valid scale
         const float* sa = p.a_scales + (int64_t(cm) * p.groups + g) * n_kt;
-        // weight scales: one per 128 x 128 block; this half's 128 columns are block
-        // 2 * blockIdx.y + half
-        // (when n_out is an odd multiple of 128 the last tile's second half is
-        // past the end: computed from other rows, never stored)
-        const bool half_live = n0 + half * 128 < p.n_out;
-        const float* sw =
-            p.w_scales + (int64_t(g) * (p.n_out / 128) + (half_live ? 2 * blockIdx.y + half : 0)) * n_kt;
-        float acc[128];
+        // weight scales: one per 128 x 128 block; this slice lies in block
+        // 2 * blockIdx.y + col0 / 128 (when n_out is an odd multiple of 128 the
+        // last tile's second half is past the end: computed, never stored)
+        const bool live = n0 + col0 < p.n_out;
+        const float* sw = p.w_scales + (int64_t(g) * (p.n_out / 128) +
+                                        (live ? 2 * blockIdx.y + col0 / 128 : 0)) * n_kt;
+        float acc[kGEpiCols];
 #pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+        for (int j = 0; j < kGEpiCols; ++j) acc[j] = 0.f;
         for (int kt = 0; kt < n_kt; ++kt) {
             const int buf = kt & 1;
             const uint32_t bph = (kt >> 1) & 1;
@@ -164,9 +174,9 @@ grouped_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
             }
             umma::fence_after_sync();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < kGEpiCols / 32; ++c) {
                 float d[32];
-                umma::ld32(tmem + (uint32_t(quad * 32) << 16) + buf * kGBN + half * 128 + c * 32, d);
+                umma::ld32(tmem + (uint32_t(quad * 32) << 16) + buf * kGBN + col0 + c * 32, d);
                 umma::wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) acc[c * 32 + j] = __fmaf_rn(d[j], sc, acc[c * 32 + j]);
@@ -174,10 +184,10 @@ grouped_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
             umma::fence_before_sync();
             mbar_arrive(tempty0 + 8 * buf);
         }
-        if (ok && gm < p.m && half_live) {
-            uint16_t* y = p.y + (int64_t(gm) * p.groups + g) * p.n_out + n0 + half * 128;
+        if (ok && gm < p.m && live) {
+            uint16_t* y = p.y + (int64_t(gm) * p.groups + g) * p.n_out + n0 + col0;
 #pragma unroll
-            for (int j = 0; j < 128; j += 8) {
+            for (int j = 0; j < kGEpiCols; j += 8) {
                 const uint4 v = make_uint4(bf16x2(acc[j], acc[j + 1]), bf16x2(acc[j + 2], acc[j + 3]),
                                            bf16x2(acc[j + 4], acc[j + 5]),
                                            bf16x2(acc[j + 6], acc[j + 7]));

@@ -1067,3 +1067,36 @@ def test_host_pipeline_full_size_in_the_bench_configuration(rq):
     torch.cuda.synchronize()
     assert torch.equal(out_h.view(torch.uint8), codes.cpu().view(torch.uint8))
     assert torch.equal(sc_h, scales.cpu())
+
+
+# ---------------------------------------------------------------- every input value
+
+@pytest.mark.parametrize("order", ["sorted", "shuffled"])
+def test_every_finite_bf16_input_value(rq, order):
+    """All 65,280 finite bf16 patterns (both zeros, subnormals, up to 3.39e38)
+    through the kernel's quantisation at position 0, where the rotation is
+    the identity (cos 1, sin 0: no overflow), bit-exact against the oracle.
+    Sorted by magnitude, neighbouring values share a block, so every scale
+    exponent from the eps floor to 2^120 occurs; shuffled, blocks mix tiny and
+    huge values."""
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    finite = bits[((bits >> 7) & 0xFF) != 0xFF].astype(np.uint16)
+    if order == "sorted":
+        mag = finite.view(np.int16).astype(np.int32) & 0x7FFF
+        finite = finite[np.argsort(mag, kind="stable")]
+    else:
+        finite = finite[np.random.default_rng(5).permutation(finite.size)]
+    rows = -(-finite.size // 512)
+    flat = np.zeros(rows * 512, np.uint16)
+    flat[:finite.size] = finite
+    heads = 8
+    toks = -(-rows // heads)
+    buf = np.zeros(toks * heads * 512, np.uint16)
+    buf[:flat.size] = flat
+    x = torch.from_numpy(buf.view(np.int16)).view(torch.bfloat16).reshape(toks, heads, 512)
+    inp = {"x": x, "positions": torch.zeros(toks, dtype=torch.int64),
+           "cos_sin_cache": W.rope_cache(16), "heads_per_group": heads}
+    gc, gs = run_inverse(rq, inp, variant=rq.VARIANT_WARP_ROWS)
+    wc, ws = oracle_inverse(inp)
+    assert np.array_equal(gc, wc)
+    assert np.array_equal(gs.view(np.uint32), ws.view(np.uint32))
