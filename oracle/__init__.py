@@ -83,7 +83,7 @@ def _load():
                                                         ctypes.c_float, ctypes.c_float, P, P]),
             "rqo_qnorm_rope_kv_rope_quant_insert": (ctypes.c_int, [P, i64, i64, i64, i64, P, i64, P,
                                                                    i64, P, i64, i64, i64, P, P, P,
-                                                                   i64, ctypes.c_double,
+                                                                   i64, ctypes.c_double, P,
                                                                    ctypes.c_float]),
         }
         for name, (res, args) in sig.items():
@@ -293,12 +293,17 @@ def rope_fp8_quant_insert(kv, positions, cos_sin_cache, slot_mapping, k_cache,
 
 def qnorm_rope_kv_rope_quant_insert(q, kv, positions, cos_sin_cache, slot_mapping, k_cache,
                                     block_size: int, q_head_padded: int, norm_eps: float = 1e-6,
-                                    quant_eps: float = 1e-10):
-    """The fused q/kv op: q [N, Hq, 512] bf16 is RMS-normalised per head (no
-    weight), forward-rotated and written into a zero-padded q_out
-    [N, q_head_padded, 512] (bf16 bit patterns, uint16); kv [N, 512] is
-    rotated, quantised and inserted into a copy of k_cache.
-    Returns (q_out, k_cache copy)."""
+                                    quant_eps: float = 1e-10, norm_weight=None):
+    """The fused q/kv op: q [N, Hq, 512] bf16 is RMS-normalised per head (times
+    ``norm_weight`` [512] bf16 when given, before the rotation), forward-rotated
+    and written into a zero-padded q_out [N, q_head_padded, 512] (bf16 bit
+    patterns, uint16); kv [N, 512] is rotated, quantised and inserted into a
+    copy of k_cache. Returns (q_out, k_cache copy)."""
+    wt = None
+    if norm_weight is not None:
+        wt = _np(norm_weight, np.uint16).reshape(-1)
+        if wt.size != HEAD_DIM:
+            raise OracleError("norm_weight must hold 512 bf16 values")
     qa = _np(q, np.uint16)
     n, hq = qa.shape[0], qa.shape[1]
     a = _np(kv, np.uint16)
@@ -310,7 +315,8 @@ def qnorm_rope_kv_rope_quant_insert(q, kv, positions, cos_sin_cache, slot_mappin
     rc = _load().rqo_qnorm_rope_kv_rope_quant_insert(
         _ptr(qa), n, hq, hq * HEAD_DIM, HEAD_DIM, _ptr(a), a.shape[1], _ptr(q_out),
         int(q_head_padded), _ptr(cache), cache.shape[0], int(block_size), cache.shape[1],
-        _ptr(slots), _ptr(pos), _ptr(cs), cs.shape[0], float(norm_eps), float(quant_eps))
+        _ptr(slots), _ptr(pos), _ptr(cs), cs.shape[0], float(norm_eps),
+        None if wt is None else _ptr(wt), float(quant_eps))
     if rc:
         raise OracleError(f"rqo_qnorm_rope_kv_rope_quant_insert status {rc}")
     return q_out, cache

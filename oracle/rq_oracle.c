@@ -55,8 +55,10 @@
  *    inverse-rotated head is written as bf16, each fp32 value rounded to
  *    the nearest bf16, ties to even, in the same [N, G, hpg*512] layout.
  *  - the fused q/kv op ([KV] S1): each q head (512 wide) is RMS-normalised
- *    over its 512 values with no weight (the op takes none), x / sqrt(mean
- *    (x^2) + eps), then forward-rotated like kv, and written as bf16 into a
+ *    over its 512 values, x / sqrt(mean(x^2) + eps), times an optional
+ *    per-dimension weight (the page's op takes none: NULL; with one, the
+ *    usual RMSNorm convention, the weight multiplies before the rotation),
+ *    then forward-rotated like kv, and written as bf16 into a
  *    q_out padded to q_head_padded heads, the pad heads all zero; kv is the
  *    insert op above. The oracle computes the q part in double and rounds
  *    the double result straight to bf16 (the pages fix no precision for it).
@@ -608,9 +610,11 @@ int rqo_rope_fp8_quant_insert(const uint16_t *kv, int64_t n_tokens,
 
 /* ------------------------------------------------- fused q + kv op ([KV] S1) */
 
-/* One q head: RMS norm over its 512 values (no weight), forward rotation of
- * dims 448..511, rounded once to bf16. All in double. */
-void rqo_qnorm_rope_row(const uint16_t *src, const float *cs_row, double eps, uint16_t *dst)
+/* One q head: RMS norm over its 512 values (times weight[k] when weight is
+ * not NULL), forward rotation of dims 448..511, rounded once to bf16. All in
+ * double. */
+void rqo_qnorm_rope_row(const uint16_t *src, const float *cs_row, double eps,
+                        const uint16_t *weight, uint16_t *dst)
 {
     double y[HEAD_DIM], ss = 0.0, r;
     int k, j;
@@ -619,8 +623,11 @@ void rqo_qnorm_rope_row(const uint16_t *src, const float *cs_row, double eps, ui
         ss += y[k] * y[k];
     }
     r = 1.0 / sqrt(ss / HEAD_DIM + eps);
-    for (k = 0; k < HEAD_DIM; ++k)
+    for (k = 0; k < HEAD_DIM; ++k) {
         y[k] *= r;
+        if (weight)            /* the norm's per-dimension weight, before the rotation */
+            y[k] *= (double)rqo_bf16_to_f32(weight[k]);
+    }
     for (j = 0; j < HALF_ROPE; ++j) {
         const double c = cs_row[j], s = cs_row[HALF_ROPE + j];
         const double e = y[NOPE_DIM + 2 * j], o = y[NOPE_DIM + 2 * j + 1];
@@ -640,7 +647,8 @@ int rqo_qnorm_rope_kv_rope_quant_insert(const uint16_t *q, int64_t n_tokens, int
                                         uint8_t *k_cache, int64_t num_blocks, int64_t block_size,
                                         int64_t block_stride, const int64_t *slots,
                                         const int64_t *pos, const float *cache,
-                                        int64_t cache_rows, double norm_eps, float quant_eps)
+                                        int64_t cache_rows, double norm_eps,
+                                        const uint16_t *norm_weight, float quant_eps)
 {
     int64_t t, h;
     int rc;
@@ -657,7 +665,7 @@ int rqo_qnorm_rope_kv_rope_quant_insert(const uint16_t *q, int64_t n_tokens, int
             uint16_t *dst = q_out + (t * q_head_padded + h) * HEAD_DIM;
             if (h < n_heads_q)
                 rqo_qnorm_rope_row(q + t * sq_t + h * sq_h, cache + pos[t] * CACHE_WIDTH,
-                                   norm_eps, dst);
+                                   norm_eps, norm_weight, dst);
             else
                 memset(dst, 0, HEAD_DIM * sizeof *dst);
         }

@@ -813,3 +813,45 @@ def test_gemm_ue8m0_oracle_matches_fp32_scales_of_the_op(oracle_lib):
     y_f32 = oracle_lib.grouped_fp8_gemm(codes.reshape(6, 1, 4096), scales.reshape(6, 1, 32), w,
                                         np.ldexp(1.0, e.astype(np.int64) - 127).astype(np.float32))
     assert np.array_equal(y_ue, y_f32)
+
+
+def _bf16_bits(v):
+    return torch.tensor(np.asarray(v, np.float32)).to(torch.bfloat16).view(torch.int16).numpy() \
+        .view(np.uint16)
+
+
+def test_qnorm_weight_of_ones_is_the_weightless_norm(oracle_lib):
+    rng = np.random.default_rng(11)
+    x = torch.tensor(rng.standard_normal((5, 3, 512)), dtype=torch.float32).to(torch.bfloat16)
+    args = _qnorm_case(x.float().numpy(), [0, 3, 9, 27, 81], 3, 3, cache_rows=4096)[:6]
+    plain = oracle_lib.qnorm_rope_kv_rope_quant_insert(*args, 4, 3, norm_eps=1e-6)[0]
+    ones = oracle_lib.qnorm_rope_kv_rope_quant_insert(*args, 4, 3, norm_eps=1e-6,
+                                                      norm_weight=_bf16_bits(np.ones(512)))[0]
+    assert np.array_equal(plain, ones)
+
+
+def test_qnorm_weight_scales_each_dimension_before_the_rotation(oracle_lib):
+    """Weight 2^a(k), equal within each rotated pair: rounding to bf16 commutes
+    with a power of two, so every output value is the weightless one times
+    2^a(k), exactly. The per-dimension pattern pins the weight's indexing, and
+    the pair rule pins that it acts before the rotation (a weight applied after
+    it would scale the pair's members differently once they mix)."""
+    rng = np.random.default_rng(12)
+    x = torch.tensor(rng.standard_normal((4, 2, 512)), dtype=torch.float32).to(torch.bfloat16)
+    args = _qnorm_case(x.float().numpy(), [1, 5, 50, 500], 2, 2, cache_rows=4096)[:6]
+    a = (np.arange(512) // 2) % 4 - 1           # -1..2, constant on each (2j, 2j+1) pair
+    w = np.ldexp(1.0, a)
+    plain = oracle_lib.qnorm_rope_kv_rope_quant_insert(*args, 4, 2, norm_eps=1e-6)[0]
+    got = oracle_lib.qnorm_rope_kv_rope_quant_insert(*args, 4, 2, norm_eps=1e-6,
+                                                     norm_weight=_bf16_bits(w))[0]
+    to_f = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(to_f(got), to_f(plain) * w)
+    # a weight that differs inside a rotated pair is not a per-dimension scaling of
+    # the output there (the rotation mixes the pair after the weight)
+    w2 = np.ones(512)
+    w2[448] = 4.0
+    got2 = oracle_lib.qnorm_rope_kv_rope_quant_insert(*args, 4, 2, norm_eps=1e-6,
+                                                      norm_weight=_bf16_bits(w2))[0]
+    f2, fp = to_f(got2), to_f(plain)
+    assert np.array_equal(f2[..., :448], fp[..., :448])
+    assert not np.array_equal(f2[..., 449], fp[..., 449])   # the partner moved with it
