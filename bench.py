@@ -367,13 +367,23 @@ def run_ours(args, world, rank, local):
             rq.qnorm_rope_kv_rope_quant_insert(fq, fkv, fpos, cache, fsl, fkc, fi["block_size"],
                                                fi["q_head_padded"], q_out=fqo)
         us = span_us(fused_call, args.mode_launches)
+        fw = W.norm_weight(W.FUSED16K.seed).to(dev)
+
+        def fused_weighted_call():
+            rq.qnorm_rope_kv_rope_quant_insert(fq, fkv, fpos, cache, fsl, fkc, fi["block_size"],
+                                               fi["q_head_padded"], q_out=fqo, norm_weight=fw)
+        us_w = span_us(fused_weighted_call, args.mode_launches)
         fb = W.fused_bytes(W.FUSED16K.n_tokens, W.FUSED16K.n_heads_q, W.FUSED16K.q_head_padded)
         fused = {"kernel": "qnorm_rope_kv_insert_kernel", "workload": "fused16k (N=16384, Hq=32 "
                  "padded to 64, kv into 512x64 slots)", "us": round(us, 2), "bytes": fb,
                  "GBs": round(fb / us / 1e3, 1),
                  "frac_of_measured_peak": round(fb / us / 1e3 / measured_peaks()[0], 4),
+                 "with_norm_weight": {"us": round(us_w, 2),
+                                      "frac_of_measured_peak":
+                                          round(fb / us_w / 1e3 / measured_peaks()[0], 4),
+                                      "what": "synthetic bf16 RMSNorm weight [512] on q"},
                  "launches": args.mode_launches}
-        del fq, fkv, fpos, fsl, fkc, fqo
+        del fq, fkv, fpos, fsl, fkc, fqo, fw
 
     # the indexer q op (RoPE through bf16 + per-head FP8 + scale fold)
     indexer = None

@@ -270,7 +270,7 @@ rq_status rq_rope_fp8_quant_insert(const void *kv_bf16, int64_t n_tokens,
  * the caller, nothing is returned). In one launch, for every token t:
  *  - each q head h < n_heads_q (bf16 [N, n_heads_q, 512], strides in
  *    elements, multiples of 8, base 16-byte aligned) is RMS-normalised over
- *    its 512 values with no weight, y = x / sqrt(mean(x^2) + norm_eps), then
+ *    its 512 values, y_k = x_k / sqrt(mean(x^2) + norm_eps) * w_k, then
  *    forward-rotated on dims 448..511 with row positions[t] of the cache,
  *    and written as bf16 (round to nearest even) to q_out[t, h, :];
  *  - heads n_heads_q <= h < q_head_padded of q_out are written as zeros;
@@ -280,6 +280,9 @@ rq_status rq_rope_fp8_quant_insert(const void *kv_bf16, int64_t n_tokens,
  *  q_head_padded   >= n_heads_q.
  *  norm_eps        >= 0 and finite (arithmetic in fp32: fp32 sum of squares,
  *                  correctly rounded reciprocal square root).
+ *  q_norm_weight   bf16 [512] device vector w, 16-byte aligned, shared by all
+ *                  heads; NULL means w = 1 (the page's op takes no weight).
+ *                  It multiplies the normalised values before the rotation.
  * The paged-cache arguments and rules are those of rq_rope_fp8_quant_insert.
  * A token whose position is outside [0, cache_rows) leaves its q heads and
  * its record untouched (its pad heads are still zeroed) and sets
@@ -290,8 +293,8 @@ rq_status rq_qnorm_rope_kv_rope_quant_insert(
     int64_t q_stride_head, const void *kv_bf16, int64_t kv_stride_token, void *q_out_bf16,
     int64_t q_head_padded, const int64_t *positions, const float *cos_sin_cache,
     int64_t cache_rows, const int64_t *slot_mapping, uint8_t *k_cache, int64_t num_blocks,
-    int64_t block_size, int64_t block_stride_bytes, float norm_eps, float quant_eps,
-    uint32_t *error_flags, void *stream);
+    int64_t block_size, int64_t block_stride_bytes, float norm_eps, const void *q_norm_weight,
+    float quant_eps, uint32_t *error_flags, void *stream);
 
 /* Which dims of the indexer head's rotary part form a rotation pair. */
 typedef enum rq_rope_style {

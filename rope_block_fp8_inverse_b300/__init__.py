@@ -49,8 +49,8 @@ ABI_SYMBOLS = {
                                                 _I64, _I64, ctypes.c_float, _P, _P]),
     "rq_qnorm_rope_kv_rope_quant_insert": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _I64, _P,
                                                           _I64, _P, _P, _I64, _P, _P, _I64, _I64,
-                                                          _I64, ctypes.c_float, ctypes.c_float,
-                                                          _P, _P]),
+                                                          _I64, ctypes.c_float, _P,
+                                                          ctypes.c_float, _P, _P]),
     "rq_indexer_q_rope_fp8_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _I64,
                                                    ctypes.c_int, _P, ctypes.c_float, ctypes.c_float,
                                                    ctypes.c_float, _P, _P, _P, _P]),
@@ -311,11 +311,13 @@ def qnorm_rope_kv_rope_quant_insert(q: torch.Tensor, kv: torch.Tensor, positions
                                     k_cache: torch.Tensor, block_size: int, q_head_padded: int,
                                     norm_eps: float = 1e-6, quant_eps: float = DEFAULT_EPS,
                                     q_out: torch.Tensor | None = None,
-                                    error_flags: torch.Tensor | None = None) -> torch.Tensor:
+                                    error_flags: torch.Tensor | None = None,
+                                    norm_weight: torch.Tensor | None = None) -> torch.Tensor:
     """The fused q/kv op (``rq_qnorm_rope_kv_rope_quant_insert``): q [N, Hq, 512]
-    bf16 is RMS-normalised per head (no weight), forward-rotated and written to
-    ``q_out`` [N, q_head_padded, 512] bf16 (pad heads zeroed); kv [N, 512] is
-    rotated, quantised and inserted into ``k_cache``. Returns ``q_out``."""
+    bf16 is RMS-normalised per head (times ``norm_weight`` [512] bf16 when given,
+    before the rotation), forward-rotated and written to ``q_out``
+    [N, q_head_padded, 512] bf16 (pad heads zeroed); kv [N, 512] is rotated,
+    quantised and inserted into ``k_cache``. Returns ``q_out``."""
     _cuda(q, "q", torch.bfloat16)
     _cuda(kv, "kv", torch.bfloat16)
     if q.dim() != 3 or q.shape[2] != HEAD_DIM or q.stride(2) != 1:
@@ -346,6 +348,13 @@ def qnorm_rope_kv_rope_quant_insert(q: torch.Tensor, kv: torch.Tensor, positions
     for t in (kv, positions, slot_mapping, cos_sin_cache, k_cache, q_out):
         if t.device != q.device:
             raise ValueError("all tensors must be on the same device")
+    wptr = 0
+    if norm_weight is not None:
+        _cuda(norm_weight, "norm_weight", torch.bfloat16)
+        if norm_weight.numel() != HEAD_DIM or not norm_weight.is_contiguous() or \
+                norm_weight.device != q.device:
+            raise ValueError("norm_weight must be a contiguous bf16 [512] tensor on q's device")
+        wptr = norm_weight.data_ptr()
     flags = 0
     if error_flags is not None:
         _cuda(error_flags, "error_flags", torch.int32)
@@ -355,7 +364,7 @@ def qnorm_rope_kv_rope_quant_insert(q: torch.Tensor, kv: torch.Tensor, positions
             q.data_ptr(), n, hq, q.stride(0), q.stride(1), kv.data_ptr(), kv.stride(0),
             q_out.data_ptr(), hpad, positions.data_ptr(), cos_sin_cache.data_ptr(),
             cos_sin_cache.shape[0], slot_mapping.data_ptr(), k_cache.data_ptr(), k_cache.shape[0],
-            int(block_size), k_cache.stride(0), float(norm_eps), float(quant_eps), flags,
+            int(block_size), k_cache.stride(0), float(norm_eps), wptr, float(quant_eps), flags,
             _stream(q.device))
     _check(st, "rq_qnorm_rope_kv_rope_quant_insert")
     return q_out

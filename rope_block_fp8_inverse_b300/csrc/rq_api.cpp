@@ -244,8 +244,8 @@ RQ_EXPORT rq_status rq_qnorm_rope_kv_rope_quant_insert(
     int64_t q_stride_head, const void* kv_bf16, int64_t kv_stride_token, void* q_out_bf16,
     int64_t q_head_padded, const int64_t* positions, const float* cos_sin_cache,
     int64_t cache_rows, const int64_t* slot_mapping, uint8_t* k_cache, int64_t num_blocks,
-    int64_t block_size, int64_t block_stride_bytes, float norm_eps, float quant_eps,
-    uint32_t* error_flags, void* stream) {
+    int64_t block_size, int64_t block_stride_bytes, float norm_eps, const void* q_norm_weight,
+    float quant_eps, uint32_t* error_flags, void* stream) {
     if (n_tokens < 0 || n_heads_q < 1 || q_head_padded < n_heads_q || cache_rows < 1 ||
         num_blocks < 1 || block_size < 1 ||
         block_size > (int64_t(1) << 40) / rq::kRecordBytesABI)
@@ -264,7 +264,8 @@ RQ_EXPORT rq_status rq_qnorm_rope_kv_rope_quant_insert(
     if (!aligned(q_bf16, 16) || q_stride_token % 8 != 0 || q_stride_head % 8 != 0 ||
         !aligned(kv_bf16, 16) || kv_stride_token % 8 != 0 || !aligned(q_out_bf16, 16) ||
         !aligned(positions, 8) || !aligned(cos_sin_cache, 16) || !aligned(slot_mapping, 8) ||
-        !aligned(k_cache, 16) || (error_flags && !aligned(error_flags, 4)))
+        !aligned(k_cache, 16) || (error_flags && !aligned(error_flags, 4)) ||
+        (q_norm_weight && !aligned(q_norm_weight, 16)))
         return RQ_ERR_ALIGN;
 
     rq::DeviceInfo dev;
@@ -272,6 +273,7 @@ RQ_EXPORT rq_status rq_qnorm_rope_kv_rope_quant_insert(
     if (e != cudaSuccess) return from_cuda(e);
 
     rq::FusedParams p;
+    p.norm_w = static_cast<const uint16_t*>(q_norm_weight);
     p.q = q_bf16;
     p.sq_t = q_stride_token;
     p.sq_h = q_stride_head;

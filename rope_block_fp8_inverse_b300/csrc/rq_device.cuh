@@ -107,6 +107,10 @@ __device__ __forceinline__ float4 ld_ro16(const float* p) {
     return __ldg(reinterpret_cast<const float4*>(p));
 }
 
+__device__ __forceinline__ uint4 ld_ro16u(const uint16_t* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
 // Streaming stores (evict-first in L2: written once, read by a later op).
 __device__ __forceinline__ void st_stream8(void* p, uint32_t lo, uint32_t hi) {
     asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(lo), "r"(hi) : "memory");
@@ -280,7 +284,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // correctly rounded reciprocal square root. Returns chunk A's 8 values in
 // *qa and chunk B's in *qb.
 __device__ __forceinline__ void qnorm_rope_row_bf16(uint4 a, uint4 b, bool rope_lane, float4 c4,
-                                                    float4 s4, float eps, uint4* qa, uint4* qb) {
+                                                    float4 s4, float eps, const uint16_t* weight,
+                                                    int ca, uint4* qa, uint4* qb) {
     Pairs p = unpack(a, b);
     float ss = 0.f;
 #pragma unroll
@@ -297,6 +302,14 @@ __device__ __forceinline__ void qnorm_rope_row_bf16(uint4 a, uint4 b, bool rope_
     for (int i = 0; i < 4; ++i) {
         p.ev[i] = __fmul2_rn(p.ev[i], rr);
         p.od[i] = __fmul2_rn(p.od[i], rr);
+    }
+    if (weight) {  // the norm's per-dimension weight (same chunks as the row), before the rotation
+        const Pairs w = unpack(ld_ro16u(weight + 8 * ca), ld_ro16u(weight + 8 * (ca + 8)));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            p.ev[i] = __fmul2_rn(p.ev[i], w.ev[i]);
+            p.od[i] = __fmul2_rn(p.od[i], w.od[i]);
+        }
     }
     if (rope_lane) rotate_b<false>(p, c4, s4);
     uint32_t w[8];

@@ -336,7 +336,8 @@ qnorm_rope_kv_insert_kernel(FusedParams p) {
                 p.q_out + (int64_t(t) * p.q_head_padded + k) * kHeadDim);
             uint4 qa = make_uint4(0, 0, 0, 0), qb = qa;
             if (k < p.n_heads_q)
-                qnorm_rope_row_bf16(a[i], b[i], rope_lane, c[i], s[i], p.norm_eps, &qa, &qb);
+                qnorm_rope_row_bf16(a[i], b[i], rope_lane, c[i], s[i], p.norm_eps, p.norm_w, ca,
+                                    &qa, &qb);
             st_stream16(dst + 16 * ca, qa);
             st_stream16(dst + 16 * (ca + 8), qb);
         }

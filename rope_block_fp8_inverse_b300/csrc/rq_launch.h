@@ -117,6 +117,7 @@ struct FusedParams {
     uint8_t* k_cache;
     int64_t num_blocks, block_size, block_stride;
     float norm_eps, quant_eps;
+    const uint16_t* norm_w;   // bf16 [512] RMSNorm weight, or null for none
     uint32_t* error_flags;
 };
 

@@ -170,9 +170,10 @@ def test_layout_bf16_needs_no_scales_and_empty_is_a_no_op(lib):
 
 
 def _fus(lib, q=A16, n=4, hq=8, sqt=4096, sqh=512, kv=A16, skv=512, qo=A16, hpad=8, pos=A16,
-         cs=A16, rows=16, slots=A16, cache=A16, nb=8, bs=64, stride=64 * 528, ne=1e-6, qe=1e-10):
+         cs=A16, rows=16, slots=A16, cache=A16, nb=8, bs=64, stride=64 * 528, ne=1e-6, qe=1e-10,
+         w=None):
     return lib.rq_qnorm_rope_kv_rope_quant_insert(q, n, hq, sqt, sqh, kv, skv, qo, hpad, pos, cs,
-                                                  rows, slots, cache, nb, bs, stride, ne, qe,
+                                                  rows, slots, cache, nb, bs, stride, ne, w, qe,
                                                   None, None)
 
 
@@ -188,6 +189,7 @@ def _fus(lib, q=A16, n=4, hq=8, sqt=4096, sqh=512, kv=A16, skv=512, qo=A16, hpad
     (dict(qo=A8), RQ_ERR_ALIGN),
     (dict(sqh=516), RQ_ERR_ALIGN),
     (dict(stride=64 * 528 + 8), RQ_ERR_ALIGN),
+    (dict(w=A8), RQ_ERR_ALIGN),          # the norm weight is read in 16-byte chunks
 ])
 def test_fused_rejects_bad_arguments(lib, kw, status):
     assert _fus(lib, **kw) == status

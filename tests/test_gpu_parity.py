@@ -503,7 +503,8 @@ def _bf16_ulp(v):
     return np.where(a >= 2.0 ** -126, np.exp2(e - 7), 2.0 ** -133)
 
 
-def run_fused(rq, inp, norm_eps=1e-6, q=None, positions=None, flags=None, q_out=None):
+def run_fused(rq, inp, norm_eps=1e-6, q=None, positions=None, flags=None, q_out=None,
+              weight=None):
     dev = torch.device("cuda:0")
     kc = inp["k_cache"].to(dev).contiguous()
     qd = (inp["q"] if q is None else q).to(dev)
@@ -511,17 +512,17 @@ def run_fused(rq, inp, norm_eps=1e-6, q=None, positions=None, flags=None, q_out=
     out = rq.qnorm_rope_kv_rope_quant_insert(
         qd, inp["kv"].to(dev), pos, inp["cos_sin_cache"].to(dev), inp["slot_mapping"].to(dev), kc,
         inp["block_size"], inp["q_head_padded"], norm_eps=norm_eps, error_flags=flags,
-        q_out=q_out)
+        q_out=q_out, norm_weight=None if weight is None else weight.to(dev))
     torch.cuda.synchronize()
     return out.view(torch.int16).cpu().numpy().view(np.uint16), kc.cpu().numpy()
 
 
-def oracle_fused(inp, norm_eps=1e-6, positions=None, slots=None):
+def oracle_fused(inp, norm_eps=1e-6, positions=None, slots=None, weight=None):
     import oracle
     return oracle.qnorm_rope_kv_rope_quant_insert(
         inp["q"], inp["kv"], inp["positions"] if positions is None else positions,
         inp["cos_sin_cache"], inp["slot_mapping"] if slots is None else slots, inp["k_cache"],
-        inp["block_size"], inp["q_head_padded"], norm_eps=norm_eps)
+        inp["block_size"], inp["q_head_padded"], norm_eps=norm_eps, norm_weight=weight)
 
 
 def assert_fused_parity(got, want, n_heads_q):
@@ -549,12 +550,26 @@ def test_fused_small_shapes(rq, n, hq, hpad):
     assert_fused_parity(run_fused(rq, inp), oracle_fused(inp), hq)
 
 
-def test_fused16k_full(rq):
-    """The 16k-token shape, every output compared."""
+@pytest.mark.parametrize("weighted", [False, True])
+def test_fused16k_full(rq, weighted):
+    """The 16k-token shape, every output compared (the page's weightless norm,
+    and with a synthetic RMSNorm weight)."""
     inp = W.fused_inputs(W.FUSED16K)
-    got = run_fused(rq, inp)
+    w = W.norm_weight(W.FUSED16K.seed) if weighted else None
+    got = run_fused(rq, inp, weight=w)
     assert got[0].shape == (16384, 64, 512)
-    assert_fused_parity(got, oracle_fused(inp), 32)
+    assert_fused_parity(got, oracle_fused(inp, weight=w), 32)
+
+
+@pytest.mark.parametrize("n,hq,hpad", [(1, 1, 1), (33, 4, 8), (130, 16, 16)])
+def test_fused_norm_weight_small_shapes(rq, n, hq, hpad):
+    """A weight with zeros, negatives and a spread of magnitudes, per dimension."""
+    spec = W.FusedSpec("fw", n, hq, hpad, 4096, 2 * W.ceil_div(n, 16) + 1, 16, seed=n + 7)
+    inp = W.fused_inputs(spec)
+    gen = torch.Generator().manual_seed(n)
+    w = (torch.randn(512, generator=gen) * 2.0).to(torch.bfloat16)
+    w[::37] = 0.0
+    assert_fused_parity(run_fused(rq, inp, weight=w), oracle_fused(inp, weight=w), hq)
 
 
 @pytest.mark.parametrize("norm_eps", [0.0, 1e-6, 1.0])

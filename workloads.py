@@ -172,6 +172,14 @@ def fused_inputs(spec: FusedSpec, cache: torch.Tensor | None = None, fill: int =
             "k_cache": k_cache, "block_size": spec.block_size, "q_head_padded": spec.q_head_padded}
 
 
+def norm_weight(seed: int = 0) -> torch.Tensor:
+    """A synthetic RMSNorm weight for the fused q/kv op: 512 bf16 values
+    uniform in [0.5, 1.5), from its own generator (seed + 1), so the op's other
+    inputs are drawn as without it."""
+    gen = torch.Generator().manual_seed(seed + 1)
+    return (torch.rand(HEAD_DIM, generator=gen) + 0.5).to(torch.bfloat16)
+
+
 def indexer_inputs(spec: IndexerSpec, cache: torch.Tensor | None = None) -> dict:
     """q [N,H,128] bf16 N(0,1) + 1% x50 outliers (drawn first), weights [N,H]
     fp32 uniform in [0.5, 1.5), positions 0..N-1."""
