@@ -73,6 +73,8 @@ typedef enum rq_status {
 #define RQ_FLAG_SLOT_RANGE 2u     /* a slot was >= num_blocks * block_size    */
 #define RQ_FLAG_TIMEOUT 4u        /* a pipeline wait gave up (never expected):
                                      the outputs of that launch are incomplete */
+#define RQ_FLAG_SLOT_DUPLICATE 8u /* two tokens map to one slot (found only by
+                                     rq_validate_indices)                       */
 
 /* Static, NUL-terminated description of a status code. */
 const char *rq_status_string(int status);
@@ -172,6 +174,31 @@ rq_status rq_inv_rope_fp8_quant_host(const void *x_bf16_host, int64_t n_tokens, 
 #define RQ_DEBUG_STREAM_STAGE 1u
 #define RQ_DEBUG_GEMM_LOADS 2u
 void rq_debug_inject(uint32_t mask, uint32_t spin_limit);
+
+/*
+ * Debug helper: checks the device-side preconditions of the ops, which the
+ * ops themselves only partly check (a repeated slot goes unnoticed there),
+ * without running them. One non-trapping kernel on `stream`, then the result
+ * word is copied to the host and `stream` is synchronised.
+ *  positions      [n_tokens] int64, device: each must be in [0, cache_rows)
+ *                 (else RQ_FLAG_POSITION_RANGE).
+ *  slot_mapping   [n_tokens] int64, device, or NULL to check positions only:
+ *                 each must be negative (the token is skipped) or below
+ *                 num_slots (else RQ_FLAG_SLOT_RANGE), and no two tokens may
+ *                 share a slot (else RQ_FLAG_SLOT_DUPLICATE).
+ *  num_slots      num_blocks * block_size of the paged cache (>= 1 when
+ *                 slot_mapping is given).
+ *  workspace      device, 16-byte aligned, at least
+ *                 rq_validate_indices_workspace(num_slots) bytes (a bitmap of
+ *                 num_slots bits and the result word); owned by the caller.
+ *  result         host uint32: the RQ_FLAG_* bits found (0 = all valid).
+ * positions and slot_mapping 8-byte aligned. n_tokens >= 0 (0 writes 0).
+ */
+int64_t rq_validate_indices_workspace(int64_t num_slots);
+rq_status rq_validate_indices(const int64_t *positions, const int64_t *slot_mapping,
+                              int64_t n_tokens, int64_t cache_rows, int64_t num_slots,
+                              void *workspace, int64_t workspace_bytes, uint32_t *result,
+                              void *stream);
 
 /* Kernel variants of rq_inv_rope_fp8_quant; all produce identical bytes. */
 typedef enum rq_inv_variant {

@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["debug_inject", "DEBUG_STREAM_STAGE", "DEBUG_GEMM_LOADS", "inv_rope_fp8_quant_host", "host_workspace_bytes", "inv_rope_fp8_quant_gemm", "grouped_fp8_gemm", "grouped_fp8_gemm_ue8m0",
+__all__ = ["validate_indices", "debug_inject", "DEBUG_STREAM_STAGE", "DEBUG_GEMM_LOADS", "inv_rope_fp8_quant_host", "host_workspace_bytes", "inv_rope_fp8_quant_gemm", "grouped_fp8_gemm", "grouped_fp8_gemm_ue8m0",
            "indexer_q_rope_quant", "qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
            "empty_outputs", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
@@ -56,6 +56,8 @@ ABI_SYMBOLS = {
                                                    ctypes.c_float, _P, _P, _P, _P]),
     "rq_grouped_fp8_gemm": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _P]),
     "rq_debug_inject": (None, [ctypes.c_uint32, ctypes.c_uint32]),
+    "rq_validate_indices_workspace": (ctypes.c_int64, [_I64]),
+    "rq_validate_indices": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _I64, _P, _P]),
     "rq_inv_rope_fp8_quant_host_workspace": (ctypes.c_int64, [_I64, _I64]),
     "rq_inv_rope_fp8_quant_host": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, ctypes.c_float,
                                                   _P, _P, _P, _I64, _I64, _P, _P]),
@@ -469,6 +471,41 @@ def grouped_fp8_gemm(a_codes: torch.Tensor, a_scales: torch.Tensor, w_codes: tor
                                        out.data_ptr(), flags, _stream(a_codes.device))
     _check(st, "rq_grouped_fp8_gemm")
     return out
+
+
+def validate_indices(positions: torch.Tensor, cache_rows: int,
+                     slot_mapping: torch.Tensor | None = None, num_slots: int = 0,
+                     workspace: torch.Tensor | None = None) -> int:
+    """Debug helper (``rq_validate_indices``, synchronous): the RQ_FLAG_* bits of
+    the device-side preconditions the given indices break (0 = all valid):
+    positions in [0, cache_rows); slots negative (skip) or below ``num_slots``
+    (= num_blocks * block_size), and no slot used twice. ``workspace``: a CUDA
+    uint8 tensor of at least ``rq_validate_indices_workspace(num_slots)`` bytes
+    (allocated when None)."""
+    _cuda(positions, "positions", torch.int64)
+    if positions.dim() != 1 or not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous [N] int64 tensor")
+    n = positions.shape[0]
+    sptr = 0
+    if slot_mapping is not None:
+        _cuda(slot_mapping, "slot_mapping", torch.int64)
+        if tuple(slot_mapping.shape) != (n,) or not slot_mapping.is_contiguous() or \
+                slot_mapping.device != positions.device:
+            raise ValueError("slot_mapping must be a contiguous [N] int64 tensor on the same device")
+        sptr = slot_mapping.data_ptr()
+    need = lib().rq_validate_indices_workspace(num_slots if slot_mapping is not None else 0)
+    if need < 0:
+        raise ValueError("num_slots out of range")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=positions.device)
+    _cuda(workspace, "workspace", torch.uint8)
+    result = ctypes.c_uint32(0)
+    with torch.cuda.device(positions.device):
+        st = lib().rq_validate_indices(positions.data_ptr(), sptr, n, int(cache_rows),
+                                       int(num_slots), workspace.data_ptr(), workspace.numel(),
+                                       ctypes.addressof(result), _stream(positions.device))
+    _check(st, "rq_validate_indices")
+    return int(result.value)
 
 
 def debug_inject(mask: int = 0, spin_limit: int = 0) -> None:

@@ -71,6 +71,53 @@ RQ_EXPORT const char* rq_status_string(int status) {
 
 RQ_EXPORT int rq_version(void) { return (kVersionMajor << 16) | kVersionMinor; }
 
+RQ_EXPORT int64_t rq_validate_indices_workspace(int64_t num_slots) {
+    if (num_slots < 0 || num_slots > (int64_t(1) << 40)) return -1;
+    const int64_t bitmap = ((num_slots + 31) / 32 * 4 + 15) / 16 * 16;
+    return bitmap + 16;  // then the result word, in its own 16 bytes
+}
+
+RQ_EXPORT rq_status rq_validate_indices(const int64_t* positions, const int64_t* slot_mapping,
+                                        int64_t n_tokens, int64_t cache_rows, int64_t num_slots,
+                                        void* workspace, int64_t workspace_bytes, uint32_t* result,
+                                        void* stream) {
+    if (n_tokens < 0 || cache_rows < 1 || num_slots < 0 || (slot_mapping && num_slots < 1))
+        return RQ_ERR_SHAPE;
+    if (!result) return RQ_ERR_NULL;
+    const int64_t need = rq_validate_indices_workspace(slot_mapping ? num_slots : 0);
+    if (need < 0) return RQ_ERR_SHAPE;
+    if (n_tokens == 0) {
+        *result = 0;
+        return RQ_OK;
+    }
+    if (!positions || !workspace) return RQ_ERR_NULL;
+    if (workspace_bytes < need) return RQ_ERR_SHAPE;
+    if (!aligned(positions, 8) || (slot_mapping && !aligned(slot_mapping, 8)) ||
+        !aligned(workspace, 16))
+        return RQ_ERR_ALIGN;
+    rq::DeviceInfo dev;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return from_cuda(e);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    rq::ValParams p;
+    p.positions = positions;
+    p.slot_mapping = slot_mapping;
+    p.n_tokens = n_tokens;
+    p.cache_rows = cache_rows;
+    p.num_slots = num_slots;
+    p.bitmap = reinterpret_cast<uint32_t*>(ws);
+    p.result = reinterpret_cast<uint32_t*>(ws + need - 16);
+    uint32_t word = 0;
+    if ((e = cudaMemsetAsync(ws, 0, size_t(need), st)) != cudaSuccess ||
+        (e = rq::launch_validate_indices(p, dev, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(&word, p.result, 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(st)) != cudaSuccess)
+        return from_cuda(e);
+    *result = word;
+    return RQ_OK;
+}
+
 RQ_EXPORT void rq_debug_inject(uint32_t mask, uint32_t spin_limit) {
     g_wait.inject = mask;
     g_wait.spin_limit = spin_limit ? spin_limit : rq::kSpinLimit;

@@ -121,6 +121,15 @@ struct FusedParams {
     uint32_t* error_flags;
 };
 
+// Arguments of the index check (rq_validate_indices).
+struct ValParams {
+    const int64_t* positions;     // [n_tokens]
+    const int64_t* slot_mapping;  // [n_tokens] or null
+    int64_t n_tokens, cache_rows, num_slots;
+    uint32_t* bitmap;             // num_slots bits, zeroed
+    uint32_t* result;             // RQ_FLAG_* bits, zeroed
+};
+
 // Arguments of the indexer q kernel (rq_indexer_q_rope_fp8_quant).
 struct IdxParams {
     const void* q;            // bf16 [N, H, 128], strides sq_t / sq_h elements
@@ -204,6 +213,8 @@ cudaError_t launch_grouped_fp8_gemm(const GemmParams& p, const uint8_t* a_codes,
                                     const uint8_t* w_codes, int dev_ordinal, cudaStream_t stream);
 cudaError_t launch_fused_inv_rope_quant_gemm(const FusedGemmParams& p, const uint8_t* w_codes,
                                              int dev_ordinal, cudaStream_t stream);
+cudaError_t launch_validate_indices(const ValParams& p, const DeviceInfo& dev,
+                                    cudaStream_t stream);
 cudaError_t launch_grouped_fp8_gemm_ue8m0(const MxGemmParams& p, const uint8_t* a_codes,
                                           const uint8_t* w_codes, const DeviceInfo& dev,
                                           cudaStream_t stream);

@@ -297,3 +297,36 @@ def test_host_rejects_bad_arguments(lib, kw, status):
 
 def test_host_empty_batch_is_a_no_op(lib):
     assert _host(lib, n=0, x=None, pos=None, out=None, sc=None, ws=None) == RQ_OK
+
+
+def test_validate_workspace_is_bitmap_plus_result_word(lib):
+    for n in (0, 1, 31, 32, 33, 32768, 10 ** 6):
+        bitmap = ((n + 31) // 32 * 4 + 15) // 16 * 16
+        assert lib.rq_validate_indices_workspace(n) == bitmap + 16
+    assert lib.rq_validate_indices_workspace(-1) == -1
+
+
+def _val(lib, pos=A16, slots=A16, n=4, rows=64, nslots=128, ws=A16, wsb=1 << 20, res=True):
+    out = ctypes.c_uint32(0xDEAD)
+    st = lib.rq_validate_indices(pos, slots, n, rows, nslots, ws, wsb,
+                                 ctypes.addressof(out) if res else None, None)
+    return st, out.value
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=-1), RQ_ERR_SHAPE),
+    (dict(rows=0), RQ_ERR_SHAPE),
+    (dict(nslots=0), RQ_ERR_SHAPE),          # slots given, but no cache slots
+    (dict(res=False), RQ_ERR_NULL),
+    (dict(pos=None), RQ_ERR_NULL),
+    (dict(ws=None), RQ_ERR_NULL),
+    (dict(wsb=16), RQ_ERR_SHAPE),            # smaller than the bitmap + result word
+    (dict(pos=A16 + 4), RQ_ERR_ALIGN),
+    (dict(ws=A16 + 8), RQ_ERR_ALIGN),
+])
+def test_validate_rejects_bad_arguments(lib, kw, status):
+    assert _val(lib, **kw)[0] == status
+
+
+def test_validate_empty_batch_reports_nothing(lib):
+    assert _val(lib, n=0, pos=None, slots=None, ws=None) == (RQ_OK, 0)

@@ -1115,3 +1115,61 @@ def test_every_finite_bf16_input_value(rq, order):
     wc, ws = oracle_inverse(inp)
     assert np.array_equal(gc, wc)
     assert np.array_equal(gs.view(np.uint32), ws.view(np.uint32))
+
+
+# ---------------------------------------------------------------- index validation helper
+
+def _expected_flags(pos, slots, cache_rows, num_slots):
+    """Plain Python statement of the preconditions (1 position, 2 slot range, 8 reuse)."""
+    f = 0
+    if any(p < 0 or p >= cache_rows for p in pos):
+        f |= 1
+    if slots is not None:
+        live = [s for s in slots if s >= 0]
+        if any(s >= num_slots for s in live):
+            f |= 2
+        inside = [s for s in live if s < num_slots]
+        if len(set(inside)) != len(inside):
+            f |= 8
+    return f
+
+
+def test_validate_indices_planted_errors(rq):
+    dev = torch.device("cuda:0")
+    base_pos = [0, 5, 63, 17, 9, 40]
+    base_slots = [3, 7, -1, 100, 0, 55]
+    cases = [
+        (base_pos, base_slots, 0),
+        ([0, 5, 64, 17, 9, 40], base_slots, 1),          # position == cache_rows
+        ([0, -1, 63, 17, 9, 40], base_slots, 1),
+        (base_pos, [3, 7, -1, 128, 0, 55], 2),            # slot == num_slots
+        (base_pos, [3, 7, -1, 100, 3, 55], 8),            # slot 3 used twice
+        (base_pos, [-5, -1, -1, -1, -7, -2], 0),          # every token skipped
+        ([70, 5, 63, 17, 9, 40], [3, 3, -1, 999, 0, 55], 11),
+    ]
+    for pos, slots, want in cases:
+        got = rq.validate_indices(torch.tensor(pos, device=dev), 64,
+                                  torch.tensor(slots, device=dev), 128)
+        assert got == want == _expected_flags(pos, slots, 64, 128), (pos, slots, got)
+    # positions only: slots are not looked at
+    assert rq.validate_indices(torch.tensor([1, 2, 64], device=dev), 64) == 1
+
+
+def test_validate_indices_at_the_insert_workload(rq):
+    """insert16k's positions and distinct slots are valid; duplicates and a
+    range error planted at random tokens are all found."""
+    ins = W.insert_inputs(W.INSERT16K)
+    dev = torch.device("cuda:0")
+    pos, slots = ins["positions"], ins["slot_mapping"]
+    n_slots = W.INSERT16K.num_blocks * W.INSERT16K.block_size
+    ws = torch.empty(rq.lib().rq_validate_indices_workspace(n_slots), dtype=torch.uint8, device=dev)
+    assert rq.validate_indices(pos.to(dev), 65536, slots.to(dev), n_slots, workspace=ws) == 0
+    gen = torch.Generator().manual_seed(4)
+    bad = slots.clone()
+    i, j = torch.randperm(16384, generator=gen)[:2].tolist()
+    bad[j] = bad[i]                                    # a repeated slot
+    got = rq.validate_indices(pos.to(dev), 65536, bad.to(dev), n_slots, workspace=ws)
+    assert got == 8 == _expected_flags(pos.tolist(), bad.tolist(), 65536, n_slots)
+    bad[i] = n_slots + 5                               # now out of range instead
+    got = rq.validate_indices(pos.to(dev), 65536, bad.to(dev), n_slots, workspace=ws)
+    assert got == _expected_flags(pos.tolist(), bad.tolist(), 65536, n_slots) == 2
