@@ -200,6 +200,25 @@ rq_status rq_validate_indices(const int64_t *positions, const int64_t *slot_mapp
                               void *workspace, int64_t workspace_bytes, uint32_t *result,
                               void *stream);
 
+/*
+ * rq_validate_indices for callers that cannot allocate device memory: a
+ * program that links only this library and has no device allocator, or an
+ * engine whose free device memory is all given to its KV cache and that must
+ * not allocate mid-step. The pages have no counterpart; this is a library
+ * convenience. Same checks, arguments and result as rq_validate_indices,
+ * without the workspace: the slot bitmap and result word live in a fixed
+ * device array of the library (131,328 bytes on every GPU that loads it, held
+ * until the process exits). num_slots above 1,048,576 (2^20) returns
+ * RQ_ERR_SHAPE. Nothing is allocated. The first call on a device looks up
+ * the array's device address (make that first call before any stream
+ * capture). Every call clears the part of the array it uses; calls whose
+ * work overlaps on the GPU (other streams or host threads) race on the
+ * shared array. The call synchronises `stream` before it returns.
+ */
+rq_status rq_validate_indices_noalloc(const int64_t *positions, const int64_t *slot_mapping,
+                                      int64_t n_tokens, int64_t cache_rows, int64_t num_slots,
+                                      uint32_t *result, void *stream);
+
 /* Kernel variants of rq_inv_rope_fp8_quant; all produce identical bytes. */
 typedef enum rq_inv_variant {
     RQ_INV_AUTO = 0,          /* the default: warp rows (measured the faster of the

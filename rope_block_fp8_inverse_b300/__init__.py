@@ -58,6 +58,7 @@ ABI_SYMBOLS = {
     "rq_debug_inject": (None, [ctypes.c_uint32, ctypes.c_uint32]),
     "rq_validate_indices_workspace": (ctypes.c_int64, [_I64]),
     "rq_validate_indices": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _I64, _P, _P]),
+    "rq_validate_indices_noalloc": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P]),
     "rq_inv_rope_fp8_quant_host_workspace": (ctypes.c_int64, [_I64, _I64]),
     "rq_inv_rope_fp8_quant_host": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, ctypes.c_float,
                                                   _P, _P, _P, _I64, _I64, _P, _P]),
