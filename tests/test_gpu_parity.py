@@ -1173,3 +1173,43 @@ def test_validate_indices_at_the_insert_workload(rq):
     bad[i] = n_slots + 5                               # now out of range instead
     got = rq.validate_indices(pos.to(dev), 65536, bad.to(dev), n_slots, workspace=ws)
     assert got == _expected_flags(pos.tolist(), bad.tolist(), 65536, n_slots) == 2
+
+
+# ---------------------------------------------------------------- random shapes
+
+def _random_shape_cases(k, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(k):
+        h = int(rng.choice([1, 2, 3, 5, 8, 12, 16, 24, 40, 64, 96, 128]))
+        divisors = [d for d in range(1, h + 1) if h % d == 0]
+        hpg = int(rng.choice(divisors))
+        n = int(rng.integers(1, 700))
+        pad_h = int(rng.choice([0, 8, 64]))        # padding between heads, in elements
+        pad_t = int(rng.choice([0, 8, 512]))       # padding between tokens
+        cases.append((i, n, h, hpg, pad_h, pad_t))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_shape_cases(16, 2024), ids=lambda c: f"r{c[0]}")
+def test_random_shapes_and_strides_bit_exact(rq, case):
+    """Seeded random token counts, head counts, every divisor as heads_per_group,
+    padded head / token strides, both kernels: codes and scales bit-exact, and
+    the layout entry's UE8M0 and bf16 outputs too."""
+    i, n, h, hpg, pad_h, pad_t = case
+    inp = W.inverse_inputs(W.InverseSpec(f"rand{i}", n, h, hpg, 8192, "uniform", True, seed=i))
+    sh = 512 + pad_h
+    st = h * sh + pad_t
+    big = torch.zeros(n * st + 512, dtype=torch.bfloat16)
+    view = big.as_strided((n, h, 512), (st, sh, 1))
+    view.copy_(inp["x"])
+    dev = torch.device("cuda:0")
+    xd = big.to(dev).as_strided((n, h, 512), (st, sh, 1))
+    wc, ws = oracle_inverse(inp)
+    for variant in (rq.VARIANT_WARP_ROWS, rq.VARIANT_STREAM):
+        gc, gs = run_inverse(rq, inp, x_override=xd, variant=variant)
+        assert np.array_equal(gc, wc), (case, variant)
+        assert np.array_equal(gs.view(np.uint32), ws.view(np.uint32)), (case, variant)
+    for mode in ("ue8m0", "bf16"):
+        got = run_layout(rq, dict(inp, x=xd), mode, "token")
+        assert_layout_parity(mode, got, oracle_layout(inp, mode))
