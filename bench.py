@@ -254,9 +254,19 @@ def cpu_baseline(inv, ins):
                                  ins["slot_mapping"], ins["k_cache"], ins["block_size"],
                                  threads=threads)
     dt = time.perf_counter() - t0
+    # single-threaded on a quarter of the inverse's tokens (bytes scaled to match)
+    q = inv["x"].shape[0] // 4
+    t1 = time.perf_counter()
+    oracle.inv_rope_fp8_quant(inv["x"][:q], inv["positions"][:q], inv["cos_sin_cache"],
+                              inv["heads_per_group"], threads=1)
+    dt1 = time.perf_counter() - t1
+    one_bytes = W.inverse_bytes(q, inv["x"].shape[1])
     return {"value": round(STEP_BYTES / dt / 1e9, 3), "unit": "GB/s", "cores": threads,
             "kind": "oracle", "seconds": round(dt, 3),
-            "sample": "one full step: inverse 16384 tok x 32 heads + insert 16384 tok"}
+            "sample": "one full step: inverse 16384 tok x 32 heads + insert 16384 tok",
+            "single_thread": {"value": round(one_bytes / dt1 / 1e9, 3), "unit": "GB/s",
+                              "cores": 1, "seconds": round(dt1, 3),
+                              "sample": f"inverse only, {q} tokens x 32 heads"}}
 
 
 def run_ours(args, world, rank, local):
