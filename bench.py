@@ -509,6 +509,40 @@ def run_ours(args, world, rank, local):
         decode = {"workload": "decode: N tokens x 32 heads, heads_per_group 8, positions "
                   "U[0,65536); graph of 100 calls, 5 replays", "us_per_call": decode}
 
+    # the configurations that fit in L2, cold: each call after a 256 MiB write
+    # that evicts L2, one event pair around the call (median of 20); the hot
+    # figures are the graph replays above and the in-step insert
+    small_cold = None
+    if args.mode_launches > 0:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+        def cold_us(fn, reps=20):
+            fn()
+            ts = []
+            for r in range(reps):
+                flush.fill_(r & 0xFF)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+                ts.append(a.elapsed_time(b) * 1e3)
+            return round(statistics.median(ts), 2)
+        small_cold = {}
+        ti = W.inverse_inputs(W.TINY)
+        tx, tp, tc = ti["x"].to(dev), ti["positions"].to(dev), ti["cos_sin_cache"].to(dev)
+        small_cold["tiny (N=64, H=8)"] = cold_us(
+            lambda: rq.inv_rope_fp8_quant(tx, tp, tc, ti["heads_per_group"]))
+        for nt in (1, 8, 64):
+            di = W.inverse_inputs(W.decode_spec(nt), cache=inv_h["cos_sin_cache"])
+            dx, dp = di["x"].to(dev), di["positions"].to(dev)
+            small_cold[f"decode N={nt}"] = cold_us(lambda: rq.inv_rope_fp8_quant(dx, dp, cache, 8))
+        small_cold["insert16k"] = cold_us(
+            lambda: rq.rope_fp8_quant_insert(kv, kpos, cache, slots, k_cache, bs))
+        small_cold = {"what": "median us per call after evicting L2 (cold); event pair around "
+                              "the call", "us": small_cold}
+        del flush
+
     # end to end through the public API from pinned host buffers
     e2e_steps = args.e2e_steps or min(args.steps, 20)
     x_host = inv_h["x"].pin_memory()
@@ -625,6 +659,7 @@ def run_ours(args, world, rank, local):
         "fused_qkv": fused,
         "indexer_q": indexer,
         "decode_latency": decode,
+        "small_configs_cold": small_cold,
         "consumer_gemm": gemm,
         "clocks": sampler.summary(),
     }
