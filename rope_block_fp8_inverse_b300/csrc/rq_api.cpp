@@ -234,7 +234,9 @@ RQ_EXPORT rq_status rq_inv_rope_quant_layout(
     p.lay.sg = scale_stride_group;
     p.lay.se = scale_stride_elem;
     // large calls whose tiles fit the layout take the TMA-ring kernel
-    const bool stream_it = int64_t(p.n_rows) >= int64_t(dev.sm_count) * rq::kStreamMinRowsPerSm &&
+    // bf16 output (no quantisation) stays on the warp-rows layout kernel at every size
+    const bool stream_it = p.lay.mode != rq::kOutBf16 &&
+                           int64_t(p.n_rows) >= int64_t(dev.sm_count) * rq::kStreamMinRowsPerSm &&
                            rq::stream_layout_ok(p);
     return from_cuda(stream_it ? rq::launch_inv_rope_fp8_quant_stream(
                                      p, dev, static_cast<cudaStream_t>(stream))

@@ -189,9 +189,10 @@ enum InvVariant {
 };
 
 // rq_inv_rope_quant_layout takes the stream kernel from this many rows per
-// SM up, when heads_per_group is a multiple of 8 (measured on B300 at 16384
-// tokens x 32 heads: fp8 0.95 vs 0.86 of the copy peak for the warp-rows
-// layout kernel, UE8M0 0.93 vs 0.86, bf16 equal).
+// SM up, for the quantising modes when heads_per_group is a multiple of 8
+// (measured on B300 at 16384 tokens x 32 heads: fp8 0.93 vs 0.92 of the copy
+// peak for the warp-rows layout kernel, UE8M0 0.925 vs 0.92; bf16 output runs
+// faster on the warp-rows layout kernel, 0.99 vs 0.95, and always takes it).
 constexpr int64_t kStreamMinRowsPerSm = 2048;
 
 
