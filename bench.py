@@ -654,8 +654,9 @@ def run_ours(args, world, rank, local):
         "secondary_timing": "output_modes, fused_qkv, indexer_q and consumer_gemm: one event pair "
                             "around N back-to-back launches, mean per launch",
         "output_modes": {"kernel": "rq_inv_rope_quant_layout (heads_per_group 8): "
-                                   "inv_rope_fp8_quant_stream_kernel for fp8 / UE8M0, "
-                                   "inv_rope_quant_layout_kernel<1> for bf16",
+                                   "inv_rope_fp8_quant_kernel for token-major UE8M0, "
+                                   "inv_rope_fp8_quant_stream_kernel for group-major fp8 / "
+                                   "UE8M0, inv_rope_quant_layout_kernel<1> for bf16",
                          "launches_each": args.mode_launches,
                          "results": modes},
         "fused_qkv": fused,

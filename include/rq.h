@@ -272,7 +272,13 @@ typedef enum rq_out_mode {
  *
  * Outputs that overlap give unspecified bytes. Positions outside
  * [0, cache_rows) are skipped and flagged as in rq_inv_rope_fp8_quant.
- * Runs one persistent warp-per-row kernel with per-thread stores.
+ * The kernel is chosen from the layout, the mode and the size; all choices
+ * write the same bytes. Row-linear token-major quantised outputs (head r =
+ * t*H + h at out + r*512, its scales at r*4 or its word at r) take the
+ * warp-rows kernel of rq_inv_rope_fp8_quant. Other quantised layouts take the
+ * TMA-ring kernel from 2048 rows per SM when heads_per_group is a multiple of
+ * 8, and the warp-rows layout kernel otherwise. bf16 output always takes the
+ * warp-rows layout kernel.
  */
 rq_status rq_inv_rope_quant_layout(const void *x_bf16, int64_t n_tokens, int64_t n_heads,
                                    int64_t x_stride_token, int64_t x_stride_head,

@@ -233,6 +233,18 @@ RQ_EXPORT rq_status rq_inv_rope_quant_layout(
     p.lay.st = scale_stride_token;
     p.lay.sg = scale_stride_group;
     p.lay.se = scale_stride_elem;
+    // A quantising layout that is row-linear (token-major, contiguous: head r =
+    // t*H + h at out + r*512, its scales at r*4 or its word at r) takes the
+    // warp-rows kernel of rq_inv_rope_fp8_quant with that scale encoding.
+    const int64_t groups = n_heads / heads_per_group;
+    const int64_t spe = out_mode == RQ_OUT_FP8_SCALE_F32 ? 4 : 1;  // scale elements per head
+    const bool row_linear =
+        quant && out_stride_token == n_heads * rq::kHeadDimABI &&
+        (groups == 1 || out_stride_group == heads_per_group * rq::kHeadDimABI) &&
+        scale_stride_elem == 1 && scale_stride_token == n_heads * spe &&
+        (groups == 1 || scale_stride_group == heads_per_group * spe) && aligned(scales, 16);
+    if (row_linear)
+        return from_cuda(rq::launch_inv_rope_rows(p, dev, out_mode, static_cast<cudaStream_t>(stream)));
     // large calls whose tiles fit the layout take the TMA-ring kernel
     // bf16 output (no quantisation) stays on the warp-rows layout kernel at every size
     const bool stream_it = p.lay.mode != rq::kOutBf16 &&

@@ -21,8 +21,11 @@ namespace rq {
 // RoPE page, S1 (head h = g*hpg + i of token t at row (t, g), offset i*512),
 // so the grouping never changes an address.
 // Held to 4 CTAs per SM (64 registers), measured 1% faster than the
-// compiler's free choice of 73 registers (3 CTAs).
-template <int kRows>
+// compiler's free choice of 73 registers (3 CTAs). kMode picks the scale
+// encoding: fp32 scales at scales + r*4, or (kOutFp8Ue8m0) one packed UE8M0
+// word per row at scales + r -- the row-linear token-major layouts of the
+// layout call, which takes this kernel for them.
+template <int kRows, int kMode = kOutFp8F32>
 __global__ void __launch_bounds__(kInvThreads, 4)
 inv_rope_fp8_quant_kernel(InvParams p) {
     pdl_wait();
@@ -77,7 +80,18 @@ inv_rope_fp8_quant_kernel(InvParams p) {
             const int64_t r = int64_t(r0) + i;
             float scale;
             const uint4 q = rope_quant_row<true>(a[i], b[i], rope_lane, c[i], s[i], p.eps, &scale);
-            store_row(p.out + r * kHeadDim, p.scales + r * 4, lane, ca, q, scale);
+            if (kMode == kOutFp8F32) {
+                store_row(p.out + r * kHeadDim, p.scales + r * 4, lane, ca, q, scale);
+            } else {
+                uint8_t* codes = p.out + r * kHeadDim;
+                st_stream8(codes + 8 * ca, q.x, q.y);
+                st_stream8(codes + 8 * (ca + 8), q.z, q.w);
+                // byte b of row r's word: block b's biased exponent
+                if ((lane & 7) == 0)
+                    st_stream1(reinterpret_cast<uint8_t*>(reinterpret_cast<uint32_t*>(p.scales) + r) +
+                                   (lane >> 3),
+                               __float_as_uint(scale) >> 23);
+            }
         }
     }
 }
@@ -352,7 +366,7 @@ namespace {
 // variant (thread-local: no locking on the launch path).
 constexpr int kMaxDevices = 64;
 // (kLay: 2 entries per output mode, one row or two rows per warp)
-enum Variant { kInv1, kInv2, kIns1, kFus1, kLay, kVariants = kLay + 6 };
+enum Variant { kInv1, kInv2, kInvU1, kInvU2, kIns1, kFus1, kLay, kVariants = kLay + 6 };
 
 template <typename K>
 int resident_blocks(int device, Variant v, K kernel, int threads) {
@@ -413,6 +427,22 @@ cudaError_t launch_layout(const InvParams& p, const DeviceInfo& dev, cudaStream_
     }
     auto k = inv_rope_quant_layout_kernel<1, kMode>;
     const int res = resident_blocks(dev.ordinal, Variant(kLay + 2 * kMode), k, kInvThreads);
+    return launch_pdl(k, grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0,
+                      stream, p);
+}
+
+cudaError_t launch_inv_rope_rows(const InvParams& p, const DeviceInfo& dev, int mode,
+                                 cudaStream_t stream) {
+    if (mode == kOutFp8F32) return launch_inv_rope_fp8_quant(p, dev, kInvWarpRows, stream);
+    constexpr int kWarps = kInvThreads / 32;
+    if (int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4) {
+        auto k = inv_rope_fp8_quant_kernel<2, kOutFp8Ue8m0>;
+        const int res = resident_blocks(dev.ordinal, kInvU2, k, kInvThreads);
+        return launch_pdl(k, grid_size(p.n_rows, kWarps * 2, dev.sm_count, res), kInvThreads, 0,
+                          stream, p);
+    }
+    auto k = inv_rope_fp8_quant_kernel<1, kOutFp8Ue8m0>;
+    const int res = resident_blocks(dev.ordinal, kInvU1, k, kInvThreads);
     return launch_pdl(k, grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0,
                       stream, p);
 }
