@@ -198,9 +198,9 @@ constexpr int64_t kStreamMinRowsPerSm = 2048;
 
 cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev, int variant,
                                       cudaStream_t stream);
-// The inverse op into a row-linear layout (head r's codes at out + r*512; its
+// The inverse op into a row-linear layout (row r's codes at out + r*512; its
 // scales at scales + r*4 (fp32) or its packed UE8M0 word at scales + r), on
-// the warp-rows kernel. mode: kOutFp8F32 or kOutFp8Ue8m0.
+// the warp-rows kernel. mode: kOutFp8F32 or kOutFp8Ue8m0. Row r = t*H + h.
 cudaError_t launch_inv_rope_rows(const InvParams& p, const DeviceInfo& dev, int mode,
                                  cudaStream_t stream);
 cudaError_t launch_inv_rope_quant_layout(const InvParams& p, const DeviceInfo& dev,
