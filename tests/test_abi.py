@@ -330,3 +330,38 @@ def test_validate_rejects_bad_arguments(lib, kw, status):
 
 def test_validate_empty_batch_reports_nothing(lib):
     assert _val(lib, n=0, pos=None, slots=None, ws=None) == (RQ_OK, 0)
+
+
+def test_header_is_plain_c_and_links(tmp_path, lib):
+    """include/rq.h compiles as C99 (no C++ in the ABI) and a C program linked
+    against librq.so calls the entry points that need no GPU."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi_check.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "rq.h"
+int main(void) {
+    uint32_t flags = 123;
+    int64_t ws = rq_validate_indices_workspace(64);
+    rq_status st = rq_validate_indices(NULL, NULL, 0, 16, 0, NULL, 0, &flags, NULL);
+    printf("%d %s %lld %d %u\n", rq_version() >> 16, rq_status_string(RQ_ERR_ALIGN),
+           (long long)ws, (int)st, flags);
+    return rq_inv_rope_fp8_quant(NULL, -1, 1, 0, 0, NULL, NULL, 1, 1, 1e-10f, NULL, NULL, NULL,
+                                 NULL) == RQ_ERR_SHAPE ? 0 : 1;
+}
+""")
+    exe = tmp_path / "abi_check"
+    libdir = os.path.dirname(rq.LIB_PATH)
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), "-L", libdir,
+                        "-lrq", f"-Wl,-rpath,{libdir}", "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    major, *rest = out.stdout.split()
+    assert major == "1" and out.stdout.split()[-3:] == ["32", "0", "0"]
