@@ -1,7 +1,10 @@
-// rq_kernels.cu -- sm_103a kernels of the inverse-RoPE + block-FP8 quant op
-// and of its forward-RoPE + paged-insert sibling, with their launchers.
+// rq_kernels.cu -- the warp-rows kernels (sm_103a) and their launchers: the
+// inverse-RoPE + block-FP8 quant op (also into row-linear UE8M0 layouts), the
+// same op into any strided layout or as bf16, its forward-RoPE + paged-insert
+// sibling, and the fused q RMS norm + RoPE + kv insert op. (The TMA-ring
+// variant of the inverse op is in rq_stream.cu.)
 //
-// Both are HBM-bound streams (about 1.5 bytes moved per fp32 op), so the
+// All are HBM-bound streams (about 1.5 bytes moved per fp32 op), so the
 // design goal is bytes in flight, not arithmetic: a persistent grid of warps
 // sized to the SM count, each warp owning whole 512-wide rows
 // (rq_device.cuh) and issuing the loads of kRows rows before it computes any
