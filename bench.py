@@ -161,7 +161,7 @@ class ClockSampler:
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
             self.nv = pynvml
         except Exception as e:
-            self.error = f"nvml: {type(e).__name__}"
+            self.error = f"nvml: {type(e).__name__}: {e}"
 
     def _run_nvml(self):
         nv = self.nv
@@ -191,7 +191,7 @@ class ClockSampler:
                 self._thread = threading.Thread(target=self._read_smi, daemon=True)
                 self._thread.start()
             except Exception as e:
-                self.error = f"nvidia-smi: {type(e).__name__}"
+                self.error = (self.error or "") + f"; nvidia-smi: {type(e).__name__}: {e}"
         return self
 
     def _read_smi(self):
@@ -242,31 +242,74 @@ def make_inputs(inv_tokens=None):
     return inv, ins
 
 
+def oracle_step_rate(inv, ins, tokens, steps, warmup, threads):
+    """Warm mean of `steps` oracle steps (after `warmup` untimed ones) over the
+    first `tokens` tokens of both ops: (GB/s of the step's algorithmic bytes,
+    seconds per step). The one method behind cpu_baseline and the reference arm."""
+    import oracle
+    oracle.build()
+    xi, pi = inv["x"][:tokens].contiguous(), inv["positions"][:tokens].contiguous()
+    kv, kp, sl = (ins["kv"][:tokens].contiguous(), ins["positions"][:tokens].contiguous(),
+                  ins["slot_mapping"][:tokens].contiguous())
+    cache = inv["cos_sin_cache"]
+    sample_bytes = W.inverse_bytes(tokens, inv["x"].shape[1]) + W.insert_bytes(tokens)
+
+    def step():
+        oracle.inv_rope_fp8_quant(xi, pi, cache, inv["heads_per_group"], threads=threads)
+        oracle.rope_fp8_quant_insert(kv, kp, cache, sl, ins["k_cache"], ins["block_size"],
+                                     threads=threads)
+
+    for _ in range(warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = (time.perf_counter() - t0) / steps
+    return sample_bytes / dt / 1e9, dt
+
+
 def cpu_baseline(inv, ins):
-    """The oracle, as it stands, on the host cores over one full step of the workload."""
+    """The oracle, as it stands, on all host cores: the warm mean of 3 full
+    steps after one untimed step (the reference arm's method), plus the inverse
+    alone on one core over a quarter of the tokens (warm)."""
     import oracle
     threads = os.cpu_count() or 1
-    oracle.build()
-    t0 = time.perf_counter()
-    oracle.inv_rope_fp8_quant(inv["x"], inv["positions"], inv["cos_sin_cache"],
-                              inv["heads_per_group"], threads=threads)
-    oracle.rope_fp8_quant_insert(ins["kv"], ins["positions"], ins["cos_sin_cache"],
-                                 ins["slot_mapping"], ins["k_cache"], ins["block_size"],
-                                 threads=threads)
-    dt = time.perf_counter() - t0
-    # single-threaded on a quarter of the inverse's tokens (bytes scaled to match)
-    q = inv["x"].shape[0] // 4
+    tokens = inv["x"].shape[0]
+    gbs, dt = oracle_step_rate(inv, ins, tokens, steps=3, warmup=1, threads=threads)
+    q = tokens // 4
+    xq, pq = inv["x"][:q].contiguous(), inv["positions"][:q].contiguous()
+    oracle.inv_rope_fp8_quant(xq[:256], pq[:256], inv["cos_sin_cache"], inv["heads_per_group"],
+                              threads=1)
     t1 = time.perf_counter()
-    oracle.inv_rope_fp8_quant(inv["x"][:q], inv["positions"][:q], inv["cos_sin_cache"],
-                              inv["heads_per_group"], threads=1)
+    oracle.inv_rope_fp8_quant(xq, pq, inv["cos_sin_cache"], inv["heads_per_group"], threads=1)
     dt1 = time.perf_counter() - t1
     one_bytes = W.inverse_bytes(q, inv["x"].shape[1])
-    return {"value": round(STEP_BYTES / dt / 1e9, 3), "unit": "GB/s", "cores": threads,
-            "kind": "oracle", "seconds": round(dt, 3),
-            "sample": "one full step: inverse 16384 tok x 32 heads + insert 16384 tok",
-            "single_thread": {"value": round(one_bytes / dt1 / 1e9, 3), "unit": "GB/s",
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seconds_per_step": round(dt, 4),
+            "sample": f"one full step (inverse {tokens} tok x {inv['x'].shape[1]} heads + insert "
+                      f"{tokens} tok), warm mean of 3 steps after 1 untimed; oracle with "
+                      f"{threads} threads",
+            "single_thread": {"value": round(one_bytes / dt1 / 1e9, 4), "unit": "GB/s",
                               "cores": 1, "seconds": round(dt1, 3),
-                              "sample": f"inverse only, {q} tokens x 32 heads"}}
+                              "sample": f"inverse only, {q} tokens x {inv['x'].shape[1]} heads, "
+                                        "after a warm call"}}
+
+
+def block_stream(stream, ms: float):
+    """Keep `stream` busy for about `ms` milliseconds (a spinning kernel), so
+    that the host enqueues the launches that follow before the device reaches
+    them: events recorded after it then time device work only, not the host's
+    launch rate (the blocking-kernel method of GPU benchmark harnesses)."""
+    clock_hz = 2.0e9
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(ms * 1e-3 * clock_hz))
+
+
+def host_us_per_call(fn, calls: int = 3) -> float:
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        fn()
+    return (time.perf_counter() - t0) / calls * 1e6
 
 
 def run_ours(args, world, rank, local):
@@ -276,6 +319,7 @@ def run_ours(args, world, rank, local):
     inv_h, ins_h = make_inputs(args.inv_tokens)
     inv_bytes = W.inverse_bytes(inv_h["x"].shape[0], inv_h["x"].shape[1])
     step_bytes = inv_bytes + INS_BYTES
+    peak, peak_src = measured_peaks()
 
     # device-resident inputs and caller-owned outputs
     x = inv_h["x"].to(dev)
@@ -292,58 +336,24 @@ def run_ours(args, world, rank, local):
     bs = ins_h["block_size"]
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def inverse_call():
         rq.inv_rope_fp8_quant(x, pos, cache, hpg, out=out, scales=scales)
+
+    def insert_call():
         rq.rope_fp8_quant_insert(kv, kpos, cache, slots, k_cache, bs)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize(dev)
-
-    # per-launch timing of the dominant kernel (events on the launching stream)
-    inv_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    ins_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    with sampler:
-        # the timed steps: one event pair around all of them, so nothing sits
-        # between the launches (the insert may start while the inverse drains)
-        start.record(stream)
-        for i in range(args.steps):
-            step()
-        end.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        # the same steps again with an event pair around each launch: the
-        # per-kernel durations (roofline, percentiles, insert time)
-        for i in range(args.steps):
-            inv_ev[i][0].record(stream)
-            rq.inv_rope_fp8_quant(x, pos, cache, hpg, out=out, scales=scales)
-            inv_ev[i][1].record(stream)
-            rq.rope_fp8_quant_insert(kv, kpos, cache, slots, k_cache, bs)
-            ins_ev[i].record(stream)
-        torch.cuda.synchronize(dev)
-    barrier(world)
-    total_ms = max_over_ranks(start.elapsed_time(end), world)
-    inv_ms = statistics.fmean(a.elapsed_time(b) for a, b in inv_ev)
-    inv_all = sorted(a.elapsed_time(b) for a, b in inv_ev)
-    inv_ms_med = statistics.median(inv_all)
-    inv_pct = {f"p{q}": round(inv_all[min(len(inv_all) - 1, int(len(inv_all) * q / 100))] * 1e3, 2)
-               for q in (10, 50, 90, 99)}
-    inv_pct["max"] = round(inv_all[-1] * 1e3, 2)
-    ins_ms = statistics.fmean(inv_ev[i][1].elapsed_time(ins_ev[i]) for i in range(args.steps))
-    ms_step = total_ms / args.steps
+    def step():
+        inverse_call()
+        insert_call()
 
     def span_us(fn, launches):
-        """Mean µs per launch of `launches` back-to-back calls, one event pair
-        around all of them on the launching stream (after 3 warm calls)."""
-        for _ in range(3):
-            fn()
+        """Mean µs per launch of `launches` back-to-back calls: one event pair
+        around all of them on the launching stream, after 3 warm calls, with
+        the stream held by a spinning kernel while the host enqueues them."""
+        host = host_us_per_call(fn, 3)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
+        block_stream(stream, 1.0 + 1.5e-3 * host * launches)
         a.record(stream)
         for _ in range(launches):
             fn()
@@ -351,199 +361,402 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize(dev)
         return a.elapsed_time(b) * 1e3 / launches
 
-    # the "next" rows of the path (other output kinds and layouts), outside the
-    # step's timed region, each as back-to-back launches
+    # clocks are sampled (read only) from before the warm-up to the end of the
+    # last GPU leg, so every leg, the timed steps included, lies inside
+    sampler = ClockSampler(local)
+    with sampler:
+        warm = max(3, args.warmup)
+        t_w = time.perf_counter()
+        for _ in range(warm):
+            step()
+        torch.cuda.synchronize(dev)
+        # at least ~0.25 s of steps before timing (bounded), so clocks and
+        # power settle; the count above is the contract's minimum
+        extra = 0
+        while time.perf_counter() - t_w < 0.25 and extra < 4000:
+            for _ in range(20):
+                step()
+            extra += 20
+            torch.cuda.synchronize(dev)
+        host_step_us = host_us_per_call(step, 3)
+        torch.cuda.synchronize(dev)
+
+        # the timed steps: one event pair around all of them, nothing between
+        # the launches (the insert may start while the inverse drains), and the
+        # launches enqueued while a spinning kernel holds the stream
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        block_stream(stream, 1.0 + min(200.0, 1.5e-3 * host_step_us * args.steps))
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        total_ms = max_over_ranks(start.elapsed_time(end), world)
+        ms_step = total_ms / args.steps
+
+        # the dominant kernel back to back (its mean launch duration in a
+        # stream of launches: the roofline's figure), and the insert alone
+        span_launches = max(50, min(300, args.steps))
+        inv_span = span_us(inverse_call, span_launches)
+        ins_span = span_us(insert_call, span_launches)
+
+        # the same steps with an event pair around each launch: the per-launch
+        # durations including each launch's own start-up and drain (no overlap
+        # with a neighbour), their percentiles
+        ev_steps = max(10, min(args.steps, 200))
+        inv_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(ev_steps)]
+        ins_ev = [torch.cuda.Event(enable_timing=True) for _ in range(ev_steps)]
+        torch.cuda.synchronize(dev)
+        block_stream(stream, 1.0 + min(200.0, 1.5e-3 * host_step_us * ev_steps))
+        for i in range(ev_steps):
+            inv_ev[i][0].record(stream)
+            inverse_call()
+            inv_ev[i][1].record(stream)
+            insert_call()
+            ins_ev[i].record(stream)
+        torch.cuda.synchronize(dev)
+        inv_all = sorted(a.elapsed_time(b) for a, b in inv_ev)
+        inv_ms_ev = statistics.fmean(inv_all)
+        inv_pct = {f"p{q}": round(inv_all[min(len(inv_all) - 1, int(len(inv_all) * q / 100))] * 1e3, 2)
+                   for q in (10, 50, 90, 99)}
+        inv_pct["max"] = round(inv_all[-1] * 1e3, 2)
+        ins_ms_ev = statistics.fmean(inv_ev[i][1].elapsed_time(ins_ev[i]) for i in range(ev_steps))
+
+        secondary = {}
+        if world == 1 and args.mode_launches > 0:
+            secondary = run_secondary(args, rq, dev, stream, inv_h, x, pos, cache, hpg, out, scales,
+                                      kv, kpos, slots, k_cache, bs, span_us, peak)
+
+        e2e = run_e2e(args, rq, dev, stream, world, inv_h, ins_h, cache, hpg, out, scales, kv,
+                      kpos, slots, k_cache, bs)
+
+    achieved = inv_bytes / (inv_span * 1e-6) / 1e9
+    achieved_ev = inv_bytes / (inv_ms_ev * 1e-3) / 1e9
+    traffic = _committed_traffic()
+    target_gbs = 6400.0  # 80% of the nominal ~8 TB/s
+    result = {
+        "metric": METRIC,
+        "value": round(world * step_bytes / (ms_step * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": warm,
+        "ms_per_step": round(ms_step, 5),
+        "us_per_step": round(ms_step * 1e3, 2),
+        "inverse_span_us": round(inv_span, 2),
+        "inverse_span_GBs": round(achieved, 1),
+        "inverse_span_frac_of_measured_peak": round(achieved / peak, 4),
+        "inverse_span_frac_of_6400_target": round(achieved / target_gbs, 4),
+        "insert_span_us": round(ins_span, 2),
+        "insert_span_frac_of_measured_peak": round(INS_BYTES / ins_span / 1e3 / peak, 4),
+        "span_launches": span_launches,
+        "inverse_us_event_pair": round(inv_ms_ev * 1e3, 2),
+        "inverse_us_event_pair_percentiles": inv_pct,
+        "insert_us_event_pair": round(ins_ms_ev * 1e3, 2),
+        "timing": "value / ms_per_step: the K timed steps under one event pair, enqueued while "
+                  "a spinning kernel held the stream; *_span_us: mean per launch of back-to-back "
+                  "launches under one event pair (same enqueue method); *_event_pair: an event "
+                  "pair around every launch (each launch's own start-up and drain, no overlap)",
+        "frac_of_nominal_8tbs": round(step_bytes / (ms_step * 1e-3) / 8e12, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in, fp32 math, e4m3 out",
+        "data": "synthetic (seeded: randn + 1% x50 outliers, bf16)",
+        "config": {
+            "workload": "prefill16k inverse RoPE+FP8 quant (N=16384,H=32,hpg=8,D=512) "
+                        "+ insert16k forward RoPE+FP8 paged insert (N=16384, 512x64 slots)",
+            "bytes_per_step": step_bytes,
+            "inverse_bytes": inv_bytes,
+            "insert_bytes": INS_BYTES,
+            "l2": f"inputs larger than L2: {step_bytes / 2**20:.0f} MiB streamed per step "
+                  f"vs {L2_BYTES / 2**20:.0f} MiB L2",
+            "parallelism": f"replicas x{world} (each rank its own full step)",
+        },
+        "roofline": {
+            "kernel": INV_KERNEL_NAME,
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                           else "fallback 6.4 TB/s",
+            "algorithmic_bytes_per_launch": inv_bytes,
+            "duration": f"mean launch duration of {span_launches} back-to-back launches "
+                        "(inverse_span_us)",
+            "event_pair_per_launch": {"achieved": round(achieved_ev, 1),
+                                      "frac": round(achieved_ev / peak, 4)},
+        },
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(),
+    }
+    result.update(secondary)
+    if args.inv_tokens and args.inv_tokens != INV_SPEC.n_tokens:
+        result["config"]["workload"] = (f"profiling case: inverse N={args.inv_tokens},H=32,hpg=8 "
+                                        "+ insert16k (not the benchmarked configuration)")
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(inv_h, ins_h)
+    return result
+
+
+def run_secondary(args, rq, dev, stream, inv_h, x, pos, cache, hpg, out, scales, kv, kpos, slots,
+                  k_cache, bs, span_us, peak):
+    """The other configurations and the "next" rows of the path, each timed
+    outside the step: config 4 (irregular grouping), the output kinds and
+    layouts, the fused q/kv op, the indexer q op, the consumer GEMMs, decode
+    latency and the L2-resident configurations cold. One GPU only."""
+    n, h = x.shape[0], x.shape[1]
+    res = {"secondary_timing": "back-to-back launches under one event pair, mean per launch "
+                               "(span_us), unless a leg says otherwise"}
+
+    # config 4: irregular grouping (N=8192, H=24, heads_per_group=6)
+    ii = W.inverse_inputs(W.IRREGULAR)
+    ix, ip, ic = ii["x"].to(dev), ii["positions"].to(dev), ii["cos_sin_cache"].to(dev)
+    ihpg = ii["heads_per_group"]
+    io = torch.empty((ix.shape[0], ix.shape[1] // ihpg, ihpg * 512), dtype=torch.uint8, device=dev)
+    isc = torch.empty((ix.shape[0], ix.shape[1] // ihpg, ihpg * 4), dtype=torch.float32, device=dev)
+    us = span_us(lambda: rq.inv_rope_fp8_quant(ix, ip, ic, ihpg, out=io, scales=isc),
+                 args.mode_launches)
+    ib = W.inverse_bytes(ix.shape[0], ix.shape[1])
+    res["irregular"] = {"kernel": INV_KERNEL_NAME, "workload": "irregular (N=8192, H=24, "
+                        "heads_per_group=6, positions U[0,32768), cache 32768 rows)",
+                        "us": round(us, 2), "bytes": ib, "GBs": round(ib / us / 1e3, 1),
+                        "frac_of_measured_peak": round(ib / us / 1e3 / peak, 4),
+                        "frac_of_6400_target": round(ib / us / 1e3 / 6400.0, 4),
+                        "launches": args.mode_launches}
+    del ix, ip, ic, io, isc
+
+    # the "next" rows of the path: other output kinds and layouts
     modes = {}
-    for name, mode, gm in ((("fp8_group_major", "fp8", True), ("ue8m0", "ue8m0", False),
-                            ("ue8m0_group_major", "ue8m0", True), ("bf16", "bf16", False))
-                           if args.mode_launches > 0 else ()):
+    for name, mode, gm in (("fp8_group_major", "fp8", True), ("ue8m0", "ue8m0", False),
+                           ("ue8m0_group_major", "ue8m0", True), ("bf16", "bf16", False)):
         mo, ms = rq.empty_outputs(n, h // hpg, hpg, mode, group_major=gm, device=dev)
         us = span_us(lambda: rq.inv_rope_quant(x, pos, cache, hpg, mode=mode, out=mo, scales=ms),
                      args.mode_launches)
         mb = W.inverse_bytes(n, h, mode)
         modes[name] = {"us": round(us, 2), "bytes": mb, "GBs": round(mb / us / 1e3, 1),
-                       "frac_of_measured_peak": round(mb / us / 1e3 / measured_peaks()[0], 4)}
+                       "frac_of_measured_peak": round(mb / us / 1e3 / peak, 4)}
         del mo, ms
+    res["output_modes"] = {"call": "rq_inv_rope_quant_layout (heads_per_group 8)",
+                           "launches_each": args.mode_launches, "results": modes}
 
     # the fused q/kv op (q RMS norm + RoPE into a padded q_out, with the kv insert)
-    fused = None
-    if args.mode_launches > 0:
-        fi = W.fused_inputs(W.FUSED16K, cache=inv_h["cos_sin_cache"])
-        fq, fkv = fi["q"].to(dev), fi["kv"].to(dev)
-        fpos, fsl, fkc = fi["positions"].to(dev), fi["slot_mapping"].to(dev), fi["k_cache"].to(dev)
-        fqo = torch.empty((fq.shape[0], fi["q_head_padded"], 512), dtype=torch.bfloat16, device=dev)
-
-        def fused_call():
-            rq.qnorm_rope_kv_rope_quant_insert(fq, fkv, fpos, cache, fsl, fkc, fi["block_size"],
-                                               fi["q_head_padded"], q_out=fqo)
-        us = span_us(fused_call, args.mode_launches)
-        fw = W.norm_weight(W.FUSED16K.seed).to(dev)
-
-        def fused_weighted_call():
-            rq.qnorm_rope_kv_rope_quant_insert(fq, fkv, fpos, cache, fsl, fkc, fi["block_size"],
-                                               fi["q_head_padded"], q_out=fqo, norm_weight=fw)
-        us_w = span_us(fused_weighted_call, args.mode_launches)
-        fb = W.fused_bytes(W.FUSED16K.n_tokens, W.FUSED16K.n_heads_q, W.FUSED16K.q_head_padded)
-        fused = {"kernel": "qnorm_rope_kv_insert_kernel", "workload": "fused16k (N=16384, Hq=32 "
-                 "padded to 64, kv into 512x64 slots)", "us": round(us, 2), "bytes": fb,
-                 "GBs": round(fb / us / 1e3, 1),
-                 "frac_of_measured_peak": round(fb / us / 1e3 / measured_peaks()[0], 4),
-                 "with_norm_weight": {"us": round(us_w, 2),
-                                      "frac_of_measured_peak":
-                                          round(fb / us_w / 1e3 / measured_peaks()[0], 4),
-                                      "what": "synthetic bf16 RMSNorm weight [512] on q"},
-                 "launches": args.mode_launches}
-        del fq, fkv, fpos, fsl, fkc, fqo, fw
+    fi = W.fused_inputs(W.FUSED16K, cache=inv_h["cos_sin_cache"])
+    fq, fkv = fi["q"].to(dev), fi["kv"].to(dev)
+    fpos, fsl, fkc = fi["positions"].to(dev), fi["slot_mapping"].to(dev), fi["k_cache"].to(dev)
+    fqo = torch.empty((fq.shape[0], fi["q_head_padded"], 512), dtype=torch.bfloat16, device=dev)
+    fw = W.norm_weight(W.FUSED16K.seed).to(dev)
+    us = span_us(lambda: rq.qnorm_rope_kv_rope_quant_insert(
+        fq, fkv, fpos, cache, fsl, fkc, fi["block_size"], fi["q_head_padded"], q_out=fqo),
+        args.mode_launches)
+    us_w = span_us(lambda: rq.qnorm_rope_kv_rope_quant_insert(
+        fq, fkv, fpos, cache, fsl, fkc, fi["block_size"], fi["q_head_padded"], q_out=fqo,
+        norm_weight=fw), args.mode_launches)
+    fb = W.fused_bytes(W.FUSED16K.n_tokens, W.FUSED16K.n_heads_q, W.FUSED16K.q_head_padded)
+    res["fused_qkv"] = {"kernel": "qnorm_rope_kv_insert_kernel", "workload": "fused16k (N=16384, "
+                        "Hq=32 padded to 64, kv into 512x64 slots)", "us": round(us, 2),
+                        "bytes": fb, "GBs": round(fb / us / 1e3, 1),
+                        "frac_of_measured_peak": round(fb / us / 1e3 / peak, 4),
+                        "with_norm_weight": {"us": round(us_w, 2),
+                                             "frac_of_measured_peak":
+                                                 round(fb / us_w / 1e3 / peak, 4),
+                                             "what": "synthetic bf16 RMSNorm weight [512] on q"},
+                        "launches": args.mode_launches}
+    del fq, fkv, fpos, fsl, fkc, fqo, fw
 
     # the indexer q op (RoPE through bf16 + per-head FP8 + scale fold)
-    indexer = None
-    if args.mode_launches > 0:
-        ii = W.indexer_inputs(W.INDEXER16K, cache=inv_h["cos_sin_cache"])
-        iq, iw, ipos = ii["q"].to(dev), ii["weights"].to(dev), ii["positions"].to(dev)
-        ico = torch.empty((iq.shape[0], iq.shape[1], 128), dtype=torch.uint8, device=dev)
-        iwo = torch.empty((iq.shape[0], iq.shape[1]), dtype=torch.float32, device=dev)
-        indexer = {}
-        for style in ("neox", "gptj"):
-            def idx_call():
-                rq.indexer_q_rope_quant(iq, ipos, cache, iw, ii["softmax_scale"], ii["head_scale"],
-                                        rope_style=style, out=ico, weights_out=iwo)
-            us = span_us(idx_call, args.mode_launches)
-            ib = W.indexer_bytes(W.INDEXER16K.n_tokens, W.INDEXER16K.n_heads)
-            indexer[style] = {"us": round(us, 2), "bytes": ib, "GBs": round(ib / us / 1e3, 1),
-                              "frac_of_measured_peak": round(ib / us / 1e3 / measured_peaks()[0], 4)}
-        indexer = {"kernel": "indexer_q_rope_quant_kernel", "workload": "indexer16k (N=16384, "
-                   "H=64, head 128, dims 0..63 rotary)", "launches_each": args.mode_launches,
-                   "results": indexer}
-        del iq, iw, ipos, ico, iwo
+    xi = W.indexer_inputs(W.INDEXER16K, cache=inv_h["cos_sin_cache"])
+    iq, iw, ipos = xi["q"].to(dev), xi["weights"].to(dev), xi["positions"].to(dev)
+    ico = torch.empty((iq.shape[0], iq.shape[1], 128), dtype=torch.uint8, device=dev)
+    iwo = torch.empty((iq.shape[0], iq.shape[1]), dtype=torch.float32, device=dev)
+    indexer = {}
+    ib = W.indexer_bytes(W.INDEXER16K.n_tokens, W.INDEXER16K.n_heads)
+    for style in ("neox", "gptj"):
+        us = span_us(lambda: rq.indexer_q_rope_quant(iq, ipos, cache, iw, xi["softmax_scale"],
+                                                     xi["head_scale"], rope_style=style, out=ico,
+                                                     weights_out=iwo), args.mode_launches)
+        indexer[style] = {"us": round(us, 2), "bytes": ib, "GBs": round(ib / us / 1e3, 1),
+                          "frac_of_measured_peak": round(ib / us / 1e3 / peak, 4)}
+    res["indexer_q"] = {"kernel": "indexer_q_rope_quant_kernel", "workload": "indexer16k "
+                        "(N=16384, H=64, head 128, dims 0..63 rotary)",
+                        "launches_each": args.mode_launches, "results": indexer}
+    del iq, iw, ipos, ico, iwo
 
-    # the consumer: grouped FP8 GEMM (wo_a-style) on the inverse op's own output,
-    # 4 groups x K = 4096, n_out = 1024 per group, tensor cores (tcgen05)
-    gemm = None
-    if args.mode_launches > 0:
-        g_out = 1024
-        gen = torch.Generator().manual_seed(7)
-        wc = torch.randint(0, 256, (h // hpg, g_out, hpg * 512), generator=gen,
-                           dtype=torch.int32).to(torch.uint8)
-        wc[(wc & 0x7F) == 0x7F] = 0x38
-        wc = wc.to(dev)
-        ws = (2.0 ** torch.randint(-10, -6, (h // hpg, g_out // 128, hpg * 4), generator=gen)
-              .float()).to(dev)
-        gy = torch.empty((n, h // hpg, g_out), dtype=torch.bfloat16, device=dev)
-        rq.inv_rope_fp8_quant(x, pos, cache, hpg, out=out, scales=scales)
+    res["consumer_gemm"] = gemm_leg(args, rq, dev, x, pos, cache, hpg, out, scales, span_us)
+    res["decode_latency"] = decode_leg(rq, dev, stream, inv_h, cache)
+    res["small_configs_cold"] = cold_leg(rq, dev, stream, inv_h, cache, kv, kpos, slots, k_cache, bs)
+    return res
 
-        def gemm_call():
-            rq.grouped_fp8_gemm(out, scales, wc, ws, out=gy)
-        gl = max(10, args.mode_launches // 6)
-        us = span_us(gemm_call, gl)
 
-        def fused_gemm_call():
-            rq.inv_rope_fp8_quant_gemm(x, pos, cache, hpg, wc, ws, out=gy)
-        us_fused = span_us(fused_gemm_call, gl)
+def gemm_leg(args, rq, dev, x, pos, cache, hpg, out, scales, span_us):
+    """The consumer of the op's output: grouped FP8 GEMM (wo_a-style), 4 groups
+    x K = 4096, n_out = 1024 per group, on the tensor cores (tcgen05). The
+    measured path of the row is the op's UE8M0 mode followed by the
+    block-scaled GEMM; the fp32-scale GEMM and the fused kernel are reported
+    beside it."""
+    n, h = x.shape[0], x.shape[1]
+    g_out = 1024
+    gen = torch.Generator().manual_seed(7)
+    wc = torch.randint(0, 256, (h // hpg, g_out, hpg * 512), generator=gen,
+                       dtype=torch.int32).to(torch.uint8)
+    wc[(wc & 0x7F) == 0x7F] = 0x38
+    wc = wc.to(dev)
+    ws = (2.0 ** torch.randint(-10, -6, (h // hpg, g_out // 128, hpg * 4), generator=gen)
+          .float()).to(dev)
+    gy = torch.empty((n, h // hpg, g_out), dtype=torch.bfloat16, device=dev)
+    gl = max(10, args.mode_launches // 6)
+    flop = 2.0 * n * h * 512 * g_out
+    fp8_peak, fp8_src = measured_tensor_peak_fp8()
 
-        # the same GEMM on the block-scaled MMA, fed by the op's UE8M0 mode
-        # (token-major packed words) and the weight scales as UE8M0 codes
-        mx_codes = torch.empty_like(out)
-        mx_words = torch.empty((n, h // hpg, hpg), dtype=torch.int32, device=dev)
+    def roof(us):
+        return {"bound": "tensor", "achieved": round(flop / us / 1e6, 1), "peak": fp8_peak,
+                "unit": "TFLOP/s", "frac": round(flop / us / 1e6 / fp8_peak, 4),
+                "peak_source": fp8_src}
+
+    # the row's path: the op writes token-major codes + packed UE8M0 words,
+    # the block-scaled MMA reads them as they are
+    mx_codes = torch.empty_like(out)
+    mx_words = torch.empty((n, h // hpg, hpg), dtype=torch.int32, device=dev)
+    w_sf = (torch.log2(ws).round().to(torch.int32) + 127).to(torch.uint8)
+
+    def op_ue8m0():
         rq.inv_rope_quant(x, pos, cache, hpg, mode="ue8m0", out=mx_codes, scales=mx_words)
-        w_sf = (torch.log2(ws).round().to(torch.int32) + 127).to(torch.uint8)
 
-        def mx_call():
-            rq.grouped_fp8_gemm_ue8m0(mx_codes, mx_words, wc, w_sf, out=gy)
-        us_mx = span_us(mx_call, gl)
-        del mx_codes, mx_words
-        flop = 2.0 * n * h * 512 * g_out
-        tf = flop / us / 1e6
-        fp8_peak, fp8_src = measured_tensor_peak_fp8()
-        gemm = {"kernel": "grouped_fp8_gemm_kernel", "workload": f"grouped FP8 GEMM: M={n}, "
-                f"G={h // hpg}, K={hpg * 512}, n_out={g_out} per group, block scales 1x128 / "
-                "128x128", "us": round(us, 2), "flop": flop,
-                "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": fp8_peak,
-                             "unit": "TFLOP/s", "frac": round(tf / fp8_peak, 4),
-                             "peak_source": fp8_src},
-                "fused": {"kernel": "fused_inv_rope_quant_gemm_kernel",
-                          "what": "inverse RoPE + block-FP8 quant produced inside the GEMM "
-                                  "from bf16 x (codes never reach HBM)",
-                          "us": round(us_fused, 2),
-                          "tflops": round(flop / us_fused / 1e6, 1),
-                          "frac": round(flop / us_fused / 1e6 / fp8_peak, 4),
-                          "unfused_op_plus_gemm_us": round(inv_ms * 1e3 + us, 2)},
-                "ue8m0": {"kernel": "grouped_fp8_gemm_ue8m0_kernel",
-                          "what": "UE8M0 block scales (the op's packed-scale output) applied "
-                                  "inside the block-scaled MMA (tcgen05 kind::mxf8f6f4)",
-                          "us": round(us_mx, 2),
-                          "roofline": {"bound": "tensor", "achieved": round(flop / us_mx / 1e6, 1),
-                                       "peak": fp8_peak, "unit": "TFLOP/s",
-                                       "frac": round(flop / us_mx / 1e6 / fp8_peak, 4),
-                                       "peak_source": fp8_src}},
-                "launches": gl}
-        del wc, ws, gy
+    def mx_call():
+        rq.grouped_fp8_gemm_ue8m0(mx_codes, mx_words, wc, w_sf, out=gy)
 
-    # decode-sized calls (N tokens x 32 heads): device time per call, taken from
-    # CUDA-graph replays of 100 back-to-back calls (host launch cost excluded)
-    decode = None
-    if args.mode_launches > 0:
-        decode = {}
-        for nt in W.DECODE_TOKENS:
-            di = W.inverse_inputs(W.decode_spec(nt), cache=inv_h["cos_sin_cache"])
-            dx, dp = di["x"].to(dev), di["positions"].to(dev)
-            do = torch.empty((nt, 4, 4096), dtype=torch.uint8, device=dev)
-            ds = torch.empty((nt, 4, 32), dtype=torch.float32, device=dev)
-            rq.inv_rope_fp8_quant(dx, dp, cache, 8, out=do, scales=ds)
-            torch.cuda.synchronize(dev)
-            g = torch.cuda.CUDAGraph()
-            gs = torch.cuda.Stream(dev)
-            gs.wait_stream(stream)
-            with torch.cuda.stream(gs):
-                with torch.cuda.graph(g, stream=gs):
-                    for _ in range(100):
-                        rq.inv_rope_fp8_quant(dx, dp, cache, 8, out=do, scales=ds)
+    op_ue8m0()
+    us_op = span_us(op_ue8m0, gl)
+    us_mx = span_us(mx_call, gl)
+    us_pair = span_us(lambda: (op_ue8m0(), mx_call()), gl)
+
+    rq.inv_rope_fp8_quant(x, pos, cache, hpg, out=out, scales=scales)
+    us = span_us(lambda: rq.grouped_fp8_gemm(out, scales, wc, ws, out=gy), gl)
+    us_fused = span_us(lambda: rq.inv_rope_fp8_quant_gemm(x, pos, cache, hpg, wc, ws, out=gy),
+                       max(5, gl // 4))
+    del mx_codes, mx_words, wc, ws, gy
+    return {"workload": f"grouped FP8 GEMM: M={n}, G={h // hpg}, K={hpg * 512}, n_out={g_out} "
+                        "per group, block scales 1x128 (A) / 128x128 (W)", "flop": flop,
+            "launches": gl,
+            "path": {"what": "the row's measured path: rq_inv_rope_quant_layout in UE8M0 mode "
+                             "(token-major) then rq_grouped_fp8_gemm_ue8m0 on its output",
+                     "op_us": round(us_op, 2), "gemm_us": round(us_mx, 2),
+                     "op_then_gemm_us": round(us_pair, 2)},
+            "ue8m0": {"kernel": "grouped_fp8_gemm_ue8m0_kernel",
+                      "what": "UE8M0 block scales (the op's packed-scale output) applied inside "
+                              "the block-scaled MMA (tcgen05 kind::mxf8f6f4)",
+                      "us": round(us_mx, 2), "roofline": roof(us_mx)},
+            "fp32_scales": {"kernel": "grouped_fp8_gemm_kernel",
+                            "what": "fp32 block scales folded per K tile in registers",
+                            "us": round(us, 2), "roofline": roof(us)},
+            "fused": {"kernel": "fused_inv_rope_quant_gemm_kernel",
+                      "what": "inverse RoPE + block-FP8 quant produced inside the fp32-scale GEMM "
+                              "from bf16 x (not the default: slower than op + GEMM)",
+                      "us": round(us_fused, 2), "roofline": roof(us_fused)}}
+
+
+def decode_leg(rq, dev, stream, inv_h, cache):
+    """Decode-sized calls (N tokens x 32 heads), hot: device time per call from
+    CUDA-graph replays of 100 back-to-back calls (host launch cost excluded)."""
+    decode = {}
+    for nt in W.DECODE_TOKENS:
+        di = W.inverse_inputs(W.decode_spec(nt), cache=inv_h["cos_sin_cache"])
+        dx, dp = di["x"].to(dev), di["positions"].to(dev)
+        do = torch.empty((nt, 4, 4096), dtype=torch.uint8, device=dev)
+        ds = torch.empty((nt, 4, 32), dtype=torch.float32, device=dev)
+        rq.inv_rope_fp8_quant(dx, dp, cache, 8, out=do, scales=ds)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(g, stream=gs):
+                for _ in range(100):
+                    rq.inv_rope_fp8_quant(dx, dp, cache, 8, out=do, scales=ds)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
             g.replay()
-            torch.cuda.synchronize(dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(5):
-                g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            decode[str(nt)] = round(e0.elapsed_time(e1) * 1e3 / 500, 2)
-        decode = {"workload": "decode: N tokens x 32 heads, heads_per_group 8, positions "
-                  "U[0,65536); graph of 100 calls, 5 replays", "us_per_call": decode}
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        decode[str(nt)] = round(e0.elapsed_time(e1) * 1e3 / 500, 2)
+    return {"workload": "decode: N tokens x 32 heads, heads_per_group 8, positions U[0,65536); "
+                        "graph of 100 calls, 5 replays", "us_per_call": decode}
 
-    # the configurations that fit in L2, cold: each call after a 256 MiB write
-    # that evicts L2, one event pair around the call (median of 20); the hot
-    # figures are the graph replays above and the in-step insert
-    small_cold = None
-    if args.mode_launches > 0:
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-        def cold_us(fn, reps=20):
-            fn()
-            ts = []
-            for r in range(reps):
-                flush.fill_(r & 0xFF)
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
+def cold_leg(rq, dev, stream, inv_h, cache, kv, kpos, slots, k_cache, bs, reps=20, rounds=7):
+    """The configurations that fit in L2, cold. Two CUDA graphs: `reps` x
+    (a 256 MiB write that evicts L2, then the call), and the same writes alone;
+    each is replayed `rounds` times under an event pair, and the cold time of
+    one call is (median with calls - median without) / reps. Launch overhead
+    inside a graph is that of a graph node, so the figure is device time."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            if fn is not None:
                 fn()
-                b.record(stream)
-                torch.cuda.synchronize(dev)
-                ts.append(a.elapsed_time(b) * 1e3)
-            return round(statistics.median(ts), 2)
-        small_cold = {}
-        ti = W.inverse_inputs(W.TINY)
-        tx, tp, tc = ti["x"].to(dev), ti["positions"].to(dev), ti["cos_sin_cache"].to(dev)
-        small_cold["tiny (N=64, H=8)"] = cold_us(
-            lambda: rq.inv_rope_fp8_quant(tx, tp, tc, ti["heads_per_group"]))
-        for nt in (1, 8, 64):
-            di = W.inverse_inputs(W.decode_spec(nt), cache=inv_h["cos_sin_cache"])
-            dx, dp = di["x"].to(dev), di["positions"].to(dev)
-            small_cold[f"decode N={nt}"] = cold_us(lambda: rq.inv_rope_fp8_quant(dx, dp, cache, 8))
-        small_cold["insert16k"] = cold_us(
-            lambda: rq.rope_fp8_quant_insert(kv, kpos, cache, slots, k_cache, bs))
-        small_cold = {"what": "median us per call after evicting L2 (cold); event pair around "
-                              "the call", "us": small_cold}
-        del flush
+            with torch.cuda.graph(g, stream=gs):
+                for r in range(reps):
+                    flush.fill_(r & 0xFF)
+                    if fn is not None:
+                        fn()
+        torch.cuda.synchronize(dev)
+        return g
 
-    # end to end through the public API from pinned host buffers
+    def timed(g):
+        g.replay()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(rounds):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    base = graph_of(None)
+    t_base = timed(base)
+    cases = {}
+    ti = W.inverse_inputs(W.TINY)
+    tx, tp, tc = ti["x"].to(dev), ti["positions"].to(dev), ti["cos_sin_cache"].to(dev)
+    cases["tiny (N=64, H=8)"] = lambda: rq.inv_rope_fp8_quant(tx, tp, tc, ti["heads_per_group"])
+    dec = {}
+    for nt in W.DECODE_TOKENS:
+        di = W.inverse_inputs(W.decode_spec(nt), cache=inv_h["cos_sin_cache"])
+        dec[nt] = (di["x"].to(dev), di["positions"].to(dev))
+    for nt in W.DECODE_TOKENS:
+        dx, dp = dec[nt]
+        cases[f"decode N={nt}"] = (lambda dx=dx, dp=dp: rq.inv_rope_fp8_quant(dx, dp, cache, 8))
+    cases["insert16k"] = lambda: rq.rope_fp8_quant_insert(kv, kpos, cache, slots, k_cache, bs)
+    us = {}
+    for name, fn in cases.items():
+        g = graph_of(fn)
+        us[name] = round((timed(g) - t_base) / reps, 2)
+        del g
+    del flush, base
+    return {"what": "device us per call after a 256 MiB write evicts L2: CUDA graphs of "
+                    f"{reps} x (write, call) minus {reps} x (write), median of {rounds} replays",
+            "flush_us": round(t_base / reps, 2), "us": us}
+
+
+def run_e2e(args, rq, dev, stream, world, inv_h, ins_h, cache, hpg, out, scales, kv, kpos, slots,
+            k_cache, bs):
+    """The same step end to end through the public API from pinned host buffers."""
     e2e_steps = args.e2e_steps or min(args.steps, 20)
     x_host = inv_h["x"].pin_memory()
     pos_host = inv_h["positions"].pin_memory()
@@ -555,11 +768,13 @@ def run_ours(args, world, rank, local):
     kc_host = torch.empty(k_cache.shape, dtype=torch.uint8).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (x_host, pos_host, kv_host, kpos_host, slots_host))
     d2h = sum(t.numel() * t.element_size() for t in (out_host, scales_host, kc_host))
+    step_bytes = W.inverse_bytes(inv_h["x"].shape[0], inv_h["x"].shape[1]) + INS_BYTES
 
     # the inverse op goes through the host-buffer C-ABI call (chunked copy-in /
     # kernel / copy-out pipeline inside the library); the insert's inputs are
     # copied in and the paged cache read back around its device call
-    ws = torch.empty(rq.host_workspace_bytes(h, args.e2e_chunk), dtype=torch.uint8, device=dev)
+    ws = torch.empty(rq.host_workspace_bytes(inv_h["x"].shape[1], args.e2e_chunk),
+                     dtype=torch.uint8, device=dev)
 
     # the insert (its copies, kernel and cache readback) runs on a second
     # stream, overlapping the inverse pipeline's transfers; both join the
@@ -589,89 +804,19 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
-
-    peak, peak_src = measured_peaks()
-    achieved = inv_bytes / (inv_ms * 1e-3) / 1e9
-    traffic = _committed_traffic()
-    result = {
-        "metric": METRIC,
-        "value": round(world * step_bytes / (ms_step * 1e-3) / 1e9, 2),
+    del ws
+    return {
+        "value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 3),
         "unit": "GB/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": max(3, args.warmup),
-        "ms_per_step": round(ms_step, 5),
-        "us_per_step": round(ms_step * 1e3, 2),
-        "inverse_us": round(inv_ms * 1e3, 2),
-        "inverse_us_median": round(inv_ms_med * 1e3, 2),
-        "inverse_us_percentiles": inv_pct,
-        "insert_us": round(ins_ms * 1e3, 2),
-        "per_launch_timing": "inverse_us, insert_us, percentiles and roofline.achieved come from "
-                             "a second pass of the same steps with an event pair around each "
-                             "launch; value and ms_per_step from the timed steps (one event pair "
-                             "around all of them)",
-        "frac_of_nominal_8tbs": round(step_bytes / (ms_step * 1e-3) / 8e12, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16 in, fp32 math, e4m3 out",
-        "data": "synthetic (seeded: randn + 1% x50 outliers, bf16)",
-        "config": {
-            "workload": "prefill16k inverse RoPE+FP8 quant (N=16384,H=32,hpg=8,D=512) "
-                        "+ insert16k forward RoPE+FP8 paged insert (N=16384, 512x64 slots)",
-            "bytes_per_step": step_bytes,
-            "inverse_bytes": inv_bytes,
-            "insert_bytes": INS_BYTES,
-            "l2": f"inputs larger than L2: {step_bytes / 2**20:.0f} MiB streamed per step "
-                  f"vs {L2_BYTES / 2**20:.0f} MiB L2",
-            "parallelism": f"replicas x{world} (each rank its own full step)",
-        },
-        "roofline": {
-            "kernel": INV_KERNEL_NAME,
-            "bound": "hbm",
-            "achieved": round(achieved, 1),
-            "peak": peak,
-            "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "traffic": traffic,
-            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                           else "fallback 6.4 TB/s",
-            "algorithmic_bytes_per_launch": inv_bytes,
-        },
-        "e2e": {
-            "value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 3),
-            "unit": "GB/s",
-            "ms_per_step": round(e2e_ms, 3),
-            "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h,
-            "steps": e2e_steps,
-            "path": "inverse: rq_inv_rope_fp8_quant_host (pinned host buffers; chunked copy-in / "
-                    "kernels / copy-out pipeline over a device workspace, "
-                    f"{args.e2e_chunk} tokens per chunk); insert, on a second stream: pinned "
-                    "host -> device copies, the device call, paged cache -> pinned host",
-        },
-        "gpu_launches": 2 * args.steps,
-        "secondary_timing": "output_modes, fused_qkv, indexer_q and consumer_gemm: one event pair "
-                            "around N back-to-back launches, mean per launch",
-        "output_modes": {"kernel": "rq_inv_rope_quant_layout (heads_per_group 8): "
-                                   "inv_rope_fp8_quant_kernel for token-major UE8M0, "
-                                   "inv_rope_fp8_quant_stream_kernel for group-major fp8 / "
-                                   "UE8M0, inv_rope_quant_layout_kernel<1> for bf16",
-                         "launches_each": args.mode_launches,
-                         "results": modes},
-        "fused_qkv": fused,
-        "indexer_q": indexer,
-        "decode_latency": decode,
-        "small_configs_cold": small_cold,
-        "consumer_gemm": gemm,
-        "clocks": sampler.summary(),
+        "ms_per_step": round(e2e_ms, 3),
+        "h2d_bytes_per_step": h2d,
+        "d2h_bytes_per_step": d2h,
+        "steps": e2e_steps,
+        "path": "inverse: rq_inv_rope_fp8_quant_host (pinned host buffers; chunked copy-in / "
+                "kernels / copy-out pipeline over a device workspace, "
+                f"{args.e2e_chunk} tokens per chunk); insert, on a second stream: pinned "
+                "host -> device copies, the device call, paged cache -> pinned host",
     }
-    if args.inv_tokens and args.inv_tokens != INV_SPEC.n_tokens:
-        result["config"]["workload"] = (f"profiling case: inverse N={args.inv_tokens},H=32,hpg=8 "
-                                        "+ insert16k (not the benchmarked configuration)")
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(inv_h, ins_h)
-    return result
 
 
 def _committed_traffic():
@@ -696,35 +841,21 @@ def _committed_traffic():
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, world, rank):
-    """The CPU oracle timed on the host cores, on a bounded sample per step."""
-    import oracle
-    oracle.build()
+    """The CPU oracle timed on the host cores, on a bounded sample per step
+    (the same warm-mean method as cpu_baseline)."""
     threads = os.cpu_count() or 1
     inv_h, ins_h = make_inputs()
-    total_steps = args.steps + max(3, args.warmup)
+    warm = max(3, args.warmup)
+    total_steps = args.steps + warm
     # ~13 us of CPU per (token, head) row: size the sample to the time budget
     budget_rows = args.ref_budget_s * threads / 13e-6 / max(1, total_steps)
     tokens = int(max(1, min(INV_SPEC.n_tokens, budget_rows // (INV_SPEC.n_heads + 1))))
-    xi, pi = inv_h["x"][:tokens].contiguous(), inv_h["positions"][:tokens].contiguous()
-    kv, kp, sl = (ins_h["kv"][:tokens].contiguous(), ins_h["positions"][:tokens].contiguous(),
-                  ins_h["slot_mapping"][:tokens].contiguous())
-    cache = inv_h["cos_sin_cache"]
+    value, dt = oracle_step_rate(inv_h, ins_h, tokens, args.steps, warm, threads)
+    value = round(value, 4)
     sample_bytes = W.inverse_bytes(tokens, INV_SPEC.n_heads) + W.insert_bytes(tokens)
-
-    def step():
-        oracle.inv_rope_fp8_quant(xi, pi, cache, inv_h["heads_per_group"], threads=threads)
-        oracle.rope_fp8_quant_insert(kv, kp, cache, sl, ins_h["k_cache"], ins_h["block_size"],
-                                     threads=threads)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = (time.perf_counter() - t0) / args.steps
-    value = round(sample_bytes / dt / 1e9, 4)
     sample = (f"first {tokens} tokens of each op per step (inverse {tokens}x32 heads, "
-              f"insert {tokens}); oracle with {threads} threads")
+              f"insert {tokens}); warm mean of {args.steps} steps after {warm} untimed; "
+              f"oracle with {threads} threads")
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -732,7 +863,7 @@ def run_reference(args, world, rank):
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
-        "warmup": max(3, args.warmup),
+        "warmup": warm,
         "ms_per_step": round(dt * 1e3, 4),
         "higher_is_better": True,
         "scaling": "weak",

@@ -16,19 +16,13 @@
 // For every group g:  Y[:, g, :] = (A_g * 2^(sa - 127)) @ (W_g * 2^(sw - 127))^T,
 // Y bf16 [M, G, n_out].
 //
-// Persistent clusters of two CTAs (one CTA per SM) walk pairs of 128 x 256
-// output tiles: the two CTAs of a cluster take M tiles 2i and 2i + 1 of the
-// same group and N tile, so they need the same W tile at every K step. Each
-// CTA loads one 128-row half of it and multicasts it into both CTAs' shared
-// memory, which cuts the L2 -> SM operand traffic from 48 KiB to 32 KiB per
-// K step and CTA (without the split the kernel is bound by that traffic, not
-// by the MMAs). A stage is refilled only when both CTAs' MMAs are done with
-// it: each MMA commit arrives on the stage's barrier in both CTAs. The N
-// tiles of one (M tile pair, group) are neighbours in the walk, so concurrent
-// clusters read the same A rows from L2.
-//   warp 0   one lane: tensor-map TMA of each 128-wide K step of A (16 KiB,
-//            this CTA's rows) and of this CTA's half of W (16 KiB, multicast)
-//            into a 4-stage ring;
+// Persistent CTAs (one per SM) walk the 128 x 256 output tiles t =
+// blockIdx.x, blockIdx.x + gridDim.x, ...; the N tiles of one (M tile,
+// group) are neighbours in the walk, so CTAs running at the same time read
+// the same A rows, and the few W tiles of a group, from L2. Each CTA loads
+// its own operands with plain tensor-map copies into its own shared memory.
+//   warp 0   one lane: tensor-map TMA of each 128-wide K step of A (16 KiB)
+//            and W (32 KiB) into a 4-stage ring;
 //   warp 1   allocates TMEM; one lane copies each tile's scale codes from
 //            shared memory to TMEM (tcgen05.cp) and issues the MMAs
 //            (M = 128, N = 256, 4 x K = 32 per K step);
@@ -51,14 +45,10 @@ namespace rq {
 namespace {
 
 constexpr int kMxBM = 128, kMxBN = 256, kMxBK = 128;
-constexpr int kMxCluster = 2;                                   // CTAs sharing each W tile
-constexpr uint16_t kMxClusterMask = (1u << kMxCluster) - 1u;
 constexpr int kMxStages = 4;
 constexpr int kMxMaxHeads = 8;                                  // K up to 8 x 512 = 4096
 constexpr uint32_t kMxATile = kMxBM * kMxBK;                    // 16 KiB
 constexpr uint32_t kMxWTile = kMxBN * kMxBK;                    // 32 KiB
-constexpr uint32_t kMxWSlice = kMxWTile / kMxCluster;           // the part one CTA loads
-constexpr int kMxWSliceRows = kMxBN / kMxCluster;
 constexpr uint32_t kSfAtom = 512;                               // 32 rows x 16 bytes
 constexpr uint32_t kSfaBytes = kMxMaxHeads * kSfAtom;           // one atom per head
 constexpr uint32_t kSfbBytes = 2 * kMxMaxHeads * kSfAtom;       // per head: two N halves
@@ -104,19 +94,19 @@ struct MxTile {
     int mt, g, nt;
 };
 
-// Tile pair t of the cluster walk, as seen by cluster rank `rank`.
-__device__ __forceinline__ MxTile mx_tile(int t, int n_nt, int groups, uint32_t rank) {
+// Tile t of the walk: N tiles innermost, then groups, then M tiles.
+__device__ __forceinline__ MxTile mx_tile(int t, int n_nt, int groups) {
     MxTile x;
     x.nt = t % n_nt;
     const int r = t / n_nt;
     x.g = r % groups;
-    x.mt = (r / groups) * kMxCluster + int(rank);
+    x.mt = r / groups;
     return x;
 }
 
 }  // namespace
 
-__global__ void __cluster_dims__(kMxCluster, 1, 1) __launch_bounds__(kMxThreads, 1)
+__global__ void __launch_bounds__(kMxThreads, 1)
 grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
                               const __grid_constant__ CUtensorMap tma_w, MxGemmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -132,15 +122,13 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_kt = p.k / kMxBK, n_heads = p.k / 512;
     const int n_nt = (p.n_out + kMxBN - 1) / kMxBN;
-    const int n_pairs = ((p.m + kMxBM * kMxCluster - 1) / (kMxBM * kMxCluster)) * p.groups * n_nt;
-    const uint32_t rank = umma::cluster_ctarank();
-    const int cluster = blockIdx.x / kMxCluster, n_clusters = gridDim.x / kMxCluster;
+    const int n_tiles = ((p.m + kMxBM - 1) / kMxBM) * p.groups * n_nt;
     const uint32_t lim = p.wait.spin_limit;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMxStages; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kMxCluster);  // one MMA commit from each CTA
+            mbar_init(empty0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sfull0 + 8 * b, 1);
@@ -157,7 +145,7 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
         umma::tmem_relinquish();
     }
     umma::fence_before_sync();
-    umma::cluster_sync();  // barriers of both CTAs initialised before any multicast
+    __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
@@ -167,8 +155,8 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
         if (lane == 0 && !starve) {
             uint32_t it = 0;  // K steps issued
             bool ok = true;
-            for (int t = cluster; t < n_pairs && ok; t += n_clusters) {
-                const MxTile x = mx_tile(t, n_nt, p.groups, rank);
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                const MxTile x = mx_tile(t, n_nt, p.groups);
                 for (int kt = 0; kt < n_kt; ++kt) {
                     const uint32_t s = it % kMxStages, ph = (it / kMxStages) & 1u;
                     if (!wait_or_abort(empty0 + 8 * s, ph ^ 1u, abort, lim)) {
@@ -178,10 +166,8 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
                     mbar_arrive_expect_tx(full0 + 8 * s, kMxATile + kMxWTile);
                     umma::tma_load_2d(a0 + s * kMxATile, &tma_a, x.g * p.k + kt * kMxBK,
                                       x.mt * kMxBM, full0 + 8 * s);
-                    umma::tma_load_2d_multicast(
-                        w0 + s * kMxWTile + rank * kMxWSlice, &tma_w, kt * kMxBK,
-                        x.g * p.n_out + x.nt * kMxBN + int(rank) * kMxWSliceRows, full0 + 8 * s,
-                        kMxClusterMask);
+                    umma::tma_load_2d(w0 + s * kMxWTile, &tma_w, kt * kMxBK,
+                                      x.g * p.n_out + x.nt * kMxBN, full0 + 8 * s);
                     ++it;
                 }
             }
@@ -194,7 +180,7 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
         if (lane == 0) {
             uint32_t it = 0, i = 0;
             bool ok = true;
-            for (int t = cluster; t < n_pairs && ok; t += n_clusters, ++i) {
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++i) {
                 const uint32_t b = i & 1u;
                 if (!wait_or_abort(sfull0 + 8 * b, (i >> 1) & 1u, abort, lim) ||
                     !wait_or_abort(tempty, (i & 1u) ^ 1u, abort, lim))
@@ -225,7 +211,7 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
                     for (int k = 0; k < kMxBK / 32; ++k)  // K = 32 bytes of e4m3 per MMA
                         umma::mma_mxf8f6f4(tmem, ad + 2 * k, wd + 2 * k, idesc, sfa_t + 4 * h,
                                            sfb_t + 8 * h, (kt | k) != 0);
-                    umma::commit_multicast(empty0 + 8 * s, kMxClusterMask);  // both CTAs' stage
+                    umma::commit(empty0 + 8 * s);
                     ++it;
                 }
                 if (ok) umma::commit(tfull);
@@ -235,8 +221,8 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
         }
     } else if (warp == 2) {
         uint32_t i = 0;
-        for (int t = cluster; t < n_pairs; t += n_clusters, ++i) {
-            const MxTile x = mx_tile(t, n_nt, p.groups, rank);
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
+            const MxTile x = mx_tile(t, n_nt, p.groups);
             const uint32_t b = i & 1u;
             if (!__all_sync(kFull, wait_or_abort(sempty0 + 8 * b, ((i >> 1) & 1u) ^ 1u, abort, lim)))
                 break;
@@ -279,8 +265,8 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
         const int quad = warp & 3;
         const int half = (warp - kMxEpiWarp0) >> 2;
         uint32_t i = 0;
-        for (int t = cluster; t < n_pairs; t += n_clusters, ++i) {
-            const MxTile x = mx_tile(t, n_nt, p.groups, rank);
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
+            const MxTile x = mx_tile(t, n_nt, p.groups);
             // the warp leaves together: the TMEM loads below are warp-collective
             if (!__all_sync(kFull, wait_or_abort(tfull, i & 1u, abort, lim))) break;
             umma::fence_after_sync();
@@ -307,7 +293,7 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
         }
     }
     umma::fence_before_sync();
-    umma::cluster_sync();  // no CTA leaves while its peer may still write into it
+    __syncthreads();
     if (threadIdx.x == 0 && *abort && p.error_flags) atomicOr(p.error_flags, RQ_FLAG_TIMEOUT);
     if (warp == 1) {
         umma::fence_after_sync();
@@ -322,31 +308,22 @@ cudaError_t launch_grouped_fp8_gemm_ue8m0(const MxGemmParams& p, const uint8_t* 
     if (!make_map(&ma, a_codes, uint64_t(p.groups) * p.k, uint64_t(p.m), uint64_t(p.groups) * p.k,
                   kMxBM) ||
         !make_map(&mw, w_codes, uint64_t(p.k), uint64_t(p.groups) * p.n_out, uint64_t(p.k),
-                  kMxWSliceRows))
+                  kMxBN))
         return cudaErrorInvalidValue;
-    // clusters that fit at once (one CTA per SM; a GPC may leave an SM over)
     constexpr int kMax = 64;
-    static thread_local int max_clusters[kMax] = {};
+    static thread_local bool attr_done[kMax] = {};
     const int d = (dev.ordinal >= 0 && dev.ordinal < kMax) ? dev.ordinal : 0;
-    if (max_clusters[d] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(
+    if (!attr_done[d]) {
+        const cudaError_t e = cudaFuncSetAttribute(
             grouped_fp8_gemm_ue8m0_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMxSmem));
         if (e != cudaSuccess) return e;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(kMxCluster * (dev.sm_count / kMxCluster));
-        cfg.blockDim = dim3(kMxThreads);
-        cfg.dynamicSmemBytes = kMxSmem;
-        int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, grouped_fp8_gemm_ue8m0_kernel, &cfg);
-        if (e != cudaSuccess) return e;
-        max_clusters[d] = n > 0 ? n : 1;
+        attr_done[d] = true;
     }
-    const int64_t pairs = int64_t((p.m + kMxBM * kMxCluster - 1) / (kMxBM * kMxCluster)) *
-                          p.groups * ((p.n_out + kMxBN - 1) / kMxBN);
-    if (pairs == 0) return cudaSuccess;
-    const int64_t clusters = pairs < max_clusters[d] ? pairs : max_clusters[d];
-    grouped_fp8_gemm_ue8m0_kernel<<<int(clusters) * kMxCluster, kMxThreads, kMxSmem, stream>>>(ma, mw,
-                                                                                            p);
+    const int64_t tiles = int64_t((p.m + kMxBM - 1) / kMxBM) * p.groups *
+                          ((p.n_out + kMxBN - 1) / kMxBN);
+    if (tiles == 0) return cudaSuccess;
+    const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
+    grouped_fp8_gemm_ue8m0_kernel<<<grid, kMxThreads, kMxSmem, stream>>>(ma, mw, p);
     return cudaGetLastError();
 }
 

@@ -136,16 +136,6 @@ __device__ __forceinline__ void commit(uint32_t bar) {
                  : "memory");
 }
 
-// The same arrive, on the mbarrier at this offset in every CTA of the
-// cluster named by `cta_mask` (bit r = cluster rank r).
-__device__ __forceinline__ void commit_multicast(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-        "[%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
 // 32*(w%4) .. 32*(w%4)+31; the address carries the lane in bits 16..31).
 __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
@@ -178,31 +168,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "%3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
-}
-
-// 2-D tensor-map TMA load multicast to the same shared-memory offset of every
-// CTA in `cta_mask`, each completing bytes on its own mbarrier at `bar`.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map,
-                                                      int32_t x, int32_t y, uint32_t bar,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::"
-        "cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
-// This CTA's rank in its cluster.
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of every CTA in the cluster (a superset of __syncthreads).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
 }
 
 // 3-D tensor-map TMA load (coordinates innermost first).

@@ -1016,10 +1016,9 @@ def test_stream_kernel_wait_runs_out_reports_timeout_and_context_stays_usable(rq
 
 @pytest.mark.parametrize("kind", ["fp32", "ue8m0"])
 def test_gemm_wait_runs_out_reports_timeout_and_context_stays_usable(rq, kind):
-    """The first CTA's TMA producer issues nothing: its MMA (and, for the
-    clustered kernel, its peer's) waits give up, RQ_FLAG_TIMEOUT is set, TMEM
-    is freed and the kernel exits; the next normal call is within the
-    oracle's bound."""
+    """The first CTA's TMA producer issues nothing: its MMA waits give up,
+    RQ_FLAG_TIMEOUT is set, TMEM is freed and the kernel exits; the next
+    normal call is within the oracle's bound."""
     import oracle
     dev = torch.device("cuda:0")
     m, g, k, n_out = 300, 2, 1024, 256
