@@ -211,7 +211,10 @@ rq_status rq_validate_indices(const int64_t *positions, const int64_t *slot_mapp
  * until the process exits). num_slots above 1,048,576 (2^20) returns
  * RQ_ERR_SHAPE. Nothing is allocated. The first call on a device looks up
  * the array's device address (make that first call before any stream
- * capture). Every call clears the part of the array it uses; calls whose
+ * capture); that address belongs to the device's primary context, so after a
+ * cudaDeviceReset the entry point must not be called again in the process.
+ * A CUDA failure returns RQ_ERR_CUDA and clears the runtime's sticky error,
+ * as the other entry points do. Every call clears the part of the array it uses; calls whose
  * work overlaps on the GPU (other streams or host threads) race on the
  * shared array. The call synchronises `stream` before it returns.
  */

@@ -30,7 +30,10 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) uint8_t g_validate_scratch[kBitmapBytes + 256];
 
 // Device address of the array, looked up once per device (host code cannot
-// use the array's name as a device pointer).
+// use the array's name as a device pointer). The address stays valid for the
+// life of the device's primary context: after a cudaDeviceReset (which
+// destroys that context and the module's copy of the array) this entry point
+// must not be called again in the same process.
 uint8_t* g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
@@ -47,6 +50,14 @@ cudaError_t scratch_for_device(int device, uint8_t** out) {
 }
 
 bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+
+// A CUDA failure as the other entry points report it: clear this runtime's
+// sticky launch error, return RQ_ERR_CUDA.
+rq_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return RQ_OK;
+    (void)cudaGetLastError();
+    return RQ_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -67,13 +78,13 @@ RQ_EXPORT rq_status rq_validate_indices_noalloc(const int64_t* positions,
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return RQ_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_status(e);
     if (dev < 0 || dev >= kMaxDevices) return RQ_ERR_ARG;
     int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return RQ_ERR_CUDA;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_status(e);
     uint8_t* scratch = nullptr;
-    if (scratch_for_device(dev, &scratch) != cudaSuccess) return RQ_ERR_CUDA;
+    if ((e = scratch_for_device(dev, &scratch)) != cudaSuccess) return cuda_status(e);
 
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t bitmap = slot_mapping ? ((num_slots + 31) / 32) * 4 : 0;
@@ -95,7 +106,7 @@ RQ_EXPORT rq_status rq_validate_indices_noalloc(const int64_t* positions,
         (e = rq::launch_validate_indices(p, info, st)) != cudaSuccess ||
         (e = cudaMemcpyAsync(&word, p.result, 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
         (e = cudaStreamSynchronize(st)) != cudaSuccess)
-        return RQ_ERR_CUDA;
+        return cuda_status(e);
     *result = word;
     return RQ_OK;
 }
