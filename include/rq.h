@@ -176,6 +176,32 @@ rq_status rq_inv_rope_fp8_quant_host(const void *x_bf16_host, int64_t n_tokens, 
 void rq_debug_inject(uint32_t mask, uint32_t spin_limit);
 
 /*
+ * TEST ONLY: the kernels' own per-block arithmetic over a range of fp32 bit
+ * patterns, so that it can be checked exhaustively against an independent
+ * statement of it. Neither is part of the op; both are stream-ordered and
+ * asynchronous, allocate nothing and write only the caller's arrays.
+ *
+ * rq_debug_block_scale: for i in [0, count), with amax = the fp32 value of
+ * bit pattern first_bits + i, writes the block scale every quantising kernel
+ * takes, 2^ceil(log2(fl32(max(amax, eps) / 448))) (the power-of-two scale of
+ * the GLM5.2 page, S1, applied to the block absmax of the inverse-RoPE page,
+ * S3), to scales[i] and its exact reciprocal to inv_scales[i] (both device
+ * fp32 [count], 4-byte aligned). Defined for finite amax; eps as in
+ * rq_inv_rope_fp8_quant. first_bits + count <= 2^32, else RQ_ERR_SHAPE.
+ *
+ * rq_debug_quant_codes: for i in [0, count), writes to codes[i] the e4m3
+ * code the kernels store for the fp32 value v of bit pattern first_bits + i
+ * in a block whose scale is 2^scale_exp: v times the exact inverse scale
+ * (round to nearest even), converted with round-to-nearest-even and
+ * saturation to +-448 (inverse-RoPE page, S3). count a multiple of 16;
+ * codes device, 16-byte aligned; scale_exp in [-126, 126] (else RQ_ERR_ARG).
+ */
+rq_status rq_debug_block_scale(uint32_t first_bits, int64_t count, float eps, float *scales,
+                               float *inv_scales, void *stream);
+rq_status rq_debug_quant_codes(uint32_t first_bits, int64_t count, int scale_exp,
+                               uint8_t *codes, void *stream);
+
+/*
  * Debug helper: checks the device-side preconditions of the ops, which the
  * ops themselves only partly check (a repeated slot goes unnoticed there),
  * without running them. One non-trapping kernel on `stream`, then the result

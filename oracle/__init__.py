@@ -66,6 +66,10 @@ def _load():
             "rqo_e4m3_decode_array": (None, [P, i64, P]),
             "rqo_ceil_log2_array": (None, [P, i64, P]),
             "rqo_block_scale_array": (None, [P, i64, P]),
+            "rqo_block_scale_bits_range": (ctypes.c_int, [ctypes.c_uint32, i64, ctypes.c_float, P,
+                                                          ctypes.c_int]),
+            "rqo_e4m3_encode_bits_range": (ctypes.c_int, [ctypes.c_uint32, i64, ctypes.c_int, P,
+                                                          ctypes.c_int]),
             "rqo_rope_rows": (ctypes.c_int, [P, i64, P, P, i64, ctypes.c_int]),
             "rqo_quant_rows": (None, [P, i64, ctypes.c_float, P, P]),
             "rqo_inv_rope_fp8_quant": (ctypes.c_int, [P, i64, i64, i64, i64, P, P, i64, i64,
@@ -155,6 +159,30 @@ def block_scale(amax) -> np.ndarray:
     a = _np(amax, np.float32)
     out = np.empty(a.shape, np.float32)
     _load().rqo_block_scale_array(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def block_scale_bits_range(first_bits: int, count: int, eps: float, threads: int = 0) -> np.ndarray:
+    """block_scale(max(amax, eps)) for every amax = fp32 bit pattern
+    first_bits + i, i < count (first_bits + count <= 2^32), over ``threads``
+    threads (0 = all cores). Same arithmetic as block_scale, element by element."""
+    out = np.empty(int(count), np.float32)
+    st = _load().rqo_block_scale_bits_range(int(first_bits), int(count), float(eps), _ptr(out),
+                                            int(threads or os.cpu_count() or 1))
+    if st:
+        raise OracleError(f"rqo_block_scale_bits_range: status {st}")
+    return out
+
+
+def e4m3_encode_bits_range(first_bits: int, count: int, scale_exp: int = 0,
+                           threads: int = 0) -> np.ndarray:
+    """E4M3 code of (fp32 bit pattern first_bits + i) / 2^scale_exp for i < count,
+    the quantisation step of the op; same arithmetic as e4m3_encode."""
+    out = np.empty(int(count), np.uint8)
+    st = _load().rqo_e4m3_encode_bits_range(int(first_bits), int(count), int(scale_exp), _ptr(out),
+                                            int(threads or os.cpu_count() or 1))
+    if st:
+        raise OracleError(f"rqo_e4m3_encode_bits_range: status {st}")
     return out
 
 

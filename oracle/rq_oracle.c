@@ -735,3 +735,83 @@ int rqo_indexer_q_rope_quant(const uint16_t *q, int64_t n_tokens, int64_t n_head
     }
     return RQO_OK;
 }
+
+/* ------------------------------------------------ bit-pattern range drivers */
+
+/* Test drivers that apply the scalar steps above to every fp32 bit pattern of
+ * a range [first, first + count) (count <= 2^32 - first), split over threads.
+ * They add no arithmetic: each element is exactly what rqo_quant_row does to
+ * one value or one block. */
+struct range_args {
+    uint32_t first;
+    float eps;
+    int e;
+    float *scales;
+    uint8_t *codes;
+    int64_t t0, t1;
+};
+
+static float bits_to_f32(uint32_t b)
+{
+    float f;
+    memcpy(&f, &b, sizeof f);
+    return f;
+}
+
+static void range_set(void *p, int64_t t0, int64_t t1)
+{
+    ((struct range_args *)p)->t0 = t0;
+    ((struct range_args *)p)->t1 = t1;
+}
+
+static void *block_scale_worker(void *p)
+{
+    const struct range_args *a = (const struct range_args *)p;
+    int64_t i;
+    for (i = a->t0; i < a->t1; ++i) {
+        float amax = bits_to_f32(a->first + (uint32_t)i);
+        if (amax < a->eps)
+            amax = a->eps;            /* the clamp of rqo_quant_row */
+        a->scales[i] = rqo_block_scale(amax);
+    }
+    return NULL;
+}
+
+static void *encode_worker(void *p)
+{
+    const struct range_args *a = (const struct range_args *)p;
+    const double scale = ldexp(1.0, a->e);
+    int64_t i;
+    for (i = a->t0; i < a->t1; ++i)   /* the code step of rqo_quant_row */
+        a->codes[i] = rqo_e4m3_encode((double)bits_to_f32(a->first + (uint32_t)i) / scale);
+    return NULL;
+}
+
+/* scales[i] = block scale of a block whose absmax is the pattern first + i
+ * (finite, >= 0), after the eps clamp. */
+int rqo_block_scale_bits_range(uint32_t first, int64_t count, float eps, float *scales,
+                               int nthreads)
+{
+    struct range_args a;
+    if (count < 0 || (uint64_t)first + (uint64_t)count > ((uint64_t)1 << 32))
+        return RQO_ERR_ARG;
+    memset(&a, 0, sizeof a);
+    a.first = first;
+    a.eps = eps;
+    a.scales = scales;
+    return split_run(block_scale_worker, &a, sizeof a, count, nthreads, range_set);
+}
+
+/* codes[i] = E4M3 code of the pattern first + i divided by 2^e. */
+int rqo_e4m3_encode_bits_range(uint32_t first, int64_t count, int e, uint8_t *codes,
+                               int nthreads)
+{
+    struct range_args a;
+    if (count < 0 || (uint64_t)first + (uint64_t)count > ((uint64_t)1 << 32))
+        return RQO_ERR_ARG;
+    memset(&a, 0, sizeof a);
+    a.first = first;
+    a.e = e;
+    a.codes = codes;
+    return split_run(encode_worker, &a, sizeof a, count, nthreads, range_set);
+}

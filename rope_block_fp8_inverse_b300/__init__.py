@@ -17,7 +17,7 @@ import threading
 
 import torch
 
-__all__ = ["validate_indices", "debug_inject", "DEBUG_STREAM_STAGE", "DEBUG_GEMM_LOADS", "inv_rope_fp8_quant_host", "host_workspace_bytes", "inv_rope_fp8_quant_gemm", "grouped_fp8_gemm", "grouped_fp8_gemm_ue8m0",
+__all__ = ["validate_indices", "debug_inject", "debug_block_scale", "debug_quant_codes", "DEBUG_STREAM_STAGE", "DEBUG_GEMM_LOADS", "inv_rope_fp8_quant_host", "host_workspace_bytes", "inv_rope_fp8_quant_gemm", "grouped_fp8_gemm", "grouped_fp8_gemm_ue8m0",
            "indexer_q_rope_quant", "qnorm_rope_kv_rope_quant_insert", "VARIANT_AUTO", "VARIANT_WARP_ROWS", "VARIANT_STREAM", "inv_rope_quant", "OUT_MODES",
            "empty_outputs", "inv_rope_fp8_quant", "rope_fp8_quant_insert", "lib", "RQError", "LIB_PATH",
            "HEAD_DIM", "RECORD_BYTES", "status_string", "ABI_SYMBOLS"]
@@ -56,6 +56,8 @@ ABI_SYMBOLS = {
                                                    ctypes.c_float, _P, _P, _P, _P]),
     "rq_grouped_fp8_gemm": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _P]),
     "rq_debug_inject": (None, [ctypes.c_uint32, ctypes.c_uint32]),
+    "rq_debug_block_scale": (ctypes.c_int, [ctypes.c_uint32, _I64, ctypes.c_float, _P, _P, _P]),
+    "rq_debug_quant_codes": (ctypes.c_int, [ctypes.c_uint32, _I64, ctypes.c_int, _P, _P]),
     "rq_validate_indices_workspace": (ctypes.c_int64, [_I64]),
     "rq_validate_indices": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _I64, _P, _P]),
     "rq_validate_indices_noalloc": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P]),
@@ -515,6 +517,37 @@ def debug_inject(mask: int = 0, spin_limit: int = 0) -> None:
     and ``RQ_FLAG_TIMEOUT`` is reported; ``debug_inject()`` restores normal
     operation. Applies to later calls from this thread."""
     lib().rq_debug_inject(mask, spin_limit)
+
+
+def debug_block_scale(first_bits: int, count: int, eps: float, device=None):
+    """TEST ONLY (``rq_debug_block_scale``): the kernels' block scale of each
+    amax = fp32 bit pattern first_bits + i (i < count), clamped below by
+    ``eps``, and its reciprocal, as two CUDA fp32 tensors [count]."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    scales = torch.empty(count, dtype=torch.float32, device=dev)
+    inv = torch.empty(count, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().rq_debug_block_scale(int(first_bits), int(count), float(eps), scales.data_ptr(),
+                                        inv.data_ptr(), _stream(dev))
+    _check(st, "rq_debug_block_scale")
+    return scales, inv
+
+
+def debug_quant_codes(first_bits: int, count: int, scale_exp: int = 0, out: torch.Tensor | None = None,
+                      device=None) -> torch.Tensor:
+    """TEST ONLY (``rq_debug_quant_codes``): the e4m3 code the kernels store for
+    the fp32 value of bit pattern first_bits + i (i < count, a multiple of 16)
+    in a block of scale 2^scale_exp, as a CUDA uint8 tensor [count]."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if out is None:
+        out = torch.empty(count, dtype=torch.uint8, device=dev)
+    if out.dtype != torch.uint8 or not out.is_cuda or out.numel() < count or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CUDA uint8 tensor of at least count bytes")
+    with torch.cuda.device(out.device):
+        st = lib().rq_debug_quant_codes(int(first_bits), int(count), int(scale_exp), out.data_ptr(),
+                                        _stream(out.device))
+    _check(st, "rq_debug_quant_codes")
+    return out[:count]
 
 
 def host_workspace_bytes(n_heads: int, chunk_tokens: int) -> int:

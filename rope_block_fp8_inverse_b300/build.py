@@ -25,7 +25,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-Xptxas", "-v", *ARCH, f"-I{INCLUDE}", f"-I{CSRC}"]
 SOURCES = ["rq_kernels.cu", "rq_stream.cu", "rq_indexer.cu", "rq_gemm.cu", "rq_gemm_mx.cu",
-           "rq_validate.cu", "rq_validate_noalloc.cu", "rq_api.cpp", "rq_host.cpp"]
+           "rq_validate.cu", "rq_validate_noalloc.cu", "rq_debug.cu", "rq_api.cpp", "rq_host.cpp"]
 
 
 def nvcc() -> str:

@@ -123,20 +123,33 @@ def test_irregular_grouping_full(rq, variant):
     assert_parity(gc, gs, wc, ws, exact=True)
 
 
+_FULL = {}
+
+
+def _full_size(name):
+    """Inputs and oracle outputs of a full-size workload, computed once per
+    test module (the multi-threaded oracle takes about a second for each)."""
+    if name not in _FULL:
+        if name == "prefill16k":
+            inp = W.inverse_inputs(W.PREFILL16K)
+            _FULL[name] = (inp, oracle_inverse(inp))
+        elif name == "prefill16k_bf16":
+            inp, _ = _full_size("prefill16k")
+            _FULL[name] = (inp, oracle_layout(inp, "bf16"))
+        elif name == "indexer16k_neox" or name == "indexer16k_gptj":
+            inp = W.indexer_inputs(W.INDEXER16K)
+            _FULL[name] = (inp, oracle_indexer(inp, name.rsplit("_", 1)[1]))
+    return _FULL[name]
+
+
 @VARIANTS
-def test_prefill16k_sampled_tokens(rq, variant):
-    """Full-size launch (N=16384, H=32, hpg=8, the benchmarked configuration);
-    the oracle recomputes a sample of tokens one by one (batch invariance
-    makes a token's output independent of the rest of the batch)."""
-    inp = W.inverse_inputs(W.PREFILL16K)
+def test_prefill16k_every_output(rq, variant):
+    """Full-size launch (N=16384, H=32, hpg=8, the benchmarked configuration):
+    every code and every scale of all 16384 tokens against the oracle."""
+    inp, (wc, ws) = _full_size("prefill16k")
     gc, gs = run_inverse(rq, inp, variant=variant)
     assert gc.shape == (16384, 4, 4096) and gs.shape == (16384, 4, 32)
-    rng = np.random.default_rng(0)
-    idx = np.unique(np.concatenate([[0, 1, 16383], rng.choice(16384, 1500, replace=False)]))
-    sub = {"x": inp["x"][idx], "positions": inp["positions"][idx],
-           "cos_sin_cache": inp["cos_sin_cache"], "heads_per_group": 8}
-    wc, ws = oracle_inverse(sub)
-    assert_parity(gc[idx], gs[idx], wc, ws, exact=True)
+    assert_parity(gc, gs, wc, ws, exact=True)
     # properties at every output: scales are powers of two, no NaN codes
     assert np.all((gs.view(np.uint32) & 0x7FFFFF) == 0)
     assert not np.any((gc & 0x7F) == 0x7F)
@@ -432,16 +445,17 @@ def test_layout_fp8_equals_the_plain_entry_at_full_size(rq):
 
 @pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("mode", ["fp8", "ue8m0", "bf16"])
-def test_layout_full_size_sampled_tokens(rq, mode, layout):
-    """Full-size calls take the TMA-ring kernel (bulk or per-lane scale stores)."""
-    inp = W.inverse_inputs(W.PREFILL16K)
+def test_layout_full_size_every_output(rq, mode, layout):
+    """Full-size calls (the kernel each layout takes at 16384 tokens x 32
+    heads): every output of all 16384 tokens against the oracle."""
+    if mode == "bf16":
+        inp, want = _full_size("prefill16k_bf16")
+    else:
+        import oracle
+        inp, (wc, ws) = _full_size("prefill16k")
+        want = (wc, oracle.pack_ue8m0(ws).view(np.int32)) if mode == "ue8m0" else (wc, ws)
     got = run_layout(rq, inp, mode, layout)
-    rng = np.random.default_rng(1)
-    idx = np.unique(np.concatenate([[0, 16383], rng.choice(16384, 600, replace=False)]))
-    sub = {"x": inp["x"][idx], "positions": inp["positions"][idx],
-           "cos_sin_cache": inp["cos_sin_cache"], "heads_per_group": 8}
-    want = oracle_layout(sub, mode)
-    assert_layout_parity(mode, (got[0][idx], None if got[1] is None else got[1][idx]), want)
+    assert_layout_parity(mode, got, want)
 
 
 @pytest.mark.parametrize("mode", ["fp8", "ue8m0"])
@@ -642,15 +656,13 @@ def test_indexer_exact(rq, style, n, h):
 
 
 @pytest.mark.parametrize("style", ["neox", "gptj"])
-def test_indexer16k_sampled_tokens(rq, style):
-    inp = W.indexer_inputs(W.INDEXER16K)
+def test_indexer16k_every_output(rq, style):
+    """Full size (16384 tokens x 64 heads of 128): every code and folded
+    weight against the oracle."""
+    inp, (wc, ww) = _full_size(f"indexer16k_{style}")
     gc, gw = run_indexer(rq, inp, style)
-    rng = np.random.default_rng(2)
-    idx = np.unique(np.concatenate([[0, 16383], rng.choice(16384, 800, replace=False)]))
-    sub = dict(inp, q=inp["q"][idx], weights=inp["weights"][idx], positions=inp["positions"][idx])
-    wc, ww = oracle_indexer(sub, style)
-    assert np.array_equal(gc[idx], wc) and np.array_equal(gw[idx].view(np.uint32),
-                                                          ww.view(np.uint32))
+    assert np.array_equal(gc, wc), f"{np.count_nonzero(gc != wc)} codes differ"
+    assert np.array_equal(gw.view(np.uint32), ww.view(np.uint32))
 
 
 def test_indexer_bad_position_flags_and_skips(rq):

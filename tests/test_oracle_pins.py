@@ -855,3 +855,33 @@ def test_qnorm_weight_scales_each_dimension_before_the_rotation(oracle_lib):
     f2, fp = to_f(got2), to_f(plain)
     assert np.array_equal(f2[..., :448], fp[..., :448])
     assert not np.array_equal(f2[..., 449], fp[..., 449])   # the partner moved with it
+
+
+def test_bit_range_drivers_are_the_scalar_steps(oracle_lib):
+    """The bit-pattern range drivers that the exhaustive GPU checks compare
+    against add no arithmetic: element by element they equal the pinned
+    encoder (on the scaled value) and the pinned block scale (on the eps-clamped
+    amax), at chunk edges, around zero, subnormals, 448, infinities and NaNs,
+    and with several threads."""
+    starts = [0, 0x00000001 - 1, 0x007FFF00, 0x3E5FFF00, 0x43DFFF80, 0x7F7FFF00, 0x7F800000,
+              0x80000000, 0x807FFF00, 0xC3DFFF80, 0xFF7FFF00, 0xFFFFFF00]
+    for first in starts:
+        n = min(256, (1 << 32) - first)
+        bits = (np.arange(n, dtype=np.uint64) + first).astype(np.uint32)
+        v = bits.view(np.float32)
+        for e in (0, -9, 5, 126, -126):
+            got = oracle_lib.e4m3_encode_bits_range(first, n, e, threads=3)
+            want = oracle_lib.e4m3_encode((v.astype(np.float64) / 2.0 ** e).astype(np.float32)) \
+                if e in (0,) else np.array([oracle_lib.e4m3_encode_scalar(float(x) / 2.0 ** e)
+                                            for x in v], np.uint8)
+            assert np.array_equal(got, want), (hex(first), e)
+    for first in (0, 0x0D7FFF00, 0x3F5FFF80, 0x43DFFF80, 0x7F7FFF00):
+        n = 256
+        amax = (np.arange(n, dtype=np.uint64) + first).astype(np.uint32).view(np.float32)
+        for eps in (2.0 ** -100, 1e-10, 1e-4):
+            e32 = np.float32(eps)
+            got = oracle_lib.block_scale_bits_range(first, n, float(e32), threads=4)
+            want = oracle_lib.block_scale(np.maximum(amax, e32))
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (hex(first), eps)
+    with pytest.raises(oracle_lib.OracleError):
+        oracle_lib.e4m3_encode_bits_range(0xFFFFFFF0, 32)
