@@ -303,8 +303,10 @@ typedef enum rq_out_mode {
  * [0, cache_rows) are skipped and flagged as in rq_inv_rope_fp8_quant.
  * The kernel is chosen from the layout, the mode and the size; all choices
  * write the same bytes. Row-linear token-major quantised outputs (head r =
- * t*H + h at out + r*512, its scales at r*4 or its word at r) take the
- * warp-rows kernel of rq_inv_rope_fp8_quant. Other quantised layouts take the
+ * t*H + h at out + r*512, its scales at r*4 or its word at r) and contiguous
+ * group-major ones ([G, N, hpg*512] codes with [G, N, hpg*4] fp32 scales or
+ * [G, N, hpg] words, 16-byte aligned) take the warp-rows kernel of
+ * rq_inv_rope_fp8_quant. Other quantised layouts take the
  * TMA-ring kernel from 2048 rows per SM when heads_per_group is a multiple of
  * 8, and the warp-rows layout kernel otherwise. bf16 output always takes the
  * warp-rows layout kernel.

@@ -244,7 +244,19 @@ RQ_EXPORT rq_status rq_inv_rope_quant_layout(
         scale_stride_elem == 1 && scale_stride_token == n_heads * spe &&
         (groups == 1 || scale_stride_group == heads_per_group * spe) && aligned(scales, 16);
     if (row_linear)
-        return from_cuda(rq::launch_inv_rope_rows(p, dev, out_mode, static_cast<cudaStream_t>(stream)));
+        return from_cuda(
+            rq::launch_inv_rope_rows(p, dev, out_mode, false, static_cast<cudaStream_t>(stream)));
+    // The contiguous group-major layout ([G, N, hpg*512] codes, [G, N, hpg*spe]
+    // scales) is row-linear in the output row (g*N + t)*hpg + i: the same
+    // kernel, storing each row there.
+    const bool group_linear =
+        quant && groups > 1 && out_stride_token == heads_per_group * rq::kHeadDimABI &&
+        out_stride_group == n_tokens * heads_per_group * rq::kHeadDimABI &&
+        scale_stride_elem == 1 && scale_stride_token == heads_per_group * spe &&
+        scale_stride_group == n_tokens * heads_per_group * spe && aligned(scales, 16);
+    if (group_linear)
+        return from_cuda(
+            rq::launch_inv_rope_rows(p, dev, out_mode, true, static_cast<cudaStream_t>(stream)));
     // large calls whose tiles fit the layout take the TMA-ring kernel
     // bf16 output (no quantisation) stays on the warp-rows layout kernel at every size
     const bool stream_it = p.lay.mode != rq::kOutBf16 &&

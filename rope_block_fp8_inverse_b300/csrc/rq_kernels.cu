@@ -1,5 +1,6 @@
 // rq_kernels.cu -- the warp-rows kernels (sm_103a) and their launchers: the
-// inverse-RoPE + block-FP8 quant op (also into row-linear UE8M0 layouts), the
+// inverse-RoPE + block-FP8 quant op (also into row-linear UE8M0 and
+// contiguous group-major layouts), the
 // same op into any strided layout or as bf16, its forward-RoPE + paged-insert
 // sibling, and the fused q RMS norm + RoPE + kv insert op. (The TMA-ring
 // variant of the inverse op is in rq_stream.cu.)
@@ -27,10 +28,12 @@ namespace rq {
 // compiler's free choice of 73 registers (3 CTAs). kMode picks the scale
 // encoding: fp32 scales at scales + r*4, or (kOutFp8Ue8m0) one packed UE8M0
 // word per row at scales + r -- the row-linear token-major layouts of the
-// layout call, which takes this kernel for them. (Group-major layouts, visited
-// in output order by the same walk, measured slower here than on the TMA-ring
-// kernel: 0.920 vs 0.930 of the copy peak for fp8.)
-template <int kRows, int kMode = kOutFp8F32>
+// layout call, which takes this kernel for them. kGroupMajor writes the
+// contiguous group-major layout instead ([G, N, hpg*512] codes and
+// [G, N, hpg*4] / [G, N, hpg] scales): the same walk over the input, each row
+// stored at its output row q = (g*N + t)*hpg + i, two integer operations more
+// per row than the token-major store.
+template <int kRows, int kMode = kOutFp8F32, bool kGroupMajor = false>
 __global__ void __launch_bounds__(kInvThreads, 4)
 inv_rope_fp8_quant_kernel(InvParams p) {
     pdl_wait();
@@ -42,8 +45,11 @@ inv_rope_fp8_quant_kernel(InvParams p) {
     const int ca = chunk_a(lane);
     const bool rope_lane = lane >= kRopeLane0;
     const int cs_col = (rope_lane ? lane - kRopeLane0 : 0) * 4;
-    // rows walked without division: (token, head), one group of all heads
-    const uint32_t wn = p.n_heads, wg = p.n_heads, wgroups = 1u;
+    // rows walked without division: (token, head); token-major output needs
+    // no groups (one group of all heads), group-major output tracks them
+    const uint32_t wn = p.n_heads;
+    const uint32_t wg = kGroupMajor ? p.lay.hpg : p.n_heads;
+    const uint32_t wgroups = kGroupMajor ? p.n_heads / p.lay.hpg : 1u;
     const RowStride step = row_stride(n_warps * kRows, wn, wg);
     const RowStride next = row_stride(1, wn, wg);
     RowPos base = row_pos(warp * kRows, wn, wg);
@@ -53,12 +59,14 @@ inv_rope_fp8_quant_kernel(InvParams p) {
         uint4 a[kRows], b[kRows];
         float4 c[kRows], s[kRows];
         bool live[kRows];
+        uint32_t q[kRows];  // output row
         RowPos w = base;
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             const uint32_t r = r0 + i;
             if (i > 0) row_advance(w, next, wn, wg, wgroups);
             live[i] = false;
+            q[i] = kGroupMajor ? (w.g * p.n_tokens + w.t) * wg + w.i : r;
             if (r < p.n_rows) {  // warp-uniform
                 const uint32_t t = w.t;
                 const uint32_t h = w.h;
@@ -83,15 +91,15 @@ inv_rope_fp8_quant_kernel(InvParams p) {
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             if (!live[i]) continue;
-            const int64_t r = int64_t(r0) + i;
+            const int64_t r = q[i];
             float scale;
-            const uint4 q = rope_quant_row<true>(a[i], b[i], rope_lane, c[i], s[i], p.eps, &scale);
+            const uint4 qc = rope_quant_row<true>(a[i], b[i], rope_lane, c[i], s[i], p.eps, &scale);
             if (kMode == kOutFp8F32) {
-                store_row(p.out + r * kHeadDim, p.scales + r * 4, lane, ca, q, scale);
+                store_row(p.out + r * kHeadDim, p.scales + r * 4, lane, ca, qc, scale);
             } else {
                 uint8_t* codes = p.out + r * kHeadDim;
-                st_stream8(codes + 8 * ca, q.x, q.y);
-                st_stream8(codes + 8 * (ca + 8), q.z, q.w);
+                st_stream8(codes + 8 * ca, qc.x, qc.y);
+                st_stream8(codes + 8 * (ca + 8), qc.z, qc.w);
                 // byte b of row r's word: block b's biased exponent
                 if ((lane & 7) == 0)
                     st_stream1(reinterpret_cast<uint8_t*>(reinterpret_cast<uint32_t*>(p.scales) + r) +
@@ -372,7 +380,9 @@ namespace {
 // variant (thread-local: no locking on the launch path).
 constexpr int kMaxDevices = 64;
 // (kLay: 2 entries per output mode, one row or two rows per warp)
-enum Variant { kInv1, kInv2, kInvU1, kInvU2, kIns1, kFus1, kLay, kVariants = kLay + 6 };
+// (kRowsVariant: 4 entries per scale encoding: one or two rows per warp,
+// token-major or group-major rows)
+enum Variant { kInv1, kInv2, kIns1, kFus1, kLay, kRowsVariant = kLay + 6, kVariants = kRowsVariant + 8 };
 
 template <typename K>
 int resident_blocks(int device, Variant v, K kernel, int threads) {
@@ -437,20 +447,29 @@ cudaError_t launch_layout(const InvParams& p, const DeviceInfo& dev, cudaStream_
                       stream, p);
 }
 
-cudaError_t launch_inv_rope_rows(const InvParams& p, const DeviceInfo& dev, int mode,
-                                 cudaStream_t stream) {
-    if (mode == kOutFp8F32) return launch_inv_rope_fp8_quant(p, dev, kInvWarpRows, stream);
+template <int kMode, bool kGroupMajor>
+cudaError_t launch_rows(const InvParams& p, const DeviceInfo& dev, cudaStream_t stream) {
     constexpr int kWarps = kInvThreads / 32;
+    constexpr int kSlot = kRowsVariant + 4 * kMode + (kGroupMajor ? 2 : 0);
     if (int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4) {
-        auto k = inv_rope_fp8_quant_kernel<2, kOutFp8Ue8m0>;
-        const int res = resident_blocks(dev.ordinal, kInvU2, k, kInvThreads);
+        auto k = inv_rope_fp8_quant_kernel<2, kMode, kGroupMajor>;
+        const int res = resident_blocks(dev.ordinal, Variant(kSlot + 1), k, kInvThreads);
         return launch_pdl(k, grid_size(p.n_rows, kWarps * 2, dev.sm_count, res), kInvThreads, 0,
                           stream, p);
     }
-    auto k = inv_rope_fp8_quant_kernel<1, kOutFp8Ue8m0>;
-    const int res = resident_blocks(dev.ordinal, kInvU1, k, kInvThreads);
+    auto k = inv_rope_fp8_quant_kernel<1, kMode, kGroupMajor>;
+    const int res = resident_blocks(dev.ordinal, Variant(kSlot), k, kInvThreads);
     return launch_pdl(k, grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0,
                       stream, p);
+}
+
+cudaError_t launch_inv_rope_rows(const InvParams& p, const DeviceInfo& dev, int mode,
+                                 bool group_major, cudaStream_t stream) {
+    if (group_major)
+        return mode == kOutFp8F32 ? launch_rows<kOutFp8F32, true>(p, dev, stream)
+                                  : launch_rows<kOutFp8Ue8m0, true>(p, dev, stream);
+    if (mode == kOutFp8F32) return launch_inv_rope_fp8_quant(p, dev, kInvWarpRows, stream);
+    return launch_rows<kOutFp8Ue8m0, false>(p, dev, stream);
 }
 
 cudaError_t launch_inv_rope_quant_layout(const InvParams& p, const DeviceInfo& dev,

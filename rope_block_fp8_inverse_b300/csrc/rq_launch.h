@@ -189,10 +189,12 @@ enum InvVariant {
 };
 
 // rq_inv_rope_quant_layout takes the stream kernel from this many rows per
-// SM up, for the quantising modes when heads_per_group is a multiple of 8
-// (measured on B300 at 16384 tokens x 32 heads: fp8 0.93 vs 0.92 of the copy
-// peak for the warp-rows layout kernel, UE8M0 0.925 vs 0.92; bf16 output runs
-// faster on the warp-rows layout kernel, 0.99 vs 0.95, and always takes it).
+// SM up, for quantising layouts that are neither row-linear token-major nor
+// contiguous group-major (those two take the warp-rows kernel) when
+// heads_per_group is a multiple of 8 (measured on B300 at 16384 tokens x 32
+// heads: fp8 0.93 vs 0.92 of the copy peak for the warp-rows layout kernel,
+// UE8M0 0.925 vs 0.92; bf16 output runs faster on the warp-rows layout
+// kernel, 0.99 vs 0.95, and always takes it).
 constexpr int64_t kStreamMinRowsPerSm = 2048;
 
 
@@ -200,9 +202,11 @@ cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev,
                                       cudaStream_t stream);
 // The inverse op into a row-linear layout (row r's codes at out + r*512; its
 // scales at scales + r*4 (fp32) or its packed UE8M0 word at scales + r), on
-// the warp-rows kernel. mode: kOutFp8F32 or kOutFp8Ue8m0. Row r = t*H + h.
+// the warp-rows kernel. mode: kOutFp8F32 or kOutFp8Ue8m0. Row r = t*H + h
+// (token-major), or with group_major r = (g*N + t)*hpg + i for head
+// h = g*hpg + i (the contiguous group-major layout; p.lay.hpg set).
 cudaError_t launch_inv_rope_rows(const InvParams& p, const DeviceInfo& dev, int mode,
-                                 cudaStream_t stream);
+                                 bool group_major, cudaStream_t stream);
 cudaError_t launch_inv_rope_quant_layout(const InvParams& p, const DeviceInfo& dev,
                                          cudaStream_t stream);
 cudaError_t launch_inv_rope_fp8_quant_stream(const InvParams& p, const DeviceInfo& dev,

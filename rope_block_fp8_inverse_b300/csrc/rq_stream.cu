@@ -1,7 +1,8 @@
 // rq_stream.cu -- the inverse-RoPE + block-FP8 quant kernel built as one
 // independent TMA stream per warp (sm_103a), and its launcher. It serves the
 // RQ_INV_STREAM variant and the layout call's large quantised layouts that
-// are not row-linear (group-major, transposed scales); the default kernel of
+// are neither row-linear nor contiguous group-major (padded or transposed
+// strides); the default kernel of
 // the plain op is the warp-rows kernel in rq_kernels.cu.
 //
 // Every warp owns a private ring of kStages shared-memory stages. A stage
