@@ -885,6 +885,7 @@ PROFILE_OPS = {
     "inverse_stream": "inv_rope_fp8_quant_stream_kernel (RQ_INV_STREAM)",
     "gemm": "grouped_fp8_gemm_kernel (M = tokens, G 4, K 4096, n_out 1024)",
     "gemm_ue8m0": "grouped_fp8_gemm_ue8m0_kernel (same shape)",
+    "gemm_fused": "fused_inv_rope_quant_gemm_kernel (same shape, A produced from x in the kernel)",
     "indexer": "indexer_q_rope_quant_kernel (tokens x 64 heads of 128, NeoX)",
     "fused_qkv": "qnorm_rope_kv_insert_kernel (tokens x 32 q heads padded to 64 + kv)",
 }
@@ -899,7 +900,7 @@ def run_profile_op(args):
     spec = W.InverseSpec(f"profile{n}", n, INV_SPEC.n_heads, INV_SPEC.heads_per_group,
                          INV_SPEC.cache_rows, "arange", True)
     op = args.profile_op
-    if op in ("inverse", "inverse_stream", "gemm", "gemm_ue8m0"):
+    if op in ("inverse", "inverse_stream", "gemm", "gemm_ue8m0", "gemm_fused"):
         inp = W.inverse_inputs(spec)
         x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
         hpg = spec.heads_per_group
@@ -918,6 +919,9 @@ def run_profile_op(args):
                 codes, scales = rq.inv_rope_fp8_quant(x, pos, cache, hpg)
                 ws = torch.ldexp(torch.ones(()), (e - 127).float()).float().to(dev)
                 call = lambda: rq.grouped_fp8_gemm(codes, scales, wc, ws)
+            elif op == "gemm_fused":
+                ws = torch.ldexp(torch.ones(()), (e - 127).float()).float().to(dev)
+                call = lambda: rq.inv_rope_fp8_quant_gemm(x, pos, cache, hpg, wc, ws)
             else:
                 codes, words = rq.inv_rope_quant(x, pos, cache, hpg, mode="ue8m0")
                 wsf = e.to(torch.uint8).to(dev)
