@@ -693,13 +693,15 @@ def decode_leg(rq, dev, stream, inv_h, cache):
                         "graph of 100 calls, 5 replays", "us_per_call": decode}
 
 
-def cold_leg(rq, dev, stream, inv_h, cache, kv, kpos, slots, k_cache, bs, reps=20, rounds=7):
+def cold_leg(rq, dev, stream, inv_h, cache, kv, kpos, slots, k_cache, bs, reps=20, rounds=15):
     """The configurations that fit in L2, cold. Two CUDA graphs: `reps` x
-    (a 256 MiB write that evicts L2, then the call), and the same writes alone;
-    each is replayed `rounds` times under an event pair, and the cold time of
-    one call is (median with calls - median without) / reps. Launch overhead
-    inside a graph is that of a graph node, so the figure is device time."""
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    (a 160 MiB write that evicts L2, then the call), and the same writes
+    alone; they are replayed alternately under event pairs, `rounds` times,
+    and the cold time of one call is the median over rounds of (with calls -
+    without) / reps (pairing the two replays cancels drift between rounds).
+    Launch overhead inside a graph is that of a graph node, so the figure is
+    device time."""
+    flush = torch.empty(160 << 20, dtype=torch.uint8, device=dev)
 
     def graph_of(fn):
         g = torch.cuda.CUDAGraph()
@@ -716,21 +718,16 @@ def cold_leg(rq, dev, stream, inv_h, cache, kv, kpos, slots, k_cache, bs, reps=2
         torch.cuda.synchronize(dev)
         return g
 
-    def timed(g):
+    def once(g):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
         g.replay()
+        b.record(stream)
         torch.cuda.synchronize(dev)
-        ts = []
-        for _ in range(rounds):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-            torch.cuda.synchronize(dev)
-            ts.append(a.elapsed_time(b) * 1e3)
-        return statistics.median(ts)
+        return a.elapsed_time(b) * 1e3
 
     base = graph_of(None)
-    t_base = timed(base)
+    base.replay()
     cases = {}
     ti = W.inverse_inputs(W.TINY)
     tx, tp, tc = ti["x"].to(dev), ti["positions"].to(dev), ti["cos_sin_cache"].to(dev)
@@ -744,14 +741,23 @@ def cold_leg(rq, dev, stream, inv_h, cache, kv, kpos, slots, k_cache, bs, reps=2
         cases[f"decode N={nt}"] = (lambda dx=dx, dp=dp: rq.inv_rope_fp8_quant(dx, dp, cache, 8))
     cases["insert16k"] = lambda: rq.rope_fp8_quant_insert(kv, kpos, cache, slots, k_cache, bs)
     us = {}
+    flush_us = []
     for name, fn in cases.items():
         g = graph_of(fn)
-        us[name] = round((timed(g) - t_base) / reps, 2)
+        g.replay()
+        diffs = []
+        for _ in range(rounds):
+            t1 = once(g)
+            t0 = once(base)
+            diffs.append(t1 - t0)
+            flush_us.append(t0)
+        us[name] = round(statistics.median(diffs) / reps, 2)
         del g
     del flush, base
-    return {"what": "device us per call after a 256 MiB write evicts L2: CUDA graphs of "
-                    f"{reps} x (write, call) minus {reps} x (write), median of {rounds} replays",
-            "flush_us": round(t_base / reps, 2), "us": us}
+    return {"what": "device us per call after a 160 MiB write evicts L2: CUDA graphs of "
+                    f"{reps} x (write, call) and {reps} x (write) replayed alternately, median "
+                    f"over {rounds} rounds of the difference / {reps}",
+            "flush_us": round(statistics.median(flush_us) / reps, 2), "us": us}
 
 
 def run_e2e(args, rq, dev, stream, world, inv_h, ins_h, cache, hpg, out, scales, kv, kpos, slots,

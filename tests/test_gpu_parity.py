@@ -1224,3 +1224,8 @@ def test_random_shapes_and_strides_bit_exact(rq, case):
     for mode in ("ue8m0", "bf16"):
         got = run_layout(rq, dict(inp, x=xd), mode, "token")
         assert_layout_parity(mode, got, oracle_layout(inp, mode))
+    # contiguous group-major outputs (the warp-rows kernel's group-major rows
+    # when there is more than one group)
+    for mode in ("fp8", "ue8m0"):
+        got = run_layout(rq, dict(inp, x=xd), mode, "group_major")
+        assert_layout_parity(mode, got, oracle_layout(inp, mode))
