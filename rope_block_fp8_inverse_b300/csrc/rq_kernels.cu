@@ -30,9 +30,14 @@ namespace rq {
 // word per row at scales + r -- the row-linear token-major layouts of the
 // layout call, which takes this kernel for them. kGroupMajor writes the
 // contiguous group-major layout instead ([G, N, hpg*512] codes and
-// [G, N, hpg*4] / [G, N, hpg] scales): the same walk over the input, each row
-// stored at its output row q = (g*N + t)*hpg + i, two integer operations more
-// per row than the token-major store.
+// [G, N, hpg*4] / [G, N, hpg] scales): the same rows, each stored at its
+// output row q = (g*N + t)*hpg + i.
+// The launcher sizes the grid so that one sweep of it (all warps, kRows rows
+// each) is a whole number of tokens (p.sweep_tokens): every warp then keeps
+// the same heads from sweep to sweep, and each of its rows advances by
+// constant steps in the input, the positions and the output. (A walk that
+// moved each warp to new (token, head) pairs cost 14% more instructions per
+// row with group-major output, measured on B300.)
 template <int kRows, int kMode = kOutFp8F32, bool kGroupMajor = false>
 __global__ void __launch_bounds__(kInvThreads, 4)
 inv_rope_fp8_quant_kernel(InvParams p) {
@@ -40,69 +45,71 @@ inv_rope_fp8_quant_kernel(InvParams p) {
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const uint32_t n_warps = (gridDim.x * blockDim.x) >> 5;
     const uint16_t* __restrict__ x = static_cast<const uint16_t*>(p.x);
     const int ca = chunk_a(lane);
     const bool rope_lane = lane >= kRopeLane0;
     const int cs_col = (rope_lane ? lane - kRopeLane0 : 0) * 4;
-    // rows walked without division: (token, head); token-major output needs
-    // no groups (one group of all heads), group-major output tracks them
-    const uint32_t wn = p.n_heads;
-    const uint32_t wg = kGroupMajor ? p.lay.hpg : p.n_heads;
-    const uint32_t wgroups = kGroupMajor ? p.n_heads / p.lay.hpg : 1u;
-    const RowStride step = row_stride(n_warps * kRows, wn, wg);
-    const RowStride next = row_stride(1, wn, wg);
-    RowPos base = row_pos(warp * kRows, wn, wg);
 
-    for (uint32_t r0 = warp * kRows; r0 < p.n_rows;
-         r0 += n_warps * kRows, row_advance(base, step, wn, wg, wgroups)) {
+    // A sweep of the grid is p.sweep_tokens (>= 1) whole tokens and n_heads
+    // is a multiple of kRows, so warp w keeps heads h0 .. h0 + kRows - 1 of
+    // one token in every sweep (rows w*kRows + j), the token advancing by
+    // sweep_tokens. Input, position and output then advance by constants (no
+    // row walk, no per-row multiply).
+    const uint32_t sweep_rows = p.sweep_tokens * p.n_heads;
+    if (warp * kRows >= sweep_rows) return;  // warp-uniform: idle warps of the grid
+    const uint32_t r0 = warp * kRows;
+    uint32_t t = r0 / p.n_heads;
+    const uint32_t h0 = r0 - t * p.n_heads;
+    const uint16_t* row = x + static_cast<int64_t>(t) * p.sx_t + static_cast<int64_t>(h0) * p.sx_h;
+    // output row of head h0 (token-major r0; group-major q), and the offset of
+    // head h0 + j from it (group-major: + (N - 1) * hpg once the heads cross
+    // into the next group)
+    uint32_t orow = r0;
+    uint32_t cross = kRows;  // first j in the next group
+    if (kGroupMajor) {
+        const uint32_t g = h0 / p.lay.hpg, i = h0 - g * p.lay.hpg;
+        orow = (g * p.n_tokens + t) * p.lay.hpg + i;
+        cross = p.lay.hpg - i;
+    }
+    const int64_t dx = static_cast<int64_t>(p.sweep_tokens) * p.sx_t;
+    const uint32_t dorow = kGroupMajor ? p.sweep_tokens * p.lay.hpg : sweep_rows;
+    for (; t < p.n_tokens; t += p.sweep_tokens, row += dx, orow += dorow) {
         uint4 a[kRows], b[kRows];
-        float4 c[kRows], s[kRows];
-        bool live[kRows];
-        uint32_t q[kRows];  // output row
-        RowPos w = base;
+        float4 c, s;
+        // the rows' reads do not wait for the position: only cos/sin do
 #pragma unroll
-        for (int i = 0; i < kRows; ++i) {
-            const uint32_t r = r0 + i;
-            if (i > 0) row_advance(w, next, wn, wg, wgroups);
-            live[i] = false;
-            q[i] = kGroupMajor ? (w.g * p.n_tokens + w.t) * wg + w.i : r;
-            if (r < p.n_rows) {  // warp-uniform
-                const uint32_t t = w.t;
-                const uint32_t h = w.h;
-                // the row's reads do not wait for its position: only cos/sin do
-                const uint16_t* row = x + static_cast<int64_t>(t) * p.sx_t +
-                                      static_cast<int64_t>(h) * p.sx_h;
-                a[i] = ld_stream16(row + 8 * ca);
-                b[i] = ld_stream16(row + 8 * (ca + 8));
-                const int64_t pos = __ldg(p.positions + t);
-                live[i] = static_cast<uint64_t>(pos) < static_cast<uint64_t>(p.cache_rows);
-                if (live[i]) {
-                    if (rope_lane) {
-                        const float* cs = p.cache + pos * kCacheWidth + cs_col;
-                        c[i] = ld_ro16(cs);
-                        s[i] = ld_ro16(cs + kHalfRope);
-                    }
-                } else if (lane == 0 && p.error_flags) {
-                    atomicOr(p.error_flags, RQ_FLAG_POSITION_RANGE);
-                }
-            }
+        for (int j = 0; j < kRows; ++j) {
+            a[j] = ld_stream16(row + j * p.sx_h + 8 * ca);
+            b[j] = ld_stream16(row + j * p.sx_h + 8 * (ca + 8));
+        }
+        const int64_t pos = __ldg(p.positions + t);
+        if (static_cast<uint64_t>(pos) >= static_cast<uint64_t>(p.cache_rows)) {  // warp-uniform
+            if (lane == 0 && p.error_flags) atomicOr(p.error_flags, RQ_FLAG_POSITION_RANGE);
+            continue;
+        }
+        if (rope_lane) {  // one cos/sin row serves the token's kRows heads
+            const float* cs = p.cache + pos * kCacheWidth + cs_col;
+            c = ld_ro16(cs);
+            s = ld_ro16(cs + kHalfRope);
         }
 #pragma unroll
-        for (int i = 0; i < kRows; ++i) {
-            if (!live[i]) continue;
-            const int64_t r = q[i];
+        for (int j = 0; j < kRows; ++j) {
+            const int64_t r = int64_t(orow) + j +
+                              (kGroupMajor && uint32_t(j) >= cross
+                                   ? int64_t(p.n_tokens - 1) * p.lay.hpg
+                                   : 0);
             float scale;
-            const uint4 qc = rope_quant_row<true>(a[i], b[i], rope_lane, c[i], s[i], p.eps, &scale);
+            const uint4 qc = rope_quant_row<true>(a[j], b[j], rope_lane, c, s, p.eps, &scale);
             if (kMode == kOutFp8F32) {
                 store_row(p.out + r * kHeadDim, p.scales + r * 4, lane, ca, qc, scale);
             } else {
                 uint8_t* codes = p.out + r * kHeadDim;
                 st_stream8(codes + 8 * ca, qc.x, qc.y);
                 st_stream8(codes + 8 * (ca + 8), qc.z, qc.w);
-                // byte b of row r's word: block b's biased exponent
+                // byte b of the row's word: block b's biased exponent
                 if ((lane & 7) == 0)
-                    st_stream1(reinterpret_cast<uint8_t*>(reinterpret_cast<uint32_t*>(p.scales) + r) +
+                    st_stream1(reinterpret_cast<uint8_t*>(reinterpret_cast<uint32_t*>(p.scales) +
+                                                          r) +
                                    (lane >> 3),
                                __float_as_uint(scale) >> 23);
             }
@@ -406,6 +413,26 @@ int grid_size(int64_t units, int units_per_block, int sm_count, int resident) {
 
 }  // namespace
 
+// The warp-rows kernel with kRows rows per warp and iteration: a persistent
+// grid of at most one full wave, and, when a sweep of that grid holds at
+// least one whole token, the sweep cut down to whole tokens (p.sweep_tokens)
+// so that every warp keeps its heads (the warps past the last whole token,
+// fewer than one token's rows per sweep, stay idle).
+template <int kRows, int kMode, bool kGroupMajor>
+cudaError_t launch_warp_rows(InvParams p, const DeviceInfo& dev, Variant slot,
+                             cudaStream_t stream) {
+    constexpr int kWarps = kInvThreads / 32;
+    auto k = inv_rope_fp8_quant_kernel<kRows, kMode, kGroupMajor>;
+    const int res = resident_blocks(dev.ordinal, slot, k, kInvThreads);
+    const int grid = grid_size(p.n_rows, kWarps * kRows, dev.sm_count, res);
+    const int64_t tokens = int64_t(grid) * kWarps * kRows / p.n_heads;
+    // more heads per token than one sweep holds (thousands): the layout
+    // kernel, which walks the rows, writes the same layout (p.lay)
+    if (tokens < 1) return launch_inv_rope_quant_layout(p, dev, stream);
+    p.sweep_tokens = static_cast<uint32_t>(tokens);
+    return launch_pdl(k, grid, kInvThreads, 0, stream, p);
+}
+
 cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev, int variant,
                                       cudaStream_t stream) {
     constexpr int kWarps = kInvThreads / 32;
@@ -416,18 +443,12 @@ cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev,
     // faster of the two from 2048 tokens x 32 heads up (0.98 vs 0.95 of the
     // copy peak at 16384 tokens).
     if (variant == kInvStream) return launch_inv_rope_fp8_quant_stream(p, dev, stream);
-    // warp-rows kernel: two rows in flight per warp when the grid fills the
-    // GPU, one otherwise (decode-sized calls spread over more warps)
-    if (int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4) {
-        auto k = inv_rope_fp8_quant_kernel<2>;
-        const int res = resident_blocks(dev.ordinal, kInv2, k, kInvThreads);
-        return launch_pdl(k, grid_size(p.n_rows, kWarps * 2, dev.sm_count, res), kInvThreads, 0,
-                          stream, p);
-    }
-    auto k = inv_rope_fp8_quant_kernel<1>;
-    const int res = resident_blocks(dev.ordinal, kInv1, k, kInvThreads);
-    return launch_pdl(k, grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0, stream,
-                      p);
+    // warp-rows kernel: two rows (heads of one token) in flight per warp when
+    // the grid fills the GPU and the head count is even, one otherwise
+    // (decode-sized calls spread over more warps)
+    if (int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4 && p.n_heads % 2 == 0)
+        return launch_warp_rows<2, kOutFp8F32, false>(p, dev, kInv2, stream);
+    return launch_warp_rows<1, kOutFp8F32, false>(p, dev, kInv1, stream);
 }
 
 template <int kMode>
@@ -451,16 +472,9 @@ template <int kMode, bool kGroupMajor>
 cudaError_t launch_rows(const InvParams& p, const DeviceInfo& dev, cudaStream_t stream) {
     constexpr int kWarps = kInvThreads / 32;
     constexpr int kSlot = kRowsVariant + 4 * kMode + (kGroupMajor ? 2 : 0);
-    if (int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4) {
-        auto k = inv_rope_fp8_quant_kernel<2, kMode, kGroupMajor>;
-        const int res = resident_blocks(dev.ordinal, Variant(kSlot + 1), k, kInvThreads);
-        return launch_pdl(k, grid_size(p.n_rows, kWarps * 2, dev.sm_count, res), kInvThreads, 0,
-                          stream, p);
-    }
-    auto k = inv_rope_fp8_quant_kernel<1, kMode, kGroupMajor>;
-    const int res = resident_blocks(dev.ordinal, Variant(kSlot), k, kInvThreads);
-    return launch_pdl(k, grid_size(p.n_rows, kWarps * 1, dev.sm_count, res), kInvThreads, 0,
-                      stream, p);
+    if (int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4 && p.n_heads % 2 == 0)
+        return launch_warp_rows<2, kMode, kGroupMajor>(p, dev, Variant(kSlot + 1), stream);
+    return launch_warp_rows<1, kMode, kGroupMajor>(p, dev, Variant(kSlot), stream);
 }
 
 cudaError_t launch_inv_rope_rows(const InvParams& p, const DeviceInfo& dev, int mode,
