@@ -536,15 +536,20 @@ def run_secondary(args, rq, dev, stream, inv_h, x, pos, cache, hpg, out, scales,
     # the "next" rows of the path: other output kinds and layouts
     modes = {}
     for name, mode, gm in (("fp8_group_major", "fp8", True), ("ue8m0", "ue8m0", False),
-                           ("ue8m0_group_major", "ue8m0", True), ("bf16", "bf16", False)):
+                           ("ue8m0_group_major", "ue8m0", True), ("bf16", "bf16", False),
+                           ("fp8_scales_transposed", "fp8", False)):
         mo, ms = rq.empty_outputs(n, h // hpg, hpg, mode, group_major=gm, device=dev)
+        if name.endswith("scales_transposed"):  # scales stored [G, hpg*4, N]
+            ms = torch.empty((h // hpg, ms.shape[2], n), dtype=ms.dtype, device=dev).permute(2, 0, 1)
         us = span_us(lambda: rq.inv_rope_quant(x, pos, cache, hpg, mode=mode, out=mo, scales=ms),
                      args.mode_launches)
         mb = W.inverse_bytes(n, h, mode)
         modes[name] = {"us": round(us, 2), "bytes": mb, "GBs": round(mb / us / 1e3, 1),
                        "frac_of_measured_peak": round(mb / us / 1e3 / peak, 4)}
         del mo, ms
-    res["output_modes"] = {"call": "rq_inv_rope_quant_layout (heads_per_group 8)",
+    res["output_modes"] = {"call": "rq_inv_rope_quant_layout (heads_per_group 8): warp-rows kernel "
+                                   "(token-major and contiguous group-major rows), warp-rows "
+                                   "layout kernel (bf16; transposed scales)",
                            "launches_each": args.mode_launches, "results": modes}
 
     # the fused q/kv op (q RMS norm + RoPE into a padded q_out, with the kv insert)

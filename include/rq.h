@@ -165,8 +165,7 @@ rq_status rq_inv_rope_fp8_quant_host(const void *x_bf16_host, int64_t n_tokens, 
  * copies in flight land, frees what it holds and exits, leaving the context
  * usable. Outputs of an injected call are unspecified. mask 0 and
  * spin_limit 0 restore normal operation.
- *   RQ_DEBUG_STREAM_STAGE  the TMA-ring inverse kernel (RQ_INV_STREAM and the
- *                          layout call's large heads_per_group % 8 == 0 case):
+ *   RQ_DEBUG_STREAM_STAGE  the TMA-ring inverse kernel (RQ_INV_STREAM):
  *                          warp 0 leaves its first tile unarmed
  *   RQ_DEBUG_GEMM_LOADS    rq_grouped_fp8_gemm and rq_grouped_fp8_gemm_ue8m0:
  *                          the first CTA's TMA producer issues no copy
@@ -306,10 +305,8 @@ typedef enum rq_out_mode {
  * t*H + h at out + r*512, its scales at r*4 or its word at r) and contiguous
  * group-major ones ([G, N, hpg*512] codes with [G, N, hpg*4] fp32 scales or
  * [G, N, hpg] words, 16-byte aligned) take the warp-rows kernel of
- * rq_inv_rope_fp8_quant. Other quantised layouts take the
- * TMA-ring kernel from 2048 rows per SM when heads_per_group is a multiple of
- * 8, and the warp-rows layout kernel otherwise. bf16 output always takes the
- * warp-rows layout kernel.
+ * rq_inv_rope_fp8_quant. Other layouts take the warp-rows layout kernel
+ * (quantising modes with each warp on fixed heads, bf16 by a row walk).
  */
 rq_status rq_inv_rope_quant_layout(const void *x_bf16, int64_t n_tokens, int64_t n_heads,
                                    int64_t x_stride_token, int64_t x_stride_head,

@@ -257,15 +257,10 @@ RQ_EXPORT rq_status rq_inv_rope_quant_layout(
     if (group_linear)
         return from_cuda(
             rq::launch_inv_rope_rows(p, dev, out_mode, true, static_cast<cudaStream_t>(stream)));
-    // large calls whose tiles fit the layout take the TMA-ring kernel
-    // bf16 output (no quantisation) stays on the warp-rows layout kernel at every size
-    const bool stream_it = p.lay.mode != rq::kOutBf16 &&
-                           int64_t(p.n_rows) >= int64_t(dev.sm_count) * rq::kStreamMinRowsPerSm &&
-                           rq::stream_layout_ok(p);
-    return from_cuda(stream_it ? rq::launch_inv_rope_fp8_quant_stream(
-                                     p, dev, static_cast<cudaStream_t>(stream))
-                               : rq::launch_inv_rope_quant_layout(
-                                     p, dev, static_cast<cudaStream_t>(stream)));
+    // any other layout: the warp-rows layout kernel (each warp on fixed heads
+    // for the quantising modes, the row walk for bf16)
+    return from_cuda(
+        rq::launch_inv_rope_quant_layout(p, dev, static_cast<cudaStream_t>(stream)));
 }
 
 RQ_EXPORT rq_status rq_rope_fp8_quant_insert(const void* kv_bf16, int64_t n_tokens,

@@ -12,6 +12,8 @@
 // of them. The pages' Triton kernel (one program per 1 to 4 heads) is prior
 // art: here a warp is the program, and the number of rows in flight per SM
 // is set by kRows x resident warps instead of by BLOCK_H.
+#include <algorithm>
+
 #include "rq_device.cuh"
 #include "rq_launch.h"
 
@@ -214,6 +216,98 @@ inv_rope_quant_layout_kernel(InvParams p) {
     }
 }
 
+// The layout kernel's fixed-head form (what the layout call launches when a
+// sweep of the grid holds at least one whole token): as in
+// inv_rope_fp8_quant_kernel, warp w keeps heads h0 .. h0 + kRows - 1 of one
+// token (n_heads a multiple of kRows) in every sweep of p.sweep_tokens
+// tokens, and its output and scale addresses advance by sweep_tokens times
+// the layout's token strides. The heads' offsets from head h0 within a token
+// are constants of the warp.
+template <int kRows, int kMode>
+__global__ void __launch_bounds__(kInvThreads, 4)
+inv_rope_quant_layout_fixed_kernel(InvParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint16_t* __restrict__ x = static_cast<const uint16_t*>(p.x);
+    const int ca = chunk_a(lane);
+    const bool rope_lane = lane >= kRopeLane0;
+    const int cs_col = (rope_lane ? lane - kRopeLane0 : 0) * 4;
+    constexpr int64_t kHeadBytes = kMode == kOutBf16 ? 2 * kHeadDim : kHeadDim;
+    // scale elements per head: 4 fp32 block scales, or one packed UE8M0 word
+    constexpr int64_t kScalesPerHead = kMode == kOutFp8F32 ? 4 : 1;
+    const uint32_t sweep_rows = p.sweep_tokens * p.n_heads;
+    if (warp * kRows >= sweep_rows) return;  // warp-uniform: idle warps of the grid
+    const uint32_t r0 = warp * kRows;
+    uint32_t t = r0 / p.n_heads;
+    const uint32_t h0 = r0 - t * p.n_heads;
+    const uint16_t* row = x + static_cast<int64_t>(t) * p.sx_t + static_cast<int64_t>(h0) * p.sx_h;
+    // head h of token t: codes at out + t*ot + g*og + i*kHeadBytes, its scale
+    // elements from scales + t*st + g*sg + i*kScalesPerHead*se
+    int64_t oo[kRows], so[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+        const uint32_t h = h0 + j, g = h / p.lay.hpg, i = h - g * p.lay.hpg;
+        oo[j] = int64_t(t) * p.lay.ot + int64_t(g) * p.lay.og + int64_t(i) * kHeadBytes;
+        so[j] = int64_t(t) * p.lay.st + int64_t(g) * p.lay.sg + int64_t(i) * kScalesPerHead * p.lay.se;
+    }
+    const int64_t dx = static_cast<int64_t>(p.sweep_tokens) * p.sx_t;
+    const int64_t doo = static_cast<int64_t>(p.sweep_tokens) * p.lay.ot;
+    const int64_t dso = static_cast<int64_t>(p.sweep_tokens) * p.lay.st;
+    for (; t < p.n_tokens; t += p.sweep_tokens, row += dx) {
+        uint4 a[kRows], b[kRows];
+        float4 c, s;
+        // the rows' reads do not wait for the position: only cos/sin do
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+            a[j] = ld_stream16(row + j * p.sx_h + 8 * ca);
+            b[j] = ld_stream16(row + j * p.sx_h + 8 * (ca + 8));
+        }
+        const int64_t pos = __ldg(p.positions + t);
+        const bool live = static_cast<uint64_t>(pos) < static_cast<uint64_t>(p.cache_rows);
+        if (live) {  // warp-uniform
+            if (rope_lane) {  // one cos/sin row serves the token's kRows heads
+                const float* cs = p.cache + pos * kCacheWidth + cs_col;
+                c = ld_ro16(cs);
+                s = ld_ro16(cs + kHalfRope);
+            }
+        } else if (lane == 0 && p.error_flags) {
+            atomicOr(p.error_flags, RQ_FLAG_POSITION_RANGE);
+        }
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+            if (live) {
+                uint8_t* head = p.out + oo[j];
+                if (kMode == kOutBf16) {
+                    uint4 qa, qb;
+                    rope_row_bf16<true>(a[j], b[j], rope_lane, c, s, &qa, &qb);
+                    st_stream16(head + 16 * ca, qa);
+                    st_stream16(head + 16 * (ca + 8), qb);
+                } else {
+                    float scale;
+                    const uint4 q = rope_quant_row<true>(a[j], b[j], rope_lane, c, s, p.eps, &scale);
+                    st_stream8(head + 8 * ca, q.x, q.y);
+                    st_stream8(head + 8 * (ca + 8), q.z, q.w);
+                    if ((lane & 7) == 0) {
+                        if (kMode == kOutFp8F32) {
+                            st_stream4f(p.scales + so[j] + (lane >> 3) * p.lay.se, scale);
+                        } else {
+                            // UE8M0: byte b of the head's word = block b's biased exponent
+                            st_stream1(reinterpret_cast<uint8_t*>(
+                                           reinterpret_cast<uint32_t*>(p.scales) + so[j]) +
+                                           (lane >> 3),
+                                       __float_as_uint(scale) >> 23);
+                        }
+                    }
+                }
+            }
+            oo[j] += doo;
+            so[j] += dso;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ insert
 
 template <int kRows>
@@ -389,7 +483,9 @@ constexpr int kMaxDevices = 64;
 // (kLay: 2 entries per output mode, one row or two rows per warp)
 // (kRowsVariant: 4 entries per scale encoding: one or two rows per warp,
 // token-major or group-major rows)
-enum Variant { kInv1, kInv2, kIns1, kFus1, kLay, kRowsVariant = kLay + 6, kVariants = kRowsVariant + 8 };
+// (kLayFixed: the same for the layout kernel's fixed-head form)
+enum Variant { kInv1, kInv2, kIns1, kFus1, kLay, kLayFixed = kLay + 6, kRowsVariant = kLayFixed + 6,
+               kVariants = kRowsVariant + 8 };
 
 template <typename K>
 int resident_blocks(int device, Variant v, K kernel, int threads) {
@@ -403,6 +499,11 @@ int resident_blocks(int device, Variant v, K kernel, int threads) {
     }
     return n;
 }
+
+// The fixed-head inverse kernels run at most 4 CTAs (32 warps) per SM: an
+// instance whose registers would allow a fifth (the bf16 layout, 48
+// registers) measured 3% slower with it on B300.
+constexpr int kMaxCtasPerSm = 4;
 
 // Persistent grid: enough CTAs for the work, at most one full wave.
 int grid_size(int64_t units, int units_per_block, int sm_count, int resident) {
@@ -423,7 +524,7 @@ cudaError_t launch_warp_rows(InvParams p, const DeviceInfo& dev, Variant slot,
                              cudaStream_t stream) {
     constexpr int kWarps = kInvThreads / 32;
     auto k = inv_rope_fp8_quant_kernel<kRows, kMode, kGroupMajor>;
-    const int res = resident_blocks(dev.ordinal, slot, k, kInvThreads);
+    const int res = std::min(resident_blocks(dev.ordinal, slot, k, kInvThreads), kMaxCtasPerSm);
     const int grid = grid_size(p.n_rows, kWarps * kRows, dev.sm_count, res);
     const int64_t tokens = int64_t(grid) * kWarps * kRows / p.n_heads;
     // more heads per token than one sweep holds (thousands): the layout
@@ -454,8 +555,42 @@ cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev,
 template <int kMode>
 cudaError_t launch_layout(const InvParams& p, const DeviceInfo& dev, cudaStream_t stream) {
     constexpr int kWarps = kInvThreads / 32;
-    // two rows per warp for the quantising modes of large calls; bf16 output
-    // keeps one (measured 0.99 of the copy peak at 16384 x 32, against 0.95)
+    // Quantising modes: each warp on fixed heads (two heads of one token when
+    // the call fills the GPU and the head count is even), when a sweep of the
+    // grid holds a whole token. Measured on B300 at 16384 x 32 heads: fp8 /
+    // UE8M0 with transposed scales 134.0 / 126.6 us, group-major with a padded
+    // group stride 127.1 / 126.8 us, against 148.6 / 149.4 and 134.7 / 134.7
+    // us on the TMA-ring kernel. bf16 output keeps the row walk at one row per
+    // warp (166.9 us against 170.2 us with fixed heads, and 0.95 of the copy
+    // peak with two rows per warp).
+    if (kMode != kOutBf16) {
+        InvParams q = p;
+        const bool two = int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4 && p.n_heads % 2 == 0;
+        if (two) {
+            auto k = inv_rope_quant_layout_fixed_kernel<2, kMode>;
+            const int res = std::min(
+                resident_blocks(dev.ordinal, Variant(kLayFixed + 2 * kMode + 1), k, kInvThreads),
+                kMaxCtasPerSm);
+            const int grid = grid_size(p.n_rows, kWarps * 2, dev.sm_count, res);
+            const int64_t tokens = int64_t(grid) * kWarps * 2 / p.n_heads;
+            if (tokens >= 1) {
+                q.sweep_tokens = static_cast<uint32_t>(tokens);
+                return launch_pdl(k, grid, kInvThreads, 0, stream, q);
+            }
+        } else {
+            auto k = inv_rope_quant_layout_fixed_kernel<1, kMode>;
+            const int res = std::min(
+                resident_blocks(dev.ordinal, Variant(kLayFixed + 2 * kMode), k, kInvThreads),
+                kMaxCtasPerSm);
+            const int grid = grid_size(p.n_rows, kWarps, dev.sm_count, res);
+            const int64_t tokens = int64_t(grid) * kWarps / p.n_heads;
+            if (tokens >= 1) {
+                q.sweep_tokens = static_cast<uint32_t>(tokens);
+                return launch_pdl(k, grid, kInvThreads, 0, stream, q);
+            }
+        }
+        // more heads per token than a sweep holds: walk the rows
+    }
     if (kMode != kOutBf16 && int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4) {
         auto k = inv_rope_quant_layout_kernel<2, kMode>;
         const int res = resident_blocks(dev.ordinal, Variant(kLay + 2 * kMode + 1), k, kInvThreads);

@@ -192,14 +192,6 @@ enum InvVariant {
     kInvStream = 2       // one TMA ring per warp (rq_stream.cu)
 };
 
-// rq_inv_rope_quant_layout takes the stream kernel from this many rows per
-// SM up, for quantising layouts that are neither row-linear token-major nor
-// contiguous group-major (those two take the warp-rows kernel) when
-// heads_per_group is a multiple of 8 (measured on B300 at 16384 tokens x 32
-// heads: fp8 0.93 vs 0.92 of the copy peak for the warp-rows layout kernel,
-// UE8M0 0.925 vs 0.92; bf16 output runs faster on the warp-rows layout
-// kernel, 0.99 vs 0.95, and always takes it).
-constexpr int64_t kStreamMinRowsPerSm = 2048;
 
 
 cudaError_t launch_inv_rope_fp8_quant(const InvParams& p, const DeviceInfo& dev, int variant,
@@ -213,10 +205,9 @@ cudaError_t launch_inv_rope_rows(const InvParams& p, const DeviceInfo& dev, int 
                                  bool group_major, cudaStream_t stream);
 cudaError_t launch_inv_rope_quant_layout(const InvParams& p, const DeviceInfo& dev,
                                          cudaStream_t stream);
+// The TMA-ring kernel (RQ_INV_STREAM) into the plain op's contiguous output.
 cudaError_t launch_inv_rope_fp8_quant_stream(const InvParams& p, const DeviceInfo& dev,
                                              cudaStream_t stream);
-// Whether the stream kernel can write p's output layout (tiles within a group).
-bool stream_layout_ok(const InvParams& p);
 cudaError_t launch_rope_fp8_quant_insert(const InsParams& p, const DeviceInfo& dev,
                                          cudaStream_t stream);
 cudaError_t launch_qnorm_rope_kv_insert(const FusedParams& p, const DeviceInfo& dev,

@@ -1,9 +1,8 @@
 // rq_stream.cu -- the inverse-RoPE + block-FP8 quant kernel built as one
-// independent TMA stream per warp (sm_103a), and its launcher. It serves the
-// RQ_INV_STREAM variant and the layout call's large quantised layouts that
-// are neither row-linear nor contiguous group-major (padded or transposed
-// strides); the default kernel of
-// the plain op is the warp-rows kernel in rq_kernels.cu.
+// independent TMA stream per warp (sm_103a), and its launcher: the
+// RQ_INV_STREAM variant of the plain op (contiguous [N, G, hpg*512] codes and
+// [N, G, hpg*4] fp32 scales). The default kernel of the plain op, and of
+// every layout, is the warp-rows kernel in rq_kernels.cu.
 //
 // Every warp owns a private ring of kStages shared-memory stages. A stage
 // holds one tile -- kRows consecutive heads of one token (1 KiB each) plus
@@ -80,10 +79,9 @@ struct TileWalk {
 
 }  // namespace
 
-// kMode: what is written per head (OutMode); kScaleBulk: the tile's scales are
-// contiguous and 16-byte aligned, so they leave with one bulk store too
-// (otherwise each goes out with its own store, at any element stride).
-template <int kRows, int kStages, int kMode, bool kScaleBulk>
+// kRows heads per tile (n_heads need not be a multiple: the last tile of a
+// token is short), kStages tiles in flight per warp.
+template <int kRows, int kStages>
 __global__ void __launch_bounds__(kStreamWarps * 32)
 inv_rope_fp8_quant_stream_kernel(InvParams p) {
     pdl_wait();
@@ -176,92 +174,44 @@ inv_rope_fp8_quant_stream_kernel(InvParams p) {
                 c4 = lds16f(st + kRows * R::kRowBytes + cs_off);
                 s4 = lds16f(st + kRows * R::kRowBytes + kHalfRope * 4 + cs_off);
             }
-            // the tile's heads h0 .. h0 + nrows - 1 lie in one output group
-            // (heads_per_group is a multiple of kRows): head hig0 + i of group g
-            const uint32_t g = h0 / p.lay.hpg;
-            const uint32_t hig0 = h0 - g * p.lay.hpg;
-            constexpr int64_t kHeadBytes = kMode == kOutBf16 ? 2 * kHeadDim : kHeadDim;
-            uint8_t* head0 = p.out + int64_t(cw.t) * p.lay.ot + int64_t(g) * p.lay.og +
-                             int64_t(hig0) * kHeadBytes;
-            const int64_t sbase = int64_t(cw.t) * p.lay.st + int64_t(g) * p.lay.sg;
-            if (kMode == kOutBf16) {
-                // no quantisation: each lane writes its 2 x 16 bytes directly
+            // contiguous output: the tile's codes and scales are contiguous
+            uint8_t* head0 = p.out + (int64_t(cw.t) * p.n_heads + h0) * kHeadDim;
+            float* scale0 = p.scales + (int64_t(cw.t) * p.n_heads + h0) * 4;
+            // the tile's codes and scales are gathered in output buffer j % 2
+            // and leave with two bulk stores: the buffer's previous stores
+            // (tile j - 2, one commit group older than the newest) must have
+            // finished reading it
+            const uint32_t ob = out0 + (j & 1u) * R::kOutBytes;
+            const uint32_t osc = ob + kRows * kHeadDim;
+            if (lane == 0) bulk_wait_read_all_but_newest();
+            __syncwarp();
 #pragma unroll
-                for (int i = 0; i < kRows; ++i) {
-                    if (uint32_t(i) < nrows) {
-                        const uint32_t row = st + i * R::kRowBytes;
-                        uint4 qa, qb;
-                        rope_row_bf16<true>(lds16(row + 16 * ca), lds16(row + 16 * (ca + 8)),
-                                            rope_lane, c4, s4, &qa, &qb);
-                        st_stream16(head0 + i * kHeadBytes + 16 * ca, qa);
-                        st_stream16(head0 + i * kHeadBytes + 16 * (ca + 8), qb);
-                    }
-                }
-            } else {
-                // the tile's codes (and, with kScaleBulk, its scales) are
-                // gathered in output buffer j % 2 and leave with bulk stores:
-                // the buffer's previous store (tile j - 2, one commit group
-                // older than the newest) must have finished reading it
-                const uint32_t ob = out0 + (j & 1u) * R::kOutBytes;
-                const uint32_t osc = ob + kRows * kHeadDim;
-                if (lane == 0) bulk_wait_read_all_but_newest();
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < kRows; ++i) {
-                    if (uint32_t(i) < nrows) {
-                        const uint32_t row = st + i * R::kRowBytes;
-                        const uint4 a = lds16(row + 16 * ca);
-                        const uint4 b = lds16(row + 16 * (ca + 8));
-                        float scale;
-                        const uint4 q =
-                            rope_quant_row<true>(a, b, rope_lane, c4, s4, p.eps, &scale);
-                        const uint32_t o = ob + i * kHeadDim;
-                        sts8(o + 8 * ca, q.x, q.y);
-                        sts8(o + 8 * (ca + 8), q.z, q.w);
-                        const int64_t hig = int64_t(hig0) + i;
-                        if (kMode == kOutFp8F32) {
-                            if ((lane & 7) == 0) {
-                                if (kScaleBulk)
-                                    sts4f(osc + i * 16 + (lane >> 3) * 4, scale);
-                                else
-                                    st_stream4f(p.scales + sbase + (hig * 4 + (lane >> 3)) * p.lay.se,
-                                                scale);
-                            }
-                        } else if ((lane & 7) == 0) {
-                            // UE8M0: the first lane of block b writes byte b of
-                            // the head's word, the scale's biased exponent
-                            const uint32_t e = __float_as_uint(scale) >> 23;
-                            if (kScaleBulk)
-                                sts1(osc + i * 4 + (lane >> 3), e);
-                            else
-                                st_stream1(reinterpret_cast<uint8_t*>(
-                                               reinterpret_cast<uint32_t*>(p.scales) + sbase +
-                                               hig * p.lay.se) +
-                                               (lane >> 3),
-                                           e);
-                        }
-                    }
-                }
-                fence_proxy_async_smem();  // this lane's writes, visible to the bulk stores
-                __syncwarp();
-                if (lane == 0) {
-                    bulk_s2g(head0, ob, nrows * kHeadDim);
-                    if (kScaleBulk) {
-                        if (kMode == kOutFp8F32)
-                            bulk_s2g(p.scales + sbase + int64_t(hig0) * 4, osc, nrows * 16);
-                        else
-                            bulk_s2g(reinterpret_cast<uint32_t*>(p.scales) + sbase + hig0, osc,
-                                     nrows * 4);
-                    }
+            for (int i = 0; i < kRows; ++i) {
+                if (uint32_t(i) < nrows) {
+                    const uint32_t row = st + i * R::kRowBytes;
+                    const uint4 a = lds16(row + 16 * ca);
+                    const uint4 b = lds16(row + 16 * (ca + 8));
+                    float scale;
+                    const uint4 q = rope_quant_row<true>(a, b, rope_lane, c4, s4, p.eps, &scale);
+                    const uint32_t o = ob + i * kHeadDim;
+                    sts8(o + 8 * ca, q.x, q.y);
+                    sts8(o + 8 * (ca + 8), q.z, q.w);
+                    if ((lane & 7) == 0) sts4f(osc + i * 16 + (lane >> 3) * 4, scale);
                 }
             }
+            fence_proxy_async_smem();  // this lane's writes, visible to the bulk stores
+            __syncwarp();
+            if (lane == 0) {
+                bulk_s2g(head0, ob, nrows * kHeadDim);
+                bulk_s2g(scale0, osc, nrows * 16);
+            }
         }
-        if (kMode != kOutBf16 && lane == 0) bulk_commit();  // one group per tile (empty if skipped)
+        if (lane == 0) bulk_commit();  // one group per tile (empty if skipped)
         cw.next();
         __syncwarp();  // every lane has read stage s: it may be refilled
         if (j + kStages < n_mine) issue(j + kStages);
     }
-    if (kMode != kOutBf16 && lane == 0) bulk_wait_all();  // no bulk store may read smem at exit
+    if (lane == 0) bulk_wait_all();  // no bulk store may read smem at exit
     __syncwarp();
     if (!ok) {
         // a wait gave up (never expected): report it, and let no copy still
@@ -283,9 +233,8 @@ constexpr int kMaxDevices = 64;
 
 // Opt in to more than 48 KiB of dynamic shared memory (once per device and
 // kernel instance) and read the resulting residency.
-template <int kMode, bool kScaleBulk>
 cudaError_t stream_setup(int device, int* resident) {
-    auto kernel = inv_rope_fp8_quant_stream_kernel<RQ_STREAM_ROWS, RQ_STREAM_STAGES, kMode, kScaleBulk>;
+    auto kernel = inv_rope_fp8_quant_stream_kernel<RQ_STREAM_ROWS, RQ_STREAM_STAGES>;
     static thread_local int cache[kMaxDevices] = {0};
     const int d = (device >= 0 && device < kMaxDevices) ? device : 0;
     if (cache[d] == 0) {
@@ -306,50 +255,20 @@ cudaError_t stream_setup(int device, int* resident) {
     return cudaSuccess;
 }
 
-template <int kMode, bool kScaleBulk>
-cudaError_t launch_stream(const InvParams& p, const DeviceInfo& dev, cudaStream_t stream) {
+}  // namespace
+
+cudaError_t launch_inv_rope_fp8_quant_stream(const InvParams& p, const DeviceInfo& dev,
+                                             cudaStream_t stream) {
     int resident = 1;
-    cudaError_t e = stream_setup<kMode, kScaleBulk>(dev.ordinal, &resident);
+    cudaError_t e = stream_setup(dev.ordinal, &resident);
     if (e != cudaSuccess) return e;
     const int64_t chunks = (p.n_heads + RQ_STREAM_ROWS - 1) / RQ_STREAM_ROWS;
     const int64_t warps_needed = int64_t(p.n_tokens) * chunks;
     const int64_t ctas_needed = (warps_needed + kStreamWarps - 1) / kStreamWarps;
     const int64_t cap = int64_t(dev.sm_count) * resident;
     const int grid = static_cast<int>(ctas_needed < cap ? ctas_needed : cap);
-    return launch_pdl(
-        inv_rope_fp8_quant_stream_kernel<RQ_STREAM_ROWS, RQ_STREAM_STAGES, kMode, kScaleBulk>, grid,
-        kStreamWarps * 32, StreamRing::kCtaBytes, stream, p);
-}
-
-}  // namespace
-
-bool stream_layout_ok(const InvParams& p) {
-    // a tile of RQ_STREAM_ROWS heads must stay inside one output group
-    return p.lay.hpg % RQ_STREAM_ROWS == 0;
-}
-
-bool stream_scale_bulk_ok(const InvParams& p) {
-    if (p.lay.mode == kOutBf16) return false;
-    // scales contiguous within the group, and every tile's run 16-byte aligned
-    // and a multiple of 16 bytes long (UE8M0: 4 bytes per head)
-    const bool full_tiles = p.lay.mode == kOutFp8F32 || p.n_heads % 4 == 0;
-    return p.lay.se == 1 && p.lay.st % 4 == 0 && p.lay.sg % 4 == 0 &&
-           (reinterpret_cast<uintptr_t>(p.scales) & 15) == 0 && full_tiles;
-}
-
-cudaError_t launch_inv_rope_fp8_quant_stream(const InvParams& p, const DeviceInfo& dev,
-                                             cudaStream_t stream) {
-    const bool bulk = stream_scale_bulk_ok(p);
-    switch (p.lay.mode) {
-        case kOutFp8F32:
-            return bulk ? launch_stream<kOutFp8F32, true>(p, dev, stream)
-                        : launch_stream<kOutFp8F32, false>(p, dev, stream);
-        case kOutFp8Ue8m0:
-            return bulk ? launch_stream<kOutFp8Ue8m0, true>(p, dev, stream)
-                        : launch_stream<kOutFp8Ue8m0, false>(p, dev, stream);
-        default:
-            return launch_stream<kOutBf16, false>(p, dev, stream);
-    }
+    return launch_pdl(inv_rope_fp8_quant_stream_kernel<RQ_STREAM_ROWS, RQ_STREAM_STAGES>, grid,
+                      kStreamWarps * 32, StreamRing::kCtaBytes, stream, p);
 }
 
 }  // namespace rq
