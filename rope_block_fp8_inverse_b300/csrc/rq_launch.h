@@ -148,6 +148,9 @@ struct IdxParams {
     uint8_t* out;             // [N, H, 128] e4m3 codes
     float* weights_out;       // [N, H] fp32
     uint32_t* error_flags;
+    // tokens per sweep of the grid when a sweep is whole tokens (set by the
+    // launcher; every 8-lane head slot then keeps its head), else 0
+    uint32_t sweep_tokens;
 };
 
 // Arguments of the grouped FP8 GEMM (rq_grouped_fp8_gemm).

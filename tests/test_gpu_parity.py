@@ -644,8 +644,11 @@ def oracle_indexer(inp, style, positions=None):
 
 
 @pytest.mark.parametrize("style", ["neox", "gptj"])
-@pytest.mark.parametrize("n,h", [(1, 1), (3, 64), (37, 7), (500, 64)])
+@pytest.mark.parametrize("n,h", [(1, 1), (3, 64), (37, 7), (500, 64), (1, 9), (5, 9)])
 def test_indexer_exact(rq, style, n, h):
+    """Small shapes against the oracle, bit-exact. (1, 9): no whole-token sweep
+    holds a multiple of 4 heads, so the row-walk kernel runs; (5, 9): the
+    fixed-head kernel over two sweeps of 4 tokens with an odd head count."""
     spec = W.IndexerSpec("idx", n, h, 4096, seed=n + h)
     inp = W.indexer_inputs(spec)
     inp["positions"] = torch.randint(0, 4096, (n,), generator=torch.Generator().manual_seed(n))
