@@ -346,19 +346,46 @@ def run_ours(args, world, rank, local):
         inverse_call()
         insert_call()
 
-    def span_us(fn, launches):
+    enqueue = {}
+
+    def held(name, body, est_host_ms, launches):
+        """Run `body` (it enqueues launches and records events on `stream`)
+        behind a spinning kernel that holds the stream until the host has
+        enqueued all of it, so the events time device work only. The host's
+        enqueue time is measured: if it outlasted the block, the device may
+        have waited on the host inside the timed region, so the run is
+        repeated with a longer block (up to three times; a loop with more
+        launches than the launch queue holds cannot be covered, and says so
+        in `enqueue`)."""
+        block = max(2.0, 2.0 * est_host_ms + 1.0)
+        tries = 3 if launches <= 1024 else 1
+        for attempt in range(tries):
+            torch.cuda.synchronize(dev)
+            block_stream(stream, block)
+            t0 = time.perf_counter()
+            body()
+            host_ms = (time.perf_counter() - t0) * 1e3
+            torch.cuda.synchronize(dev)
+            covered = host_ms < 0.9 * block
+            if covered:
+                break
+            block = min(4000.0, 2.0 * host_ms + 5.0)
+        enqueue[name] = {"host_ms": round(host_ms, 2), "block_ms": round(block, 2),
+                         "covered": covered, "tries": attempt + 1}
+
+    def span_us(fn, launches, name):
         """Mean µs per launch of `launches` back-to-back calls: one event pair
         around all of them on the launching stream, after 3 warm calls, with
         the stream held by a spinning kernel while the host enqueues them."""
         host = host_us_per_call(fn, 3)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        block_stream(stream, 1.0 + 1.5e-3 * host * launches)
-        a.record(stream)
-        for _ in range(launches):
-            fn()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
+
+        def body():
+            a.record(stream)
+            for _ in range(launches):
+                fn()
+            b.record(stream)
+        held(name, body, host * launches * 1e-3, launches)
         return a.elapsed_time(b) * 1e3 / launches
 
     # clocks are sampled (read only) from before the warm-up to the end of the
@@ -385,14 +412,14 @@ def run_ours(args, world, rank, local):
         # the launches (the insert may start while the inverse drains), and the
         # launches enqueued while a spinning kernel holds the stream
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def timed_steps():
+            start.record(stream)
+            for _ in range(args.steps):
+                step()
+            end.record(stream)
         barrier(world)
-        torch.cuda.synchronize(dev)
-        block_stream(stream, 1.0 + min(200.0, 1.5e-3 * host_step_us * args.steps))
-        start.record(stream)
-        for _ in range(args.steps):
-            step()
-        end.record(stream)
-        torch.cuda.synchronize(dev)
+        held("timed_steps", timed_steps, host_step_us * args.steps * 1e-3, 2 * args.steps)
         barrier(world)
         total_ms = max_over_ranks(start.elapsed_time(end), world)
         ms_step = total_ms / args.steps
@@ -400,8 +427,8 @@ def run_ours(args, world, rank, local):
         # the dominant kernel back to back (its mean launch duration in a
         # stream of launches: the roofline's figure), and the insert alone
         span_launches = max(50, min(300, args.steps))
-        inv_span = span_us(inverse_call, span_launches)
-        ins_span = span_us(insert_call, span_launches)
+        inv_span = span_us(inverse_call, span_launches, "inverse_span")
+        ins_span = span_us(insert_call, span_launches, "insert_span")
 
         # the same steps with an event pair around each launch: the per-launch
         # durations including each launch's own start-up and drain (no overlap
@@ -410,15 +437,15 @@ def run_ours(args, world, rank, local):
         inv_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(ev_steps)]
         ins_ev = [torch.cuda.Event(enable_timing=True) for _ in range(ev_steps)]
-        torch.cuda.synchronize(dev)
-        block_stream(stream, 1.0 + min(200.0, 1.5e-3 * host_step_us * ev_steps))
-        for i in range(ev_steps):
-            inv_ev[i][0].record(stream)
-            inverse_call()
-            inv_ev[i][1].record(stream)
-            insert_call()
-            ins_ev[i].record(stream)
-        torch.cuda.synchronize(dev)
+
+        def event_pairs():
+            for i in range(ev_steps):
+                inv_ev[i][0].record(stream)
+                inverse_call()
+                inv_ev[i][1].record(stream)
+                insert_call()
+                ins_ev[i].record(stream)
+        held("event_pairs", event_pairs, 2.0 * host_step_us * ev_steps * 1e-3, 2 * ev_steps)
         inv_all = sorted(a.elapsed_time(b) for a, b in inv_ev)
         inv_ms_ev = statistics.fmean(inv_all)
         inv_pct = {f"p{q}": round(inv_all[min(len(inv_all) - 1, int(len(inv_all) * q / 100))] * 1e3, 2)
@@ -496,6 +523,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(),
+        "enqueue": enqueue,
     }
     result.update(secondary)
     if args.inv_tokens and args.inv_tokens != INV_SPEC.n_tokens:
@@ -523,7 +551,7 @@ def run_secondary(args, rq, dev, stream, inv_h, x, pos, cache, hpg, out, scales,
     io = torch.empty((ix.shape[0], ix.shape[1] // ihpg, ihpg * 512), dtype=torch.uint8, device=dev)
     isc = torch.empty((ix.shape[0], ix.shape[1] // ihpg, ihpg * 4), dtype=torch.float32, device=dev)
     us = span_us(lambda: rq.inv_rope_fp8_quant(ix, ip, ic, ihpg, out=io, scales=isc),
-                 args.mode_launches)
+                 args.mode_launches, "irregular")
     ib = W.inverse_bytes(ix.shape[0], ix.shape[1])
     res["irregular"] = {"kernel": INV_KERNEL_NAME, "workload": "irregular (N=8192, H=24, "
                         "heads_per_group=6, positions U[0,32768), cache 32768 rows)",
@@ -542,7 +570,7 @@ def run_secondary(args, rq, dev, stream, inv_h, x, pos, cache, hpg, out, scales,
         if name.endswith("scales_transposed"):  # scales stored [G, hpg*4, N]
             ms = torch.empty((h // hpg, ms.shape[2], n), dtype=ms.dtype, device=dev).permute(2, 0, 1)
         us = span_us(lambda: rq.inv_rope_quant(x, pos, cache, hpg, mode=mode, out=mo, scales=ms),
-                     args.mode_launches)
+                     args.mode_launches, name)
         mb = W.inverse_bytes(n, h, mode)
         modes[name] = {"us": round(us, 2), "bytes": mb, "GBs": round(mb / us / 1e3, 1),
                        "frac_of_measured_peak": round(mb / us / 1e3 / peak, 4)}
@@ -560,10 +588,10 @@ def run_secondary(args, rq, dev, stream, inv_h, x, pos, cache, hpg, out, scales,
     fw = W.norm_weight(W.FUSED16K.seed).to(dev)
     us = span_us(lambda: rq.qnorm_rope_kv_rope_quant_insert(
         fq, fkv, fpos, cache, fsl, fkc, fi["block_size"], fi["q_head_padded"], q_out=fqo),
-        args.mode_launches)
+        args.mode_launches, "fused_qkv")
     us_w = span_us(lambda: rq.qnorm_rope_kv_rope_quant_insert(
         fq, fkv, fpos, cache, fsl, fkc, fi["block_size"], fi["q_head_padded"], q_out=fqo,
-        norm_weight=fw), args.mode_launches)
+        norm_weight=fw), args.mode_launches, "fused_qkv_weighted")
     fb = W.fused_bytes(W.FUSED16K.n_tokens, W.FUSED16K.n_heads_q, W.FUSED16K.q_head_padded)
     res["fused_qkv"] = {"kernel": "qnorm_rope_kv_insert_kernel", "workload": "fused16k (N=16384, "
                         "Hq=32 padded to 64, kv into 512x64 slots)", "us": round(us, 2),
@@ -586,10 +614,11 @@ def run_secondary(args, rq, dev, stream, inv_h, x, pos, cache, hpg, out, scales,
     for style in ("neox", "gptj"):
         us = span_us(lambda: rq.indexer_q_rope_quant(iq, ipos, cache, iw, xi["softmax_scale"],
                                                      xi["head_scale"], rope_style=style, out=ico,
-                                                     weights_out=iwo), args.mode_launches)
+                                                     weights_out=iwo), args.mode_launches,
+                     f"indexer_{style}")
         indexer[style] = {"us": round(us, 2), "bytes": ib, "GBs": round(ib / us / 1e3, 1),
                           "frac_of_measured_peak": round(ib / us / 1e3 / peak, 4)}
-    res["indexer_q"] = {"kernel": "indexer_q_rope_quant_kernel", "workload": "indexer16k "
+    res["indexer_q"] = {"kernel": "indexer_q_rope_quant_fixed_kernel", "workload": "indexer16k "
                         "(N=16384, H=64, head 128, dims 0..63 rotary)",
                         "launches_each": args.mode_launches, "results": indexer}
     del iq, iw, ipos, ico, iwo
@@ -638,14 +667,14 @@ def gemm_leg(args, rq, dev, x, pos, cache, hpg, out, scales, span_us):
         rq.grouped_fp8_gemm_ue8m0(mx_codes, mx_words, wc, w_sf, out=gy)
 
     op_ue8m0()
-    us_op = span_us(op_ue8m0, gl)
-    us_mx = span_us(mx_call, gl)
-    us_pair = span_us(lambda: (op_ue8m0(), mx_call()), gl)
+    us_op = span_us(op_ue8m0, gl, "gemm_path_op")
+    us_mx = span_us(mx_call, gl, "gemm_ue8m0")
+    us_pair = span_us(lambda: (op_ue8m0(), mx_call()), gl, "gemm_path_pair")
 
     rq.inv_rope_fp8_quant(x, pos, cache, hpg, out=out, scales=scales)
-    us = span_us(lambda: rq.grouped_fp8_gemm(out, scales, wc, ws, out=gy), gl)
+    us = span_us(lambda: rq.grouped_fp8_gemm(out, scales, wc, ws, out=gy), gl, "gemm_fp32")
     us_fused = span_us(lambda: rq.inv_rope_fp8_quant_gemm(x, pos, cache, hpg, wc, ws, out=gy),
-                       max(5, gl // 4))
+                       max(5, gl // 4), "gemm_fused")
     del mx_codes, mx_words, wc, ws, gy
     return {"workload": f"grouped FP8 GEMM: M={n}, G={h // hpg}, K={hpg * 512}, n_out={g_out} "
                         "per group, block scales 1x128 (A) / 128x128 (W)", "flop": flop,
