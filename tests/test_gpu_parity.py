@@ -366,7 +366,8 @@ def test_insert_strided_kv(rq):
 
 # ---------------------------------------------------------------- output kinds and layouts
 
-LAYOUTS = ["token_major", "group_major", "scales_transposed"]
+LAYOUTS = ["token_major", "group_major", "scales_transposed", "group_major_padded"]
+GROUP_PAD = 3  # tokens of padding after each group in the padded group-major storage
 
 
 def _outputs(rq, n, g, hpg, mode, layout):
@@ -375,6 +376,13 @@ def _outputs(rq, n, g, hpg, mode, layout):
     if layout == "scales_transposed" and sc is not None:
         w = sc.shape[2]
         sc = torch.empty((g, w, n), dtype=sc.dtype, device=dev).permute(2, 0, 1)
+    if layout == "group_major_padded":
+        # [G, N + pad, W] storage: a group stride that is not N * W
+        out = torch.empty((g, n + GROUP_PAD, out.shape[2]), dtype=out.dtype,
+                          device=dev)[:, :n].permute(1, 0, 2)
+        if sc is not None:
+            sc = torch.empty((g, n + GROUP_PAD, sc.shape[2]), dtype=sc.dtype,
+                             device=dev)[:, :n].permute(1, 0, 2)
     return out, sc
 
 
@@ -456,6 +464,38 @@ def test_layout_full_size_every_output(rq, mode, layout):
         want = (wc, oracle.pack_ue8m0(ws).view(np.int32)) if mode == "ue8m0" else (wc, ws)
     got = run_layout(rq, inp, mode, layout)
     assert_layout_parity(mode, got, want)
+
+
+@pytest.mark.parametrize("mode", ["fp8", "ue8m0", "bf16"])
+def test_layout_padded_group_major_leaves_the_padding_alone(rq, mode):
+    """Padded group-major storage: every output byte equals the oracle's and
+    the padding tokens after each group keep their sentinel (no write lands
+    outside the view)."""
+    inp = W.inverse_inputs(W.InverseSpec("pad", 300, 32, 8, 4096, "uniform", True, seed=5))
+    dev = torch.device("cuda:0")
+    n, g, hpg = 300, 4, 8
+    w = hpg * 512
+    odt = torch.bfloat16 if mode == "bf16" else torch.uint8
+    ost = torch.empty((g, n + GROUP_PAD, w), dtype=odt, device=dev)
+    ost.view(torch.uint8).fill_(0xA5)
+    out = ost[:, :n].permute(1, 0, 2)
+    sst, sc = None, None
+    if mode != "bf16":
+        sw, sdt = (hpg * 4, torch.float32) if mode == "fp8" else (hpg, torch.int32)
+        sst = torch.empty((g, n + GROUP_PAD, sw), dtype=sdt, device=dev)
+        sst.view(torch.uint8).fill_(0xA5)
+        sc = sst[:, :n].permute(1, 0, 2)
+    rq.inv_rope_quant(inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev),
+                      hpg, mode=mode, out=out, scales=sc)
+    torch.cuda.synchronize()
+    assert torch.all(ost[:, n:].view(torch.uint8) == 0xA5)
+    if sst is not None:
+        assert torch.all(sst[:, n:].view(torch.uint8) == 0xA5)
+    if mode == "bf16":
+        got = (out.contiguous().view(torch.int16).cpu().numpy().view(np.uint16), None)
+    else:
+        got = (out.contiguous().view(torch.uint8).cpu().numpy(), sc.contiguous().cpu().numpy())
+    assert_layout_parity(mode, got, oracle_layout(inp, mode))
 
 
 @pytest.mark.parametrize("mode", ["fp8", "ue8m0"])
