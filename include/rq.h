@@ -47,6 +47,9 @@
  *    but no memory access depends on them.
  *  - Every pointer is a device pointer (or managed / mapped memory the
  *    device can reach) on the current device.
+ *  - No input may overlap an output of the same call: the kernels read
+ *    their inputs through the non-coherent read-only path, so bytes written
+ *    over an input during the call may or may not be seen.
  */
 #ifndef RQ_H_
 #define RQ_H_

@@ -177,7 +177,6 @@ grouped_fp8_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
             for (int c = 0; c < kGEpiCols / 32; ++c) {
                 float d[32];
                 umma::ld32(tmem + (uint32_t(quad * 32) << 16) + buf * kGBN + col0 + c * 32, d);
-                umma::wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) acc[c * 32 + j] = __fmaf_rn(d[j], sc, acc[c * 32 + j]);
             }
@@ -349,7 +348,6 @@ fused_inv_rope_quant_gemm_kernel(const __grid_constant__ CUtensorMap tma_x,
             for (int c = 0; c < 2; ++c) {
                 float d[32];
                 umma::ld32(tmem + (uint32_t(quad * 32) << 16) + buf * kBN + half * 64 + c * 32, d);
-                umma::wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) acc[c * 32 + j] = __fmaf_rn(d[j], sc, acc[c * 32 + j]);
             }

@@ -275,7 +275,6 @@ grouped_fp8_gemm_ue8m0_kernel(const __grid_constant__ CUtensorMap tma_a,
             for (int c = 0; c < 4; ++c) {
                 float d[32];
                 umma::ld32(tmem + (uint32_t(quad * 32) << 16) + half * 128 + c * 32, d);
-                umma::wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) packed[c * 16 + j] = bf16x2(d[2 * j], d[2 * j + 1]);
             }

@@ -82,9 +82,8 @@ struct InvParams {
     uint8_t* out;             // [N*H, 512] codes
     float* scales;            // [N*H, 4]
     uint32_t* error_flags;    // may be null
-    // warp-rows kernel (set by its launcher): tokens per sweep of the grid
-    // when a sweep is whole tokens, so that every warp keeps its heads;
-    // 0 = walk the rows instead
+    // warp-rows kernels (set by their launchers, >= 1): tokens per sweep of
+    // the grid; a sweep is whole tokens, so that every warp keeps its heads
     uint32_t sweep_tokens;
     OutLayout lay;            // used by the layout kernel only
     WaitCtl wait;             // used by the stream kernel only

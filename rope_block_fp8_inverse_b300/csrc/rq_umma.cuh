@@ -138,12 +138,16 @@ __device__ __forceinline__ void commit(uint32_t bar) {
 
 // 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
 // 32*(w%4) .. 32*(w%4)+31; the address carries the lane in bits 16..31).
+// The load and its tcgen05.wait::ld are one asm statement, so the compiler
+// cannot schedule a use of the registers before the wait that makes them
+// valid.
 __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
         "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-        "%30, %31}, [%32];"
+        "%30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
           "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
@@ -153,10 +157,6 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // 2-D tensor-map TMA load of one box into this CTA's shared memory,
