@@ -565,7 +565,8 @@ def run_secondary(args, rq, dev, stream, inv_h, x, pos, cache, hpg, out, scales,
     modes = {}
     for name, mode, gm in (("fp8_group_major", "fp8", True), ("ue8m0", "ue8m0", False),
                            ("ue8m0_group_major", "ue8m0", True), ("bf16", "bf16", False),
-                           ("fp8_scales_transposed", "fp8", False)):
+                           ("fp8_scales_transposed", "fp8", False),
+                           ("ue8m0_scales_transposed", "ue8m0", False)):
         mo, ms = rq.empty_outputs(n, h // hpg, hpg, mode, group_major=gm, device=dev)
         if name.endswith("scales_transposed"):  # scales stored [G, hpg*4, N]
             ms = torch.empty((h // hpg, ms.shape[2], n), dtype=ms.dtype, device=dev).permute(2, 0, 1)
@@ -576,8 +577,10 @@ def run_secondary(args, rq, dev, stream, inv_h, x, pos, cache, hpg, out, scales,
                        "frac_of_measured_peak": round(mb / us / 1e3 / peak, 4)}
         del mo, ms
     res["output_modes"] = {"call": "rq_inv_rope_quant_layout (heads_per_group 8): warp-rows kernel "
-                                   "(token-major and contiguous group-major rows), warp-rows "
-                                   "layout kernel (bf16; transposed scales)",
+                                   "(token-major and contiguous group-major rows), token-tiled "
+                                   "layout kernel (fp32 scales stored transposed, [G, hpg*4, N]), "
+                                   "warp-rows layout kernel (bf16; UE8M0 words stored transposed, "
+                                   "[G, hpg, N])",
                            "launches_each": args.mode_launches, "results": modes}
 
     # the fused q/kv op (q RMS norm + RoPE into a padded q_out, with the kv insert)
@@ -928,6 +931,9 @@ PROFILE_OPS = {
     "gemm_fused": "fused_inv_rope_quant_gemm_kernel (same shape, A produced from x in the kernel)",
     "indexer": "indexer_q_rope_quant_kernel (tokens x 64 heads of 128, NeoX)",
     "fused_qkv": "qnorm_rope_kv_insert_kernel (tokens x 32 q heads padded to 64 + kv)",
+    "insert": "rope_fp8_quant_insert_kernel (tokens into 512 x 64 slots)",
+    "layout_transposed": "the layout kernel for fp32 scales stored [G, hpg*4, N] (token-tiled "
+                         "from 8192 tokens x 32 heads, fixed-head below)",
 }
 
 
@@ -966,6 +972,20 @@ def run_profile_op(args):
                 codes, words = rq.inv_rope_quant(x, pos, cache, hpg, mode="ue8m0")
                 wsf = e.to(torch.uint8).to(dev)
                 call = lambda: rq.grouped_fp8_gemm_ue8m0(codes, words, wc, wsf)
+    elif op == "insert":
+        ii = W.insert_inputs(W.InsertSpec(f"profile{n}", n, 65536, 512, 64))
+        kv, kpos, cache, slots, kc = (ii[k].to(dev) for k in
+                                      ("kv", "positions", "cos_sin_cache", "slot_mapping",
+                                       "k_cache"))
+        call = lambda: rq.rope_fp8_quant_insert(kv, kpos, cache, slots, kc, ii["block_size"])
+    elif op == "layout_transposed":
+        inp = W.inverse_inputs(spec)
+        x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
+        hpg = spec.heads_per_group
+        g = spec.n_heads // hpg
+        mo, _ = rq.empty_outputs(n, g, hpg, "fp8", device=dev)
+        ms = torch.empty((g, hpg * 4, n), dtype=torch.float32, device=dev).permute(2, 0, 1)
+        call = lambda: rq.inv_rope_quant(x, pos, cache, hpg, mode="fp8", out=mo, scales=ms)
     elif op == "indexer":
         ii = W.indexer_inputs(W.IndexerSpec(f"profile{n}", n, 64, 65536))
         q, w, pos, cache = (ii[k].to(dev) for k in ("q", "weights", "positions", "cos_sin_cache"))

@@ -308,8 +308,12 @@ typedef enum rq_out_mode {
  * t*H + h at out + r*512, its scales at r*4 or its word at r) and contiguous
  * group-major ones ([G, N, hpg*512] codes with [G, N, hpg*4] fp32 scales or
  * [G, N, hpg] words, 16-byte aligned) take the warp-rows kernel of
- * rq_inv_rope_fp8_quant. Other layouts take the warp-rows layout kernel
- * (quantising modes with each warp on fixed heads, bf16 by a row walk).
+ * rq_inv_rope_fp8_quant. fp32 scales stored token-contiguous
+ * (scale_stride_token == 1, e.g. transposed [G, hpg*4, N]) take a
+ * token-tiled kernel that stores 8 tokens' scales at once, when the call is
+ * large enough (at least 6 tiles of 8 tokens per warp). Other layouts take
+ * the warp-rows layout kernel (quantising modes with each warp on fixed
+ * heads, bf16 by a row walk).
  */
 rq_status rq_inv_rope_quant_layout(const void *x_bf16, int64_t n_tokens, int64_t n_heads,
                                    int64_t x_stride_token, int64_t x_stride_head,

@@ -1,9 +1,10 @@
 // rq_kernels.cu -- the warp-rows kernels (sm_103a) and their launchers: the
 // inverse-RoPE + block-FP8 quant op (also into row-linear UE8M0 and
-// contiguous group-major layouts), the
-// same op into any strided layout or as bf16, its forward-RoPE + paged-insert
-// sibling, and the fused q RMS norm + RoPE + kv insert op. (The TMA-ring
-// variant of the inverse op is in rq_stream.cu.)
+// contiguous group-major layouts), the same op into any strided layout
+// (fixed heads per warp, or token tiles per warp for token-contiguous fp32
+// scales) or as bf16, its forward-RoPE + paged-insert sibling, and the fused
+// q RMS norm + RoPE + kv insert op. (The TMA-ring variant of the inverse op
+// is in rq_stream.cu.)
 //
 // All are HBM-bound streams (about 1.5 bytes moved per fp32 op), so the
 // design goal is bytes in flight, not arithmetic: a persistent grid of warps
@@ -308,6 +309,90 @@ inv_rope_quant_layout_fixed_kernel(InvParams p) {
     }
 }
 
+// ------------------------------------------------------------------ inverse, token-contiguous scales
+
+// The layout kernel for fp32 scales whose elements of consecutive tokens are
+// adjacent (scale token stride 1: [G, hpg*4, N], the scales stored
+// transposed, as an M-major GEMM scale operand takes them). Stored row by row
+// such scales cost four partial 32-byte sectors per row, a quarter more
+// write sectors than the codes. Here warp w keeps head h = w % n_heads and
+// walks tiles of kScaleTile consecutive tokens of it, two rows at a time;
+// lane 8b + k keeps block b's scale of the tile's token k, and the tile's 32
+// scales leave in one store of four whole sectors. Loads, arithmetic and
+// code stores are those of the other warp-rows kernels; each row fetches its
+// own cos/sin (its token differs from the other row's), after the previous
+// row's arithmetic, which keeps the kernel within 64 registers.
+constexpr uint32_t kScaleTile = 8;
+
+__global__ void __launch_bounds__(kInvThreads, 4)
+inv_rope_quant_layout_tiled_kernel(InvParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint16_t* __restrict__ x = static_cast<const uint16_t*>(p.x);
+    const int ca = chunk_a(lane);
+    const bool rope_lane = lane >= kRopeLane0;
+    const int cs_col = (rope_lane ? lane - kRopeLane0 : 0) * 4;
+    // A sweep of the grid is p.sweep_tokens tokens (whole tiles) of every
+    // head: warp w has head w % n_heads and, in each sweep, tile w / n_heads.
+    const uint32_t tile = warp / p.n_heads;
+    if (tile * kScaleTile >= p.sweep_tokens) return;  // warp-uniform: idle warps of the grid
+    const uint32_t h = warp - tile * p.n_heads;
+    const uint32_t g = h / p.lay.hpg, i = h - g * p.lay.hpg;
+    const uint16_t* xh = x + static_cast<int64_t>(h) * p.sx_h;
+    uint8_t* oh = p.out + int64_t(g) * p.lay.og + int64_t(i) * kHeadDim;
+    // the tile token k and block b of the scale this lane stores, and that
+    // scale's element for token 0
+    const uint32_t kk = lane & 7;
+    float* sl = p.scales + int64_t(g) * p.lay.sg + (int64_t(i) * 4 + (lane >> 3)) * p.lay.se;
+    for (uint32_t t0 = tile * kScaleTile; t0 < p.n_tokens; t0 += p.sweep_tokens) {
+        const uint32_t n_here = min(kScaleTile, p.n_tokens - t0);
+        // the tile's positions, lane k holding token t0 + k's (-1 past the end)
+        int64_t tpos = -1;
+        if (uint32_t(lane) < n_here) tpos = __ldg(p.positions + t0 + lane);
+        float keep = 0.f;  // block (lane >> 3)'s scale of token t0 + kk
+        bool have = false;
+        for (uint32_t k = 0; k < n_here; k += 2) {  // warp-uniform
+            const bool second = k + 1 < n_here;
+            const uint16_t* row = xh + static_cast<int64_t>(t0 + k) * p.sx_t;
+            uint4 a[2], b[2];
+            // the rows' reads do not wait for the positions: only cos/sin do
+            a[0] = ld_stream16(row + 8 * ca);
+            b[0] = ld_stream16(row + 8 * (ca + 8));
+            if (second) {
+                a[1] = ld_stream16(row + p.sx_t + 8 * ca);
+                b[1] = ld_stream16(row + p.sx_t + 8 * (ca + 8));
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if (j == 1 && !second) break;  // warp-uniform
+                const int64_t pos = __shfl_sync(kFull, tpos, k + j);
+                if (static_cast<uint64_t>(pos) >= static_cast<uint64_t>(p.cache_rows)) {
+                    if (lane == 0 && p.error_flags) atomicOr(p.error_flags, RQ_FLAG_POSITION_RANGE);
+                    continue;  // warp-uniform: the row is skipped
+                }
+                float4 c, s;
+                if (rope_lane) {
+                    const float* cs = p.cache + pos * kCacheWidth + cs_col;
+                    c = ld_ro16(cs);
+                    s = ld_ro16(cs + kHalfRope);
+                }
+                float scale;
+                const uint4 q = rope_quant_row<true>(a[j], b[j], rope_lane, c, s, p.eps, &scale);
+                uint8_t* head = oh + int64_t(t0 + k + j) * p.lay.ot;
+                st_stream8(head + 8 * ca, q.x, q.y);
+                st_stream8(head + 8 * (ca + 8), q.z, q.w);
+                if (kk == k + j) {
+                    keep = scale;
+                    have = true;
+                }
+            }
+        }
+        if (have) st_stream4f(sl + t0 + kk, keep);  // token stride 1
+    }
+}
+
 // ------------------------------------------------------------------ insert
 
 template <int kRows>
@@ -484,8 +569,9 @@ constexpr int kMaxDevices = 64;
 // (kRowsVariant: 4 entries per scale encoding: one or two rows per warp,
 // token-major or group-major rows)
 // (kLayFixed: the same for the layout kernel's fixed-head form)
+// (kLayTiled: the token-tiled layout kernel)
 enum Variant { kInv1, kInv2, kIns1, kFus1, kLay, kLayFixed = kLay + 6, kRowsVariant = kLayFixed + 6,
-               kVariants = kRowsVariant + 8 };
+               kLayTiled = kRowsVariant + 8, kVariants = kLayTiled + 1 };
 
 template <typename K>
 int resident_blocks(int device, Variant v, K kernel, int threads) {
@@ -563,6 +649,32 @@ cudaError_t launch_layout(const InvParams& p, const DeviceInfo& dev, cudaStream_
     // us on the TMA-ring kernel. bf16 output keeps the row walk at one row per
     // warp (166.9 us against 170.2 us with fixed heads, and 0.95 of the copy
     // peak with two rows per warp).
+    if (kMode == kOutFp8F32 && p.lay.st == 1) {
+        // fp32 scales stored token-contiguous: the token-tiled kernel, when
+        // every warp gets at least 6 tiles. Measured on B300 against the
+        // fixed-head kernel (us): 16384 x 32 heads 126.3 / 133.2, 12288 x 32
+        // 96.8 / 102.1, 8192 x 32 64.5 / 67.3, 16384 x 24 96.9 / 100.8, 8192 x
+        // 64 126.8 / 133.9; with fewer tiles per warp its coarser last sweep
+        // costs more than the sectors save (8192 x 24, 5.2 tiles per warp:
+        // 51.9 / 51.2; 4096 x 32: 33.0 / 31.1). UE8M0 words stay on the
+        // fixed-head kernel, whose one word per row already fills a single
+        // sector (equal or faster at every size measured).
+        auto k = inv_rope_quant_layout_tiled_kernel;
+        const int res =
+            std::min(resident_blocks(dev.ordinal, kLayTiled, k, kInvThreads), kMaxCtasPerSm);
+        const int64_t n_tiles = (int64_t(p.n_tokens) + kScaleTile - 1) / kScaleTile;
+        int grid = grid_size(n_tiles * p.n_heads, kWarps, dev.sm_count, res);
+        int64_t tiles = int64_t(grid) * kWarps / p.n_heads;  // per sweep
+        if (tiles >= 1 && n_tiles >= 6 * tiles) {
+            // the same number of sweeps with the tiles spread evenly over them
+            const int64_t sweeps = (n_tiles + tiles - 1) / tiles;
+            tiles = (n_tiles + sweeps - 1) / sweeps;
+            grid = static_cast<int>((tiles * p.n_heads + kWarps - 1) / kWarps);
+            InvParams q = p;
+            q.sweep_tokens = static_cast<uint32_t>(tiles * kScaleTile);
+            return launch_pdl(k, grid, kInvThreads, 0, stream, q);
+        }
+    }
     if (kMode != kOutBf16) {
         InvParams q = p;
         const bool two = int64_t(p.n_rows) >= int64_t(dev.sm_count) * kWarps * 4 && p.n_heads % 2 == 0;

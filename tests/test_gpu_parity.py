@@ -530,6 +530,41 @@ def test_layout_bad_position_flags_and_skips(rq):
                                                                want[1].view(np.uint32))
 
 
+def test_layout_token_contiguous_fp32_scales_ragged_with_skips(rq):
+    """fp32 scales stored token-contiguous ([G, hpg*4, N] inside a padded
+    [G, hpg*4, N + 5] buffer) at 8191 tokens x 32 heads, a size at which the
+    layout call takes the token-tiled kernel on B300 (tiles of 8 tokens, at
+    least 6 per warp): a ragged last tile, and out-of-range positions at a
+    tile's first and last token, mid-call and in the ragged tile. The skipped
+    tokens are flagged and their codes and scales keep their sentinels, the
+    padding after each scale row keeps its sentinel, and every other output
+    equals the oracle's."""
+    n, h, hpg = 8191, 32, 8
+    g = h // hpg
+    inp = W.inverse_inputs(W.InverseSpec("tok-contig", n, h, hpg, 65536, "uniform", True, seed=11))
+    pos = inp["positions"].clone()
+    bad = [0, 7, 8, 4000, 8184, 8190]
+    pos[bad] = 65536
+    pos[4000] = -3
+    dev = torch.device("cuda:0")
+    out = torch.full((n, g, hpg * 512), 0x5A, dtype=torch.uint8, device=dev)
+    sst = torch.full((g, hpg * 4, n + 5), -7.0, dtype=torch.float32, device=dev)
+    sc = sst[:, :, :n].permute(2, 0, 1)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    rq.inv_rope_quant(inp["x"].to(dev), pos.to(dev), inp["cos_sin_cache"].to(dev), hpg,
+                      mode="fp8", out=out, scales=sc, error_flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 1
+    assert torch.all(sst[:, :, n:] == -7.0)
+    o, s = out.cpu().numpy(), sc.contiguous().cpu().numpy()
+    assert np.all(o[bad] == 0x5A) and np.all(s[bad] == -7.0)
+    keep = sorted(set(range(n)) - set(bad))
+    sub = {"x": inp["x"][keep], "positions": pos[keep], "cos_sin_cache": inp["cos_sin_cache"],
+           "heads_per_group": hpg}
+    want = oracle_layout(sub, "fp8")
+    assert_layout_parity("fp8", (o[keep], s[keep]), want)
+
+
 # ---------------------------------------------------------------- fused q/kv op
 
 # q_out tolerance (fp32 kernel vs the fp64 oracle, both rounded to bf16):
