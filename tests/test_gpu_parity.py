@@ -364,6 +364,55 @@ def test_insert_strided_kv(rq):
     _assert_cache_parity(got, want)
 
 
+def test_outputs_past_4gib(rq):
+    """Byte offsets past 2^32: 270,000 tokens x 32 heads (8.64 M rows; x is 8.8
+    GB and the codes 4.4 GB, so the last rows' offsets exceed 4 GiB) through
+    the plain op, the layout call with group-major codes, and the layout call
+    with transposed fp32 scales (the token-tiled kernel). The first and last 48
+    tokens and 64 others are compared with the oracle run on those tokens
+    alone. x follows the input recipe (randn, 1% of values x50, bf16),
+    generated on the device in chunks from a seeded generator."""
+    n, h, hpg = 270_000, 32, 8
+    g = h // hpg
+    dev = torch.device("cuda:0")
+    gen = torch.Generator(device=dev).manual_seed(2024)
+    x = torch.empty((n, h, 512), dtype=torch.bfloat16, device=dev)
+    for c in range(0, n, 16384):
+        v = torch.randn((min(16384, n - c), h, 512), generator=gen, device=dev)
+        m = torch.rand(v.shape, generator=gen, device=dev) < W.OUTLIER_RATE
+        x[c:c + v.shape[0]] = torch.where(m, v * W.OUTLIER_GAIN, v).to(torch.bfloat16)
+        del v, m
+    cache = W.rope_cache(65536)
+    pos = torch.randint(0, 65536, (n,), generator=gen, device=dev)
+    cache_d = cache.to(dev)
+    mid = torch.randint(48, n - 48, (64,), generator=torch.Generator().manual_seed(5)).tolist()
+    sample = sorted(set(range(48)) | set(range(n - 48, n)) | set(mid))
+    idx = torch.tensor(sample, device=dev)
+    sub = {"x": x[idx].cpu(), "positions": pos[idx].cpu(), "cos_sin_cache": cache,
+           "heads_per_group": hpg}
+    wc, ws = oracle_inverse(sub)
+
+    def check(codes, scales):
+        torch.cuda.synchronize()
+        gc = codes[idx].contiguous().view(torch.uint8).cpu().numpy()
+        gs = scales[idx].contiguous().cpu().numpy()
+        assert_parity(gc, gs, wc, ws, exact=True)
+
+    codes, scales = rq.inv_rope_fp8_quant(x, pos, cache_d, hpg)
+    check(codes, scales)
+    del codes, scales
+    out, sc = rq.empty_outputs(n, g, hpg, "fp8", group_major=True, device=dev)
+    rq.inv_rope_quant(x, pos, cache_d, hpg, mode="fp8", out=out, scales=sc)
+    check(out, sc)
+    del out, sc
+    out = torch.empty((n, g, hpg * 512), dtype=torch.uint8, device=dev)
+    sc = torch.empty((g, hpg * 4, n), dtype=torch.float32, device=dev).permute(2, 0, 1)
+    rq.inv_rope_quant(x, pos, cache_d, hpg, mode="fp8", out=out, scales=sc)
+    check(out, sc)
+    del out, sc, x
+    torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------- output kinds and layouts
 
 LAYOUTS = ["token_major", "group_major", "scales_transposed", "group_major_padded"]
