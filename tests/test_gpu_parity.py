@@ -310,6 +310,41 @@ def test_insert16k_full(rq):
     assert got.shape == (512, 64 * 528)
 
 
+def test_insert_records_past_4gib(rq):
+    """A paged k_cache larger than 4 GiB (131,072 blocks of 64 records of 528
+    bytes, 4.43 GB): 16,384 tokens go to distinct slots, half of them drawn
+    from the slots whose records start past byte 2^32. Every written record
+    equals the oracle's record of the same token (computed into a small cache
+    with slots 0..N-1: a record's bytes do not depend on its slot), and the
+    untouched records of a sample and the cache's last record keep the
+    sentinel."""
+    n, num_blocks, bs = 16384, 131072, 64
+    inp = W.insert_inputs(W.InsertSpec("ins4g", n, 65536, n // bs, bs, seed=3))
+    n_slots = num_blocks * bs
+    first_high = (2 ** 32 + 527) // 528  # first slot whose record starts past 2^32
+    gen = torch.Generator().manual_seed(11)
+    hi = first_high + torch.randperm(n_slots - first_high, generator=gen)[: n // 2]
+    lo = torch.randperm(first_high, generator=gen)[: n // 2]
+    slots = torch.cat([hi, lo])[torch.randperm(n, generator=gen)]
+    dev = torch.device("cuda:0")
+    kc = torch.full((num_blocks, bs * 528), 0xA5, dtype=torch.uint8, device=dev)
+    rq.rope_fp8_quant_insert(inp["kv"].to(dev), inp["positions"].to(dev),
+                             inp["cos_sin_cache"].to(dev), slots.to(dev), kc, bs)
+    torch.cuda.synchronize()
+    records = kc.view(-1, 528)
+    got = records[slots.to(dev)].cpu().numpy()
+    want = oracle_insert(inp, slots=torch.arange(n, dtype=torch.int64)).reshape(-1, 528)
+    assert np.array_equal(got, want), f"{int((got != want).any(axis=1).sum())} records differ"
+    taken = torch.zeros(n_slots, dtype=torch.bool)
+    taken[slots] = True
+    others = torch.randint(0, n_slots, (8192,), generator=gen)
+    others = torch.cat([others[~taken[others]], torch.tensor([n_slots - 1])])
+    others = others[~taken[others]]
+    assert torch.all(records[others.to(dev)] == 0xA5)
+    del kc, records
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("n", [1, 5, 64, 1000])
 def test_insert_ragged_and_padded_blocks(rq, n):
     blocks = 2 * W.ceil_div(n, 16) + 1
