@@ -627,6 +627,7 @@ def run_secondary(args, rq, dev, stream, inv_h, x, pos, cache, hpg, out, scales,
     del iq, iw, ipos, ico, iwo
 
     res["consumer_gemm"] = gemm_leg(args, rq, dev, x, pos, cache, hpg, out, scales, span_us)
+    res["consumer_gemm"]["decode"] = decode_gemm_leg(rq, dev, stream, inv_h, cache)
     res["decode_latency"] = decode_leg(rq, dev, stream, inv_h, cache)
     res["small_configs_cold"] = cold_leg(rq, dev, stream, inv_h, cache, kv, kpos, slots, k_cache, bs)
     return res
@@ -728,6 +729,78 @@ def decode_leg(rq, dev, stream, inv_h, cache):
         decode[str(nt)] = round(e0.elapsed_time(e1) * 1e3 / 500, 2)
     return {"workload": "decode: N tokens x 32 heads, heads_per_group 8, positions U[0,65536); "
                         "graph of 100 calls, 5 replays", "us_per_call": decode}
+
+
+def decode_gemm_leg(rq, dev, stream, inv_h, cache, reps=20, rounds=9):
+    """The consumer at decode sizes: N = 1, 16, 64 tokens x 32 heads through
+    the op's UE8M0 mode and the block-scaled GEMM (4 groups, K 4096, 1024
+    outputs per group; up to 64 tokens the GEMM runs its split-K kernel).
+    Device time per call from CUDA graphs of `reps` calls: hot (replayed back
+    to back) and cold (each call after a 160 MiB write that evicts L2, minus a
+    graph of the writes alone, paired replays, median over `rounds`)."""
+    gen = torch.Generator().manual_seed(11)
+    wc = torch.randint(0, 256, (4, 1024, 4096), generator=gen, dtype=torch.int32).to(torch.uint8)
+    wc[(wc & 0x7F) == 0x7F] = 0x38
+    wc = wc.to(dev)
+    w_sf = torch.randint(118, 124, (4, 8, 32), generator=gen, dtype=torch.int32).to(torch.uint8).to(dev)
+    flush = torch.empty(160 << 20, dtype=torch.uint8, device=dev)
+
+    def graph_of(fn, with_flush):
+        g = torch.cuda.CUDAGraph()
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            if fn is not None:
+                fn()
+            with torch.cuda.graph(g, stream=gs):
+                for r in range(reps):
+                    if with_flush:
+                        flush.fill_(r & 0xFF)
+                    if fn is not None:
+                        fn()
+        torch.cuda.synchronize(dev)
+        return g
+
+    def once(g):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) * 1e3
+
+    base = graph_of(None, True)
+    base.replay()
+    out = {}
+    for nt in (1, 16, 64):
+        di = W.inverse_inputs(W.decode_spec(nt), cache=inv_h["cos_sin_cache"])
+        dx, dp = di["x"].to(dev), di["positions"].to(dev)
+        codes = torch.empty((nt, 4, 4096), dtype=torch.uint8, device=dev)
+        words = torch.empty((nt, 4, 8), dtype=torch.int32, device=dev)
+        y = torch.empty((nt, 4, 1024), dtype=torch.bfloat16, device=dev)
+        op = lambda: rq.inv_rope_quant(dx, dp, cache, 8, mode="ue8m0", out=codes, scales=words)
+        gemm = lambda: rq.grouped_fp8_gemm_ue8m0(codes, words, wc, w_sf, out=y)
+        pair = lambda: (op(), gemm())
+        row = {}
+        for name, fn in (("gemm", gemm), ("op_then_gemm", pair)):
+            g = graph_of(fn, False)
+            g.replay()
+            row[name + "_hot"] = round(once(g) / reps, 2)
+            g = graph_of(fn, True)
+            g.replay()
+            diffs = []
+            for _ in range(rounds):
+                t1 = once(g)
+                diffs.append(t1 - once(base))
+            row[name + "_cold"] = round(statistics.median(diffs) / reps, 2)
+            del g
+        out[str(nt)] = row
+    del flush, base, wc
+    return {"what": "decode: N tokens x 32 heads -> op (UE8M0) -> grouped GEMM (4 groups, K 4096, "
+                    "1024 outputs per group), device us per call; hot: graphs of "
+                    f"{reps} calls back to back; cold: each call after a 160 MiB write, minus "
+                    "the writes alone", "kernel": "grouped_fp8_gemm_ue8m0_small_kernel (split K "
+                    "over 8-CTA clusters)", "us": out}
 
 
 def cold_leg(rq, dev, stream, inv_h, cache, kv, kpos, slots, k_cache, bs, reps=20, rounds=15):

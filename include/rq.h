@@ -467,6 +467,14 @@ rq_status rq_grouped_fp8_gemm(const uint8_t *a_codes, const float *a_scales, int
  * Code 255 (NaN in the UE8M0 encoding) gives unspecified outputs. Any
  * n_tokens >= 0. A bounded wait that gives up sets RQ_FLAG_TIMEOUT (never
  * expected).
+ * Up to 64 tokens (decode) the call runs a split-K kernel: clusters of 8 CTAs
+ * (4 when k_per_group is not a multiple of 1024) each accumulate a run of K
+ * blocks in fp32 and the partials are summed in fp32 in a fixed order, so
+ * results are deterministic and within the same fp32 accumulation error. It
+ * is launched with programmatic dependent launch: while the previous kernel
+ * in the stream finishes it may prefetch w_codes into L2 (a prefetch reads
+ * no data into the kernel); every read of the call's data happens after
+ * that kernel has completed.
  */
 rq_status rq_grouped_fp8_gemm_ue8m0(const uint8_t *a_codes, const uint32_t *a_sf,
                                     int64_t n_tokens, int64_t groups, int64_t k_per_group,

@@ -1049,6 +1049,63 @@ def test_gemm_ue8m0_random_codes(rq, m, g, k, n_out):
     assert np.all(err <= bound), f"{np.count_nonzero(err > bound)} outputs beyond the bound"
 
 
+@pytest.mark.parametrize("m,g,k,n_out", [(1, 4, 4096, 1024), (2, 1, 1024, 128), (7, 3, 2048, 384),
+                                         (16, 2, 4096, 256), (33, 1, 3072, 640), (64, 4, 4096, 1024),
+                                         (1, 2, 512, 128), (9, 1, 1536, 256), (64, 3, 2560, 384)])
+def test_gemm_ue8m0_decode_sizes(rq, m, g, k, n_out):
+    """Up to 64 tokens the block-scaled GEMM runs split over K on clusters of
+    CTAs (8 ways when K is a multiple of 1024, else 4) with the operands
+    swapped; every output against the float64 oracle's bound, including K
+    runs that cross scale words and token counts that are not multiples of
+    16."""
+    import oracle
+    a, a_sf, w, w_sf, sa, sw = _ue8m0_case(m, g, k, n_out, seed=1000 + m * 7 + k)
+    dev = torch.device("cuda:0")
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = rq.grouped_fp8_gemm_ue8m0(a.to(dev), a_sf.to(dev), w.to(dev), w_sf.to(dev),
+                                  error_flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    want = oracle.grouped_fp8_gemm_ue8m0(a.numpy(), a_sf.numpy().view(np.uint32), w.numpy(),
+                                         w_sf.numpy())
+    bound = _gemm_bound(a, sa.numpy(), w, sw.numpy(), want)
+    err = np.abs(y.double().cpu().numpy() - want)
+    assert np.all(err <= bound), f"{np.count_nonzero(err > bound)} outputs beyond the bound"
+
+
+def test_gemm_ue8m0_decode_reads_what_the_op_just_wrote(rq):
+    """Decode steps: the op (UE8M0 mode) rewrites the same activation buffers
+    and the GEMM, launched with programmatic dependent launch right behind
+    it, consumes them; five rounds with different inputs, each against the
+    oracle (a read of the activations before the dependency wait would show
+    the previous round's values)."""
+    import oracle
+    dev = torch.device("cuda:0")
+    gen = torch.Generator().manual_seed(21)
+    w = _rand_codes((4, 1024, 4096), gen)
+    w_sf = torch.randint(120, 126, (4, 8, 32), generator=gen, dtype=torch.int32).to(torch.uint8)
+    wd, wsd = w.to(dev), w_sf.to(dev)
+    codes = torch.empty((8, 4, 4096), dtype=torch.uint8, device=dev)
+    words = torch.empty((8, 4, 8), dtype=torch.int32, device=dev)
+    y = torch.empty((8, 4, 1024), dtype=torch.bfloat16, device=dev)
+    sw = np.ldexp(1.0, w_sf.numpy().astype(np.int64) - 127).astype(np.float32)
+    ins = [W.inverse_inputs(W.InverseSpec("dec", 8, 32, 8, 4096, "uniform", True, seed=40 + r))
+           for r in range(5)]
+    got = []
+    for inp in ins:
+        rq.inv_rope_quant(inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev),
+                          8, mode="ue8m0", out=codes, scales=words)
+        rq.grouped_fp8_gemm_ue8m0(codes, words, wd, wsd, out=y)
+        got.append(y.clone())
+    torch.cuda.synchronize()
+    for inp, yr in zip(ins, got):
+        wc, ws = oracle_inverse(inp)
+        want = oracle.grouped_fp8_gemm(wc, ws, w.numpy(), sw)
+        bound = _gemm_bound(torch.from_numpy(wc), ws, w, sw, want)
+        err = np.abs(yr.double().cpu().numpy() - want)
+        assert np.all(err <= bound), f"{np.count_nonzero(err > bound)} outputs beyond the bound"
+
+
 def test_gemm_ue8m0_consumes_the_op_ue8m0_output(rq):
     """The op's UE8M0 mode (packed words, token-major) feeds the block-scaled
     GEMM directly; the result matches the fp32-scale GEMM on the op's fp32
@@ -1188,14 +1245,15 @@ def test_stream_kernel_wait_runs_out_reports_timeout_and_context_stays_usable(rq
     assert np.array_equal(scales.cpu().numpy(), ws)
 
 
-@pytest.mark.parametrize("kind", ["fp32", "ue8m0"])
+@pytest.mark.parametrize("kind", ["fp32", "ue8m0", "ue8m0_decode"])
 def test_gemm_wait_runs_out_reports_timeout_and_context_stays_usable(rq, kind):
     """The first CTA's TMA producer issues nothing: its MMA waits give up,
-    RQ_FLAG_TIMEOUT is set, TMEM is freed and the kernel exits; the next
-    normal call is within the oracle's bound."""
+    RQ_FLAG_TIMEOUT is set, TMEM is freed and the kernel exits (on the
+    decode-size kernel, after both cluster barriers); the next normal call is
+    within the oracle's bound."""
     import oracle
     dev = torch.device("cuda:0")
-    m, g, k, n_out = 300, 2, 1024, 256
+    m, g, k, n_out = (16 if kind == "ue8m0_decode" else 300), 2, 1024, 256
     a, a_sf, w, w_sf, sa, sw = _ue8m0_case(m, g, k, n_out, seed=9)
     ad, wd = a.to(dev), w.to(dev)
     if kind == "fp32":
