@@ -1005,6 +1005,8 @@ PROFILE_OPS = {
     "indexer": "indexer_q_rope_quant_kernel (tokens x 64 heads of 128, NeoX)",
     "fused_qkv": "qnorm_rope_kv_insert_kernel (tokens x 32 q heads padded to 64 + kv)",
     "insert": "rope_fp8_quant_insert_kernel (tokens into 512 x 64 slots)",
+    "gemm_decode": "grouped_fp8_gemm_ue8m0_small_kernel after the op's UE8M0 mode (tokens x 32 "
+                   "heads, at most 64 tokens; default 1)",
     "layout_transposed": "the layout kernel for fp32 scales stored [G, hpg*4, N] (token-tiled "
                          "from 8192 tokens x 32 heads, fixed-head below)",
 }
@@ -1015,10 +1017,10 @@ def run_profile_op(args):
     import rope_block_fp8_inverse_b300 as rq
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    n = args.inv_tokens or 4096
+    op = args.profile_op
+    n = args.inv_tokens or (1 if op == "gemm_decode" else 4096)
     spec = W.InverseSpec(f"profile{n}", n, INV_SPEC.n_heads, INV_SPEC.heads_per_group,
                          INV_SPEC.cache_rows, "arange", True)
-    op = args.profile_op
     if op in ("inverse", "inverse_stream", "gemm", "gemm_ue8m0", "gemm_fused"):
         inp = W.inverse_inputs(spec)
         x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
@@ -1045,6 +1047,22 @@ def run_profile_op(args):
                 codes, words = rq.inv_rope_quant(x, pos, cache, hpg, mode="ue8m0")
                 wsf = e.to(torch.uint8).to(dev)
                 call = lambda: rq.grouped_fp8_gemm_ue8m0(codes, words, wc, wsf)
+    elif op == "gemm_decode":
+        if n > 64:
+            raise SystemExit("gemm_decode takes at most 64 tokens")
+        inp = W.inverse_inputs(spec)
+        x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
+        gen = torch.Generator().manual_seed(7)
+        wc = torch.randint(0, 256, (4, 1024, 4096), generator=gen, dtype=torch.int32).to(torch.uint8)
+        wc[(wc & 0x7F) == 0x7F] = 0x38
+        wc = wc.to(dev)
+        wsf = torch.randint(117, 121, (4, 8, 32), generator=gen, dtype=torch.int32).to(torch.uint8).to(dev)
+        codes = torch.empty((n, 4, 4096), dtype=torch.uint8, device=dev)
+        words = torch.empty((n, 4, 8), dtype=torch.int32, device=dev)
+
+        def call():
+            rq.inv_rope_quant(x, pos, cache, 8, mode="ue8m0", out=codes, scales=words)
+            rq.grouped_fp8_gemm_ue8m0(codes, words, wc, wsf)
     elif op == "insert":
         ii = W.insert_inputs(W.InsertSpec(f"profile{n}", n, 65536, 512, 64))
         kv, kpos, cache, slots, kc = (ii[k].to(dev) for k in
