@@ -90,12 +90,6 @@ __device__ __forceinline__ void sts16(uint32_t addr, uint32_t a, uint32_t b, uin
                  : "memory");
 }
 
-__device__ __forceinline__ float lds4f_(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 struct MxTile {
     int mt, g, nt;
 };
@@ -498,9 +492,9 @@ grouped_fp8_gemm_ue8m0_small_kernel(const __grid_constant__ CUtensorMap tma_x,
         uint16_t* y = p.y + int64_t(g) * p.n_out + rt * kSmRows + int(rank) * L::kRowsPer + r;
         for (int c = threadIdx.x / L::kRowsPer; c < tok_here; c += kTokStep) {
             const uint32_t a = base + uint32_t(c * L::kRowsPer + r) * 4;
-            float sum = lds4f_(a);
+            float sum = lds4f(a);
 #pragma unroll
-            for (int q = 1; q < kSplit; ++q) sum = __fadd_rn(sum, lds4f_(a + q * slot_bytes));
+            for (int q = 1; q < kSplit; ++q) sum = __fadd_rn(sum, lds4f(a + q * slot_bytes));
             y[(int64_t(tt) * kSmMaxTok + c) * p.groups * p.n_out] = uint16_t(bf16x2(sum, 0.f));
         }
     }
