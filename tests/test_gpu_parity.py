@@ -1106,6 +1106,47 @@ def test_gemm_ue8m0_decode_reads_what_the_op_just_wrote(rq):
         assert np.all(err <= bound), f"{np.count_nonzero(err > bound)} outputs beyond the bound"
 
 
+def test_two_streams_at_once_match_one_stream(rq):
+    """Two independent op + GEMM chains (a decode-size one on the split-K
+    cluster kernel with programmatic dependent launch, and a 512-token one on
+    the tile kernel) enqueued alternately on two streams, so their kernels
+    run at the same time, give the bytes of the same calls run one after the
+    other on one stream."""
+    dev = torch.device("cuda:0")
+    gen = torch.Generator().manual_seed(31)
+    w = _rand_codes((4, 1024, 4096), gen).to(dev)
+    w_sf = torch.randint(120, 126, (4, 8, 32), generator=gen, dtype=torch.int32).to(torch.uint8).to(dev)
+    chains = []
+    for n in (8, 512):
+        inp = W.inverse_inputs(W.InverseSpec("conc", n, 32, 8, 4096, "uniform", True, seed=n))
+        x, pos, cache = inp["x"].to(dev), inp["positions"].to(dev), inp["cos_sin_cache"].to(dev)
+        codes = torch.empty((n, 4, 4096), dtype=torch.uint8, device=dev)
+        words = torch.empty((n, 4, 8), dtype=torch.int32, device=dev)
+        y = torch.empty((n, 4, 1024), dtype=torch.bfloat16, device=dev)
+
+        def step(x=x, pos=pos, cache=cache, codes=codes, words=words, y=y):
+            rq.inv_rope_quant(x, pos, cache, 8, mode="ue8m0", out=codes, scales=words)
+            rq.grouped_fp8_gemm_ue8m0(codes, words, w, w_sf, out=y)
+        chains.append((step, codes, words, y))
+    for step, *_ in chains:
+        step()
+    torch.cuda.synchronize()
+    want = [tuple(t.clone() for t in c[1:]) for c in chains]
+    for t in (c[3] for c in chains):
+        t.zero_()
+    streams = [torch.cuda.Stream(dev) for _ in chains]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for _ in range(20):
+        for (step, *_), s in zip(chains, streams):
+            with torch.cuda.stream(s):
+                step()
+    torch.cuda.synchronize()
+    for c, wv in zip(chains, want):
+        for got, exp in zip(c[1:], wv):
+            assert torch.equal(got, exp)
+
+
 def test_gemm_ue8m0_consumes_the_op_ue8m0_output(rq):
     """The op's UE8M0 mode (packed words, token-major) feeds the block-scaled
     GEMM directly; the result matches the fp32-scale GEMM on the op's fp32
