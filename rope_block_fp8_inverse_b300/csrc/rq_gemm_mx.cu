@@ -348,7 +348,7 @@ struct SmLayout {
 };
 
 template <int kSplit>
-__global__ void __launch_bounds__(kSmThreads)
+__global__ void __launch_bounds__(kSmThreads, 1)
 grouped_fp8_gemm_ue8m0_small_kernel(const __grid_constant__ CUtensorMap tma_x,
                                     const __grid_constant__ CUtensorMap tma_w, MxGemmParams p,
                                     int n_tok) {
