@@ -616,13 +616,13 @@ def test_layout_bad_position_flags_and_skips(rq):
 
 def test_layout_token_contiguous_fp32_scales_ragged_with_skips(rq):
     """fp32 scales stored token-contiguous ([G, hpg*4, N] inside a padded
-    [G, hpg*4, N + 5] buffer) at 8191 tokens x 32 heads, a size at which the
-    layout call takes the token-tiled kernel on B300 (tiles of 8 tokens, at
-    least 6 per warp): a ragged last tile, and out-of-range positions at a
-    tile's first and last token, mid-call and in the ragged tile. The skipped
-    tokens are flagged and their codes and scales keep their sentinels, the
-    padding after each scale row keeps its sentinel, and every other output
-    equals the oracle's."""
+    [G, hpg*4, N + 5] buffer) from x with padded strides, at 8191 tokens x 32
+    heads, a size at which the layout call takes the token-tiled kernel on
+    B300 (tiles of 8 tokens, at least 6 per warp): a ragged last tile, and
+    out-of-range positions at a tile's first and last token, mid-call and in
+    the ragged tile. The skipped tokens are flagged and their codes and
+    scales keep their sentinels, the padding after each scale row keeps its
+    sentinel, and every other output equals the oracle's."""
     n, h, hpg = 8191, 32, 8
     g = h // hpg
     inp = W.inverse_inputs(W.InverseSpec("tok-contig", n, h, hpg, 65536, "uniform", True, seed=11))
@@ -635,7 +635,10 @@ def test_layout_token_contiguous_fp32_scales_ragged_with_skips(rq):
     sst = torch.full((g, hpg * 4, n + 5), -7.0, dtype=torch.float32, device=dev)
     sc = sst[:, :, :n].permute(2, 0, 1)
     flags = torch.zeros(1, dtype=torch.int32, device=dev)
-    rq.inv_rope_quant(inp["x"].to(dev), pos.to(dev), inp["cos_sin_cache"].to(dev), hpg,
+    # x with padded head and token strides (520 and 33 * 520 elements)
+    wide = torch.zeros((n, h + 1, 520), dtype=torch.bfloat16, device=dev)
+    wide[:, :h, :512] = inp["x"].to(dev)
+    rq.inv_rope_quant(wide[:, :h, :512], pos.to(dev), inp["cos_sin_cache"].to(dev), hpg,
                       mode="fp8", out=out, scales=sc, error_flags=flags)
     torch.cuda.synchronize()
     assert int(flags.item()) == 1
