@@ -436,6 +436,10 @@ rq_status rq_indexer_q_rope_fp8_quant(const void *q_bf16, int64_t n_tokens, int6
  *  y_bf16      [n_tokens, groups, n_out] bf16, 16-byte aligned.
  *  k_per_group, n_out: multiples of 128. Any n_tokens >= 0.
  * A bounded wait that gives up sets RQ_FLAG_TIMEOUT (never expected).
+ * Every size runs the 128-token tile kernel: at decode sizes (about 17 us
+ * at one token for 4 groups, K 4096, n_out 1024) the UE8M0 form,
+ * rq_grouped_fp8_gemm_ue8m0 after the op's RQ_OUT_FP8_SCALE_UE8M0 mode, is
+ * the fast path (its split-K kernel, about 6 us).
  */
 rq_status rq_grouped_fp8_gemm(const uint8_t *a_codes, const float *a_scales, int64_t n_tokens,
                               int64_t groups, int64_t k_per_group, const uint8_t *w_codes,
