@@ -743,6 +743,7 @@ def decode_gemm_leg(rq, dev, stream, inv_h, cache, reps=20, rounds=9):
     wc[(wc & 0x7F) == 0x7F] = 0x38
     wc = wc.to(dev)
     w_sf = torch.randint(118, 124, (4, 8, 32), generator=gen, dtype=torch.int32).to(torch.uint8).to(dev)
+    w32 = torch.ldexp(torch.ones((), device=dev), (w_sf.to(torch.int32) - 127).float())
     flush = torch.empty(160 << 20, dtype=torch.uint8, device=dev)
 
     def graph_of(fn, with_flush):
@@ -777,12 +778,18 @@ def decode_gemm_leg(rq, dev, stream, inv_h, cache, reps=20, rounds=9):
         dx, dp = di["x"].to(dev), di["positions"].to(dev)
         codes = torch.empty((nt, 4, 4096), dtype=torch.uint8, device=dev)
         words = torch.empty((nt, 4, 8), dtype=torch.int32, device=dev)
+        s32 = torch.empty((nt, 4, 32), dtype=torch.float32, device=dev)
         y = torch.empty((nt, 4, 1024), dtype=torch.bfloat16, device=dev)
         op = lambda: rq.inv_rope_quant(dx, dp, cache, 8, mode="ue8m0", out=codes, scales=words)
         gemm = lambda: rq.grouped_fp8_gemm_ue8m0(codes, words, wc, w_sf, out=y)
         pair = lambda: (op(), gemm())
+        # the op's default output (fp32 scales) into the fp32-scale GEMM
+        op32 = lambda: rq.inv_rope_fp8_quant(dx, dp, cache, 8, out=codes, scales=s32)
+        gemm32 = lambda: rq.grouped_fp8_gemm(codes, s32, wc, w32, out=y)
+        pair32 = lambda: (op32(), gemm32())
         row = {}
-        for name, fn in (("gemm", gemm), ("op_then_gemm", pair)):
+        for name, fn in (("gemm", gemm), ("op_then_gemm", pair), ("gemm_fp32", gemm32),
+                         ("op_then_gemm_fp32", pair32)):
             g = graph_of(fn, False)
             g.replay()
             row[name + "_hot"] = round(once(g) / reps, 2)
@@ -796,11 +803,12 @@ def decode_gemm_leg(rq, dev, stream, inv_h, cache, reps=20, rounds=9):
             del g
         out[str(nt)] = row
     del flush, base, wc
-    return {"what": "decode: N tokens x 32 heads -> op (UE8M0) -> grouped GEMM (4 groups, K 4096, "
-                    "1024 outputs per group), device us per call; hot: graphs of "
+    return {"what": "decode: N tokens x 32 heads -> op (UE8M0 words; *_fp32: the default fp32 "
+                    "scales) -> grouped GEMM (4 groups, K 4096, 1024 outputs per group), device "
+                    "us per call; hot: graphs of "
                     f"{reps} calls back to back; cold: each call after a 160 MiB write, minus "
-                    "the writes alone", "kernel": "grouped_fp8_gemm_ue8m0_small_kernel (split K "
-                    "over 8-CTA clusters)", "us": out}
+                    "the writes alone", "kernel": "grouped_fp8_gemm_ue8m0_small_kernel / "
+                    "grouped_fp8_gemm_f32_small_kernel (split K over 8-CTA clusters)", "us": out}
 
 
 def cold_leg(rq, dev, stream, inv_h, cache, kv, kpos, slots, k_cache, bs, reps=20, rounds=15):

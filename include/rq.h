@@ -436,10 +436,14 @@ rq_status rq_indexer_q_rope_fp8_quant(const void *q_bf16, int64_t n_tokens, int6
  *  y_bf16      [n_tokens, groups, n_out] bf16, 16-byte aligned.
  *  k_per_group, n_out: multiples of 128. Any n_tokens >= 0.
  * A bounded wait that gives up sets RQ_FLAG_TIMEOUT (never expected).
- * Every size runs the 128-token tile kernel: at decode sizes (about 17 us
- * at one token for 4 groups, K 4096, n_out 1024) the UE8M0 form,
- * rq_grouped_fp8_gemm_ue8m0 after the op's RQ_OUT_FP8_SCALE_UE8M0 mode, is
- * the fast path (its split-K kernel, about 6 us).
+ * Up to 64 tokens with k_per_group a multiple of 512 (decode) the call runs
+ * a split-K kernel on clusters of 8 CTAs (4 when k_per_group is not a
+ * multiple of 1024): one fp32 accumulator per 128-wide K block, the block's
+ * a_scales * w_scales folded per block in K order, the clusters' partials
+ * summed in a fixed order (deterministic, within the same accumulation
+ * error). It is launched with programmatic dependent launch and may
+ * prefetch w_codes into L2 before the previous kernel in the stream has
+ * finished (a prefetch reads no data into the kernel).
  */
 rq_status rq_grouped_fp8_gemm(const uint8_t *a_codes, const float *a_scales, int64_t n_tokens,
                               int64_t groups, int64_t k_per_group, const uint8_t *w_codes,
@@ -497,7 +501,8 @@ rq_status rq_grouped_fp8_gemm_ue8m0(const uint8_t *a_codes, const uint32_t *a_sf
  * groups, K 4096, n_out 1024) it takes about 2.5 ms against about 336 us for
  * rq_inv_rope_quant_layout in RQ_OUT_FP8_SCALE_UE8M0 mode followed by
  * rq_grouped_fp8_gemm_ue8m0, the recommended pair; at one token, about
- * 86 us against about 8 us for that pair (whose GEMM then runs split over K).
+ * 86 us against about 7 us for that pair or for rq_inv_rope_fp8_quant
+ * followed by rq_grouped_fp8_gemm (both GEMMs then run split over K).
  *  x_bf16 .. eps   as in rq_inv_rope_fp8_quant, with heads_per_group <= 8
  *                  and both strides > 0 (the input is read by tensor-map TMA).
  *  w_codes, w_scales, n_out, y_bf16   as in rq_grouped_fp8_gemm, with

@@ -537,6 +537,9 @@ bool make_x_map(CUtensorMap* map, const FusedGemmParams& p) {
 
 cudaError_t launch_grouped_fp8_gemm(const GemmParams& p, const uint8_t* a_codes,
                                     const uint8_t* w_codes, int dev_ordinal, cudaStream_t stream) {
+    // up to 64 tokens with K a multiple of 512: the split-K decode kernel
+    if (p.m <= 64 && p.k % 512 == 0)
+        return launch_grouped_fp8_gemm_small(p, a_codes, w_codes, dev_ordinal, stream);
     CUtensorMap ma, mw;
     if (!make_map(&ma, a_codes, uint64_t(p.groups) * p.k, uint64_t(p.m), uint64_t(p.groups) * p.k,
                   128) ||

@@ -347,6 +347,46 @@ struct SmLayout {
     static_assert((kMaxSteps + 3) / 4 + 1 <= kSmMaxHeads, "scale words per CTA");
 };
 
+// The split-K kernels' reduction (128 threads; every CTA of the cluster
+// calls it). Thread (w, l) holds its row 32w + l of this CTA's partial tile
+// for tokens 0 .. n_tok - 1 in d0 (tokens 0-31) and d1 (32-63). After a
+// cluster barrier (every CTA's stage region is free) it stores the row into
+// the shared memory of the CTA that owns it (CTA (32w + l) / kRowsPer, slot =
+// this CTA's rank, laid out [token][row within that CTA's rows]); after a
+// second one each CTA sums its rows' kSplit partials in rank order and
+// stores them as bf16: y_tile[token * y_token_stride + row], for the first
+// tok_here tokens.
+template <int kSplit>
+__device__ __forceinline__ void small_reduce_store(uint32_t base, uint32_t rank,
+                                                   const float (&d0)[32], const float (&d1)[32],
+                                                   int n_tok, int tok_here, uint16_t* y_tile,
+                                                   int64_t y_token_stride) {
+    using L = SmLayout<kSplit>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    umma::cluster_sync();  // every CTA's stage region is free
+    const uint32_t slot_bytes = uint32_t(n_tok) * L::kRowsPer * 4;
+    {
+        const int row = warp * 32 + lane;
+        const uint32_t dst = umma::cluster_addr(
+            base + rank * slot_bytes + uint32_t(row % L::kRowsPer) * 4, uint32_t(row / L::kRowsPer));
+#pragma unroll
+        for (int c = 0; c < kSmMaxTok; ++c)
+            if (c < n_tok)
+                umma::st_cluster_f32(dst + uint32_t(c * L::kRowsPer * 4), c < 32 ? d0[c] : d1[c - 32]);
+    }
+    umma::cluster_sync();  // every partial has arrived
+    const int r = threadIdx.x % L::kRowsPer;
+    constexpr int kTokStep = kSmThreads / L::kRowsPer;
+    uint16_t* y = y_tile + int(rank) * L::kRowsPer + r;
+    for (int c = threadIdx.x / L::kRowsPer; c < min(n_tok, tok_here); c += kTokStep) {
+        const uint32_t a = base + uint32_t(c * L::kRowsPer + r) * 4;
+        float sum = lds4f(a);
+#pragma unroll
+        for (int q = 1; q < kSplit; ++q) sum = __fadd_rn(sum, lds4f(a + q * slot_bytes));
+        y[int64_t(c) * y_token_stride] = uint16_t(bf16x2(sum, 0.f));
+    }
+}
+
 template <int kSplit>
 __global__ void __launch_bounds__(kSmThreads, 1)
 grouped_fp8_gemm_ue8m0_small_kernel(const __grid_constant__ CUtensorMap tma_x,
@@ -471,37 +511,142 @@ grouped_fp8_gemm_ue8m0_small_kernel(const __grid_constant__ CUtensorMap tma_x,
     umma::ld32(tmem + (uint32_t(warp * 32) << 16), d0);
     if (n_tok > 32) umma::ld32(tmem + (uint32_t(warp * 32) << 16) + 32u, d1);
     umma::fence_before_sync();
-    umma::cluster_sync();  // every CTA's stage region is free
-    // row 32w + l belongs to CTA (32w + l) / kRowsPer, slot `rank` there,
-    // laid out [token][row within the CTA's rows]
-    const uint32_t slot_bytes = uint32_t(n_tok) * L::kRowsPer * 4;
-    {
-        const int row = warp * 32 + lane;
-        const uint32_t dst = umma::cluster_addr(
-            base + rank * slot_bytes + uint32_t(row % L::kRowsPer) * 4, uint32_t(row / L::kRowsPer));
-#pragma unroll
-        for (int c = 0; c < kSmMaxTok; ++c)
-            if (c < n_tok)
-                umma::st_cluster_f32(dst + uint32_t(c * L::kRowsPer * 4), c < 32 ? d0[c] : d1[c - 32]);
-    }
-    umma::cluster_sync();  // every partial has arrived
-    {
-        const int tok_here = min(n_tok, p.m - tt * kSmMaxTok);
-        const int r = threadIdx.x % L::kRowsPer;
-        constexpr int kTokStep = kSmThreads / L::kRowsPer;
-        uint16_t* y = p.y + int64_t(g) * p.n_out + rt * kSmRows + int(rank) * L::kRowsPer + r;
-        for (int c = threadIdx.x / L::kRowsPer; c < tok_here; c += kTokStep) {
-            const uint32_t a = base + uint32_t(c * L::kRowsPer + r) * 4;
-            float sum = lds4f(a);
-#pragma unroll
-            for (int q = 1; q < kSplit; ++q) sum = __fadd_rn(sum, lds4f(a + q * slot_bytes));
-            y[(int64_t(tt) * kSmMaxTok + c) * p.groups * p.n_out] = uint16_t(bf16x2(sum, 0.f));
-        }
-    }
+    small_reduce_store<kSplit>(base, rank, d0, d1, n_tok, p.m - tt * kSmMaxTok,
+                               p.y + int64_t(tt) * kSmMaxTok * p.groups * p.n_out +
+                                   int64_t(g) * p.n_out + rt * kSmRows,
+                               int64_t(p.groups) * p.n_out);
     if (threadIdx.x == 0 && *abort && p.error_flags) atomicOr(p.error_flags, RQ_FLAG_TIMEOUT);
     if (warp == 1) {
         umma::fence_after_sync();
         umma::tmem_dealloc(tmem, kSmTmemCols);
+    }
+}
+
+// The same decode-size split-K kernel for fp32 block scales (the op's default
+// output, rq_grouped_fp8_gemm): the plain kind::f8f6f4 MMA into one TMEM
+// accumulator per K step (128 x n_tok fp32 each, n_tmem columns in all, at
+// most 512 per SM: 256 per CTA and two CTAs per SM with the 8-way split, 512
+// and one CTA per SM with the 4-way split), then each thread folds its row:
+//   part[token] = sum over its K steps s, in order, of
+//                 (w_scale[s] * a_scale[token, s]) * D_s[row, token]
+// and the cluster sums the parts as in the UE8M0 kernel. The A scales of the
+// tile's tokens and K steps are staged in shared memory; W's scale of a K step
+// is the same for the tile's 128 rows.
+template <int kSplit>
+__global__ void __launch_bounds__(kSmThreads, 1)
+grouped_fp8_gemm_f32_small_kernel(const __grid_constant__ CUtensorMap tma_x,
+                                  const __grid_constant__ CUtensorMap tma_w, GemmParams p,
+                                  int n_tok, uint32_t n_tmem) {
+    using L = SmLayout<kSplit>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t sa0 = base + L::kOffSf, full0 = base + L::kOffBar;
+    const uint32_t done = full0 + 8 * L::kMaxSteps;
+    uint8_t* slot = smem_raw + (base + L::kOffSlot - raw);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(slot);
+    volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(slot + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = umma::cluster_ctarank();
+    const int n_rt = p.n_out / kSmRows;
+    const int tile = blockIdx.x / kSplit;
+    const int rt = tile % n_rt, g = (tile / n_rt) % p.groups, tt = tile / (n_rt * p.groups);
+    const int n_kt = p.k / kMxBK;
+    const int steps = n_kt / kSplit;              // >= 1 (the launcher checks)
+    const int kt0 = int(rank) * steps;
+    const uint32_t lim = p.wait.spin_limit;
+    const uint32_t tok_bytes = uint32_t(n_tok) * kMxBK;
+    const bool starve = (p.wait.inject & kInjectGemmLoads) && blockIdx.x == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < steps; ++s) mbar_init(full0 + 8 * s, 1);
+        mbar_init(done, 1);
+        *abort = 0u;
+        mbar_init_fence();
+        // only a prefetch of W (no data returned) before the dependency wait
+        for (int s = 0; s < steps; ++s)
+            umma::tma_prefetch_l2_2d(&tma_w, (kt0 + s) * kMxBK, g * p.n_out + rt * kSmRows);
+    }
+    if (warp == 1) {
+        umma::tmem_alloc(base + L::kOffSlot, n_tmem);
+        umma::tmem_relinquish();
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (threadIdx.x == 0 && !starve) {  // all K steps' copies at once
+        for (int s = 0; s < steps; ++s) {
+            const uint32_t st = base + s * kSmStage;
+            const int kt = kt0 + s;
+            mbar_arrive_expect_tx(full0 + 8 * s, kSmWTile + tok_bytes);
+            umma::tma_load_2d(st, &tma_w, kt * kMxBK, g * p.n_out + rt * kSmRows, full0 + 8 * s);
+            umma::tma_load_2d(st + kSmWTile, &tma_x, g * p.k + kt * kMxBK, tt * kSmMaxTok,
+                              full0 + 8 * s);
+        }
+    }
+    // the tile's A scales, [K step][token] (0 past the last token)
+    for (int i = threadIdx.x; i < steps * n_tok; i += kSmThreads) {
+        const int s = i / n_tok, c = i - s * n_tok, tok = tt * kSmMaxTok + c;
+        sts4f(sa0 + 4u * uint32_t(i),
+              tok < p.m ? __ldg(p.a_scales + (int64_t(tok) * p.groups + g) * n_kt + kt0 + s) : 0.f);
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 1 && lane == 0) {
+        const uint32_t idesc = umma::idesc_e4m3_f32(kSmRows, n_tok);
+        for (int s = 0; s < steps; ++s) {
+            if (!wait_or_abort(full0 + 8 * s, 0, abort, lim)) break;
+            umma::fence_after_sync();
+            const uint32_t st = base + s * kSmStage;
+            const uint64_t wd = umma::smem_desc_sw128(st);
+            const uint64_t xd = umma::smem_desc_sw128(st + kSmWTile);
+#pragma unroll
+            for (int k = 0; k < kMxBK / 32; ++k)
+                umma::mma_f8f6f4(tmem + uint32_t(s * n_tok), wd + 2 * k, xd + 2 * k, idesc, k != 0);
+        }
+        umma::commit(done);  // also after an abort: every issued MMA completes first
+    }
+    if (!mbar_wait(done, 0, lim)) *abort = 1u;
+    if (warp == 0 && lane == 0 && !starve) {
+        for (int s = 0; s < steps; ++s)
+            if (!mbar_wait(full0 + 8 * s, 0, lim)) *abort = 1u;
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    // fold this thread's row over the K steps, in order
+    float d0[32], d1[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) d0[c] = d1[c] = 0.f;
+    const float* ws = p.w_scales + (int64_t(g) * n_rt + rt) * n_kt + kt0;
+    for (int s = 0; s < steps; ++s) {
+        const float sw = __ldg(ws + s);
+        const uint32_t col = tmem + (uint32_t(warp * 32) << 16) + uint32_t(s * n_tok);
+        float d[32];
+        umma::ld32(col, d);
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            if (c < n_tok)
+                d0[c] = __fadd_rn(d0[c], __fmul_rn(__fmul_rn(sw, lds4f(sa0 + 4u * uint32_t(s * n_tok + c))), d[c]));
+        if (n_tok > 32) {
+            umma::ld32(col + 32u, d);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (32 + c < n_tok)
+                    d1[c] = __fadd_rn(d1[c], __fmul_rn(__fmul_rn(sw, lds4f(sa0 + 4u * uint32_t(s * n_tok + 32 + c))), d[c]));
+        }
+    }
+    umma::fence_before_sync();
+    small_reduce_store<kSplit>(base, rank, d0, d1, n_tok, p.m - tt * kSmMaxTok,
+                               p.y + int64_t(tt) * kSmMaxTok * p.groups * p.n_out +
+                                   int64_t(g) * p.n_out + rt * kSmRows,
+                               int64_t(p.groups) * p.n_out);
+    if (threadIdx.x == 0 && *abort && p.error_flags) atomicOr(p.error_flags, RQ_FLAG_TIMEOUT);
+    if (warp == 1) {
+        umma::fence_after_sync();
+        umma::tmem_dealloc(tmem, n_tmem);
     }
 }
 
@@ -559,7 +704,68 @@ cudaError_t launch_grouped_fp8_gemm_ue8m0_small(const MxGemmParams& p, const uin
     return launch_small<4>(p, a_codes, w_codes, dev, stream);
 }
 
+// The fp32-scale decode kernel; n_tmem covers one accumulator per K step
+// plus the columns a 32-wide TMEM read past the last one touches.
+template <int kSplit>
+cudaError_t launch_f32_small(const GemmParams& p, const uint8_t* a_codes, const uint8_t* w_codes,
+                             int dev_ordinal, cudaStream_t stream) {
+    using L = SmLayout<kSplit>;
+    const int n_tok = p.m >= kSmMaxTok ? kSmMaxTok : (p.m + 15) / 16 * 16;
+    const int steps = p.k / kMxBK / kSplit;
+    const uint32_t need = uint32_t(steps * n_tok + (n_tok % 32 ? 32 - n_tok % 32 : 0));
+    uint32_t n_tmem = 32;
+    while (n_tmem < need) n_tmem <<= 1;
+    // The CTAs that fit on an SM (228 KiB of shared memory, 1 KiB reserved per
+    // CTA) must never ask for more than its 512 TMEM columns together, so an
+    // allocation never waits on a CTA that is itself waiting at a cluster
+    // barrier: 256 columns at most with the 8-way split (two CTAs per SM),
+    // 512 with the 4-way split (one). Always true for K <= 4096.
+    const uint32_t ctas_per_sm = 233472u / (L::kSmem + 1024u);
+    if (n_tmem * ctas_per_sm > 512u) return cudaErrorInvalidValue;
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, a_codes, uint64_t(p.groups) * p.k, uint64_t(p.m), uint64_t(p.groups) * p.k,
+                  uint32_t(n_tok)) ||
+        !make_map(&mw, w_codes, uint64_t(p.k), uint64_t(p.groups) * p.n_out, uint64_t(p.k),
+                  kSmRows))
+        return cudaErrorInvalidValue;
+    auto k = grouped_fp8_gemm_f32_small_kernel<kSplit>;
+    constexpr int kMax = 64;
+    static thread_local bool attr_done[kMax] = {};
+    const int d = (dev_ordinal >= 0 && dev_ordinal < kMax) ? dev_ordinal : 0;
+    if (!attr_done[d]) {
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   int(L::kSmem));
+        if (e != cudaSuccess) return e;
+        attr_done[d] = true;
+    }
+    const int64_t tiles = int64_t((p.m + kSmMaxTok - 1) / kSmMaxTok) * p.groups * (p.n_out / kSmRows);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(tiles * kSplit));
+    cfg.blockDim = dim3(kSmThreads);
+    cfg.dynamicSmemBytes = L::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k, mx, mw, p, n_tok, n_tmem);
+}
+
 }  // namespace
+
+// fp32 block scales, up to 64 tokens, K a multiple of 512 (the 8-way split
+// when K is a multiple of 1024).
+cudaError_t launch_grouped_fp8_gemm_small(const GemmParams& p, const uint8_t* a_codes,
+                                          const uint8_t* w_codes, int dev_ordinal,
+                                          cudaStream_t stream) {
+    if ((p.k / kMxBK) % 8 == 0) return launch_f32_small<8>(p, a_codes, w_codes, dev_ordinal, stream);
+    return launch_f32_small<4>(p, a_codes, w_codes, dev_ordinal, stream);
+}
 
 cudaError_t launch_grouped_fp8_gemm_ue8m0(const MxGemmParams& p, const uint8_t* a_codes,
                                           const uint8_t* w_codes, const DeviceInfo& dev,

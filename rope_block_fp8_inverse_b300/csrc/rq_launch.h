@@ -218,6 +218,10 @@ cudaError_t launch_indexer_q_rope_quant(const IdxParams& p, const DeviceInfo& de
                                         cudaStream_t stream);
 cudaError_t launch_grouped_fp8_gemm(const GemmParams& p, const uint8_t* a_codes,
                                     const uint8_t* w_codes, int dev_ordinal, cudaStream_t stream);
+// The fp32-scale GEMM's decode-size split-K kernel (p.m <= 64, p.k % 512 == 0).
+cudaError_t launch_grouped_fp8_gemm_small(const GemmParams& p, const uint8_t* a_codes,
+                                          const uint8_t* w_codes, int dev_ordinal,
+                                          cudaStream_t stream);
 cudaError_t launch_fused_inv_rope_quant_gemm(const FusedGemmParams& p, const uint8_t* w_codes,
                                              int dev_ordinal, cudaStream_t stream);
 cudaError_t launch_validate_indices(const ValParams& p, const DeviceInfo& dev,

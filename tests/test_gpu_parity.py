@@ -960,6 +960,54 @@ def test_gemm_random_codes(rq, m, g, k, n_out):
     assert_gemm_parity(y, a, sa, w, sw)
 
 
+@pytest.mark.parametrize("m,g,k,n_out", [(1, 4, 4096, 1024), (2, 1, 512, 128), (7, 3, 1536, 384),
+                                         (16, 2, 2048, 256), (33, 1, 3072, 640), (64, 4, 4096, 1024),
+                                         (9, 2, 2560, 128), (48, 1, 3584, 256)])
+def test_gemm_fp32_decode_sizes(rq, m, g, k, n_out):
+    """Up to 64 tokens (K a multiple of 512) the fp32-scale GEMM runs its
+    split-K cluster kernel: one accumulator per K block, the two scales folded
+    per block. Scales here are arbitrary fp32 values (not powers of two), and
+    every output is compared with the float64 oracle's bound."""
+    gen = torch.Generator().manual_seed(500 + m * 7 + k)
+    a, w = _rand_codes((m, g, k), gen), _rand_codes((g, n_out, k), gen)
+    sa = (torch.rand((m, g, k // 128), generator=gen) + 0.5) * 2.0 ** torch.randint(
+        -8, 4, (m, g, k // 128), generator=gen).float()
+    sw = (torch.rand((g, n_out // 128, k // 128), generator=gen) + 0.5) * 2.0 ** torch.randint(
+        -12, -4, (g, n_out // 128, k // 128), generator=gen).float()
+    dev = torch.device("cuda:0")
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = rq.grouped_fp8_gemm(a.to(dev), sa.to(dev), w.to(dev), sw.to(dev), error_flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    assert_gemm_parity(y, a, sa.numpy(), w, sw.numpy())
+
+
+def test_gemm_fp32_decode_consumes_the_op_output(rq):
+    """Decode steps with the op's default output (fp32 scales): the op
+    rewrites the same buffers and the split-K GEMM reads them right behind it,
+    five rounds, each against the oracle."""
+    dev = torch.device("cuda:0")
+    gen = torch.Generator().manual_seed(23)
+    w = _rand_codes((4, 1024, 4096), gen)
+    sw = (torch.rand((4, 8, 32), generator=gen) + 0.5) * 2.0 ** -8
+    wd, swd = w.to(dev), sw.to(dev)
+    codes = torch.empty((8, 4, 4096), dtype=torch.uint8, device=dev)
+    scales = torch.empty((8, 4, 32), dtype=torch.float32, device=dev)
+    y = torch.empty((8, 4, 1024), dtype=torch.bfloat16, device=dev)
+    ins = [W.inverse_inputs(W.InverseSpec("decf", 8, 32, 8, 4096, "uniform", True, seed=60 + r))
+           for r in range(5)]
+    got = []
+    for inp in ins:
+        rq.inv_rope_fp8_quant(inp["x"].to(dev), inp["positions"].to(dev),
+                              inp["cos_sin_cache"].to(dev), 8, out=codes, scales=scales)
+        rq.grouped_fp8_gemm(codes, scales, wd, swd, out=y)
+        got.append(y.clone())
+    torch.cuda.synchronize()
+    for inp, yr in zip(ins, got):
+        wc, ws = oracle_inverse(inp)
+        assert_gemm_parity(yr, torch.from_numpy(wc), ws, w, sw.numpy())
+
+
 def test_gemm_consumes_the_inverse_op_output(rq):
     """The op's own codes and scales (bit-exact with the oracle) feed the GEMM."""
     inp = W.inverse_inputs(W.InverseSpec("gemm", 200, 16, 8, 4096, "uniform", True, seed=4))
@@ -1289,7 +1337,7 @@ def test_stream_kernel_wait_runs_out_reports_timeout_and_context_stays_usable(rq
     assert np.array_equal(scales.cpu().numpy(), ws)
 
 
-@pytest.mark.parametrize("kind", ["fp32", "ue8m0", "ue8m0_decode"])
+@pytest.mark.parametrize("kind", ["fp32", "ue8m0", "ue8m0_decode", "fp32_decode"])
 def test_gemm_wait_runs_out_reports_timeout_and_context_stays_usable(rq, kind):
     """The first CTA's TMA producer issues nothing: its MMA waits give up,
     RQ_FLAG_TIMEOUT is set, TMEM is freed and the kernel exits (on the
@@ -1297,10 +1345,10 @@ def test_gemm_wait_runs_out_reports_timeout_and_context_stays_usable(rq, kind):
     within the oracle's bound."""
     import oracle
     dev = torch.device("cuda:0")
-    m, g, k, n_out = (16 if kind == "ue8m0_decode" else 300), 2, 1024, 256
+    m, g, k, n_out = (16 if kind.endswith("_decode") else 300), 2, 1024, 256
     a, a_sf, w, w_sf, sa, sw = _ue8m0_case(m, g, k, n_out, seed=9)
     ad, wd = a.to(dev), w.to(dev)
-    if kind == "fp32":
+    if kind.startswith("fp32"):
         sad, swd = sa.to(dev), sw.to(dev)
         call = lambda fl: rq.grouped_fp8_gemm(ad, sad, wd, swd, error_flags=fl)
         want = oracle.grouped_fp8_gemm(a.numpy(), sa.numpy(), w.numpy(), sw.numpy())
